@@ -1,0 +1,388 @@
+"""Pins for the fp64 CPU oracle, independent of the oracle's own code.
+
+Each test checks the oracle against something other than itself: brute-force
+loop nests written here, closed forms, adjoint identities, hand-derived MX
+values (tests/golden/mx_blocks.txt), torch's own float8 decoders and casts, and
+lossless round trips.  A plausible slip in the oracle (a transposed operand, a
+dropped group, a wrong offset, a wrong sign, a wrong rounding tie) fails at
+least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import grouped_gemm as og
+from oracle import mx as omx
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_lens(rng, G, M, zeros=1):
+    cuts = np.sort(rng.integers(0, M + 1, size=G - 1))
+    lens = np.diff(np.concatenate([[0], cuts, [M]])).astype(np.int32)
+    for g in rng.choice(G, size=min(zeros, G), replace=False):
+        lens[(g + 1) % G] += lens[g]
+        lens[g] = 0
+    return lens
+
+
+# ---------------------------------------------------------------------------
+# grouped GEMM: brute force, identities, closed forms
+# ---------------------------------------------------------------------------
+
+def _brute(X, W, dY, lens):
+    """Pure-Python loops, token by token: which group owns row r is found by walking lens."""
+    M, K = X.shape
+    G, N, _ = W.shape
+    owner = []
+    for g, n in enumerate(lens):
+        owner += [g] * int(n)
+    Y = [[0.0] * N for _ in range(M)]
+    dX = [[0.0] * K for _ in range(M)]
+    dW = [[[0.0] * K for _ in range(N)] for _ in range(G)]
+    for r in range(M):
+        g = owner[r]
+        for n in range(N):
+            for k in range(K):
+                Y[r][n] += float(X[r, k]) * float(W[g, n, k])
+                dX[r][k] += float(dY[r, n]) * float(W[g, n, k])
+                dW[g][n][k] += float(dY[r, n]) * float(X[r, k])
+    return np.array(Y), np.array(dX), np.array(dW)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_grouped_gemm_vs_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    G = int(rng.integers(1, 6))
+    M = int(rng.integers(0, 17))
+    N = int(rng.integers(1, 7))
+    K = int(rng.integers(1, 7))
+    lens = _rand_lens(rng, G, M, zeros=1 if G > 1 else 0)
+    X = rng.standard_normal((M, K))
+    W = rng.standard_normal((G, N, K))
+    dY = rng.standard_normal((M, N))
+    Yb, dXb, dWb = _brute(X, W, dY, lens)
+    np.testing.assert_allclose(og.grouped_gemm_fwd(X, W, lens), Yb.reshape(M, N), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(og.grouped_gemm_dgrad(dY, W, lens), dXb.reshape(M, K), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(og.grouped_gemm_wgrad(X, dY, lens), dWb.reshape(G, N, K), rtol=1e-12, atol=1e-12)
+
+
+def test_adjoint_identity():
+    # <fwd(X,W), dY> = <X, dgrad(dY,W)> = <W, wgrad(X,dY)>: all three are the same trilinear form
+    rng = np.random.default_rng(7)
+    G, M, N, K = 6, 200, 48, 40
+    lens = _rand_lens(rng, G, M, zeros=2)
+    X, W, dY = rng.standard_normal((M, K)), rng.standard_normal((G, N, K)), rng.standard_normal((M, N))
+    a = np.sum(og.grouped_gemm_fwd(X, W, lens) * dY)
+    b = np.sum(X * og.grouped_gemm_dgrad(dY, W, lens))
+    c = np.sum(W * og.grouped_gemm_wgrad(X, dY, lens))
+    assert abs(a - b) < 1e-9 * (1 + abs(a)) and abs(a - c) < 1e-9 * (1 + abs(a))
+
+
+def test_groups_concatenate():
+    rng = np.random.default_rng(8)
+    G, M, N, K = 5, 90, 12, 10
+    lens = _rand_lens(rng, G, M, zeros=1)
+    X, W, dY = rng.standard_normal((M, K)), rng.standard_normal((G, N, K)), rng.standard_normal((M, N))
+    Y, dX, dW = og.grouped_gemm_fwd(X, W, lens), og.grouped_gemm_dgrad(dY, W, lens), og.grouped_gemm_wgrad(X, dY, lens)
+    off = np.concatenate([[0], np.cumsum(lens)])
+    for g in range(G):
+        a, b = off[g], off[g + 1]
+        one = np.array([b - a], dtype=np.int32)
+        np.testing.assert_array_equal(og.grouped_gemm_fwd(X[a:b], W[g:g + 1], one), Y[a:b])
+        np.testing.assert_array_equal(og.grouped_gemm_dgrad(dY[a:b], W[g:g + 1], one), dX[a:b])
+        np.testing.assert_array_equal(og.grouped_gemm_wgrad(X[a:b], dY[a:b], one)[0], dW[g])
+
+
+def test_one_hot_picks_weight_entries():
+    # X rows one-hot at k_r: Y[r, n] = W[g(r), n, k_r]; dY one-hot at n_r: dX[r, k] = W[g(r), n_r, k]
+    rng = np.random.default_rng(9)
+    G, N, K = 3, 5, 4
+    lens = np.array([2, 0, 3], dtype=np.int32)
+    owner = [0, 0, 2, 2, 2]
+    M = 5
+    W = rng.standard_normal((G, N, K))
+    kr = rng.integers(0, K, size=M)
+    nr = rng.integers(0, N, size=M)
+    X = np.zeros((M, K)); X[np.arange(M), kr] = 1.0
+    dY = np.zeros((M, N)); dY[np.arange(M), nr] = 1.0
+    Y = og.grouped_gemm_fwd(X, W, lens)
+    dX = og.grouped_gemm_dgrad(dY, W, lens)
+    for r in range(M):
+        np.testing.assert_array_equal(Y[r], W[owner[r], :, kr[r]])
+        np.testing.assert_array_equal(dX[r], W[owner[r], nr[r], :])
+    dW = og.grouped_gemm_wgrad(X, dY, lens)
+    assert np.all(dW[1] == 0.0)
+    expect = np.zeros((N, K))
+    for r in (2, 3, 4):
+        expect[nr[r], kr[r]] += 1.0
+    np.testing.assert_array_equal(dW[2], expect)
+
+
+def test_empty_groups_and_validation():
+    X = np.ones((3, 2)); dY = np.ones((3, 4))
+    dW = og.grouped_gemm_wgrad(X, dY, [0, 3, 0])
+    assert np.all(dW[0] == 0) and np.all(dW[2] == 0) and np.all(dW[1] == 3.0)
+    with pytest.raises(ValueError):
+        og.group_offsets([2, -1, 2], 3)
+    with pytest.raises(ValueError):
+        og.group_offsets([2, 2], 3)
+    assert og.grouped_gemm_fwd(np.zeros((0, 2)), np.ones((2, 4, 2)), [0, 0]).shape == (0, 4)
+
+
+def test_bf16_decode_exact():
+    vals = np.array([1.0, -2.5, 3.140625, 0.0, -0.0, 2.0 ** -133, 65280.0 * 2 ** 112], dtype=np.float64)
+    bits = torch.tensor(vals, dtype=torch.float64).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(og.bf16_to_f64(bits), vals)
+
+
+# ---------------------------------------------------------------------------
+# SwiGLU forward / backward
+# ---------------------------------------------------------------------------
+
+def test_swiglu_closed_forms():
+    H = np.array([[0.0, 1.0, 5.0, 7.0],      # gate 0 -> A = 0
+                  [1.0, 30.0, 2.0, 3.0],      # A = silu(1)*2, silu(30)*3 ~ 30*3
+                  [-1.0, -40.0, 4.0, 1.0]])   # silu(-1)*4; silu(-40) ~ -40*e^-40
+    A = og.swiglu_fwd(H)
+    silu1 = 1.0 / (1.0 + math.exp(-1.0))
+    assert A[0, 0] == 0.0 and A[0, 1] == pytest.approx(silu1 * 7.0, rel=1e-15)
+    assert A[1, 0] == pytest.approx(silu1 * 2.0, rel=1e-15)
+    assert A[1, 1] == pytest.approx(90.0, rel=1e-12)
+    assert A[2, 0] == pytest.approx(-1.0 / (1.0 + math.e) * 4.0, rel=1e-15)
+    assert abs(A[2, 1]) < 1e-15
+
+
+def test_swiglu_bwd_finite_difference():
+    rng = np.random.default_rng(11)
+    H = rng.standard_normal((4, 6)) * 2
+    dA = rng.standard_normal((4, 3))
+    dH = og.swiglu_bwd(dA, H)
+    eps = 1e-6
+    num = np.zeros_like(H)
+    for i in range(H.shape[0]):
+        for j in range(H.shape[1]):
+            Hp, Hm = H.copy(), H.copy()
+            Hp[i, j] += eps; Hm[i, j] -= eps
+            num[i, j] = np.sum(dA * (og.swiglu_fwd(Hp) - og.swiglu_fwd(Hm))) / (2 * eps)
+    np.testing.assert_allclose(dH, num, rtol=1e-7, atol=1e-8)
+
+
+def test_fc1_fc2_compositions():
+    rng = np.random.default_rng(12)
+    G, M, I, K = 3, 20, 4, 6
+    lens = np.array([7, 0, 13], dtype=np.int32)
+    X, W1 = rng.standard_normal((M, K)), rng.standard_normal((G, 2 * I, K))
+    A, H = og.grouped_fc1_swiglu(X, W1, lens)
+    Yb, _, _ = _brute(X, W1, np.zeros((M, 2 * I)), lens)
+    np.testing.assert_allclose(H, Yb, rtol=1e-12, atol=1e-12)
+    g, u = Yb[:, :I], Yb[:, I:]
+    np.testing.assert_allclose(A, g / (1 + np.exp(-g)) * u, rtol=1e-12, atol=1e-12)
+    W2 = rng.standard_normal((G, K, I))
+    dY = rng.standard_normal((M, K))
+    dH = og.grouped_fc2_dgrad_swiglu_bwd(dY, W2, H, lens)
+    # chain rule through a perturbation: d/dt <dY, fwd(swiglu(H + t V), W2)> = <dH, V>
+    V = rng.standard_normal(H.shape)
+    f = lambda t: np.sum(dY * og.grouped_gemm_fwd(og.swiglu_fwd(H + t * V), W2, lens))
+    num = (f(1e-6) - f(-1e-6)) / 2e-6
+    assert np.sum(dH * V) == pytest.approx(num, rel=1e-6)
+
+
+def test_within_tol():
+    ref = np.array([1.0, -1.0, 0.0, 100.0])
+    assert og.within_tol(ref, ref)[0]
+    assert not og.within_tol(ref + np.array([0, 0, 0, 2.0]), ref)[0]
+    assert not og.within_tol(np.array([np.nan, -1, 0, 100]), ref)[0]
+
+
+# ---------------------------------------------------------------------------
+# MX formats
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = omx.decode_e4m3(codes)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9
+
+
+def test_e8m0_decode_matches_torch():
+    codes = np.arange(255, dtype=np.uint8)  # 0xFF is NaN in both
+    ref = torch.from_numpy(codes).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    np.testing.assert_array_equal(omx.decode_e8m0(codes), ref)
+    assert np.isnan(omx.decode_e8m0(0xFF))
+
+
+def test_e2m1_decode_table():
+    table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    np.testing.assert_array_equal(omx.decode_e2m1(np.arange(8)), table)
+    np.testing.assert_array_equal(omx.decode_e2m1(np.arange(8, 16)), [-v for v in table])
+
+
+def _golden_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "mx_blocks.txt")) as f:
+        for line in f:
+            if not line.strip() or line.startswith("#"):
+                continue
+            p = line.split()
+            cases.append((p[0], float.fromhex(p[1]), float.fromhex(p[2]), int(p[3], 16), int(p[4], 16)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_cases())
+def test_mx_golden_blocks(case):
+    fmt, amax, v, scale, code = case
+    blk = np.zeros((1, 32))
+    blk[0, 0], blk[0, 1] = amax, v
+    s, c = omx.quantize_blocks(fmt, blk)
+    assert int(s[0]) == scale
+    assert int(c[0, 1]) == code
+
+
+def test_e4m3_rounding_matches_torch_cast_in_range():
+    rng = np.random.default_rng(13)
+    v = rng.uniform(-440, 440, size=20000)
+    v = np.concatenate([v, rng.uniform(-2.0 ** -6, 2.0 ** -6, size=5000)])
+    # include exact ties: midpoints between consecutive grid values
+    grid = omx.decode_e4m3(np.arange(0x7E))
+    mids = (grid[:-1] + np.diff(grid) / 2)
+    v = np.concatenate([v, mids, -mids])
+    ref = torch.tensor(v, dtype=torch.float64).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(omx.round_to_grid("e4m3", v), ref)
+
+
+def test_mx_roundtrip_and_idempotence():
+    rng = np.random.default_rng(14)
+    for fmt in omx.FORMATS:
+        grid = omx._grid(fmt)
+        # values already on a block's grid: code * 2^E with the block's amax setting E
+        E = rng.integers(-20, 20, size=(64, 1))
+        codes = rng.integers(0, len(grid), size=(64, 32))
+        codes[:, 0] = len(grid) - 1  # amax = top of the grid, so the rule picks this E back
+        vals = grid[codes] * np.ldexp(1.0, E + 0) * np.where(rng.random((64, 32)) < 0.5, -1, 1)
+        # rule: floor(log2(amax)) - emax = E + floor(log2(grid max)) - emax = E
+        s, c = omx.quantize_blocks(fmt, vals)
+        np.testing.assert_array_equal(s.astype(np.int64) - 127, E[:, 0])
+        deq = omx.decode(fmt, c) * omx.decode_e8m0(s)[:, None]
+        np.testing.assert_array_equal(deq, vals)
+        s2, c2 = omx.quantize_blocks(fmt, deq)
+        np.testing.assert_array_equal(s2, s)
+        np.testing.assert_array_equal(c2, c)
+
+
+def test_mx_monotone_and_top_binade():
+    rng = np.random.default_rng(15)
+    for fmt in omx.FORMATS:
+        v = np.sort(rng.uniform(0, 3, size=4000))
+        c = omx.round_to_grid(fmt, v)
+        assert np.all(np.diff(omx.decode(fmt, c)) >= 0)
+        blocks = rng.standard_normal((200, 32)) * np.ldexp(1.0, rng.integers(-30, 30, size=(200, 1)))
+        s, _ = omx.quantize_blocks(fmt, blocks)
+        scaled_amax = np.max(np.abs(blocks), axis=1) * omx.decode_e8m0(s) ** -1
+        assert np.all(scaled_amax >= 2.0 ** omx.EMAX[fmt]) and np.all(scaled_amax < 2.0 ** (omx.EMAX[fmt] + 1))
+
+
+def test_e2m1_pack_order():
+    codes = np.array([[0x1, 0x2, 0x7, 0x8]], dtype=np.uint8)
+    packed = omx.pack_e2m1(codes)
+    np.testing.assert_array_equal(packed, [[0x21, 0x87]])
+    np.testing.assert_array_equal(omx.unpack_e2m1(packed), codes)
+
+
+def _bf16_bits(a):
+    return torch.tensor(a, dtype=torch.float64).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_colwise_equals_rowwise_of_group_slices():
+    # colwise on [M, C] == rowwise on each group's transposed, zero-padded slice
+    rng = np.random.default_rng(16)
+    lens = np.array([33, 0, 5, 64, 1], dtype=np.int32)
+    M, C = int(lens.sum()), 8
+    bits = _bf16_bits(rng.standard_normal((M, C)) * 3)
+    P = 128
+    M_pad = 4 * P + P
+    for fmt in omx.FORMATS:
+        ct, st = omx.mx_quantize_colwise(bits, lens, fmt, M_pad, P)
+        if fmt == "e2m1":
+            ct = omx.unpack_e2m1(ct)
+        off = 0
+        poff = 0
+        for n in lens:
+            n = int(n)
+            if n:
+                nb = -(-n // 32)
+                sl = np.zeros((C, nb * 32), dtype=np.uint16)
+                sl[:, :n] = bits[off:off + n].T
+                rc, rs = omx.mx_quantize_rowwise(sl, fmt)
+                if fmt == "e2m1":
+                    rc = omx.unpack_e2m1(rc)
+                np.testing.assert_array_equal(ct[:, poff:poff + n], rc[:, :n])
+                assert np.all(ct[:, poff + n:poff + -(-n // P) * P] == 0)
+                np.testing.assert_array_equal(st[:, poff // 32:poff // 32 + nb], rs)
+            off += n
+            poff += -(-n // P) * P
+        assert np.all(ct[:, poff:] == 0) and np.all(st[:, poff // 32:] == 0)
+
+
+def _grid_operand(rng, fmt, rows, cols):
+    """bf16 bits of values that MX-quantize losslessly (block amax on the grid top)."""
+    grid = omx._grid(fmt)
+    codes = rng.integers(0, len(grid), size=(rows, cols))
+    codes[:, ::32] = len(grid) - 1
+    E = rng.integers(-4, 4, size=(rows, cols // 32)).repeat(32, axis=1)
+    vals = grid[codes] * np.ldexp(1.0, E) * np.where(rng.random((rows, cols)) < 0.5, -1, 1)
+    return _bf16_bits(vals), vals
+
+
+@pytest.mark.parametrize("fmt", omx.FORMATS)
+def test_mx_grouped_gemm_lossless_equals_fp64(fmt):
+    # operands on the MX grid quantize exactly, so the block-scaled GEMM must equal the fp64 one
+    rng = np.random.default_rng(17)
+    G, N, K = 3, 64, 96
+    lens = np.array([40, 0, 57], dtype=np.int32)
+    M = int(lens.sum())
+    xb, X = _grid_operand(rng, fmt, M, K)
+    wb, W = _grid_operand(rng, fmt, G * N, K)
+    A, SA = omx.mx_quantize_rowwise(xb, fmt)
+    B, SB = omx.mx_quantize_rowwise(wb, fmt)
+    Y = omx.mx_grouped_gemm_fwd(fmt, A, SA, B, SB, lens, G)
+    np.testing.assert_array_equal(Y, og.grouped_gemm_fwd(X, W.reshape(G, N, K), lens))
+    # dgrad: dY [M, N] rowwise; W quantized along N, stored [K, G*N]
+    dyb, dY = _grid_operand(rng, fmt, M, N)
+    wtb, Wt = _grid_operand(rng, fmt, K, G * N)
+    Ad, SAd = omx.mx_quantize_rowwise(dyb, fmt)
+    Bt, SBt = omx.mx_quantize_rowwise(wtb, fmt)
+    dX = omx.mx_grouped_gemm_dgrad(fmt, Ad, SAd, Bt, SBt, lens, G)
+    np.testing.assert_array_equal(dX, og.grouped_gemm_dgrad(dY, Wt.T.reshape(G, N, K), lens))
+    # wgrad: column-wise (group-aligned) operands; lossless when each group block is on the grid
+    P = 128
+    M_pad = 3 * P
+    dyc_b, dYc = _colwise_grid(rng, fmt, lens, N)
+    xc_b, Xc = _colwise_grid(rng, fmt, lens, K)
+    At, SAt = omx.mx_quantize_colwise(dyc_b, lens, fmt, M_pad, P)
+    Bt2, SBt2 = omx.mx_quantize_colwise(xc_b, lens, fmt, M_pad, P)
+    dW = omx.mx_grouped_gemm_wgrad(fmt, At, SAt, Bt2, SBt2, lens, P)
+    np.testing.assert_array_equal(dW, og.grouped_gemm_wgrad(Xc, dYc, lens))
+
+
+def _colwise_grid(rng, fmt, lens, C):
+    grid = omx._grid(fmt)
+    parts_b, parts = [], []
+    for n in lens:
+        n = int(n)
+        if not n:
+            continue
+        codes = rng.integers(0, len(grid), size=(n, C))
+        codes[::32, :] = len(grid) - 1  # first row of each 32-row block holds the grid top
+        E = np.repeat(rng.integers(-4, 4, size=(-(-n // 32), C)), 32, axis=0)[:n]
+        v = grid[codes] * np.ldexp(1.0, E) * np.where(rng.random((n, C)) < 0.5, -1, 1)
+        parts.append(v)
+    vals = np.concatenate(parts, axis=0)
+    return _bf16_bits(vals), vals

@@ -1,0 +1,185 @@
+/*
+ * pgg.h -- C ABI of the GB300 (sm_103a) MoE expert grouped GEMM library.
+ *
+ * The operation (from "Enabling DeepSeek-V4-Flash Training on AMD Instinct
+ * MI355X GPUs with Primus", section "Expert parallelism: DeepEP and the grouped
+ * GEMM"): tokens are already sorted by expert; each local expert multiplies its
+ * own, different number of tokens by its own weights, and one kernel runs all
+ * of the experts' GEMMs over the ragged batch instead of a per-expert loop.
+ * The per-expert token counts ("m_splits" in "[Megatron-LM] feat: add grouped
+ * gemm fp4 support ... Pull Request #891", review comments) are produced by
+ * routing and bounded by the token count; here they are `group_lens`.
+ *
+ * Notation: G groups (experts), M = sum(group_lens) rows; group g owns rows
+ * [off_g, off_g + len_g) with off_0 = 0 and off_{g+1} = off_g + len_g.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers, row-major, densely packed, and
+ *    16-byte aligned; "bf16" means IEEE bfloat16 (2 bytes).
+ *  - group_lens is a device int32[G]; it is scanned on the device (no host
+ *    synchronisation).  1 <= G <= 1024.
+ *  - The caller owns and allocates every buffer; the library allocates
+ *    nothing and keeps no state beyond pgg_init's device properties.
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).
+ *  - Host-detectable problems (null pointer, bad size, misalignment, an
+ *    unsupported format or device) return a non-zero pgg_status and launch
+ *    nothing.
+ *  - Device-detectable problems (a negative group length, sum(group_lens) !=
+ *    M, a bounded wait that expired) write a code to *err (a device int32,
+ *    first error wins; may be NULL) and the kernel still terminates, writing
+ *    no output for bad group_lens.  Clear *err to 0 before the call.
+ *  - Results are deterministic: no atomics in any reduction.
+ */
+#ifndef PGG_H_
+#define PGG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PGG_OK = 0,
+  PGG_ERR_INVALID_ARG = 1,   /* null pointer, non-positive or too large size, bad enum */
+  PGG_ERR_UNSUPPORTED = 2,   /* device is not sm_103, or a shape the kernels do not cover */
+  PGG_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned, or a dimension off its multiple */
+  PGG_ERR_NOT_INITIALIZED = 4,
+  PGG_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  /* codes written to the device error word */
+  PGG_ERR_BAD_GROUP_LENS = 16, /* some len < 0, or sum(len) != M */
+  PGG_ERR_TIMEOUT = 17,        /* a bounded pipeline wait expired; output incomplete */
+  PGG_ERR_PAD_OVERFLOW = 18    /* column-wise MX: sum(round_up(len, 128)) > M_pad */
+} pgg_status;
+
+typedef enum { PGG_FMT_E4M3 = 1, PGG_FMT_E2M1 = 2 } pgg_mx_fmt;
+typedef enum { PGG_MODE_FWD = 0, PGG_MODE_DGRAD = 1, PGG_MODE_WGRAD = 2 } pgg_mode;
+typedef enum { PGG_EPI_NONE = 0, PGG_EPI_SWIGLU = 1 } pgg_epilogue;
+
+/* Padding granule of the column-wise MX layout (rows per group are rounded up to it). */
+#define PGG_MX_PAD 128
+
+/* Library ABI version (major*100 + minor). */
+int pgg_version(void);
+
+/* Select `device` and check that it is an sm_103 GPU (compute capability
+ * 10.3), caching its SM count.  Called implicitly by every entry point on the
+ * current device; calling it first surfaces PGG_ERR_UNSUPPORTED early.  The
+ * pages' counterpart is the hardware capability check made when the MXFP4
+ * recipe is entered (Pull Request #891, review comments). */
+int pgg_init(int device);
+
+/* Static string for a status code. */
+const char* pgg_status_string(int status);
+
+/* Copy the device error word to *host_out, synchronising `stream` first. */
+int pgg_read_error(const int32_t* err_dev, int32_t* host_out, void* stream);
+
+/* ---------------------------------------------------------------- BF16 */
+
+/* Forward: Y_g = X_g . W_g^T for every group.
+ *   X [M, K] bf16, W [G, N, K] bf16 (K contiguous), Y [M, N] bf16 (out).
+ *   fp32 accumulation in tensor memory, bf16 round-to-nearest-even output.
+ *   K >= 8, K % 8 == 0, N % 8 == 0.  M == 0 is a no-op. */
+int pgg_grouped_gemm_fwd(const void* X, const void* W, const int32_t* group_lens, void* Y,
+                         int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream);
+
+/* Dgrad: dX_g = dY_g . W_g (same grouping, weight used transposed; W is read
+ * in place, no transposed copy -- cf. the transposed-weight cache that Pull
+ * Request #891, "Changes", stops reusing).
+ *   dY [M, N] bf16, W [G, N, K] bf16, dX [M, K] bf16 (out).
+ *   N >= 8, N % 8 == 0, K % 8 == 0. */
+int pgg_grouped_gemm_dgrad(const void* dY, const void* W, const int32_t* group_lens, void* dX,
+                           int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream);
+
+/* Variable-K wgrad: dW_g = dY_g^T . X_g, reduced over group g's own len_g
+ * rows; a group with len_g == 0 gets dW_g = 0 (the backward emits dW1/dW2:
+ * "Enabling DeepSeek-V4-Flash ...", section "MegaMoE", backward order).
+ *   X [M, K] bf16, dY [M, N] bf16, dW [G, N, K] bf16 (out, fully written).
+ *   N % 8 == 0, K % 8 == 0. */
+int pgg_grouped_gemm_wgrad(const void* X, const void* dY, const int32_t* group_lens, void* dW,
+                           int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream);
+
+/* FC1 with SwiGLU folded into the epilogue ("Primus-Turbo" README, "What's
+ * New": fused GroupedMLP with SwiGLU folded into the grouped GEMM; weight
+ * layout w1 [g, 2I, H] "gate + up" from the MegaMoE section).
+ *   H_g = X_g . W1_g^T  [len_g, 2I];  A = silu(H[:, :I]) * H[:, I:]
+ *   X [M, K] bf16, W1 [G, 2I, K] bf16 (rows 0..I-1 gate, I..2I-1 up),
+ *   A [M, I] bf16 (out), H [M, 2I] bf16 (out, optional: NULL skips it; it is
+ *   the pre-activation the backward needs).  silu(x) = x / (1 + exp(-x)),
+ *   evaluated in fp32 from the fp32 accumulators.  I % 8 == 0, K % 8 == 0. */
+int pgg_grouped_fc1_swiglu(const void* X, const void* W1, const int32_t* group_lens, void* A,
+                           void* H, int64_t M, int64_t I, int64_t K, int G, int32_t* err,
+                           void* stream);
+
+/* FC2 dgrad with the SwiGLU backward in the epilogue:
+ *   dA_g = dY_g . W2_g  [len_g, I];  with g = H[:, :I], u = H[:, I:], s = sigmoid(g):
+ *   dH[:, :I] = dA * u * s * (1 + g * (1 - s)),  dH[:, I:] = dA * g * s
+ *   dY [M, Hd] bf16, W2 [G, Hd, I] bf16, H [M, 2I] bf16 (saved by FC1),
+ *   dH [M, 2I] bf16 (out).  Hd % 8 == 0, I % 8 == 0. */
+int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void* H,
+                                     const int32_t* group_lens, void* dH, int64_t M, int64_t Hd,
+                                     int64_t I, int G, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------- MX (microscaling) */
+
+/* Row-wise MX quantization: one E8M0 scale per block of 32 consecutive
+ * elements along C ("Primus-Turbo" README: MXFP8 / MXFP4 grouped GEMM; Pull
+ * Request #891, "Changes": MXFP4 weights built as float4_e2m1fn_x2 buffers).
+ * Rule (OCP Microscaling v1.0): E = clamp(floor(log2(amax)) - emax, -127, 127)
+ * with emax 8 (e4m3) or 2 (e2m1), scale code E + 127, element code =
+ * round-to-nearest-even(v * 2^-E) saturated to +-448 / +-6, sign of zero kept;
+ * a block with a NaN or Inf gets scale 0xFF and zero codes.
+ *   in [R, C] bf16; C % 32 == 0 (e4m3) or C % 64 == 0 (e2m1).
+ *   codes [R, C] u8 (e4m3) or [R, C/2] u8 (e2m1: element 2j in the low
+ *   nibble of byte j); scales [R, C/32] u8. */
+int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                            uint8_t* scales, void* stream);
+
+/* Group-aware column-wise MX quantization (the wgrad operands, quantized
+ * along the token axis).  Blocks of 32 rows run inside one group, starting at
+ * the group's first row; group g is stored transposed in columns
+ * [P_g, P_g + round_up(len_g, 32)) of the output, where P_g is the exclusive
+ * prefix sum of round_up(len_h, PGG_MX_PAD).  Tail positions and everything
+ * past the last group up to M_pad hold code 0 and scale 0.
+ *   in [M, C] bf16; group_lens may be NULL for one group of M rows.
+ *   codes_t [C, M_pad] u8 (e4m3) or [C, M_pad/2] (e2m1); scales_t [C, M_pad/32].
+ *   M_pad % PGG_MX_PAD == 0 and M_pad >= sum(round_up(len_g, PGG_MX_PAD))
+ *   (else *err = PGG_ERR_PAD_OVERFLOW and nothing is written);
+ *   M + G * (PGG_MX_PAD - 1) rounded up to PGG_MX_PAD always suffices. */
+int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens,
+                            int G, int fmt, uint8_t* codes_t, uint8_t* scales_t, int64_t M_pad,
+                            int32_t* err, void* stream);
+
+/* Block-scaled grouped GEMM on MX operands (both operands in `fmt`, scales
+ * applied per 32-element block of the reduction axis, fp32 accumulation,
+ * bf16 output):
+ *   PGG_MODE_FWD:   out[M, N] = deq(A)_g . deq(B)_g^T
+ *                   A [M, K] row-wise codes, SA [M, K/32];
+ *                   B [G*N, K] row-wise codes (W), SB [G*N, K/32].
+ *                   epilogue PGG_EPI_SWIGLU: N = 2I, out = A_act [M, I],
+ *                   out2 = H [M, 2I] or NULL (as pgg_grouped_fc1_swiglu).
+ *   PGG_MODE_DGRAD: out[M, K] = deq(A)_g . W_g with A = dY [M, N] row-wise
+ *                   codes (blocks along N), SA [M, N/32]; B = W quantized
+ *                   along N and stored transposed, [K, G*N] codes, SB
+ *                   [K, G*N/32] (pgg_mx_quantize_colwise of W viewed as
+ *                   [G*N, K] with G groups of N rows produces exactly this).
+ *                   epilogue PGG_EPI_SWIGLU: the SwiGLU backward with the
+ *                   saved bf16 H [M, 2K]; out = dH [M, 2K].
+ *   PGG_MODE_WGRAD: out[G, N, K] = sum over group g's padded columns of
+ *                   deq(A)[:, r] deq(B)[:, r]^T with A = dY column-wise
+ *                   codes [N, M_pad], B = X column-wise codes [K, M_pad]
+ *                   (pgg_mx_quantize_colwise); empty groups give 0.
+ * Sizes: the reduction axis is a multiple of 128 (fwd K, dgrad N); N, K
+ * multiples of 32 elsewhere; e2m1 codes are packed two per byte. */
+int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const uint8_t* SA,
+                        const uint8_t* B, const uint8_t* SB, const void* H,
+                        const int32_t* group_lens, void* out, void* out2, int64_t M, int64_t N,
+                        int64_t K, int G, int64_t M_pad, int32_t* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PGG_H_ */

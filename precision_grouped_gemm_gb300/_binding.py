@@ -1,0 +1,231 @@
+"""ctypes binding of libpgg.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+PAD = 128
+FMT_E4M3, FMT_E2M1 = 1, 2
+MODE_FWD, MODE_DGRAD, MODE_WGRAD = 0, 1, 2
+EPI_NONE, EPI_SWIGLU = 0, 1
+_FMT = {"e4m3": FMT_E4M3, "e2m1": FMT_E2M1, FMT_E4M3: FMT_E4M3, FMT_E2M1: FMT_E2M1}
+
+_P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+
+# name -> argument types (all return int status)
+SIGNATURES = {
+    "pgg_version": [],
+    "pgg_init": [_I32],
+    "pgg_read_error": [_P, _P, _P],
+    "pgg_grouped_gemm_fwd": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_grouped_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_grouped_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_grouped_fc1_swiglu": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_grouped_fc2_dgrad_swiglu_bwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_mx_quantize_rowwise": [_P, _I64, _I64, _I32, _P, _P, _P],
+    "pgg_mx_quantize_colwise": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P],
+    "pgg_mx_grouped_gemm": [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
+                            _I32, _I64, _P, _P],
+}
+
+
+class PggError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().pgg_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{where}: pgg status {status} ({msg})")
+        self.status = status
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libpgg.so")
+
+
+def lib():
+    """Load libpgg.so (raises if it has not been built: there is no fallback)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with precision_grouped_gemm_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        for name, args in SIGNATURES.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.pgg_status_string.argtypes = [ctypes.c_int]
+        L.pgg_status_string.restype = ctypes.c_char_p
+        _LIB = L
+    return _LIB
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise PggError(st, where)
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("tensors must live on the CUDA device")
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+
+
+def _lens(group_lens):
+    if group_lens.dtype != torch.int32:
+        raise ValueError("group_lens must be int32")
+    return group_lens
+
+
+def version() -> int:
+    return lib().pgg_version()
+
+
+def init(device: int = 0):
+    _check(lib().pgg_init(device), "pgg_init")
+
+
+def read_error(err, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _check(lib().pgg_read_error(_ptr(err), ctypes.byref(out), _stream(stream)), "pgg_read_error")
+    return out.value
+
+
+def grouped_gemm_fwd(X, W, group_lens, Y=None, err=None, stream=None):
+    """Y_g = X_g . W_g^T; X [M,K] bf16, W [G,N,K] bf16 -> Y [M,N] bf16."""
+    M, K = X.shape
+    G, N, _ = W.shape
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.bfloat16, device=X.device)
+    _dev(X, W, group_lens, Y, err)
+    _check(lib().pgg_grouped_gemm_fwd(_ptr(X), _ptr(W), _ptr(_lens(group_lens)), _ptr(Y), M, N, K, G,
+                                      _ptr(err), _stream(stream)), "pgg_grouped_gemm_fwd")
+    return Y
+
+
+def grouped_gemm_dgrad(dY, W, group_lens, dX=None, err=None, stream=None):
+    """dX_g = dY_g . W_g; dY [M,N] bf16, W [G,N,K] bf16 -> dX [M,K] bf16."""
+    M, N = dY.shape
+    G, _, K = W.shape
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device)
+    _dev(dY, W, group_lens, dX, err)
+    _check(lib().pgg_grouped_gemm_dgrad(_ptr(dY), _ptr(W), _ptr(_lens(group_lens)), _ptr(dX), M, N, K,
+                                        G, _ptr(err), _stream(stream)), "pgg_grouped_gemm_dgrad")
+    return dX
+
+
+def grouped_gemm_wgrad(X, dY, group_lens, dW=None, err=None, stream=None):
+    """dW_g = dY_g^T . X_g; X [M,K], dY [M,N] bf16 -> dW [G,N,K] bf16 (0 for empty groups)."""
+    M, K = X.shape
+    N = dY.shape[1]
+    G = group_lens.numel()
+    if dW is None:
+        dW = torch.empty((G, N, K), dtype=torch.bfloat16, device=X.device)
+    _dev(X, dY, group_lens, dW, err)
+    _check(lib().pgg_grouped_gemm_wgrad(_ptr(X), _ptr(dY), _ptr(_lens(group_lens)), _ptr(dW), M, N, K,
+                                        G, _ptr(err), _stream(stream)), "pgg_grouped_gemm_wgrad")
+    return dW
+
+
+def grouped_fc1_swiglu(X, W1, group_lens, A=None, H=None, save_h=True, err=None, stream=None):
+    """FC1 + SwiGLU: W1 [G,2I,K] (gate | up) -> A [M,I] and (optionally) H [M,2I]."""
+    M, K = X.shape
+    G, I2, _ = W1.shape
+    I = I2 // 2
+    if A is None:
+        A = torch.empty((M, I), dtype=torch.bfloat16, device=X.device)
+    if H is None and save_h:
+        H = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=X.device)
+    _dev(X, W1, group_lens, A, H, err)
+    _check(lib().pgg_grouped_fc1_swiglu(_ptr(X), _ptr(W1), _ptr(_lens(group_lens)), _ptr(A), _ptr(H),
+                                        M, I, K, G, _ptr(err), _stream(stream)), "pgg_grouped_fc1_swiglu")
+    return A, H
+
+
+def grouped_fc2_dgrad_swiglu_bwd(dY, W2, H, group_lens, dH=None, err=None, stream=None):
+    """dA = dY . W2_g (W2 [G,Hd,I]); dH [M,2I] = SwiGLU backward of dA at the saved H."""
+    M, Hd = dY.shape
+    G, _, I = W2.shape
+    if dH is None:
+        dH = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=dY.device)
+    _dev(dY, W2, H, group_lens, dH, err)
+    _check(lib().pgg_grouped_fc2_dgrad_swiglu_bwd(_ptr(dY), _ptr(W2), _ptr(H), _ptr(_lens(group_lens)),
+                                                  _ptr(dH), M, Hd, I, G, _ptr(err), _stream(stream)),
+           "pgg_grouped_fc2_dgrad_swiglu_bwd")
+    return dH
+
+
+def mx_quantize_rowwise(x, fmt, codes=None, scales=None, stream=None):
+    """bf16 [R,C] -> (codes [R,C] or [R,C/2] u8, scales [R,C/32] u8), blocks along C."""
+    R, C = x.shape
+    f = _FMT[fmt]
+    if codes is None:
+        codes = torch.empty((R, C if f == FMT_E4M3 else C // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((R, C // 32), dtype=torch.uint8, device=x.device)
+    _dev(x, codes, scales)
+    _check(lib().pgg_mx_quantize_rowwise(_ptr(x), R, C, f, _ptr(codes), _ptr(scales), _stream(stream)),
+           "pgg_mx_quantize_rowwise")
+    return codes, scales
+
+
+def mx_pad_rows(M: int, G: int) -> int:
+    """An M_pad that always holds sum(round_up(len_g, PAD)) for any split of M rows in G groups."""
+    return -(-(M + G * (PAD - 1)) // PAD) * PAD
+
+
+def mx_quantize_colwise(x, group_lens, fmt, M_pad=None, codes_t=None, scales_t=None, err=None,
+                        stream=None):
+    """bf16 [M,C] + group_lens -> transposed (codes_t [C,M_pad] or [C,M_pad/2], scales_t [C,M_pad/32])."""
+    M, C = x.shape
+    f = _FMT[fmt]
+    G = 1 if group_lens is None else group_lens.numel()
+    if M_pad is None:
+        M_pad = mx_pad_rows(M, G)
+    if codes_t is None:
+        codes_t = torch.empty((C, M_pad if f == FMT_E4M3 else M_pad // 2), dtype=torch.uint8, device=x.device)
+    if scales_t is None:
+        scales_t = torch.empty((C, M_pad // 32), dtype=torch.uint8, device=x.device)
+    _dev(x, group_lens, codes_t, scales_t, err)
+    lens = None if group_lens is None else _lens(group_lens)
+    _check(lib().pgg_mx_quantize_colwise(_ptr(x), M, C, _ptr(lens), G, f, _ptr(codes_t), _ptr(scales_t),
+                                         M_pad, _ptr(err), _stream(stream)), "pgg_mx_quantize_colwise")
+    return codes_t, scales_t
+
+
+def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2=None, H=None,
+                    epilogue=EPI_NONE, M_pad=0, err=None, stream=None):
+    """Block-scaled grouped GEMM on MX operands (see pgg.h for the per-mode layouts)."""
+    f = _FMT[fmt]
+    G = group_lens.numel()
+    dev = A.device
+    if out is None:
+        if mode == MODE_FWD:
+            shape = (M, N // 2) if epilogue == EPI_SWIGLU else (M, N)
+        elif mode == MODE_DGRAD:
+            shape = (M, 2 * K) if epilogue == EPI_SWIGLU else (M, K)
+        else:
+            shape = (G, N, K)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    _dev(A, SA, B, SB, group_lens, out, out2, H, err)
+    _check(lib().pgg_mx_grouped_gemm(mode, f, epilogue, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(H),
+                                     _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), M, N, K, G, M_pad,
+                                     _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
+    return out

@@ -1,0 +1,95 @@
+// Host launchers of the BF16 grouped GEMM family (see gemm_bf16.cuh).
+#include <algorithm>
+
+#include "gemm_bf16.cuh"
+#include "internal.h"
+
+namespace pgg {
+namespace {
+
+constexpr int kBN = 256;
+constexpr int kStages = 4;
+
+template <int MODE, int EPI>
+int run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int grid,
+        cudaStream_t s) {
+  using L = GemmSmem<kBN, kStages>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, kStages>;
+  const size_t smem = L::bytes(args.G);
+  static bool attr_done = false;  // per instantiation; the attribute is per device function
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L::bytes(kMaxGroups));
+    if (e != cudaSuccess) return cuda_status(e);
+    attr_done = true;
+  }
+  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, args);
+  return cuda_status(cudaGetLastError());
+}
+
+int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+
+int launch_bf16(const Bf16Call& c) {
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  const uint32_t sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUtensorMap ta, tb;
+  GemmArgs a{};
+  a.group_lens = c.group_lens;
+  a.G = c.G;
+  a.M = c.M;
+  a.out = c.out;
+  a.out2 = c.out2;
+  a.aux = c.aux;
+  a.err = c.err;
+  a.I = (int)c.I;
+  int tiles_ub = 0;
+
+  if (c.mode == 0) {  // forward (optionally FC1 + SwiGLU): B = W [G, Nw, K]
+    const int64_t Nw = c.epi == 1 ? 2 * c.I : c.N;
+    uint64_t da[2] = {(uint64_t)c.K, (uint64_t)c.M}, sa[1] = {(uint64_t)c.K * 2};
+    uint32_t ba[2] = {64, 128};
+    uint64_t db[3] = {(uint64_t)c.K, (uint64_t)Nw, (uint64_t)c.G};
+    uint64_t sb[2] = {(uint64_t)c.K * 2, (uint64_t)(Nw * c.K * 2)};
+    uint32_t bb[3] = {64, c.epi == 1 ? (uint32_t)(kBN / 2) : (uint32_t)kBN, 1};
+    if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, ba, (CUtensorMapSwizzle)sw))) return st;
+    if ((st = encode_tmap(&tb, bf, 3, c.b, db, sb, bb, (CUtensorMapSwizzle)sw))) return st;
+    a.out_cols = (int)(c.epi == 1 ? c.I : c.N);
+    a.red = (int)c.K;
+    const int tcw = c.epi == 1 ? kBN / 2 : kBN;
+    tiles_ub = (ceil_div(c.M, kBM) + c.G) * ceil_div(a.out_cols, tcw);
+  } else if (c.mode == 1) {  // dgrad (optionally FC2 dgrad + SwiGLU bwd): A = dY [M, N]
+    uint64_t da[2] = {(uint64_t)c.N, (uint64_t)c.M}, sa[1] = {(uint64_t)c.N * 2};
+    uint32_t ba[2] = {64, 128};
+    uint64_t db[3] = {(uint64_t)c.K, (uint64_t)c.N, (uint64_t)c.G};
+    uint64_t sb[2] = {(uint64_t)c.K * 2, (uint64_t)(c.N * c.K * 2)};
+    uint32_t bb[3] = {64, 64, 1};
+    if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, ba, (CUtensorMapSwizzle)sw))) return st;
+    if ((st = encode_tmap(&tb, bf, 3, c.b, db, sb, bb, (CUtensorMapSwizzle)sw))) return st;
+    a.out_cols = (int)c.K;
+    a.red = (int)c.N;
+    tiles_ub = (ceil_div(c.M, kBM) + c.G) * ceil_div(c.K, kBN);
+  } else {  // wgrad: A = dY [M, N] MN-major, B = X [M, K] MN-major
+    uint64_t da[2] = {(uint64_t)c.N, (uint64_t)c.M}, sa[1] = {(uint64_t)c.N * 2};
+    uint64_t db[2] = {(uint64_t)c.K, (uint64_t)c.M}, sb[1] = {(uint64_t)c.K * 2};
+    uint32_t bx[2] = {64, (uint32_t)kBK};
+    if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, bx, (CUtensorMapSwizzle)sw))) return st;
+    if ((st = encode_tmap(&tb, bf, 2, c.b, db, sb, bx, (CUtensorMapSwizzle)sw))) return st;
+    a.out_cols = (int)c.K;
+    a.wg_rows = (int)c.N;
+    tiles_ub = c.G * ceil_div(c.N, kBM) * ceil_div(c.K, kBN);
+  }
+  const int grid = std::max(1, std::min(dev.sms, tiles_ub));
+  if (c.mode == 0 && c.epi == 0) return run<kFwd, kEpiStore>(ta, tb, a, grid, c.stream);
+  if (c.mode == 0 && c.epi == 1) return run<kFwd, kEpiSwiGLU>(ta, tb, a, grid, c.stream);
+  if (c.mode == 1 && c.epi == 0) return run<kDgrad, kEpiStore>(ta, tb, a, grid, c.stream);
+  if (c.mode == 1 && c.epi == 2) return run<kDgrad, kEpiSwiGLUBwd>(ta, tb, a, grid, c.stream);
+  if (c.mode == 2 && c.epi == 0) return run<kWgrad, kEpiStore>(ta, tb, a, grid, c.stream);
+  return PGG_ERR_INVALID_ARG;
+}
+
+}  // namespace pgg

@@ -1,0 +1,454 @@
+// BF16 grouped GEMM on the 5th-generation tensor cores (tcgen05, kind::f16).
+//
+// Problem ("Enabling DeepSeek-V4-Flash Training on AMD Instinct MI355X GPUs
+// with Primus", section "Expert parallelism: DeepEP and the grouped GEMM"):
+// one kernel runs every expert's GEMM over a ragged, expert-sorted token
+// batch.  Three operand arrangements share this kernel:
+//
+//   kFwd   Y_g  = X_g  . W_g^T   A = X  [M,K] K-major,   B = W [G,N,K] K-major
+//   kDgrad dX_g = dY_g . W_g     A = dY [M,N] K-major,   B = W [G,N,K] read MN-major
+//   kWgrad dW_g = dY_g^T . X_g   A = dY [M,N] MN-major,  B = X [M,K] MN-major,
+//                                reduction over group g's own rows (variable K)
+//
+// and three epilogues: plain bf16 store, the FC1 SwiGLU (A = silu(gate)*up with
+// the optional pre-activation H saved), and the FC2-dgrad SwiGLU backward (dH
+// from dA and the saved H) -- the expert path GEMM1 -> SwiGLU -> GEMM2 of the
+// same page, section "MegaMoE: fusing communication into the grouped GEMM".
+//
+// CTA = 6 warps: warp 0 issues TMA loads into a STAGES-deep shared-memory ring,
+// warp 1 owns TMEM and issues tcgen05.mma from one lane, warps 2..5 drain the
+// double-buffered fp32 accumulator (2 x BN TMEM columns) with tcgen05.ld and
+// store bf16 results bounded to the tile's group.  Persistent: one CTA per SM.
+#pragma once
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace pgg {
+
+enum GemmMode : int { kFwd = 0, kDgrad = 1, kWgrad = 2 };
+enum GemmEpi : int { kEpiStore = 0, kEpiSwiGLU = 1, kEpiSwiGLUBwd = 2 };
+
+constexpr int kBM = 128;          // MMA M (TMEM lanes)
+constexpr int kBK = 64;           // reduction step per stage: one 128-byte swizzle atom of bf16
+constexpr int kGemmThreads = 192;
+constexpr int kErrBadGroupLens = 16;
+constexpr int kErrTimeout = 17;
+
+struct GemmArgs {
+  const int32_t* group_lens;
+  int G;
+  int64_t M;        // rows of the ragged operand (sum of group_lens)
+  int out_cols;     // columns of the accumulator space: fwd N, dgrad K, wgrad K, swiglu I
+  int red;          // reduction length for fwd / dgrad (K resp. N)
+  int wg_rows;      // wgrad: N (rows of dW_g)
+  int I;            // SwiGLU width (gate/up halves)
+  void* out;        // Y, dX, dW, A or dH (bf16)
+  void* out2;       // SwiGLU forward: H (bf16 [M, 2I]) or nullptr
+  const void* aux;  // SwiGLU backward: saved H (bf16 [M, 2I])
+  int32_t* err;     // device error word or nullptr
+};
+
+template <int BN, int STAGES>
+struct GemmSmem {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kGroupOff = kBarOff + kBarBytes;
+  static __host__ __device__ constexpr size_t bytes(int G) {
+    return 1024 + (size_t)kGroupOff + 8 * (size_t)(G + 1) + 16;
+  }
+};
+
+struct Tile {
+  int g, row0, rows, col0, nkb, red0, red_valid;
+};
+
+template <int MODE, int EPI, int BN>
+__device__ __forceinline__ int tile_cols() {
+  return EPI == kEpiSwiGLU ? BN / 2 : BN;
+}
+
+template <int MODE, int EPI, int BN>
+__device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int32_t* s_off,
+                                            const int32_t* s_tile) {
+  Tile T;
+  const int ncol = (a.out_cols + tile_cols<MODE, EPI, BN>() - 1) / tile_cols<MODE, EPI, BN>();
+  const int g = find_group(s_tile, a.G, t);
+  const int local = t - s_tile[g];
+  const int off = s_off[g], len = s_off[g + 1] - s_off[g];
+  T.g = g;
+  if (MODE == kWgrad) {
+    const int nrt = (a.wg_rows + kBM - 1) / kBM;
+    const int rt = local % nrt, ct = local / nrt;
+    T.row0 = rt * kBM;
+    T.rows = min(kBM, a.wg_rows - T.row0);
+    T.col0 = ct * BN;
+    T.nkb = (len + kBK - 1) / kBK;
+    T.red0 = off;
+    T.red_valid = len;
+  } else {
+    const int nmt = (len + kBM - 1) / kBM;
+    const int mt = local % nmt, ct = local / nmt;
+    (void)ncol;
+    T.row0 = off + mt * kBM;
+    T.rows = min(kBM, len - mt * kBM);
+    T.col0 = ct * tile_cols<MODE, EPI, BN>();
+    T.nkb = (a.red + kBK - 1) / kBK;
+    T.red0 = 0;
+    T.red_valid = a.red;
+  }
+  return T;
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+// Store 32 consecutive fp32 values of one row as bf16 at dst[0..31], columns
+// limited to ncols (<= 32).  16-byte vector stores when the chunk is whole.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v, int ncols) {
+  if (ncols >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      d4[q] = w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) dst[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v, int ncols) {
+  if (ncols >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w = __ldg(s4 + q);
+      v[q * 8 + 0] = bf16_lo(w.x); v[q * 8 + 1] = bf16_hi(w.x);
+      v[q * 8 + 2] = bf16_lo(w.y); v[q * 8 + 3] = bf16_hi(w.y);
+      v[q * 8 + 4] = bf16_lo(w.z); v[q * 8 + 5] = bf16_hi(w.z);
+      v[q * 8 + 6] = bf16_lo(w.w); v[q * 8 + 7] = bf16_hi(w.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < ncols ? __bfloat162float(src[j]) : 0.0f;
+  }
+}
+
+template <int MODE, int EPI, int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
+                             const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
+  using L = GemmSmem<BN, STAGES>;
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
+  static_assert(EPI != kEpiSwiGLU || (MODE == kFwd && BN == 256), "SwiGLU fwd tile");
+  static_assert(EPI != kEpiSwiGLUBwd || MODE == kDgrad, "SwiGLU bwd tile");
+  constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
+  constexpr bool kAmn = (MODE == kWgrad);
+  constexpr bool kBmn = (MODE != kFwd);
+  constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* full = bars;                 // [STAGES]
+  uint64_t* empty = bars + STAGES;       // [STAGES]
+  uint64_t* tfull = bars + 2 * STAGES;   // [2]
+  uint64_t* tempty = tfull + 2;          // [2]
+  uint64_t* drain = tempty + 2;          // [1]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
+  int32_t* s_tile = s_off + (args.G + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    TileCount tc;
+    if (MODE == kWgrad) {
+      tc.bm = 0;
+      tc.per_row_tile = ((args.wg_rows + kBM - 1) / kBM) * ((args.out_cols + BN - 1) / BN);
+    } else {
+      constexpr int tcw = EPI == kEpiSwiGLU ? BN / 2 : BN;
+      tc.bm = kBM;
+      tc.per_row_tile = (args.out_cols + tcw - 1) / tcw;
+    }
+    bool bad = scan_groups(args.group_lens, args.G, args.M, tc, s_off, s_tile, nullptr, 0, lane);
+    if (lane == 0) {
+      *s_bad = bad ? 1 : 0;
+      if (bad && blockIdx.x == 0) set_error(args.err, kErrBadGroupLens);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *s_tmem;
+  const int total_tiles = *s_bad ? 0 : s_tile[args.G];
+  const uint32_t smem_a0 = smem_u32(smem);
+  const uint32_t smem_b0 = smem_a0 + STAGES * L::kABytes;
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
+      for (int kb = 0; kb < T.nkb; ++kb) {
+        if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
+        if (lane == 0) {
+          const uint32_t fb = smem_u32(&full[stage]);
+          const uint32_t sa = smem_a0 + stage * L::kABytes;
+          const uint32_t sb = smem_b0 + stage * L::kBBytes;
+          mbar_arrive_expect_tx(fb, L::kStageBytes);
+          const int kr = kb * kBK;
+          if (MODE == kFwd) {
+            tma_load_2d(sa, &tmA, fb, kr, T.row0);
+            if (EPI == kEpiSwiGLU) {
+              tma_load_3d(sb, &tmB, fb, kr, T.col0, T.g);
+              tma_load_3d(sb + (BN / 2) * 128, &tmB, fb, kr, args.I + T.col0, T.g);
+            } else {
+              tma_load_3d(sb, &tmB, fb, kr, T.col0, T.g);
+            }
+          } else if (MODE == kDgrad) {
+            tma_load_2d(sa, &tmA, fb, kr, T.row0);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, kr, T.g);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kBK * 128, &tmA, fb, T.row0 + 64 * j, T.red0 + kr);
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, T.red0 + kr);
+          }
+        }
+        __syncwarp();
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (aborted && lane == 0) {
+      // drain: wait for the loads still in flight before the CTA's smem goes away
+      long long n = issued < STAGES ? issued : STAGES;
+      int s = stage;
+      uint32_t p = phase;
+      for (long long i = 0; i < n; ++i) {
+        if (--s < 0) { s = STAGES - 1; p ^= 1u; }
+        mbar_wait(smem_u32(&full[s]), p, nullptr, kDrainTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
+      if (T.nkb == 0) continue;  // empty wgrad group: the epilogue writes zeros
+      if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * BN;
+      for (int kb = 0; kb < T.nkb; ++kb) {
+        if (!warp_wait(smem_u32(&full[stage]), phase, s_abort)) { aborted = true; break; }
+        tc_fence_after();
+        const uint32_t sa = smem_a0 + stage * L::kABytes;
+        const uint32_t sb = smem_b0 + stage * L::kBBytes;
+        if (MODE == kWgrad) {
+          // variable-K tail: rows of this k-block past the group's end belong to
+          // the next group (or lie past M); zero them in both operands
+          const int valid = T.red_valid - kb * kBK;
+          if (valid < kBK) {
+            const int nz = kBK - valid;
+            uint4 z = make_uint4(0, 0, 0, 0);
+            uint8_t* pa = smem + (sa - smem_a0);
+            uint8_t* pb = smem + (sb - smem_a0);
+            // each atom column is [kBK rows][128 B]; zero rows valid..kBK-1
+            for (int i = lane; i < nz * 8 * (kBM / 64); i += 32) {
+              int atom = i / (nz * 8), rem = i % (nz * 8);
+              int row = valid + rem / 8, c16 = rem % 8;
+              *reinterpret_cast<uint4*>(pa + atom * kBK * 128 + row * 128 + c16 * 16) = z;
+            }
+            for (int i = lane; i < nz * 8 * (BN / 64); i += 32) {
+              int atom = i / (nz * 8), rem = i % (nz * 8);
+              int row = valid + rem / 8, c16 = rem % 8;
+              *reinterpret_cast<uint4*>(pb + atom * kBK * 128 + row * 128 + c16 * 16) = z;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            uint64_t ad, bd;
+            if (kAmn) ad = smem_desc(sa + ks * 2048, kBK * 128, 1024, kSwizzle128B);
+            else ad = smem_desc(sa + ks * 32, 16, 1024, kSwizzle128B);
+            if (kBmn) bd = smem_desc(sb + ks * 2048, kBK * 128, 1024, kSwizzle128B);
+            else bd = smem_desc(sb + ks * 32, 16, 1024, kSwizzle128B);
+            mma_f16(d_tmem, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&empty[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (aborted) break;
+      if (lane == 0) mma_commit(smem_u32(&tfull[acc]));
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (aborted && lane == 0) {
+      mma_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0, nullptr, kDrainTimeoutNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;         // accumulator row held by this thread
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
+      const bool row_ok = r < T.rows;
+      if (MODE == kWgrad && T.nkb == 0) {
+        if (row_ok) {
+          float zero[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) zero[j] = 0.0f;
+          __nv_bfloat16* dst = out + ((size_t)T.g * args.wg_rows + T.row0 + r) * args.out_cols;
+          for (int c = 0; c < BN / 32; ++c) {
+            const int c0 = T.col0 + c * 32;
+            if (c0 < args.out_cols) store_row32(dst + c0, zero, min(32, args.out_cols - c0));
+          }
+        }
+        continue;
+      }
+      if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+      if (EPI == kEpiSwiGLU) {
+        const int I = args.I;
+        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out2);
+        const size_t grow = (size_t)T.row0 + r;
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          uint32_t rg[32], ru[32];
+          tmem_ld32(tb + c * 32, rg);
+          tmem_ld32(tb + BN / 2 + c * 32, ru);
+          tmem_ld_wait();
+          const int c0 = T.col0 + c * 32;
+          if (row_ok && c0 < I) {
+            float g[32], u[32], a[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              g[j] = __uint_as_float(rg[j]);
+              u[j] = __uint_as_float(ru[j]);
+              a[j] = silu_f(g[j]) * u[j];
+            }
+            const int nc = min(32, I - c0);
+            store_row32(out + grow * I + c0, a, nc);
+            if (H) {
+              store_row32(H + grow * (2 * (size_t)I) + c0, g, nc);
+              store_row32(H + grow * (2 * (size_t)I) + I + c0, u, nc);
+            }
+          }
+        }
+      } else if (EPI == kEpiSwiGLUBwd) {
+        const int I = args.I;
+        const __nv_bfloat16* H = reinterpret_cast<const __nv_bfloat16*>(args.aux);
+        const size_t grow = (size_t)T.row0 + r;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t rd[32];
+          tmem_ld32(tb + c * 32, rd);
+          tmem_ld_wait();
+          const int c0 = T.col0 + c * 32;
+          if (row_ok && c0 < I) {
+            const int nc = min(32, I - c0);
+            float hg[32], hu[32], dg[32], du[32];
+            load_row32(H + grow * (2 * (size_t)I) + c0, hg, nc);
+            load_row32(H + grow * (2 * (size_t)I) + I + c0, hu, nc);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float da = __uint_as_float(rd[j]);
+              const float s = 1.0f / (1.0f + __expf(-hg[j]));
+              dg[j] = da * hu[j] * s * (1.0f + hg[j] * (1.0f - s));
+              du[j] = da * hg[j] * s;
+            }
+            store_row32(out + grow * (2 * (size_t)I) + c0, dg, nc);
+            store_row32(out + grow * (2 * (size_t)I) + I + c0, du, nc);
+          }
+        }
+      } else {
+        __nv_bfloat16* dst;
+        if (MODE == kWgrad) dst = out + ((size_t)T.g * args.wg_rows + T.row0 + r) * args.out_cols;
+        else dst = out + ((size_t)T.row0 + r) * args.out_cols;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t rv[32];
+          tmem_ld32(tb + c * 32, rv);
+          tmem_ld_wait();
+          const int c0 = T.col0 + c * 32;
+          if (row_ok && c0 < args.out_cols) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rv[j]);
+            store_row32(dst + c0, v, min(32, args.out_cols - c0));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[acc]));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  if (aborted && lane == 0) set_error(args.err, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace pgg

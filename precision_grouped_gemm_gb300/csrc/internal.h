@@ -1,0 +1,70 @@
+// Internal host-side declarations shared by the library's translation units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pgg.h"
+
+namespace pgg {
+
+struct DeviceInfo {
+  int device = -1;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  size_t smem_optin = 0;
+};
+
+// Returns PGG_OK and fills `info` for the current device (initialising it on first use).
+int current_device(DeviceInfo* info);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+// dims/strides in elements/bytes as the driver expects; rank 2 or 3.
+int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                CUtensorMapSwizzle swizzle);
+
+int cuda_status(cudaError_t e);
+
+// BF16 grouped GEMM family (gemm_bf16.cu)
+struct Bf16Call {
+  int mode;      // 0 fwd, 1 dgrad, 2 wgrad
+  int epi;       // 0 store, 1 swiglu fwd, 2 swiglu bwd
+  const void* a; // fwd: X; dgrad: dY; wgrad: dY
+  const void* b; // fwd/dgrad: W; wgrad: X
+  const int32_t* group_lens;
+  void* out;
+  void* out2;
+  const void* aux;
+  int64_t M, N, K;  // fwd: Y[M,N]=X[M,K]W^T; dgrad: dX[M,K]=dY[M,N]W; wgrad: dW[G,N,K]
+  int64_t I;        // SwiGLU width
+  int G;
+  int32_t* err;
+  cudaStream_t stream;
+};
+int launch_bf16(const Bf16Call& c);
+
+// MX quantize (mx_quant.cu)
+int launch_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t s);
+int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens,
+                               int G, int fmt, uint8_t* codes_t, uint8_t* scales_t,
+                               int64_t M_pad, int32_t* err, cudaStream_t s);
+
+// Block-scaled grouped GEMM (gemm_mx.cu)
+struct MxCall {
+  int mode, fmt, epi;
+  const uint8_t *A, *SA, *B, *SB;
+  const void* H;
+  const int32_t* group_lens;
+  void* out;
+  void* out2;
+  int64_t M, N, K, M_pad;
+  int G;
+  int32_t* err;
+  cudaStream_t stream;
+};
+int launch_mx_gemm(const MxCall& c);
+
+}  // namespace pgg

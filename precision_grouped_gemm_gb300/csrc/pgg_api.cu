@@ -1,0 +1,249 @@
+// C ABI of the library: argument validation, device checks, tensor-map
+// encoding and dispatch to the kernel launchers.  No entry point allocates
+// memory or synchronises (except pgg_read_error, which exists to synchronise).
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "sched.cuh"
+
+namespace pgg {
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? PGG_OK : PGG_ERR_CUDA; }
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+int init_device(int device) {
+  if (device < 0 || device >= kMaxDevices) return PGG_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[device];
+  if (d.device == device) return PGG_OK;
+  cudaDeviceProp p;
+  if (cudaGetDeviceProperties(&p, device) != cudaSuccess) return PGG_ERR_CUDA;
+  if (!(p.major == 10 && p.minor == 3)) return PGG_ERR_UNSUPPORTED;
+  d.sms = p.multiProcessorCount;
+  d.cc_major = p.major;
+  d.cc_minor = p.minor;
+  d.smem_optin = p.sharedMemPerBlockOptin;
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return PGG_ERR_CUDA;
+    g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  d.device = device;
+  return PGG_OK;
+}
+}  // namespace
+
+int current_device(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PGG_ERR_CUDA;
+  int st = init_device(dev);
+  if (st != PGG_OK) return st;
+  *info = g_dev[dev];
+  return PGG_OK;
+}
+
+int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                CUtensorMapSwizzle swizzle) {
+  cuuint64_t d[3], s[2];
+  cuuint32_t b[3], e[3] = {1, 1, 1};
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
+  CUresult r = g_encode(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, s, b, e,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? PGG_OK : PGG_ERR_INVALID_ARG;
+}
+
+}  // namespace pgg
+
+using namespace pgg;
+
+namespace {
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+constexpr int64_t kMaxRows = (int64_t)1 << 31;
+
+int check_common(int64_t M, int G, const int32_t* lens) {
+  if (G < 1 || G > kMaxGroups) return PGG_ERR_INVALID_ARG;
+  if (M < 0 || M >= kMaxRows) return PGG_ERR_INVALID_ARG;
+  if (!lens) return PGG_ERR_INVALID_ARG;
+  return PGG_OK;
+}
+
+int check_dim(int64_t x, int mult) {
+  if (x < mult || x >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+  if (x % mult) return PGG_ERR_ALIGNMENT;
+  return PGG_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pgg_version(void) { return 100; }
+
+int pgg_init(int device) {
+  if (cudaSetDevice(device) != cudaSuccess) return PGG_ERR_CUDA;
+  DeviceInfo d;
+  return current_device(&d);
+}
+
+const char* pgg_status_string(int s) {
+  switch (s) {
+    case PGG_OK: return "ok";
+    case PGG_ERR_INVALID_ARG: return "invalid argument";
+    case PGG_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case PGG_ERR_ALIGNMENT: return "misaligned pointer or dimension";
+    case PGG_ERR_NOT_INITIALIZED: return "not initialized";
+    case PGG_ERR_CUDA: return "CUDA runtime error";
+    case PGG_ERR_BAD_GROUP_LENS: return "bad group_lens (negative length or sum != M)";
+    case PGG_ERR_TIMEOUT: return "bounded pipeline wait expired";
+    case PGG_ERR_PAD_OVERFLOW: return "padded column-wise layout exceeds M_pad";
+    default: return "unknown status";
+  }
+}
+
+int pgg_read_error(const int32_t* err_dev, int32_t* host_out, void* stream) {
+  if (!err_dev || !host_out) return PGG_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(host_out, err_dev, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                      as_stream(stream)) != cudaSuccess)
+    return PGG_ERR_CUDA;
+  return cuda_status(cudaStreamSynchronize(as_stream(stream)));
+}
+
+int pgg_grouped_gemm_fwd(const void* X, const void* W, const int32_t* group_lens, void* Y,
+                         int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream) {
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!X || !W || !Y) return PGG_ERR_INVALID_ARG;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return PGG_ERR_ALIGNMENT;
+  if (M == 0) return PGG_OK;
+  Bf16Call c{0, 0, X, W, group_lens, Y, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
+  return launch_bf16(c);
+}
+
+int pgg_grouped_gemm_dgrad(const void* dY, const void* W, const int32_t* group_lens, void* dX,
+                           int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream) {
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!dY || !W || !dX) return PGG_ERR_INVALID_ARG;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (!aligned16(dY) || !aligned16(W) || !aligned16(dX)) return PGG_ERR_ALIGNMENT;
+  if (M == 0) return PGG_OK;
+  Bf16Call c{1, 0, dY, W, group_lens, dX, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
+  return launch_bf16(c);
+}
+
+int pgg_grouped_gemm_wgrad(const void* X, const void* dY, const int32_t* group_lens, void* dW,
+                           int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream) {
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!X || !dY || !dW) return PGG_ERR_INVALID_ARG;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(dW)) return PGG_ERR_ALIGNMENT;
+  if (M == 0) {  // every group is empty: dW = 0
+    return cuda_status(cudaMemsetAsync(dW, 0, (size_t)G * N * K * 2, as_stream(stream)));
+  }
+  Bf16Call c{2, 0, dY, X, group_lens, dW, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
+  return launch_bf16(c);
+}
+
+int pgg_grouped_fc1_swiglu(const void* X, const void* W1, const int32_t* group_lens, void* A,
+                           void* H, int64_t M, int64_t I, int64_t K, int G, int32_t* err,
+                           void* stream) {
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!X || !W1 || !A) return PGG_ERR_INVALID_ARG;
+  if ((st = check_dim(I, 8)) || (st = check_dim(K, 8))) return st;
+  if (!aligned16(X) || !aligned16(W1) || !aligned16(A) || (H && !aligned16(H)))
+    return PGG_ERR_ALIGNMENT;
+  if (M == 0) return PGG_OK;
+  Bf16Call c{0, 1, X, W1, group_lens, A, H, nullptr, M, 2 * I, K, I, G, err, as_stream(stream)};
+  return launch_bf16(c);
+}
+
+int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void* H,
+                                     const int32_t* group_lens, void* dH, int64_t M, int64_t Hd,
+                                     int64_t I, int G, int32_t* err, void* stream) {
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!dY || !W2 || !H || !dH) return PGG_ERR_INVALID_ARG;
+  if ((st = check_dim(Hd, 8)) || (st = check_dim(I, 8))) return st;
+  if (!aligned16(dY) || !aligned16(W2) || !aligned16(H) || !aligned16(dH))
+    return PGG_ERR_ALIGNMENT;
+  if (M == 0) return PGG_OK;
+  Bf16Call c{1, 2, dY, W2, group_lens, dH, nullptr, H, M, Hd, I, I, G, err, as_stream(stream)};
+  return launch_bf16(c);
+}
+
+int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                            uint8_t* scales, void* stream) {
+  if (!in || !codes || !scales) return PGG_ERR_INVALID_ARG;
+  if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
+  if (R < 0 || R >= kMaxRows || C <= 0 || C >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+  if (C % (fmt == PGG_FMT_E2M1 ? 64 : 32)) return PGG_ERR_ALIGNMENT;
+  if (!aligned16(in) || !aligned16(codes) || !aligned16(scales)) return PGG_ERR_ALIGNMENT;
+  if (R == 0) return PGG_OK;
+  return launch_mx_quantize_rowwise(in, R, C, fmt, codes, scales, as_stream(stream));
+}
+
+int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens,
+                            int G, int fmt, uint8_t* codes_t, uint8_t* scales_t, int64_t M_pad,
+                            int32_t* err, void* stream) {
+  if (!in || !codes_t || !scales_t) return PGG_ERR_INVALID_ARG;
+  if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
+  if (group_lens ? (G < 1 || G > kMaxGroups) : (G != 1 && G != 0)) return PGG_ERR_INVALID_ARG;
+  if (M < 0 || M >= kMaxRows || C <= 0 || C >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+  if (M_pad <= 0 || M_pad >= kMaxRows || M_pad % PGG_MX_PAD) return PGG_ERR_ALIGNMENT;
+  if (C % 8) return PGG_ERR_ALIGNMENT;
+  if (!aligned16(in) || !aligned16(codes_t) || !aligned16(scales_t)) return PGG_ERR_ALIGNMENT;
+  return launch_mx_quantize_colwise(in, M, C, group_lens, group_lens ? G : 1, fmt, codes_t,
+                                    scales_t, M_pad, err, as_stream(stream));
+}
+
+int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const uint8_t* SA,
+                        const uint8_t* B, const uint8_t* SB, const void* H,
+                        const int32_t* group_lens, void* out, void* out2, int64_t M, int64_t N,
+                        int64_t K, int G, int64_t M_pad, int32_t* err, void* stream) {
+  int st;
+  if (mode < 0 || mode > 2) return PGG_ERR_INVALID_ARG;
+  if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
+  if (epilogue != PGG_EPI_NONE && epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
+  if (epilogue == PGG_EPI_SWIGLU && mode == PGG_MODE_WGRAD) return PGG_ERR_INVALID_ARG;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!A || !SA || !B || !SB || !out) return PGG_ERR_INVALID_ARG;
+  if (mode == PGG_MODE_DGRAD && epilogue == PGG_EPI_SWIGLU && !H) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
+      (H && !aligned16(H)))
+    return PGG_ERR_ALIGNMENT;
+  if ((st = check_dim(N, 32)) || (st = check_dim(K, 32))) return st;
+  if (mode == PGG_MODE_FWD && K % 128) return PGG_ERR_ALIGNMENT;
+  if (mode == PGG_MODE_DGRAD && N % 128) return PGG_ERR_ALIGNMENT;
+  if (mode == PGG_MODE_WGRAD && (M_pad <= 0 || M_pad % PGG_MX_PAD || M_pad >= kMaxRows))
+    return PGG_ERR_ALIGNMENT;
+  if (M == 0 && mode != PGG_MODE_WGRAD) return PGG_OK;
+  MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, M, N, K, M_pad, G, err,
+           as_stream(stream)};
+  return launch_mx_gemm(c);
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+"""CPU-side checks of the C ABI: the library loads without a GPU and exports
+every entry point that include/pgg.h declares; no compute call is made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pgg.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pgg_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from precision_grouped_gemm_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_hot_path():
+    syms = declared_symbols()
+    for name in ["pgg_grouped_gemm_fwd", "pgg_grouped_gemm_dgrad", "pgg_grouped_gemm_wgrad",
+                 "pgg_grouped_fc1_swiglu", "pgg_grouped_fc2_dgrad_swiglu_bwd",
+                 "pgg_mx_quantize_rowwise", "pgg_mx_quantize_colwise", "pgg_mx_grouped_gemm"]:
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+
+
+def test_binding_signatures_cover_header():
+    from precision_grouped_gemm_gb300 import _binding
+    for s in declared_symbols():
+        if s != "pgg_status_string":
+            assert s in _binding.SIGNATURES, s
+
+
+def test_status_strings_and_version(lib):
+    lib.pgg_status_string.restype = ctypes.c_char_p
+    assert lib.pgg_status_string(0) == b"ok"
+    assert b"group_lens" in lib.pgg_status_string(16)
+    assert lib.pgg_version() >= 100
+
+
+def test_host_validation_without_gpu(lib):
+    # argument checks run before any CUDA call, so they answer on a machine without a GPU
+    P = ctypes.c_void_p
+    f = lib.pgg_grouped_gemm_fwd
+    f.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P]
+    good = 1 << 20
+    assert f(None, good, good, good, 8, 64, 64, 1, None, None) == 1       # null X
+    assert f(good, good, good, good, 8, 64, 60, 1, None, None) == 3       # K % 8
+    assert f(good, good, good, good, 8, 64, 64, 2000, None, None) == 1    # G > 1024
+    assert f(good + 8, good, good, good, 8, 64, 64, 1, None, None) == 3   # misaligned
+    q = lib.pgg_mx_quantize_rowwise
+    q.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P]
+    assert q(good, 4, 48, 1, good, good, None) == 3                        # C % 32
+    assert q(good, 4, 64, 7, good, good, None) == 1                        # bad format

@@ -1,0 +1,28 @@
+"""Shared helpers for the tests: seeded inputs, bf16 <-> numpy, tolerance check."""
+import numpy as np
+import torch
+
+from oracle import grouped_gemm as og
+from precision_grouped_gemm_gb300 import workloads as wl
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor (any device) -> numpy uint16 bit patterns."""
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> exact fp64 values, decoded by the oracle's own decoder."""
+    return og.bf16_to_f64(bits(t))
+
+
+def gen(key, nrows, cols, std=1.0, seed=0, device="cpu", row0=0):
+    return wl.gen_matrix(key, nrows, cols, std, seed, device=device, row0=row0)
+
+
+def assert_close(got: torch.Tensor, ref: np.ndarray, what: str = ""):
+    """|got - ref| <= 1e-2 |ref| + 1e-2 rms(ref) per element (bf16 output vs fp64 oracle)."""
+    g = f64(got) if got.dtype == torch.bfloat16 else got.detach().cpu().double().numpy()
+    ok, ratio = og.within_tol(g, ref)
+    assert ok, f"{what}: tolerance exceeded, worst err/bound = {ratio:.3g}"
+    return ratio

@@ -1,0 +1,445 @@
+#!/usr/bin/env python
+"""Benchmark: grouped GEMM TFLOP/s for one MoE expert layer, fwd + dgrad + wgrad.
+
+Workload (default): the DeepSeek-V4-Flash-shaped BF16 MoE layer -- hidden 4096,
+256 routed experts, top-6 of softmax over seeded logits for 4096 tokens
+(M = 24576 rows), FC1 4096 -> 2x2048 with SwiGLU fused, FC2 2048 -> 4096,
+weights ~ N(0, 0.02).  One step = the six grouped-GEMM launches of
+precision_grouped_gemm_gb300.layer (fc1 fwd+SwiGLU, fc2 fwd, fc2 dgrad+SwiGLU
+backward, fc2 wgrad, fc1 dgrad, fc1 wgrad).
+
+Prints one JSON line.  `value` counts 2*M*N*K flops per GEMM (padding rows the
+MMA wastes are not counted) over all ranks divided by the slowest rank's time.
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload instead (the only other code path this file runs).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from precision_grouped_gemm_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "grouped GEMM TFLOP/s fwd+dgrad+wgrad, % of GB300 dense BF16/MXFP8 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="pgg", choices=["pgg", "reference"])
+    p.add_argument("--workload", default=wl.DSV4_BF16.name, choices=sorted(wl.WORKLOADS))
+    p.add_argument("--e2e-steps", type=int, default=2)
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--experts-cap", type=int, default=0,
+                   help="keep only the first N experts (same per-expert shapes; small profiling case)")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) >= 9:
+                    rows.append(p)
+        os.unlink(self.path)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        sm, mx, pw = [], [], []
+        for p in rows:
+            try:
+                sm.append(float(p[1])); mx.append(float(p[2])); pw.append(float(p[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# inputs
+# ----------------------------------------------------------------------------
+
+def workload_lens(w, cap=0):
+    lens, row_token = w.group_lens()
+    if cap:
+        lens = lens[:cap].copy()
+        row_token = row_token[:int(lens.sum())]
+    return lens, row_token
+
+
+def build_device_inputs(w, device, cap=0):
+    from precision_grouped_gemm_gb300.layer import ExpertLayerBuffers
+    lens, row_token = workload_lens(w, cap)
+    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
+    rt = torch.from_numpy(row_token).to(device)
+    xtok = wl.gen_matrix(wl.KEY_X, w.tokens, Hd, 1.0, w.seed, device=device)
+    X = xtok[rt].contiguous()
+    del xtok
+    W1 = wl.gen_matrix(wl.KEY_W1, G * 2 * I, Hd, w.w_std, w.seed, device=device).view(G, 2 * I, Hd)
+    W2 = wl.gen_matrix(wl.KEY_W2, G * Hd, I, w.w_std, w.seed, device=device).view(G, Hd, I)
+    dY = wl.gen_matrix(wl.KEY_DY, M, Hd, 1.0, w.seed, device=device)
+    gl = torch.from_numpy(lens).to(device)
+    torch.cuda.synchronize()
+    return lens, ExpertLayerBuffers(X, W1, W2, dY, gl).allocate()
+
+
+def layer_flops(lens, w):
+    return 18.0 * float(lens.sum()) * w.inter * w.hidden
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and reference arm)
+# ----------------------------------------------------------------------------
+
+def _oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads") for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+class OracleSample:
+    """The fp64 oracle on whole experts of the workload, one expert per call."""
+
+    def __init__(self, w):
+        from oracle import grouped_gemm as og
+        self.og = og
+        self.w = w
+        self.lens, self.row_token = w.group_lens()
+        self.off = np.concatenate([[0], np.cumsum(self.lens)])
+
+    def inputs(self, e):
+        w, a, b = self.w, int(self.off[e]), int(self.off[e + 1])
+        rows = torch.from_numpy(self.row_token[a:b])
+        X = wl.gen_bf16(wl.KEY_X, rows, w.hidden, 1.0, w.seed)
+        W1 = wl.gen_matrix(wl.KEY_W1, 2 * w.inter, w.hidden, w.w_std, w.seed, row0=e * 2 * w.inter)
+        W2 = wl.gen_matrix(wl.KEY_W2, w.hidden, w.inter, w.w_std, w.seed, row0=e * w.hidden)
+        dY = wl.gen_matrix(wl.KEY_DY, b - a, w.hidden, 1.0, w.seed, row0=a)
+        to_bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+        return [to_bits(t) for t in (X, W1, W2, dY)], b - a
+
+    def run(self, bits, n):
+        og = self.og
+        X, W1, W2, dY = [og.bf16_to_f64(x) for x in bits]
+        W1 = W1.reshape(1, 2 * self.w.inter, self.w.hidden)
+        W2 = W2.reshape(1, self.w.hidden, self.w.inter)
+        lens = np.array([n], dtype=np.int32)
+        A, H = og.grouped_fc1_swiglu(X, W1, lens)
+        og.grouped_gemm_fwd(A, W2, lens)
+        dH = og.grouped_fc2_dgrad_swiglu_bwd(dY, W2, H, lens)
+        og.grouped_gemm_wgrad(A, dY, lens)
+        og.grouped_gemm_dgrad(dH, W1, lens)
+        og.grouped_gemm_wgrad(X, dH, lens)
+
+    def flops(self, n):
+        return 18.0 * n * self.w.inter * self.w.hidden
+
+
+def cpu_baseline(w, seconds):
+    s = OracleSample(w)
+    done_flops, t_total, experts = 0.0, 0.0, 0
+    for e in range(w.experts):
+        if s.lens[e] == 0:
+            continue
+        bits, n = s.inputs(e)
+        t0 = time.perf_counter()
+        s.run(bits, n)
+        t_total += time.perf_counter() - t0
+        done_flops += s.flops(n)
+        experts += 1
+        if t_total >= seconds:
+            break
+    return {"value": done_flops / t_total / 1e12, "unit": "TFLOP/s", "cores": _oracle_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 oracle (numpy) on the first {experts} non-empty experts of {w.name} "
+                      f"({done_flops / 1e9:.1f} GFLOP of the layer's fwd+dgrad+wgrad, {t_total:.1f} s), "
+                      f"one expert per call, inputs decoded from bf16 inside the timed region"}
+
+
+def run_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    s = OracleSample(w)
+    nz = [e for e in range(w.experts) if s.lens[e] > 0]
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))
+    cache = {}
+
+    def step(k):
+        e = nz[k % len(nz)]
+        if e not in cache:
+            cache[e] = s.inputs(e)
+        bits, n = cache[e]
+        t0 = time.perf_counter()
+        s.run(bits, n)
+        return time.perf_counter() - t0, s.flops(n)
+
+    for k in range(args.warmup):
+        step(k)
+    # one expert per step; budget only decides whether that already fits
+    tt, ff = 0.0, 0.0
+    for k in range(args.steps):
+        dt, f = step(args.warmup + k)
+        tt += dt
+        ff += f
+    value = ff / tt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tt / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator; routing by top-k of softmax over generated logits)",
+        "config": {"workload": w.name, "parallelism": "replicas" if args.gpus > 1 else "single",
+                   "step": "the layer's fwd+dgrad+wgrad on one whole expert per step (bounded sample)",
+                   "per_step_budget_s": budget},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": _oracle_threads(), "kind": "oracle",
+                         "sample": "one whole expert per step, cycling over the non-empty experts"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+# ----------------------------------------------------------------------------
+
+def kernel_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel sources still match."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    from precision_grouped_gemm_gb300.build import source_digest
+    if d.get("source_digest") != source_digest():
+        return None
+    k = d.get("kernels", {}).get(name)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+def run_pgg(args, w):
+    import precision_grouped_gemm_gb300 as pgg
+    from precision_grouped_gemm_gb300.layer import STEP_NAMES, expert_layer_step, layer_work
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pgg.init(local)
+    peaks, peak_src = load_peaks()
+
+    lens, buf = build_device_inputs(w, device, args.experts_cap)
+    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
+    flops = layer_flops(lens, w)
+    work = layer_work(M, G, Hd, I)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        expert_layer_step(buf)
+    torch.cuda.synchronize()
+    if pgg.read_error(buf.err) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STEP_NAMES) + 1)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(K):
+        row = ev[k]
+        expert_layer_step(buf, between=lambda i, row=row: row[i].record())
+    t1.record()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if pgg.read_error(buf.err) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    per = {}
+    for i, name in enumerate(STEP_NAMES):
+        d = [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)]
+        avg = sum(d) / len(d)
+        f, b = work[name]
+        per[name] = {"ms": avg, "tflops": f / avg / 1e9, "gbs": b / avg / 1e6,
+                     "algo_bytes": b, "flops": f}
+    dom = max(per, key=lambda n: per[n]["ms"])
+    f, b = work[dom]
+    hbm, tc = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]), peaks.get("bf16_tflops_sustained", 1700.0)
+    bound = "hbm" if b / (hbm * 1e9) >= f / (tc * 1e12) else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = per[dom]["gbs"], hbm, "GB/s"
+    else:
+        achieved, peak, unit = per[dom]["tflops"], tc, "TFLOP/s"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                "frac": achieved / peak, "traffic": kernel_traffic(dom),
+                "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops_sustained'})",
+                "algo_bytes_per_launch": b, "flops_per_launch": f}
+
+    value = world * flops / (ms / K) / 1e9  # TFLOP/s over all ranks
+    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
+    attain = sum(max(work[n][1] / (hbm * 1e9), work[n][0] / (bf16_peak * 1e12)) for n in STEP_NAMES)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, buf, flops)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; routing by top-k of softmax over generated logits)",
+        "config": {"workload": w.name + (f"_first{G}experts" if args.experts_cap else ""), "tokens": w.tokens, "experts": G, "top_k": w.topk, "hidden": Hd,
+                   "intermediate": I, "rows_M": M, "group_lens_min": int(lens.min()),
+                   "group_lens_max": int(lens.max()),
+                   "l2": f"inputs larger than L2 ({(buf.W1.numel() + buf.W2.numel()) * 2 / 1e9:.1f} GB of "
+                         f"expert weights streamed per step), no flush",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "pct_of_dense_bf16_peak": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
+        "pct_of_attainable_roofline": (attain * 1e3) / (ms / K),
+        "roofline": roofline, "kernels": per, "gpu_launches": len(STEP_NAMES) * K,
+        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, buf, flops):
+    """Same metric through the public API with host buffers: H2D of the step's inputs from
+    pinned memory, the six calls, D2H of the step's results, all inside the timed region."""
+    from precision_grouped_gemm_gb300.layer import expert_layer_step
+    ins = [buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens]
+    outs = [buf.Y, buf.dX, buf.dW1, buf.dW2]
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    for h, t in zip(h_in, ins):
+        h.copy_(t)
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    bi = sum(t.numel() * t.element_size() for t in ins)
+    bo = sum(t.numel() * t.element_size() for t in outs)
+
+    def step():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        expert_layer_step(buf)
+        for h, d in zip(h_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    n = max(1, args.e2e_steps)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(n):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    return {"value": flops / ms / 1e9, "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "ms_per_step": ms, "steps": n}
+
+
+def main():
+    args = parse_args()
+    w = wl.WORKLOADS[args.workload]
+    if not w.swiglu or w.fmt != "bf16":
+        raise SystemExit("bench.py times the BF16 expert-layer workloads")
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_pgg(args, w)
+
+
+if __name__ == "__main__":
+    main()

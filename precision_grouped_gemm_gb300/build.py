@@ -71,3 +71,14 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
 if __name__ == "__main__":
     print(build(verbose=True))
+
+
+def source_digest() -> str:
+    """sha256 over the CUDA sources and headers (identifies the kernels a profile was taken on)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]

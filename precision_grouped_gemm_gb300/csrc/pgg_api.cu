@@ -133,10 +133,10 @@ int pgg_grouped_gemm_fwd(const void* X, const void* W, const int32_t* group_lens
                          int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream) {
   int st;
   if ((st = check_common(M, G, group_lens))) return st;
-  if (!X || !W || !Y) return PGG_ERR_INVALID_ARG;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
-  if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return PGG_ERR_ALIGNMENT;
   if (M == 0) return PGG_OK;
+  if (!X || !W || !Y) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(W) || !aligned16(Y)) return PGG_ERR_ALIGNMENT;
   Bf16Call c{0, 0, X, W, group_lens, Y, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
   return launch_bf16(c);
 }
@@ -145,10 +145,10 @@ int pgg_grouped_gemm_dgrad(const void* dY, const void* W, const int32_t* group_l
                            int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream) {
   int st;
   if ((st = check_common(M, G, group_lens))) return st;
-  if (!dY || !W || !dX) return PGG_ERR_INVALID_ARG;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
-  if (!aligned16(dY) || !aligned16(W) || !aligned16(dX)) return PGG_ERR_ALIGNMENT;
   if (M == 0) return PGG_OK;
+  if (!dY || !W || !dX) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(dY) || !aligned16(W) || !aligned16(dX)) return PGG_ERR_ALIGNMENT;
   Bf16Call c{1, 0, dY, W, group_lens, dX, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
   return launch_bf16(c);
 }
@@ -157,12 +157,13 @@ int pgg_grouped_gemm_wgrad(const void* X, const void* dY, const int32_t* group_l
                            int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream) {
   int st;
   if ((st = check_common(M, G, group_lens))) return st;
-  if (!X || !dY || !dW) return PGG_ERR_INVALID_ARG;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
-  if (!aligned16(X) || !aligned16(dY) || !aligned16(dW)) return PGG_ERR_ALIGNMENT;
+  if (!dW || !aligned16(dW)) return dW ? PGG_ERR_ALIGNMENT : PGG_ERR_INVALID_ARG;
   if (M == 0) {  // every group is empty: dW = 0
     return cuda_status(cudaMemsetAsync(dW, 0, (size_t)G * N * K * 2, as_stream(stream)));
   }
+  if (!X || !dY) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(dY)) return PGG_ERR_ALIGNMENT;
   Bf16Call c{2, 0, dY, X, group_lens, dW, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
   return launch_bf16(c);
 }
@@ -172,11 +173,11 @@ int pgg_grouped_fc1_swiglu(const void* X, const void* W1, const int32_t* group_l
                            void* stream) {
   int st;
   if ((st = check_common(M, G, group_lens))) return st;
-  if (!X || !W1 || !A) return PGG_ERR_INVALID_ARG;
   if ((st = check_dim(I, 8)) || (st = check_dim(K, 8))) return st;
+  if (M == 0) return PGG_OK;
+  if (!X || !W1 || !A) return PGG_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(W1) || !aligned16(A) || (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
-  if (M == 0) return PGG_OK;
   Bf16Call c{0, 1, X, W1, group_lens, A, H, nullptr, M, 2 * I, K, I, G, err, as_stream(stream)};
   return launch_bf16(c);
 }
@@ -186,11 +187,11 @@ int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void*
                                      int64_t I, int G, int32_t* err, void* stream) {
   int st;
   if ((st = check_common(M, G, group_lens))) return st;
-  if (!dY || !W2 || !H || !dH) return PGG_ERR_INVALID_ARG;
   if ((st = check_dim(Hd, 8)) || (st = check_dim(I, 8))) return st;
+  if (M == 0) return PGG_OK;
+  if (!dY || !W2 || !H || !dH) return PGG_ERR_INVALID_ARG;
   if (!aligned16(dY) || !aligned16(W2) || !aligned16(H) || !aligned16(dH))
     return PGG_ERR_ALIGNMENT;
-  if (M == 0) return PGG_OK;
   Bf16Call c{1, 2, dY, W2, group_lens, dH, nullptr, H, M, Hd, I, I, G, err, as_stream(stream)};
   return launch_bf16(c);
 }

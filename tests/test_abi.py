@@ -57,6 +57,7 @@ def test_host_validation_without_gpu(lib):
     f.argtypes = [P, P, P, P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P]
     good = 1 << 20
     assert f(None, good, good, good, 8, 64, 64, 1, None, None) == 1       # null X
+    assert f(None, None, good, None, 0, 64, 64, 1, None, None) == 0       # M == 0 is a no-op
     assert f(good, good, good, good, 8, 64, 60, 1, None, None) == 3       # K % 8
     assert f(good, good, good, good, 8, 64, 64, 2000, None, None) == 1    # G > 1024
     assert f(good + 8, good, good, good, 8, 64, 64, 1, None, None) == 3   # misaligned

@@ -8,13 +8,18 @@ namespace pgg {
 namespace {
 
 constexpr int kBN = 256;
-constexpr int kStages = 4;
+
+// stages per mode: fwd/dgrad stream W through 4 stages; wgrad's short reductions
+// need fewer and leave room for the TMA-store staging buffers
+template <int MODE>
+constexpr int stages() { return MODE == kWgrad ? 3 : 4; }
 
 template <int MODE, int EPI>
-int run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int grid,
-        cudaStream_t s) {
-  using L = GemmSmem<kBN, kStages>;
-  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, kStages>;
+int run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
+        int grid, cudaStream_t s) {
+  constexpr int S = stages<MODE>();
+  using L = GemmSmem<kBN, S, epi_bytes<MODE>()>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, S>;
   const size_t smem = L::bytes(args.G);
   static bool attr_done = false;  // per instantiation; the attribute is per device function
   if (!attr_done) {
@@ -23,7 +28,7 @@ int run(const CUtensorMap& ta, const CUtensorMap& tb, const GemmArgs& args, int 
     if (e != cudaSuccess) return cuda_status(e);
     attr_done = true;
   }
-  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, args);
+  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, tc, args);
   return cuda_status(cudaGetLastError());
 }
 
@@ -37,7 +42,7 @@ int launch_bf16(const Bf16Call& c) {
   if (st != PGG_OK) return st;
   const uint32_t sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   GemmArgs a{};
   a.group_lens = c.group_lens;
   a.G = c.G;
@@ -79,16 +84,21 @@ int launch_bf16(const Bf16Call& c) {
     uint32_t bx[2] = {64, (uint32_t)kBK};
     if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, bx, (CUtensorMapSwizzle)sw))) return st;
     if ((st = encode_tmap(&tb, bf, 2, c.b, db, sb, bx, (CUtensorMapSwizzle)sw))) return st;
+    uint64_t dc[3] = {(uint64_t)c.K, (uint64_t)c.N, (uint64_t)c.G};
+    uint64_t sc[2] = {(uint64_t)c.K * 2, (uint64_t)(c.N * c.K * 2)};
+    uint32_t bc[3] = {64, 32, 1};
+    if ((st = encode_tmap(&tc, bf, 3, c.out, dc, sc, bc, (CUtensorMapSwizzle)sw))) return st;
     a.out_cols = (int)c.K;
     a.wg_rows = (int)c.N;
     tiles_ub = c.G * ceil_div(c.N, kBM) * ceil_div(c.K, kBN);
   }
+  if (c.mode != 2) tc = ta;  // unused outside wgrad
   const int grid = std::max(1, std::min(dev.sms, tiles_ub));
-  if (c.mode == 0 && c.epi == 0) return run<kFwd, kEpiStore>(ta, tb, a, grid, c.stream);
-  if (c.mode == 0 && c.epi == 1) return run<kFwd, kEpiSwiGLU>(ta, tb, a, grid, c.stream);
-  if (c.mode == 1 && c.epi == 0) return run<kDgrad, kEpiStore>(ta, tb, a, grid, c.stream);
-  if (c.mode == 1 && c.epi == 2) return run<kDgrad, kEpiSwiGLUBwd>(ta, tb, a, grid, c.stream);
-  if (c.mode == 2 && c.epi == 0) return run<kWgrad, kEpiStore>(ta, tb, a, grid, c.stream);
+  if (c.mode == 0 && c.epi == 0) return run<kFwd, kEpiStore>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 0 && c.epi == 1) return run<kFwd, kEpiSwiGLU>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 1 && c.epi == 0) return run<kDgrad, kEpiStore>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 1 && c.epi == 2) return run<kDgrad, kEpiSwiGLUBwd>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 2 && c.epi == 0) return run<kWgrad, kEpiStore>(ta, tb, tc, a, grid, c.stream);
   return PGG_ERR_INVALID_ARG;
 }
 

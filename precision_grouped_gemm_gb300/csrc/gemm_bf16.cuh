@@ -48,18 +48,26 @@ struct GemmArgs {
   int32_t* err;     // device error word or nullptr
 };
 
-template <int BN, int STAGES>
+// Shared memory: STAGES x (A tile | B tile), the epilogue staging buffers
+// (wgrad: 4 warps x 2 x 4 KB, 1024-byte aligned for the 128-byte swizzle), the
+// mbarriers and the group scan arrays.
+template <int BN, int STAGES, int EPI_BYTES>
 struct GemmSmem {
   static constexpr int kABytes = kBM * kBK * 2;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kBarOff = STAGES * kStageBytes;
+  static constexpr int kEpiOff = STAGES * kStageBytes;
+  static constexpr int kBarOff = kEpiOff + EPI_BYTES;
   static constexpr int kBarBytes = 256;
   static constexpr int kGroupOff = kBarOff + kBarBytes;
   static __host__ __device__ constexpr size_t bytes(int G) {
     return 1024 + (size_t)kGroupOff + 8 * (size_t)(G + 1) + 16;
   }
 };
+
+// Epilogue staging bytes per mode: wgrad stores its full tiles with TMA.
+template <int MODE>
+constexpr int epi_bytes() { return MODE == kWgrad ? 4 * 2 * 4096 : 0; }
 
 struct Tile {
   int g, row0, rows, col0, nkb, red0, red_valid;
@@ -150,8 +158,9 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v, i
 template <int MODE, int EPI, int BN, int STAGES>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                             const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
-  using L = GemmSmem<BN, STAGES>;
+                             const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
+  using L = GemmSmem<BN, STAGES, epi_bytes<MODE>()>;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != kEpiSwiGLU || (MODE == kFwd && BN == 256), "SwiGLU fwd tile");
   static_assert(EPI != kEpiSwiGLUBwd || MODE == kDgrad, "SwiGLU bwd tile");
@@ -346,9 +355,62 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 8192;  // wgrad: this warp's two 4 KB buffers
+    int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
       const bool row_ok = r < T.rows;
+      if (MODE == kWgrad) {
+        // rows q*32..q*32+31 of the tile go out as 32 x 64 bf16 boxes through a
+        // 128B-swizzled staging buffer and a bulk tensor store (clipped at N, K)
+        const bool zero = T.nkb == 0;  // empty group: dW_g = 0
+        if (!zero) {
+          if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+          tc_fence_after();
+        }
+        const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          // a box that starts past N or K holds nothing to store (warp-uniform test);
+          // skipping it keeps one committed store per used staging buffer
+          if (T.row0 + q * 32 >= args.wg_rows || T.col0 + c * 64 >= args.out_cols) continue;
+          uint32_t ra[32], rb[32];
+          if (!zero) {
+            tmem_ld32(tb + c * 64, ra);
+            tmem_ld32(tb + c * 64 + 32, rb);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) { ra[j] = 0u; rb[j] = 0u; }
+          }
+          uint8_t* sb = stg + (nstore & 1) * 4096;
+          if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t* v = j < 4 ? &ra[j * 8] : &rb[(j - 4) * 8];
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+            w.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+            w.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+            w.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+            *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tmC, smem_u32(sb), T.col0 + c * 64, T.row0 + q * 32, T.g);
+            bulk_commit();
+          }
+          ++nstore;
+        }
+        if (!zero) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&tempty[acc]));
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        continue;
+      }
       if (MODE == kWgrad && T.nkb == 0) {
         if (row_ok) {
           float zero[32];
@@ -442,6 +504,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
 
+  if (MODE == kWgrad && warp >= 2 && lane == 0) bulk_wait<0>();
   if (aborted && lane == 0) set_error(args.err, kErrTimeout);
   tc_fence_before();
   __syncthreads();

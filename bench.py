@@ -127,28 +127,11 @@ class ClockSampler:
 # inputs
 # ----------------------------------------------------------------------------
 
-def workload_lens(w, cap=0):
-    lens, row_token = w.group_lens()
-    if cap:
-        lens = lens[:cap].copy()
-        row_token = row_token[:int(lens.sum())]
-    return lens, row_token
-
-
 def build_device_inputs(w, device, cap=0):
-    from precision_grouped_gemm_gb300.layer import ExpertLayerBuffers
-    lens, row_token = workload_lens(w, cap)
-    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
-    rt = torch.from_numpy(row_token).to(device)
-    xtok = wl.gen_matrix(wl.KEY_X, w.tokens, Hd, 1.0, w.seed, device=device)
-    X = xtok[rt].contiguous()
-    del xtok
-    W1 = wl.gen_matrix(wl.KEY_W1, G * 2 * I, Hd, w.w_std, w.seed, device=device).view(G, 2 * I, Hd)
-    W2 = wl.gen_matrix(wl.KEY_W2, G * Hd, I, w.w_std, w.seed, device=device).view(G, Hd, I)
-    dY = wl.gen_matrix(wl.KEY_DY, M, Hd, 1.0, w.seed, device=device)
-    gl = torch.from_numpy(lens).to(device)
+    from precision_grouped_gemm_gb300.layer import build_layer_inputs
+    lens, _, buf = build_layer_inputs(w, device, cap)
     torch.cuda.synchronize()
-    return lens, ExpertLayerBuffers(X, W1, W2, dY, gl).allocate()
+    return lens, buf
 
 
 def layer_flops(lens, w):

@@ -132,7 +132,7 @@ int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void*
  * with emax 8 (e4m3) or 2 (e2m1), scale code E + 127, element code =
  * round-to-nearest-even(v * 2^-E) saturated to +-448 / +-6, sign of zero kept;
  * a block with a NaN or Inf gets scale 0xFF and zero codes.
- *   in [R, C] bf16; C % 32 == 0 (e4m3) or C % 64 == 0 (e2m1).
+ *   in [R, C] bf16; C % 32 == 0.
  *   codes [R, C] u8 (e4m3) or [R, C/2] u8 (e2m1: element 2j in the low
  *   nibble of byte j); scales [R, C/32] u8. */
 int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,

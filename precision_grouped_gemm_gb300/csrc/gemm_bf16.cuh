@@ -305,20 +305,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // the next group (or lie past M); zero them in both operands
           const int valid = T.red_valid - kb * kBK;
           if (valid < kBK) {
-            const int nz = kBK - valid;
-            uint4 z = make_uint4(0, 0, 0, 0);
+            const uint4 z = make_uint4(0, 0, 0, 0);
             uint8_t* pa = smem + (sa - smem_a0);
             uint8_t* pb = smem + (sb - smem_a0);
-            // each atom column is [kBK rows][128 B]; zero rows valid..kBK-1
-            for (int i = lane; i < nz * 8 * (kBM / 64); i += 32) {
-              int atom = i / (nz * 8), rem = i % (nz * 8);
-              int row = valid + rem / 8, c16 = rem % 8;
-              *reinterpret_cast<uint4*>(pa + atom * kBK * 128 + row * 128 + c16 * 16) = z;
-            }
-            for (int i = lane; i < nz * 8 * (BN / 64); i += 32) {
-              int atom = i / (nz * 8), rem = i % (nz * 8);
-              int row = valid + rem / 8, c16 = rem % 8;
-              *reinterpret_cast<uint4*>(pb + atom * kBK * 128 + row * 128 + c16 * 16) = z;
+            // each atom column is [kBK rows][128 B]; lane writes 16-byte chunk
+            // (lane & 7) of rows valid + (lane >> 3), +4, ... (swizzle stays inside a row)
+            const int c16 = (lane & 7) * 16;
+            for (int row = valid + (lane >> 3); row < kBK; row += 4) {
+#pragma unroll
+              for (int atom = 0; atom < kBM / 64; ++atom)
+                *reinterpret_cast<uint4*>(pa + atom * kBK * 128 + row * 128 + c16) = z;
+#pragma unroll
+              for (int atom = 0; atom < BN / 64; ++atom)
+                *reinterpret_cast<uint4*>(pb + atom * kBK * 128 + row * 128 + c16) = z;
             }
             fence_proxy_async_smem();
             __syncwarp();

@@ -1,12 +1,259 @@
-// MX quantize kernels (row-wise and group-aware column-wise).
+// MX (microscaling) quantization kernels: bf16 -> e4m3 or e2m1 codes with one
+// E8M0 scale per 32-element block (the MXFP8 / MXFP4 operands of the
+// block-scaled grouped GEMM; "Primus-Turbo" README, "What's New"; Pull Request
+// #891, "Changes": MXFP4 weights as float4_e2m1fn_x2 buffers).
+//
+// Rule (OCP Microscaling v1.0): amax = max |v| over the block; E =
+// clamp(floor(log2 amax) - emax, -127, 127), emax 8 (e4m3) / 2 (e2m1); scale
+// code E + 127; code = RNE(v * 2^-E) saturated to the largest finite value,
+// sign of zero kept; a block holding NaN or Inf gets scale 0xFF and zero codes.
+// For bf16 inputs floor(log2 amax) is the exponent field minus 127 (zero and
+// subnormal amax clamp to E = -127), and v * 2^-E is exact in fp32 for every
+// value that can round to a non-zero code, so the conversion instruction's
+// single rounding is the rule's rounding.
+#include <algorithm>
+
 #include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
 
 namespace pgg {
-int launch_mx_quantize_rowwise(const void*, int64_t, int64_t, int, uint8_t*, uint8_t*, cudaStream_t) {
-  return PGG_ERR_UNSUPPORTED;
+namespace {
+
+constexpr int kE4M3 = 1;
+constexpr int kE2M1 = 2;
+
+template <int FMT>
+__device__ __forceinline__ int emax() { return FMT == kE4M3 ? 8 : 2; }
+
+// amax bits (bf16 magnitude bits, ordered as integers) -> (scale code, fp32 multiplier 2^-E);
+// returns false for a non-finite block.
+template <int FMT>
+__device__ __forceinline__ bool block_scale(uint32_t amax_bits, uint32_t& code, float& mult) {
+  if (amax_bits >= 0x7F80u) {
+    code = 0xFFu;
+    mult = 0.0f;
+    return false;
+  }
+  int e = (int)(amax_bits >> 7) - 127 - emax<FMT>();
+  e = max(e, -127);  // upper clamp is never reached from bf16 (max exponent 127)
+  code = (uint32_t)(e + 127);
+  mult = __uint_as_float((uint32_t)(127 - e) << 23);
+  return true;
 }
-int launch_mx_quantize_colwise(const void*, int64_t, int64_t, const int32_t*, int, int, uint8_t*,
-                               uint8_t*, int64_t, int32_t*, cudaStream_t) {
-  return PGG_ERR_UNSUPPORTED;
+
+// two fp32 -> two e4m3 bytes (lo in the low byte)
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
+// two fp32 -> one byte of two e2m1 nibbles (lo in the low nibble)
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
+      "cvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ------------------------------------------------------------------ row-wise
+// The tensor is a flat run of 32-element blocks (C % 32 == 0), so block i's
+// scale is scales[i] and its codes start at byte 32 i (e4m3) or 16 i (e2m1).
+// Four lanes own one block: each loads 8 bf16 (16 B, fully coalesced across the
+// warp), the block amax is a 2-step xor shuffle, each lane writes 8 (e4m3) or
+// 4 (e2m1) bytes and lane%4 == 0 writes the scale byte.
+template <int FMT>
+__global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __restrict__ in,
+                                                               uint8_t* __restrict__ codes,
+                                                               uint8_t* __restrict__ scales,
+                                                               int64_t n_chunks) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n_chunks;
+       i += stride) {
+    const bool live = i < n_chunks;
+    uint4 v = live ? __ldg(in + i) : make_uint4(0, 0, 0, 0);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t am = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) am = max(am, max(w[j] & 0x7FFFu, (w[j] >> 16) & 0x7FFFu));
+    am = max(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    am = max(am, __shfl_xor_sync(0xffffffffu, am, 2));
+    if (!live) continue;
+    uint32_t sc;
+    float mult;
+    const bool fin = block_scale<FMT>(am, sc, mult);
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = bf16_lo(w[j]) * mult;
+      f[2 * j + 1] = bf16_hi(w[j]) * mult;
+    }
+    if (FMT == kE4M3) {
+      uint2 o;
+      o.x = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+      o.y = cvt_e4m3x2(f[4], f[5]) | (cvt_e4m3x2(f[6], f[7]) << 16);
+      if (!fin) o = make_uint2(0, 0);
+      reinterpret_cast<uint2*>(codes)[i] = o;
+    } else {
+      uint32_t o = cvt_e2m1x2(f[0], f[1]) | (cvt_e2m1x2(f[2], f[3]) << 8) |
+                   (cvt_e2m1x2(f[4], f[5]) << 16) | (cvt_e2m1x2(f[6], f[7]) << 24);
+      if (!fin) o = 0;
+      reinterpret_cast<uint32_t*>(codes)[i] = o;
+    }
+    if ((threadIdx.x & 3) == 0) scales[i >> 2] = (uint8_t)sc;
+  }
+}
+
+// ------------------------------------------------------------------ column-wise
+// Output column space [0, M_pad) is cut into 32-wide blocks; block j holds
+// rows off_g + 32 b .. of group g for j = pb_g + b with pb_g the prefix of
+// round_up(len_g, 128) / 32, or nothing (pad) -- every output byte is written
+// once.  A CTA tile is one block j x 128 input columns: 32 rows x 128 columns
+// are staged in smem (coalesced 16-byte loads), then thread c quantizes column
+// c down the 32 rows and writes its 32 (e4m3) or 16 (e2m1) code bytes.
+constexpr int kColTile = 128;
+constexpr int kColThreads = 128;
+constexpr int kSmemPitch = kColTile + 8;  // bf16 elements per staged row (bank spread)
+
+template <int FMT>
+__global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
+    const __nv_bfloat16* __restrict__ in, int64_t M, int C, const int32_t* __restrict__ lens,
+    int G, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int64_t M_pad,
+    int32_t* err) {
+  extern __shared__ int32_t s_dyn[];
+  int32_t* s_off = s_dyn;             // [G+1] row offsets
+  int32_t* s_blk = s_dyn + (G + 1);   // [G+1] prefix of 32-blocks in the padded layout
+  __shared__ __align__(16) uint16_t tile[32 * kSmemPitch];
+  __shared__ int s_bad;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    bool bad;
+    if (lens) {
+      TileCount tc;
+      tc.bm = PGG_MX_PAD;
+      tc.per_row_tile = PGG_MX_PAD / 32;
+      bad = scan_groups(lens, G, M, tc, s_off, s_blk, nullptr, 0, lane);
+    } else {
+      if (lane == 0) {
+        s_off[0] = 0; s_off[1] = (int32_t)M;
+        s_blk[0] = 0; s_blk[1] = (int32_t)(((M + PGG_MX_PAD - 1) / PGG_MX_PAD) * (PGG_MX_PAD / 32));
+      }
+      bad = false;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      int code = bad ? PGG_ERR_BAD_GROUP_LENS
+                     : ((int64_t)s_blk[G] * 32 > M_pad ? PGG_ERR_PAD_OVERFLOW : 0);
+      s_bad = code;
+      if (code && blockIdx.x == 0) set_error(err, code);
+    }
+  }
+  __syncthreads();
+  if (s_bad) return;
+  const int nblk = (int)(M_pad / 32);
+  const int nct = (C + kColTile - 1) / kColTile;
+  const int64_t total = (int64_t)nblk * nct;
+  const int used = s_blk[G];
+  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
+    const int j = (int)(t / nct);
+    const int c0 = (int)(t % nct) * kColTile;
+    int valid = 0;
+    int64_t row0 = 0;
+    if (j < used) {
+      const int g = find_group(s_blk, G, j);
+      const int b = j - s_blk[g];
+      const int len = s_off[g + 1] - s_off[g];
+      valid = min(32, max(0, len - 32 * b));
+      row0 = (int64_t)s_off[g] + 32 * b;
+    }
+    __syncthreads();  // previous tile fully consumed
+    // stage rows row0 .. row0+valid-1, columns c0 .. c0+127 (16-byte chunks)
+    for (int q = threadIdx.x; q < 32 * (kColTile / 8); q += kColThreads) {
+      const int r = q / (kColTile / 8), cc = (q % (kColTile / 8)) * 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < valid && c0 + cc < C) v = __ldg(reinterpret_cast<const uint4*>(in + (row0 + r) * C + c0 + cc));
+      *reinterpret_cast<uint4*>(&tile[r * kSmemPitch + cc]) = v;
+    }
+    __syncthreads();
+    const int c = c0 + threadIdx.x;
+    if (c >= C) continue;
+    uint32_t am = 0;
+    for (int r = 0; r < valid; ++r) am = max(am, (uint32_t)(tile[r * kSmemPitch + threadIdx.x] & 0x7FFFu));
+    uint32_t sc = 0;
+    float mult = 0.0f;
+    bool fin = true;
+    if (valid > 0) fin = block_scale<FMT>(am, sc, mult);
+    float f[32];
+#pragma unroll
+    for (int r = 0; r < 32; ++r)
+      f[r] = (r < valid && fin) ? __uint_as_float((uint32_t)tile[r * kSmemPitch + threadIdx.x] << 16) * mult : 0.0f;
+    if (valid == 0 || !fin) {
+#pragma unroll
+      for (int r = 0; r < 32; ++r) f[r] = 0.0f;  // pad block or non-finite block: +0 codes
+    }
+    if (FMT == kE4M3) {
+      uint4 o[2];
+      uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        ow[k] = cvt_e4m3x2(f[4 * k], f[4 * k + 1]) | (cvt_e4m3x2(f[4 * k + 2], f[4 * k + 3]) << 16);
+      uint4* dst = reinterpret_cast<uint4*>(codes_t + (int64_t)c * M_pad + (int64_t)j * 32);
+      dst[0] = o[0];
+      dst[1] = o[1];
+    } else {
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        ow[k] = cvt_e2m1x2(f[8 * k], f[8 * k + 1]) | (cvt_e2m1x2(f[8 * k + 2], f[8 * k + 3]) << 8) |
+                (cvt_e2m1x2(f[8 * k + 4], f[8 * k + 5]) << 16) |
+                (cvt_e2m1x2(f[8 * k + 6], f[8 * k + 7]) << 24);
+      *reinterpret_cast<uint4*>(codes_t + (int64_t)c * (M_pad / 2) + (int64_t)j * 16) = o;
+    }
+    scales_t[(int64_t)c * (M_pad / 32) + j] = (uint8_t)(valid > 0 ? sc : 0u);
+  }
+}
+
+}  // namespace
+
+int launch_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                               uint8_t* scales, cudaStream_t s) {
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  const int64_t n_chunks = R * C / 8;
+  const int threads = 256;
+  const int64_t want = (n_chunks + threads - 1) / threads;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
+  if (fmt == PGG_FMT_E4M3)
+    mx_quant_rowwise_kernel<kE4M3><<<grid, threads, 0, s>>>(static_cast<const uint4*>(in), codes,
+                                                             scales, n_chunks);
+  else
+    mx_quant_rowwise_kernel<kE2M1><<<grid, threads, 0, s>>>(static_cast<const uint4*>(in), codes,
+                                                             scales, n_chunks);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens,
+                               int G, int fmt, uint8_t* codes_t, uint8_t* scales_t,
+                               int64_t M_pad, int32_t* err, cudaStream_t s) {
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  const int64_t total = (M_pad / 32) * ((C + kColTile - 1) / kColTile);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(total, (int64_t)dev.sms * 8));
+  const size_t smem = 8 * (size_t)(G + 1);
+  auto* x = static_cast<const __nv_bfloat16*>(in);
+  if (fmt == PGG_FMT_E4M3)
+    mx_quant_colwise_kernel<kE4M3><<<grid, kColThreads, smem, s>>>(x, M, (int)C, group_lens, G,
+                                                                   codes_t, scales_t, M_pad, err);
+  else
+    mx_quant_colwise_kernel<kE2M1><<<grid, kColThreads, smem, s>>>(x, M, (int)C, group_lens, G,
+                                                                   codes_t, scales_t, M_pad, err);
+  return cuda_status(cudaGetLastError());
+}
+
 }  // namespace pgg

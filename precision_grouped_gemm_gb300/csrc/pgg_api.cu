@@ -201,7 +201,7 @@ int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8
   if (!in || !codes || !scales) return PGG_ERR_INVALID_ARG;
   if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
   if (R < 0 || R >= kMaxRows || C <= 0 || C >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
-  if (C % (fmt == PGG_FMT_E2M1 ? 64 : 32)) return PGG_ERR_ALIGNMENT;
+  if (C % 32) return PGG_ERR_ALIGNMENT;
   if (!aligned16(in) || !aligned16(codes) || !aligned16(scales)) return PGG_ERR_ALIGNMENT;
   if (R == 0) return PGG_OK;
   return launch_mx_quantize_rowwise(in, R, C, fmt, codes, scales, as_stream(stream));

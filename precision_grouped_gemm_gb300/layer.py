@@ -18,9 +18,11 @@ from __future__ import annotations
 
 import dataclasses
 
+import numpy as np
 import torch
 
 from . import _binding as B
+from . import workloads as wl
 
 STEP_NAMES = ("fc1_fwd_swiglu", "fc2_fwd", "fc2_dgrad_swiglu_bwd", "fc2_wgrad", "fc1_dgrad",
               "fc1_wgrad")
@@ -92,3 +94,35 @@ def layer_work(M: int, G: int, Hd: int, I: int) -> dict:
         "fc1_dgrad": (f1, H + W1b + X + lens),
         "fc1_wgrad": (f1, X + H + W1b + lens),
     }
+
+
+def build_layer_inputs(w, device, cap: int = 0):
+    """Seeded inputs of workload `w` on `device` (only the first `cap` experts when cap > 0).
+
+    X rows are the generated token activations gathered in expert-sorted row order;
+    W1, W2 and dY come straight from the counter-based generator."""
+    lens, row_token = w.group_lens()
+    if cap:
+        lens = lens[:cap].copy()
+        row_token = row_token[:int(lens.sum())]
+    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
+    rt = torch.from_numpy(row_token).to(device)
+    xtok = wl.gen_matrix(wl.KEY_X, w.tokens, Hd, 1.0, w.seed, device=device)
+    X = xtok[rt].contiguous()
+    del xtok
+    W1 = wl.gen_matrix(wl.KEY_W1, G * 2 * I, Hd, w.w_std, w.seed, device=device).view(G, 2 * I, Hd)
+    W2 = wl.gen_matrix(wl.KEY_W2, G * Hd, I, w.w_std, w.seed, device=device).view(G, Hd, I)
+    dY = wl.gen_matrix(wl.KEY_DY, M, Hd, 1.0, w.seed, device=device)
+    gl = torch.from_numpy(np.ascontiguousarray(lens)).to(device)
+    return lens, row_token, ExpertLayerBuffers(X, W1, W2, dY, gl).allocate()
+
+
+def expert_inputs_cpu(w, lens, row_token, e: int):
+    """The same generator values for expert e alone, on the CPU (bf16 tensors)."""
+    off = np.concatenate([[0], np.cumsum(lens)])
+    a, b = int(off[e]), int(off[e + 1])
+    X = wl.gen_bf16(wl.KEY_X, torch.from_numpy(row_token[a:b]), w.hidden, 1.0, w.seed)
+    W1 = wl.gen_matrix(wl.KEY_W1, 2 * w.inter, w.hidden, w.w_std, w.seed, row0=e * 2 * w.inter)
+    W2 = wl.gen_matrix(wl.KEY_W2, w.hidden, w.inter, w.w_std, w.seed, row0=e * w.hidden)
+    dY = wl.gen_matrix(wl.KEY_DY, b - a, w.hidden, 1.0, w.seed, row0=a)
+    return X, W1, W2, dY, (a, b)

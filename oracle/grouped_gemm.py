@@ -130,6 +130,35 @@ def grouped_fc2_dgrad_swiglu_bwd(dY: np.ndarray, W2: np.ndarray, H: np.ndarray, 
     return swiglu_bwd(dA, H)
 
 
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value, ties to even (8 significant bits,
+    normal exponent floor -126, subnormal quantum 2^-133); returns fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)                       # |x| = f * 2^e, f in [0.5, 1)
+    q = np.ldexp(1.0, np.maximum(e, -125) - 8)  # quantum of x's bf16 binade
+    return np.rint(x / q) * q                # rint: round half to even
+
+
+def expert_layer_chain(X, W1, W2, dY, group_lens):
+    """The expert layer fwd + bwd as the library's six calls compute it.
+
+    A, H = FC1+SwiGLU(X); Y = FC2(A); dH = SwiGLU'(dY . W2_g, H); dW2 = dY_g^T A_g;
+    dX = dH . W1_g; dW1 = dH_g^T X_g.  The tensors that one call hands to the next
+    (A, H, dH) are stored in bf16 by the library, so the downstream calls here
+    consume their bf16 roundings; every returned array is the unrounded fp64
+    result of its own call."""
+    Hf = grouped_gemm_fwd(X, W1, group_lens)
+    Af = swiglu_fwd(Hf)
+    A, H = round_bf16(Af), round_bf16(Hf)
+    Y = grouped_gemm_fwd(A, W2, group_lens)
+    dHf = grouped_fc2_dgrad_swiglu_bwd(dY, W2, H, group_lens)
+    dH = round_bf16(dHf)
+    return {"A": Af, "H": Hf, "Y": Y, "dH": dHf,
+            "dW2": grouped_gemm_wgrad(A, dY, group_lens),
+            "dX": grouped_gemm_dgrad(dH, W1, group_lens),
+            "dW1": grouped_gemm_wgrad(X, dH, group_lens)}
+
+
 def rms(x: np.ndarray) -> float:
     x = np.asarray(x, dtype=np.float64)
     return float(np.sqrt(np.mean(x * x))) if x.size else 0.0

@@ -48,6 +48,7 @@ _IH4_SD = 37837.23  # standard deviation of the sum of four uniform 16-bit integ
 
 # tensor keys: distinct integers per logical tensor
 KEY_X, KEY_W1, KEY_W2, KEY_DY, KEY_DA, KEY_H, KEY_LOGITS = 11, 12, 13, 14, 15, 16, 17
+KEY_A, KEY_DH = 18, 19
 
 
 def _mul32(x: torch.Tensor, c: int) -> torch.Tensor:

@@ -386,3 +386,39 @@ def _colwise_grid(rng, fmt, lens, C):
         parts.append(v)
     vals = np.concatenate(parts, axis=0)
     return _bf16_bits(vals), vals
+
+
+def test_round_bf16_matches_torch_cast():
+    # fp32 inputs make torch's fp32 -> bf16 cast a single RNE rounding, the same rule
+    rng = np.random.default_rng(21)
+    v = (rng.standard_normal(50000) * np.ldexp(1.0, rng.integers(-140, 120, 50000))).astype(np.float32)
+    # exact ties: bf16 midpoints (9 significant bits with the last one set)
+    m = rng.integers(256, 512, 5000) * 2 + 1
+    ties = np.ldexp(m.astype(np.float64), rng.integers(-120, 100, 5000)).astype(np.float32)
+    v = np.concatenate([v, ties, -ties, np.float32([0.0, -0.0, 2.0 ** -133, 2.0 ** -134, 3 * 2.0 ** -134])])
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(og.round_bf16(v.astype(np.float64)), ref)
+
+
+def test_layer_chain_matches_step_by_step():
+    rng = np.random.default_rng(22)
+    lens = np.array([9, 0, 14], dtype=np.int32)
+    M, Hd, I = 23, 16, 8
+    X, dY = rng.standard_normal((M, Hd)), rng.standard_normal((M, Hd))
+    W1, W2 = rng.standard_normal((3, 2 * I, Hd)) * 0.3, rng.standard_normal((3, Hd, I)) * 0.3
+    out = og.expert_layer_chain(X, W1, W2, dY, lens)
+    Yb, _, _ = _brute(X, W1, np.zeros((M, 2 * I)), lens)
+    np.testing.assert_allclose(out["H"], Yb, rtol=1e-12, atol=1e-12)
+    g, u = Yb[:, :I], Yb[:, I:]
+    np.testing.assert_allclose(out["A"], g / (1 + np.exp(-g)) * u, rtol=1e-12, atol=1e-12)
+    # downstream calls consume the bf16 roundings of A, H and dH
+    A16, H16 = og.round_bf16(out["A"]), og.round_bf16(out["H"])
+    Y2, _, dW2 = _brute(A16, W2, dY, lens)
+    np.testing.assert_allclose(out["Y"], Y2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["dW2"], dW2, rtol=1e-12, atol=1e-12)
+    _, dA, _ = _brute(np.zeros((M, I)), W2, dY, lens)
+    np.testing.assert_allclose(out["dH"], og.swiglu_bwd(dA, H16), rtol=1e-12, atol=1e-12)
+    dH16 = og.round_bf16(out["dH"])
+    _, dXb, dW1b = _brute(X, W1, dH16, lens)
+    np.testing.assert_allclose(out["dX"], dXb, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out["dW1"], dW1b, rtol=1e-12, atol=1e-12)

@@ -172,8 +172,9 @@ int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t*
  *                   deq(A)[:, r] deq(B)[:, r]^T with A = dY column-wise
  *                   codes [N, M_pad], B = X column-wise codes [K, M_pad]
  *                   (pgg_mx_quantize_colwise); empty groups give 0.
- * Sizes: the reduction axis is a multiple of 128 (fwd K, dgrad N); N, K
- * multiples of 32 elsewhere; e2m1 codes are packed two per byte. */
+ * Sizes: the reduction axis is a multiple of 128 (fwd K, dgrad N); the other
+ * dimensions are multiples of 8 (N of a SwiGLU forward a multiple of 16); e2m1
+ * codes are packed two per byte.  fp32 accumulation, bf16 output. */
 int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const uint8_t* SA,
                         const uint8_t* B, const uint8_t* SB, const void* H,
                         const int32_t* group_lens, void* out, void* out2, int64_t M, int64_t N,

@@ -1,0 +1,181 @@
+// Epilogues shared by the grouped GEMM kernels: drain one accumulator tile
+// from TMEM (tcgen05.ld, 32 lanes x 32 fp32 columns per load) and write bf16.
+//
+// Thread (warp quarter q, lane) owns accumulator row q*32 + lane; `tb` is the
+// TMEM address of that warp's lane quarter at the tile's first column.
+#pragma once
+#include "ptx.cuh"
+
+namespace pgg {
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+// Store 32 consecutive fp32 values of one row as bf16 at dst[0..31], columns
+// limited to ncols (<= 32).  16-byte vector stores when the chunk is whole.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v, int ncols) {
+  if (ncols >= 32) {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+      d4[q] = w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) dst[j] = __float2bfloat16_rn(v[j]);
+  }
+}
+
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v, int ncols) {
+  if (ncols >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w = __ldg(s4 + q);
+      v[q * 8 + 0] = bf16_lo(w.x); v[q * 8 + 1] = bf16_hi(w.x);
+      v[q * 8 + 2] = bf16_lo(w.y); v[q * 8 + 3] = bf16_hi(w.y);
+      v[q * 8 + 4] = bf16_lo(w.z); v[q * 8 + 5] = bf16_hi(w.z);
+      v[q * 8 + 6] = bf16_lo(w.w); v[q * 8 + 7] = bf16_hi(w.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = j < ncols ? __bfloat162float(src[j]) : 0.0f;
+  }
+}
+
+// Plain store: row `dst_row` (already offset to this thread's output row),
+// accumulator columns 0..BN-1 -> output columns col0.., bounded by ncols.
+template <int BN>
+__device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* dst_row, bool row_ok, int col0,
+                                          int ncols) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t rv[32];
+    tmem_ld32(tb + c * 32, rv);
+    tmem_ld_wait();
+    const int c0 = col0 + c * 32;
+    if (row_ok && c0 < ncols) {
+      float v[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rv[j]);
+      store_row32(dst_row + c0, v, min(32, ncols - c0));
+    }
+  }
+}
+
+// FC1 SwiGLU: accumulator columns [0, BN/2) are gate columns col0.., [BN/2, BN)
+// the matching up columns.  A[row, col0 + c] = silu(gate) * up (fp32), and the
+// pre-activation H[row, col0 + c] = gate, H[row, I + col0 + c] = up when H != null.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t grow,
+                                           bool row_ok, int col0, int I) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 64; ++c) {
+    uint32_t rg[32], ru[32];
+    tmem_ld32(tb + c * 32, rg);
+    tmem_ld32(tb + BN / 2 + c * 32, ru);
+    tmem_ld_wait();
+    const int c0 = col0 + c * 32;
+    if (row_ok && c0 < I) {
+      float g[32], u[32], a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        g[j] = __uint_as_float(rg[j]);
+        u[j] = __uint_as_float(ru[j]);
+        a[j] = silu_f(g[j]) * u[j];
+      }
+      const int nc = min(32, I - c0);
+      store_row32(A + grow * I + c0, a, nc);
+      if (H) {
+        store_row32(H + grow * (2 * (size_t)I) + c0, g, nc);
+        store_row32(H + grow * (2 * (size_t)I) + I + c0, u, nc);
+      }
+    }
+  }
+}
+
+// FC2 dgrad + SwiGLU backward: accumulator = dA[row, col0 ..]; with g, u from
+// the saved H: dH[:, c] = dA u s (1 + g (1 - s)), dH[:, I + c] = dA g s, s = sigmoid(g).
+template <int BN>
+__device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
+                                               size_t grow, bool row_ok, int col0, int I) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t rd[32];
+    tmem_ld32(tb + c * 32, rd);
+    tmem_ld_wait();
+    const int c0 = col0 + c * 32;
+    if (row_ok && c0 < I) {
+      const int nc = min(32, I - c0);
+      float hg[32], hu[32], dg[32], du[32];
+      load_row32(H + grow * (2 * (size_t)I) + c0, hg, nc);
+      load_row32(H + grow * (2 * (size_t)I) + I + c0, hu, nc);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float da = __uint_as_float(rd[j]);
+        const float s = 1.0f / (1.0f + __expf(-hg[j]));
+        dg[j] = da * hu[j] * s * (1.0f + hg[j] * (1.0f - s));
+        du[j] = da * hg[j] * s;
+      }
+      store_row32(dH + grow * (2 * (size_t)I) + c0, dg, nc);
+      store_row32(dH + grow * (2 * (size_t)I) + I + c0, du, nc);
+    }
+  }
+}
+
+// Full-tile store through shared memory and TMA: this warp's 32 rows go out as
+// 32 x 64 bf16 boxes (4 KB, 128B-swizzled) staged in two alternating buffers
+// at `stg`, written by bulk tensor stores of the 3-D map {cols, rows, G} at
+// (col0 + 64 c, row0, g) that clip at the tensor bounds.  zero: write zeros
+// without touching TMEM.  A box starting past rows_total / cols_total is
+// skipped (warp-uniform), keeping one committed store per used buffer.
+template <int BN>
+__device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8_t* stg, int& nstore,
+                                                   const CUtensorMap* tmC, int row0, int col0, int g,
+                                                   int rows_total, int cols_total, int lane) {
+#pragma unroll 1
+  for (int c = 0; c < BN / 64; ++c) {
+    if (row0 >= rows_total || col0 + c * 64 >= cols_total) continue;
+    uint32_t ra[32], rb[32];
+    if (!zero) {
+      tmem_ld32(tb + c * 64, ra);
+      tmem_ld32(tb + c * 64 + 32, rb);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) { ra[j] = 0u; rb[j] = 0u; }
+    }
+    uint8_t* sb = stg + (nstore & 1) * 4096;
+    if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t* v = j < 4 ? &ra[j * 8] : &rb[(j - 4) * 8];
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+      w.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+      w.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+      w.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+      *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmC, smem_u32(sb), col0 + c * 64, row0, g);
+      bulk_commit();
+    }
+    ++nstore;
+  }
+}
+
+}  // namespace pgg

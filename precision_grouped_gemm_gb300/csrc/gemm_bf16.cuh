@@ -20,19 +20,15 @@
 // double-buffered fp32 accumulator (2 x BN TMEM columns) with tcgen05.ld and
 // store bf16 results bounded to the tile's group.  Persistent: one CTA per SM.
 #pragma once
+#include "epilogue.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
 namespace pgg {
 
-enum GemmMode : int { kFwd = 0, kDgrad = 1, kWgrad = 2 };
-enum GemmEpi : int { kEpiStore = 0, kEpiSwiGLU = 1, kEpiSwiGLUBwd = 2 };
-
 constexpr int kBM = 128;          // MMA M (TMEM lanes)
 constexpr int kBK = 64;           // reduction step per stage: one 128-byte swizzle atom of bf16
 constexpr int kGemmThreads = 192;
-constexpr int kErrBadGroupLens = 16;
-constexpr int kErrTimeout = 17;
 
 struct GemmArgs {
   const int32_t* group_lens;
@@ -108,51 +104,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int3
     T.red_valid = a.red;
   }
   return T;
-}
-
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  bool ok = mbar_wait(bar, parity, abort);
-  return __all_sync(0xffffffffu, ok);
-}
-
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
-
-// Store 32 consecutive fp32 values of one row as bf16 at dst[0..31], columns
-// limited to ncols (<= 32).  16-byte vector stores when the chunk is whole.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v, int ncols) {
-  if (ncols >= 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-      d4[q] = w;
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < ncols) dst[j] = __float2bfloat16_rn(v[j]);
-  }
-}
-
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v, int ncols) {
-  if (ncols >= 32) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w = __ldg(s4 + q);
-      v[q * 8 + 0] = bf16_lo(w.x); v[q * 8 + 1] = bf16_hi(w.x);
-      v[q * 8 + 2] = bf16_lo(w.y); v[q * 8 + 3] = bf16_hi(w.y);
-      v[q * 8 + 4] = bf16_lo(w.z); v[q * 8 + 5] = bf16_hi(w.z);
-      v[q * 8 + 6] = bf16_lo(w.w); v[q * 8 + 7] = bf16_hi(w.w);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < ncols ? __bfloat162float(src[j]) : 0.0f;
-  }
 }
 
 template <int MODE, int EPI, int BN, int STAGES>
@@ -360,49 +311,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
-        // rows q*32..q*32+31 of the tile go out as 32 x 64 bf16 boxes through a
-        // 128B-swizzled staging buffer and a bulk tensor store (clipped at N, K)
-        const bool zero = T.nkb == 0;  // empty group: dW_g = 0
+        const bool zero = T.nkb == 0;  // empty group: dW_g = 0, no accumulator
         if (!zero) {
           if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
           tc_fence_after();
         }
-        const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          // a box that starts past N or K holds nothing to store (warp-uniform test);
-          // skipping it keeps one committed store per used staging buffer
-          if (T.row0 + q * 32 >= args.wg_rows || T.col0 + c * 64 >= args.out_cols) continue;
-          uint32_t ra[32], rb[32];
-          if (!zero) {
-            tmem_ld32(tb + c * 64, ra);
-            tmem_ld32(tb + c * 64 + 32, rb);
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) { ra[j] = 0u; rb[j] = 0u; }
-          }
-          uint8_t* sb = stg + (nstore & 1) * 4096;
-          if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t* v = j < 4 ? &ra[j * 8] : &rb[(j - 4) * 8];
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
-            w.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
-            w.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
-            w.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
-            *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmC, smem_u32(sb), T.col0 + c * 64, T.row0 + q * 32, T.g);
-            bulk_commit();
-          }
-          ++nstore;
-        }
+        epi_tma_store_rows<BN>(tmem_base + acc * BN + ((uint32_t)(q * 32) << 16), zero, stg, nstore,
+                               &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, args.out_cols, lane);
         if (!zero) {
           tc_fence_before();
           mbar_arrive(smem_u32(&tempty[acc]));
@@ -410,92 +325,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         continue;
       }
-      if (MODE == kWgrad && T.nkb == 0) {
-        if (row_ok) {
-          float zero[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) zero[j] = 0.0f;
-          __nv_bfloat16* dst = out + ((size_t)T.g * args.wg_rows + T.row0 + r) * args.out_cols;
-          for (int c = 0; c < BN / 32; ++c) {
-            const int c0 = T.col0 + c * 32;
-            if (c0 < args.out_cols) store_row32(dst + c0, zero, min(32, args.out_cols - c0));
-          }
-        }
-        continue;
-      }
       if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+      const size_t grow = (size_t)T.row0 + r;
       if (EPI == kEpiSwiGLU) {
-        const int I = args.I;
-        __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(args.out2);
-        const size_t grow = (size_t)T.row0 + r;
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          uint32_t rg[32], ru[32];
-          tmem_ld32(tb + c * 32, rg);
-          tmem_ld32(tb + BN / 2 + c * 32, ru);
-          tmem_ld_wait();
-          const int c0 = T.col0 + c * 32;
-          if (row_ok && c0 < I) {
-            float g[32], u[32], a[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              g[j] = __uint_as_float(rg[j]);
-              u[j] = __uint_as_float(ru[j]);
-              a[j] = silu_f(g[j]) * u[j];
-            }
-            const int nc = min(32, I - c0);
-            store_row32(out + grow * I + c0, a, nc);
-            if (H) {
-              store_row32(H + grow * (2 * (size_t)I) + c0, g, nc);
-              store_row32(H + grow * (2 * (size_t)I) + I + c0, u, nc);
-            }
-          }
-        }
+        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
       } else if (EPI == kEpiSwiGLUBwd) {
-        const int I = args.I;
-        const __nv_bfloat16* H = reinterpret_cast<const __nv_bfloat16*>(args.aux);
-        const size_t grow = (size_t)T.row0 + r;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t rd[32];
-          tmem_ld32(tb + c * 32, rd);
-          tmem_ld_wait();
-          const int c0 = T.col0 + c * 32;
-          if (row_ok && c0 < I) {
-            const int nc = min(32, I - c0);
-            float hg[32], hu[32], dg[32], du[32];
-            load_row32(H + grow * (2 * (size_t)I) + c0, hg, nc);
-            load_row32(H + grow * (2 * (size_t)I) + I + c0, hu, nc);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float da = __uint_as_float(rd[j]);
-              const float s = 1.0f / (1.0f + __expf(-hg[j]));
-              dg[j] = da * hu[j] * s * (1.0f + hg[j] * (1.0f - s));
-              du[j] = da * hg[j] * s;
-            }
-            store_row32(out + grow * (2 * (size_t)I) + c0, dg, nc);
-            store_row32(out + grow * (2 * (size_t)I) + I + c0, du, nc);
-          }
-        }
+        epi_swiglu_bwd<BN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
+                           args.I);
       } else {
-        __nv_bfloat16* dst;
-        if (MODE == kWgrad) dst = out + ((size_t)T.g * args.wg_rows + T.row0 + r) * args.out_cols;
-        else dst = out + ((size_t)T.row0 + r) * args.out_cols;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t rv[32];
-          tmem_ld32(tb + c * 32, rv);
-          tmem_ld_wait();
-          const int c0 = T.col0 + c * 32;
-          if (row_ok && c0 < args.out_cols) {
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rv[j]);
-            store_row32(dst + c0, v, min(32, args.out_cols - c0));
-          }
-        }
+        epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));

@@ -1,6 +1,479 @@
-// Block-scaled (MX) grouped GEMM.
+// Block-scaled (MX) grouped GEMM on tcgen05: e4m3 x e4m3 (kind::mxf8f6f4,
+// scale_vec::1X) and packed e2m1 x e2m1 (kind::mxf4, scale_vec::2X), UE8M0
+// scales per 32-element block of the reduction axis, fp32 accumulation in TMEM,
+// bf16 output ("Primus-Turbo" README, "What's New": MXFP8 / MXFP4 grouped GEMM;
+// Pull Request #891, "Changes": MXFP4 grouped GEMM on float4_e2m1fn_x2 buffers).
+//
+// Both operands are K-major along the reduction axis (the quantizers write them
+// that way), tiles are 128 x 128 with a 128-element k-block: 128 bytes per row
+// with the 128-byte swizzle for e4m3, 64 bytes with the 64-byte swizzle for
+// packed e2m1.  The producer warp loads codes with TMA and gathers the k-block's
+// scale factors with 4-byte cp.async straight into the 512-byte atom the MMA
+// wants (row m's 4 scales at byte 16 (m % 32) + 4 (m / 32)); the MMA warp copies
+// each atom into TMEM with tcgen05.cp (32x128b, replicated to the four lane
+// quarters) and issues the block-scaled MMAs selecting scale bytes by ID.
+//
+//   fwd    out[M, N]    = A[M, K] . B_g[N, K]^T     A = X rows, B = W [G, N, K]
+//   dgrad  out[M, K]    = A[M, N] . Bt_g[K, N]^T    Bt = W^T [K, G*N] (blocks along N)
+//   wgrad  out[G, N, K] = At_g[N, .] . Bt_g[K, .]^T over group g's padded columns of
+//                         the column-wise operands At = dY^T [N, M_pad], Bt = X^T [K, M_pad]
+#include <algorithm>
+
+#include "epilogue.cuh"
 #include "internal.h"
+#include "ptx.cuh"
+#include "sched.cuh"
 
 namespace pgg {
-int launch_mx_gemm(const MxCall&) { return PGG_ERR_UNSUPPORTED; }
+namespace {
+
+constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
+constexpr int kMxThreads = 192;
+constexpr int kE4M3 = 1;
+
+struct MxArgs {
+  const int32_t* group_lens;
+  int G;
+  int64_t M;
+  const uint8_t* SA;      // scale tensors, row-major [rows, red/32]
+  const uint8_t* SB;
+  int64_t sa_ld, sb_ld;   // scale row strides (bytes)
+  int a_rows, b_rows;     // rows of the A / B scale tensors that exist (zero-filled beyond)
+  int out_cols;           // fwd N (or I with SwiGLU), dgrad K, wgrad K
+  int red;                // fwd K / dgrad N (elements)
+  int wg_rows;            // wgrad N
+  int nw;                 // fwd: rows of W per group (N or 2I)
+  int I;
+  void* out;
+  void* out2;
+  const void* aux;
+  int32_t* err;
+  int64_t M_pad;
+};
+
+template <int FMT>
+struct MxCfg {
+  static constexpr int kRowBytes = FMT == kE4M3 ? 128 : 64;       // bytes per row per k-block
+  static constexpr uint32_t kSwizzle = FMT == kE4M3 ? kSwizzle128B : kSwizzle64B;
+  static constexpr uint32_t kSbo = 8 * kRowBytes;                 // 8-row swizzle atom
+  static constexpr int kMmas = FMT == kE4M3 ? 4 : 2;              // MMAs per k-block
+  static constexpr uint32_t kElem = FMT == kE4M3 ? 0 : 1;         // idesc element type code
+  static constexpr int kTileBytes = 128 * kRowBytes;
+};
+
+template <int FMT, int STAGES, int EPI_BYTES>
+struct MxSmem {
+  static constexpr int kA = MxCfg<FMT>::kTileBytes;
+  static constexpr int kB = MxCfg<FMT>::kTileBytes;
+  static constexpr int kSF = 1024;  // SFA atom (512 B) + SFB atom (512 B)
+  static constexpr int kStage = kA + kB + kSF;
+  static constexpr int kEpiOff = STAGES * kStage;
+  static constexpr int kBarOff = kEpiOff + EPI_BYTES;
+  static constexpr int kGroupOff = kBarOff + 256;
+  static constexpr size_t bytes(int G) { return 1024 + (size_t)kGroupOff + 12 * (size_t)(G + 1) + 16; }
+};
+
+struct MxTile {
+  int g, row0, rows, col0, nkb, poff;
+};
+
+template <int MODE, int EPI>
+__device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? kMxBN / 2 : kMxBN; }
+
+template <int MODE, int EPI>
+__device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_t* s_off,
+                                            const int32_t* s_tile, const int32_t* s_poff) {
+  MxTile T;
+  const int g = find_group(s_tile, a.G, t);
+  const int local = t - s_tile[g];
+  const int len = s_off[g + 1] - s_off[g];
+  T.g = g;
+  T.poff = s_poff[g];
+  if (MODE == kWgrad) {
+    const int nrt = (a.wg_rows + kMxBM - 1) / kMxBM;
+    T.row0 = (local % nrt) * kMxBM;
+    T.rows = min(kMxBM, a.wg_rows - T.row0);
+    T.col0 = (local / nrt) * kMxBN;
+    T.nkb = (len + kMxBK - 1) / kMxBK;
+  } else {
+    const int nmt = (len + kMxBM - 1) / kMxBM;
+    const int mt = local % nmt;
+    T.row0 = s_off[g] + mt * kMxBM;
+    T.rows = min(kMxBM, len - mt * kMxBM);
+    T.col0 = (local / nmt) * mx_tile_cols<MODE, EPI>();
+    T.nkb = (a.red + kMxBK - 1) / kMxBK;
+  }
+  return T;
+}
+
+template <int FMT, int MODE, int EPI, int STAGES>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
+  using C = MxCfg<FMT>;
+  using L = MxSmem<FMT, STAGES, MODE == kWgrad ? 32768 : 0>;
+  constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, kMxBN);
+  constexpr uint32_t kTmemCols = 512;
+  constexpr uint32_t kSfCol0 = 2 * kMxBN;  // scale-factor columns after the two accumulators
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
+  int32_t* s_tile = s_off + (args.G + 1);
+  int32_t* s_poff = s_tile + (args.G + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1 + 32);  // expect_tx arrive + 32 cp.async arrives
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *s_abort = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(s_tmem), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 2) {
+    TileCount tc;
+    if (MODE == kWgrad) {
+      tc.bm = 0;
+      tc.per_row_tile = ((args.wg_rows + kMxBM - 1) / kMxBM) * ((args.out_cols + kMxBN - 1) / kMxBN);
+    } else {
+      constexpr int tcw = EPI == kEpiSwiGLU ? kMxBN / 2 : kMxBN;
+      tc.bm = kMxBM;
+      tc.per_row_tile = (args.out_cols + tcw - 1) / tcw;
+    }
+    bool bad = scan_groups(args.group_lens, args.G, args.M, tc, s_off, s_tile, s_poff, kMxBK, lane);
+    int code = bad ? kErrBadGroupLens : 0;
+    if (!bad && MODE == kWgrad && (int64_t)s_poff[args.G] > args.M_pad) code = kErrPadOverflow;
+    if (lane == 0) {
+      *s_bad = code;
+      if (code && blockIdx.x == 0) set_error(args.err, code);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = *s_tmem;
+  const int total_tiles = *s_bad ? 0 : s_tile[args.G];
+  const uint32_t smem0 = smem_u32(smem);
+  bool aborted = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer: TMA codes + cp.async scales
+    int stage = 0;
+    uint32_t phase = 0;
+    long long issued = 0;
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff);
+      for (int kb = 0; kb < T.nkb; ++kb) {
+        if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
+        const uint32_t sa = smem0 + stage * L::kStage;
+        const uint32_t sb = sa + L::kA;
+        const uint32_t ssf = sb + L::kB;
+        const uint32_t fb = smem_u32(&full[stage]);
+        const int kbyte = kb * C::kRowBytes;  // byte offset of this k-block along a row
+        if (lane == 0) {
+          mbar_arrive_expect_tx(fb, L::kA + L::kB);
+          if (MODE == kFwd) {
+            tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
+            if (EPI == kEpiSwiGLU) {
+              tma_load_3d(sb, &tmB, fb, kbyte, T.col0, T.g);
+              tma_load_3d(sb + 64 * C::kRowBytes, &tmB, fb, kbyte, args.I + T.col0, T.g);
+            } else {
+              tma_load_3d(sb, &tmB, fb, kbyte, T.col0, T.g);
+            }
+          } else if (MODE == kDgrad) {
+            tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
+            tma_load_2d(sb, &tmB, fb, T.g * (args.red / kMxBK) * C::kRowBytes + kbyte, T.col0);
+          } else {
+            const int pb = (T.poff / kMxBK) * C::kRowBytes + kbyte;
+            tma_load_2d(sa, &tmA, fb, pb, T.row0);
+            tma_load_2d(sb, &tmB, fb, pb, T.col0);
+          }
+        }
+        // scale factors: lane l fetches rows l, l+32, l+64, l+96 of each operand tile
+        // (4 bytes = the k-block's 4 block scales) into word 4 l + i of the atom
+        int sfa_col, sfb_col;  // byte column of this k-block in the scale tensors
+        if (MODE == kWgrad) {
+          sfa_col = sfb_col = T.poff / 32 + kb * 4;
+        } else if (MODE == kDgrad) {
+          sfa_col = kb * 4;
+          sfb_col = T.g * (args.red / 32) + kb * 4;
+        } else {
+          sfa_col = sfb_col = kb * 4;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int m = lane + 32 * i;
+          // A rows: fwd/dgrad token rows; wgrad rows of dY^T (n)
+          const int ar = T.row0 + m;
+          const bool aok = ar < args.a_rows;
+          cp_async_4(ssf + (lane * 4 + i) * 4, args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0),
+                     aok ? 4u : 0u);
+          // B rows
+          int br;
+          bool bok;
+          if (MODE == kFwd) {
+            const int n = (EPI == kEpiSwiGLU) ? (m < 64 ? T.col0 + m : args.I + T.col0 + (m - 64))
+                                              : T.col0 + m;
+            const int lim = (EPI == kEpiSwiGLU) ? (m < 64 ? args.I : 2 * args.I) : args.nw;
+            bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m & 63) < args.I);
+            br = T.g * args.nw + n;
+          } else {
+            br = T.col0 + m;
+            bok = br < args.b_rows;
+          }
+          cp_async_4(ssf + 512 + (lane * 4 + i) * 4, args.SB + (bok ? (int64_t)br * args.sb_ld + sfb_col : 0),
+                     bok ? 4u : 0u);
+        }
+        cp_async_arrive_noinc(fb);
+        __syncwarp();
+        ++issued;
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (aborted && lane == 0) {
+      long long n = issued < STAGES ? issued : STAGES;
+      int s = stage;
+      uint32_t p = phase;
+      for (long long i = 0; i < n; ++i) {
+        if (--s < 0) { s = STAGES - 1; p ^= 1u; }
+        mbar_wait(smem_u32(&full[s]), p, nullptr, kDrainTimeoutNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff);
+      if (T.nkb == 0) continue;
+      if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * kMxBN;
+      for (int kb = 0; kb < T.nkb; ++kb) {
+        if (!warp_wait(smem_u32(&full[stage]), phase, s_abort)) { aborted = true; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t sa = smem0 + stage * L::kStage;
+          const uint32_t sb = sa + L::kA;
+          const uint32_t ssf = sb + L::kB;
+          const uint32_t sfa_t = tmem_base + kSfCol0 + stage * 8;
+          const uint32_t sfb_t = sfa_t + 4;
+          fence_proxy_async_smem();  // cp.async-written scales -> async proxy
+          tmem_cp_32x128b_x4(sfa_t, smem_desc(ssf, 0, 128, kSwizzleNone));
+          tmem_cp_32x128b_x4(sfb_t, smem_desc(ssf + 512, 0, 128, kSwizzleNone));
+#pragma unroll
+          for (int j = 0; j < C::kMmas; ++j) {
+            const uint64_t ad = smem_desc(sa + j * 32, 16, C::kSbo, C::kSwizzle);
+            const uint64_t bd = smem_desc(sb + j * 32, 16, C::kSbo, C::kSwizzle);
+            const uint32_t sfid = FMT == kE4M3 ? (uint32_t)j : (uint32_t)(2 * j);
+            const uint32_t id = kIdesc | idesc_sf_ids(sfid, sfid);
+            if (FMT == kE4M3) mma_mxf8(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || j > 0) ? 1u : 0u);
+            else mma_mxf4(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&empty[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (aborted) break;
+      if (lane == 0) mma_commit(smem_u32(&tfull[acc]));
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+    if (aborted && lane == 0) {
+      mma_commit(smem_u32(drain));
+      mbar_wait(smem_u32(drain), 0, nullptr, kDrainTimeoutNs);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 8192;
+    int nstore = 0;
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff);
+      const bool row_ok = r < T.rows;
+      if (MODE == kWgrad) {
+        const bool zero = T.nkb == 0;
+        if (!zero) {
+          if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+          tc_fence_after();
+        }
+        epi_tma_store_rows<kMxBN>(tmem_base + acc * kMxBN + ((uint32_t)(q * 32) << 16), zero, stg, nstore,
+                                  &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, args.out_cols, lane);
+        if (!zero) {
+          tc_fence_before();
+          mbar_arrive(smem_u32(&tempty[acc]));
+          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        continue;
+      }
+      if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + acc * kMxBN + ((uint32_t)(q * 32) << 16);
+      const size_t grow = (size_t)T.row0 + r;
+      if (EPI == kEpiSwiGLU) {
+        epi_swiglu<kMxBN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
+      } else if (EPI == kEpiSwiGLUBwd) {
+        epi_swiglu_bwd<kMxBN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
+                              args.I);
+      } else {
+        epi_store<kMxBN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[acc]));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  if (MODE == kWgrad && warp >= 2 && lane == 0) bulk_wait<0>();
+  if (aborted && lane == 0) set_error(args.err, kErrTimeout);
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <int FMT, int MODE, int EPI, int STAGES>
+int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a, int grid,
+           cudaStream_t s) {
+  using L = MxSmem<FMT, STAGES, MODE == kWgrad ? 32768 : 0>;
+  auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)L::bytes(kMaxGroups));
+    if (e != cudaSuccess) return cuda_status(e);
+    attr_done = true;
+  }
+  kern<<<grid, kMxThreads, L::bytes(a.G), s>>>(ta, tb, tc, a);
+  return cuda_status(cudaGetLastError());
+}
+
+template <int FMT>
+int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const MxArgs& a, int grid, cudaStream_t s) {
+  constexpr int kS = FMT == kE4M3 ? 6 : 8;       // stages for fwd / dgrad
+  constexpr int kSw = FMT == kE4M3 ? 5 : 8;      // wgrad keeps 32 KB for its TMA-store staging
+  if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS>(ta, tb, tc, a, grid, s);
+  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw>(ta, tb, tc, a, grid, s);
+  return PGG_ERR_INVALID_ARG;
+}
+
+int cdiv(int64_t x, int64_t y) { return (int)((x + y - 1) / y); }
+
+}  // namespace
+
+int launch_mx_gemm(const MxCall& c) {
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  const bool e4 = c.fmt == PGG_FMT_E4M3;
+  const uint32_t rb = e4 ? 128 : 64;  // bytes per row per 128-element k-block
+  auto bytes = [&](int64_t elems) { return (uint64_t)(e4 ? elems : elems / 2); };
+  const auto sw = e4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUtensorMap ta, tb, tc;
+  MxArgs a{};
+  a.group_lens = c.group_lens;
+  a.G = c.G;
+  a.M = c.M;
+  a.SA = c.SA;
+  a.SB = c.SB;
+  a.out = c.out;
+  a.out2 = c.out2;
+  a.aux = c.H;
+  a.err = c.err;
+  a.M_pad = c.M_pad;
+  int tiles_ub;
+  if (c.mode == 0) {
+    const int64_t N = c.N, K = c.K;
+    uint64_t da[2] = {bytes(K), (uint64_t)c.M}, sa[1] = {bytes(K)};
+    uint32_t ba[2] = {rb, 128};
+    uint64_t db[3] = {bytes(K), (uint64_t)N, (uint64_t)c.G}, sb[2] = {bytes(K), bytes(K) * (uint64_t)N};
+    uint32_t bb[3] = {rb, c.epi ? 64u : 128u, 1};
+    if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, ba, sw))) return st;
+    if ((st = encode_tmap(&tb, u8, 3, c.B, db, sb, bb, sw))) return st;
+    a.sa_ld = a.sb_ld = K / 32;
+    a.a_rows = (int)c.M;
+    a.nw = (int)N;
+    a.I = (int)(N / 2);
+    a.out_cols = (int)(c.epi ? N / 2 : N);
+    a.red = (int)K;
+    tiles_ub = (cdiv(c.M, kMxBM) + c.G) * cdiv(a.out_cols, c.epi ? kMxBN / 2 : kMxBN);
+  } else if (c.mode == 1) {
+    const int64_t N = c.N, K = c.K;
+    uint64_t da[2] = {bytes(N), (uint64_t)c.M}, sa[1] = {bytes(N)};
+    uint64_t db[2] = {bytes(N) * (uint64_t)c.G, (uint64_t)K}, sb[1] = {bytes(N) * (uint64_t)c.G};
+    uint32_t bx[2] = {rb, 128};
+    if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
+    if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bx, sw))) return st;
+    a.sa_ld = N / 32;
+    a.sb_ld = c.G * N / 32;
+    a.a_rows = (int)c.M;
+    a.b_rows = (int)K;
+    a.I = (int)K;
+    a.out_cols = (int)K;
+    a.red = (int)N;
+    tiles_ub = (cdiv(c.M, kMxBM) + c.G) * cdiv(K, kMxBN);
+  } else {
+    const int64_t N = c.N, K = c.K, Mp = c.M_pad;
+    uint64_t da[2] = {bytes(Mp), (uint64_t)N}, sa[1] = {bytes(Mp)};
+    uint64_t db[2] = {bytes(Mp), (uint64_t)K}, sb[1] = {bytes(Mp)};
+    uint32_t bx[2] = {rb, 128};
+    if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
+    if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bx, sw))) return st;
+    uint64_t dc[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)c.G}, sc[2] = {(uint64_t)K * 2, (uint64_t)(N * K * 2)};
+    uint32_t bc[3] = {64, 32, 1};
+    if ((st = encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.out, dc, sc, bc,
+                          CU_TENSOR_MAP_SWIZZLE_128B)))
+      return st;
+    a.sa_ld = a.sb_ld = Mp / 32;
+    a.a_rows = (int)N;
+    a.b_rows = (int)K;
+    a.out_cols = (int)K;
+    a.wg_rows = (int)N;
+    tiles_ub = c.G * cdiv(N, kMxBM) * cdiv(K, kMxBN);
+  }
+  if (c.mode != 2) tc = ta;  // unused outside wgrad
+  const int grid = std::max(1, std::min(dev.sms, tiles_ub));
+  return e4 ? dispatch_mx<kE4M3>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream)
+            : dispatch_mx<2>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream);
+}
+
 }  // namespace pgg

@@ -236,8 +236,9 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
   if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
       (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
-  if ((st = check_dim(N, 32)) || (st = check_dim(K, 32))) return st;
-  if (mode == PGG_MODE_FWD && K % 128) return PGG_ERR_ALIGNMENT;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
+    return PGG_ERR_ALIGNMENT;
   if (mode == PGG_MODE_DGRAD && N % 128) return PGG_ERR_ALIGNMENT;
   if (mode == PGG_MODE_WGRAD && (M_pad <= 0 || M_pad % PGG_MX_PAD || M_pad >= kMaxRows))
     return PGG_ERR_ALIGNMENT;

@@ -187,6 +187,50 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Block-scaled MMAs: D[tmem] (+)= (A * sfA) (B * sfB)^T with UE8M0 scale factors
+// read from TMEM.  mxf8f6f4 + scale_vec::1X: K = 32 per instruction (one scale per
+// row); mxf4 + scale_vec::2X: K = 64 packed e2m1 (two scales per row).
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared -> tensor memory copy of a 32-row x 128-bit matrix, replicated into all
+// four 32-lane quarters (the layout block-scaled MMAs read scale factors from).
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (zero-filled when src_bytes == 0), and
+// an arrive on `bar` once all of this thread's prior cp.async copies complete
+// (no increment of the barrier's expected count).
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // ---------------------------------------------------------------- descriptors
 // Shared-memory matrix descriptor (tcgen05 format): start>>4 in [0,14), leading
 // byte offset>>4 in [16,30), stride byte offset>>4 in [32,46), fixed 0b001 in
@@ -212,6 +256,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
          | (1u << 10)                   // B format: bf16
          | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor for the block-scaled kinds (fp32 D implied): A/B element
+// type codes (mxf8f6f4: e4m3 = 0; mxf4: e2m1 = 1), K-major operands, N>>3 at
+// [17,23), UE8M0 scales (bit 23), M>>4 at [24,29); the scale-factor byte selectors
+// (B at [4,6), A at [29,31)) are or-ed in per instruction.
+__host__ __device__ constexpr uint32_t idesc_mx(uint32_t elem_type, uint32_t M, uint32_t N) {
+  return (elem_type << 7) | (elem_type << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4) | (sfa_id << 29);
 }
 
 // ---------------------------------------------------------------- misc

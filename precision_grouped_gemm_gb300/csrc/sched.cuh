@@ -13,6 +13,15 @@ namespace pgg {
 
 constexpr int kMaxGroups = 1024;
 
+// GEMM modes and epilogues shared by the BF16 and block-scaled kernels.
+enum GemmMode : int { kFwd = 0, kDgrad = 1, kWgrad = 2 };
+enum GemmEpi : int { kEpiStore = 0, kEpiSwiGLU = 1, kEpiSwiGLUBwd = 2 };
+
+// Device error-word codes (the public values of pgg_status).
+constexpr int kErrBadGroupLens = 16;
+constexpr int kErrTimeout = 17;
+constexpr int kErrPadOverflow = 18;
+
 // Tiles of one group as a function of its length.
 struct TileCount {
   int per_row_tile;     // column tiles (fwd/dgrad) or constant tiles per group (wgrad)

@@ -48,6 +48,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-extra", action="store_true", help="skip the other workloads' summary")
+    p.add_argument("--extra-steps", type=int, default=30)
     p.add_argument("--experts-cap", type=int, default=0,
                    help="keep only the first N experts (same per-expert shapes; small profiling case)")
     return p.parse_args()
@@ -126,13 +128,6 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # inputs
 # ----------------------------------------------------------------------------
-
-def build_device_inputs(w, device, cap=0):
-    from precision_grouped_gemm_gb300.layer import build_layer_inputs
-    lens, _, buf = build_layer_inputs(w, device, cap)
-    torch.cuda.synchronize()
-    return lens, buf
-
 
 def layer_flops(lens, w):
     return 18.0 * float(lens.sum()) * w.inter * w.hidden
@@ -257,7 +252,7 @@ def run_reference(args, w):
 # the CUDA path
 # ----------------------------------------------------------------------------
 
-def kernel_traffic(name):
+def kernel_traffic(workload, name):
     """DRAM bytes per launch from the committed ncu summary, if the kernel sources still match."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -268,14 +263,122 @@ def kernel_traffic(name):
     from precision_grouped_gemm_gb300.build import source_digest
     if d.get("source_digest") != source_digest():
         return None
-    k = d.get("kernels", {}).get(name)
+    k = d.get("workloads", {}).get(workload, {}).get(name)
     return None if k is None else k.get("dram_bytes_per_launch")
+
+
+PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}  # dense tensor peak vs bf16 (nominal ratios)
+
+
+def setup_workload(w, device, cap=0):
+    """Inputs and the step function for workload w: (lens, step, names, work, ins, outs, err)."""
+    from precision_grouped_gemm_gb300.layer import (MX_STEP_NAMES, STEP_NAMES, MxLayerBuffers, build_layer_inputs,
+                                                    expert_layer_step, layer_work, mx_layer_step, mx_layer_work)
+    lens, _, buf = build_layer_inputs(w, device, cap, allocate=(w.fmt == "bf16"))
+    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
+    if w.fmt == "bf16":
+        work = layer_work(M, G, Hd, I)
+        ins = [buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens]
+        outs = [buf.Y, buf.dX, buf.dW1, buf.dW2]
+        return lens, (lambda between=None: expert_layer_step(buf, between)), STEP_NAMES, work, ins, outs, buf.err
+    mb = MxLayerBuffers.build(w.fmt, buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens)
+    del buf
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    work = mx_layer_work(w.fmt, M, G, Hd, I, mb.M_pad)
+    ins = [mb.X, mb.dY, mb.group_lens, *mb.W1q, *mb.W1t, *mb.W2q, *mb.W2t]
+    u = mb.bufs
+    outs = [u["Y"], u["dX"], u["dW1"], u["dW2"]]
+    return lens, (lambda between=None: mx_layer_step(mb, between)), MX_STEP_NAMES, work, ins, outs, u["err"]
+
+
+def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample_clocks=True):
+    import precision_grouped_gemm_gb300 as pgg
+    lens, step, names, work, ins, outs, err = setup_workload(w, device, cap)
+    flops = layer_flops(lens, w)
+    warmup = max(3, warmup)
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if pgg.read_error(err) != 0:
+        raise RuntimeError(f"{w.name}: device error word set during warm-up")
+    K = steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    sampler = ClockSampler(torch.cuda.current_device()) if sample_clocks else None
+    if sampler:
+        sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for k in range(K):
+        row = ev[k]
+        step(lambda i, row=row: row[i].record())
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if pgg.read_error(err) != 0:
+        raise RuntimeError(f"{w.name}: device error word set during the timed region")
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    tc = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * PEAK_RATIO[w.fmt]
+    per = {}
+    for i, name in enumerate(names):
+        d = [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)]
+        avg = sum(d) / len(d)
+        f, b = work[name]
+        per[name] = {"ms": avg, "tflops": f / avg / 1e9, "gbs": b / avg / 1e6, "algo_bytes": b, "flops": f}
+    dom = max(per, key=lambda n: per[n]["ms"])
+    f, b = work[dom]
+    bound = "hbm" if b / (hbm * 1e9) >= f / (tc * 1e12) else "tensor"
+    if bound == "hbm":
+        achieved, peak, unit = per[dom]["gbs"], hbm, "GB/s"
+        src = "hbm_gbs"
+    else:
+        achieved, peak, unit = per[dom]["tflops"], tc, "TFLOP/s"
+        src = "bf16_tflops_sustained" + (f" x {PEAK_RATIO[w.fmt]:g} (nominal {w.fmt}/bf16 ratio)"
+                                         if w.fmt != "bf16" else "")
+    attain = sum(max(work[n][1] / (hbm * 1e9), work[n][0] / (tc * 1e12)) for n in names)
+    res = {
+        "value": world * flops / (ms / K) / 1e9, "unit": "TFLOP/s", "ms_per_step": ms / K, "steps": K,
+        "warmup": warmup, "dtype": w.fmt, "rows_M": int(lens.sum()), "group_lens_min": int(lens.min()),
+        "group_lens_max": int(lens.max()), "groups_under_128": int((lens < 128).sum()),
+        "empty_groups": int((lens == 0).sum()),
+        "pct_of_dense_peak": flops / (ms / K) / 1e9 / (peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+                                                       * PEAK_RATIO[w.fmt]),
+        "pct_of_attainable_roofline": (attain * 1e3) / (ms / K),
+        "roofline": {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": kernel_traffic(w.name, dom),
+                     "peak_source": f"{load_peaks()[1]} ({src})", "algo_bytes_per_launch": b,
+                     "flops_per_launch": f},
+        "kernels": per, "gpu_launches": len(names) * K, "clocks": clocks,
+        "weights_gb": sum(t.numel() * t.element_size() for t in ins[1:3]) / 1e9 if w.fmt == "bf16" else None,
+    }
+    if e2e_steps:
+        res["e2e"] = run_e2e(step, ins, outs, flops, e2e_steps)
+    del ins, outs, step
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+EXTRA = [wl.DSV4_MXFP8, wl.GPTOSS_BF16, wl.ZIPF_MXFP4]
 
 
 def run_pgg(args, w):
     import precision_grouped_gemm_gb300 as pgg
-    from precision_grouped_gemm_gb300.layer import STEP_NAMES, expert_layer_step, layer_work
-
     world, rank, local = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -283,94 +386,37 @@ def run_pgg(args, w):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     pgg.init(local)
-    peaks, peak_src = load_peaks()
-
-    lens, buf = build_device_inputs(w, device, args.experts_cap)
-    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
-    flops = layer_flops(lens, w)
-    work = layer_work(M, G, Hd, I)
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-
-    for _ in range(max(3, args.warmup)):
-        expert_layer_step(buf)
-    torch.cuda.synchronize()
-    if pgg.read_error(buf.err) != 0:
-        raise RuntimeError("device error word set during warm-up")
-
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STEP_NAMES) + 1)] for _ in range(K)]
-    sampler = ClockSampler(torch.cuda.current_device())
-    sampler.start()
-    barrier()
-    torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for k in range(K):
-        row = ev[k]
-        expert_layer_step(buf, between=lambda i, row=row: row[i].record())
-    t1.record()
-    torch.cuda.synchronize()
-    barrier()
-    clocks = sampler.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    if pgg.read_error(buf.err) != 0:
-        raise RuntimeError("device error word set during the timed region")
-
-    per = {}
-    for i, name in enumerate(STEP_NAMES):
-        d = [ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)]
-        avg = sum(d) / len(d)
-        f, b = work[name]
-        per[name] = {"ms": avg, "tflops": f / avg / 1e9, "gbs": b / avg / 1e6,
-                     "algo_bytes": b, "flops": f}
-    dom = max(per, key=lambda n: per[n]["ms"])
-    f, b = work[dom]
-    hbm, tc = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]), peaks.get("bf16_tflops_sustained", 1700.0)
-    bound = "hbm" if b / (hbm * 1e9) >= f / (tc * 1e12) else "tensor"
-    if bound == "hbm":
-        achieved, peak, unit = per[dom]["gbs"], hbm, "GB/s"
-    else:
-        achieved, peak, unit = per[dom]["tflops"], tc, "TFLOP/s"
-    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "traffic": kernel_traffic(dom),
-                "peak_source": f"{peak_src} ({'hbm_gbs' if bound == 'hbm' else 'bf16_tflops_sustained'})",
-                "algo_bytes_per_launch": b, "flops_per_launch": f}
-
-    value = world * flops / (ms / K) / 1e9  # TFLOP/s over all ranks
-    bf16_peak = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"])
-    attain = sum(max(work[n][1] / (hbm * 1e9), work[n][0] / (bf16_peak * 1e12)) for n in STEP_NAMES)
-
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, w, buf, flops)
+    peaks, _ = load_peaks()
+    main = measure(w, args.steps, args.warmup, device, peaks, args.experts_cap,
+                   0 if args.no_e2e else args.e2e_steps, world)
+    extra = {}
+    if not args.no_extra and not args.experts_cap:
+        for ew in EXTRA:
+            if ew.name != w.name:
+                r = measure(ew, args.extra_steps, 3, device, peaks, 0, 0, world, sample_clocks=False)
+                extra[ew.name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "dtype", "pct_of_dense_peak",
+                                                    "pct_of_attainable_roofline", "roofline", "rows_M",
+                                                    "group_lens_min", "group_lens_max", "groups_under_128",
+                                                    "empty_groups", "steps")}
+                extra[ew.name]["kernels_ms"] = {k: round(v["ms"], 4) for k, v in r["kernels"].items()}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)
-
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": K,
-        "warmup": max(3, args.warmup), "ms_per_step": ms / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "metric": METRIC, "value": main["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": main["steps"],
+        "warmup": main["warmup"], "ms_per_step": main["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.fmt,
         "data": "synthetic (seeded counter-based generator; routing by top-k of softmax over generated logits)",
-        "config": {"workload": w.name + (f"_first{G}experts" if args.experts_cap else ""), "tokens": w.tokens, "experts": G, "top_k": w.topk, "hidden": Hd,
-                   "intermediate": I, "rows_M": M, "group_lens_min": int(lens.min()),
-                   "group_lens_max": int(lens.max()),
-                   "l2": f"inputs larger than L2 ({(buf.W1.numel() + buf.W2.numel()) * 2 / 1e9:.1f} GB of "
-                         f"expert weights streamed per step), no flush",
+        "config": {"workload": w.name + (f"_first{args.experts_cap}experts" if args.experts_cap else ""),
+                   "tokens": w.tokens, "experts": args.experts_cap or w.experts, "top_k": w.topk,
+                   "hidden": w.hidden, "intermediate": w.inter, "rows_M": main["rows_M"],
+                   "group_lens_min": main["group_lens_min"], "group_lens_max": main["group_lens_max"],
+                   "l2": "inputs larger than L2 (all expert weights streamed every step), no flush",
                    "parallelism": "replicas" if world > 1 else "single"},
-        "pct_of_dense_bf16_peak": value / world / peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]),
-        "pct_of_attainable_roofline": (attain * 1e3) / (ms / K),
-        "roofline": roofline, "kernels": per, "gpu_launches": len(STEP_NAMES) * K,
-        "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
+        "pct_of_dense_bf16_peak": main["pct_of_dense_peak"],
+        "pct_of_attainable_roofline": main["pct_of_attainable_roofline"],
+        "roofline": main["roofline"], "kernels": main["kernels"], "gpu_launches": main["gpu_launches"],
+        "clocks": main["clocks"], "e2e": main.get("e2e"), "cpu_baseline": cpu, "extra": extra,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -379,12 +425,9 @@ def run_pgg(args, w):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, buf, flops):
+def run_e2e(step, ins, outs, flops, n):
     """Same metric through the public API with host buffers: H2D of the step's inputs from
-    pinned memory, the six calls, D2H of the step's results, all inside the timed region."""
-    from precision_grouped_gemm_gb300.layer import expert_layer_step
-    ins = [buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens]
-    outs = [buf.Y, buf.dX, buf.dW1, buf.dW2]
+    pinned memory, the layer's calls, D2H of the step's results, all inside the timed region."""
     h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
     for h, t in zip(h_in, ins):
         h.copy_(t)
@@ -392,20 +435,19 @@ def run_e2e(args, w, buf, flops):
     bi = sum(t.numel() * t.element_size() for t in ins)
     bo = sum(t.numel() * t.element_size() for t in outs)
 
-    def step():
+    def one():
         for d, h in zip(ins, h_in):
             d.copy_(h, non_blocking=True)
-        expert_layer_step(buf)
+        step()
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
 
-    step()
+    one()
     torch.cuda.synchronize()
-    n = max(1, args.e2e_steps)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for _ in range(n):
-        step()
+        one()
     t1.record()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / n
@@ -416,8 +458,8 @@ def run_e2e(args, w, buf, flops):
 def main():
     args = parse_args()
     w = wl.WORKLOADS[args.workload]
-    if not w.swiglu or w.fmt != "bf16":
-        raise SystemExit("bench.py times the BF16 expert-layer workloads")
+    if not w.swiglu:
+        raise SystemExit("bench.py times the expert-layer workloads")
     if args.impl == "reference":
         run_reference(args, w)
     else:

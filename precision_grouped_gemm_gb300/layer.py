@@ -96,7 +96,7 @@ def layer_work(M: int, G: int, Hd: int, I: int) -> dict:
     }
 
 
-def build_layer_inputs(w, device, cap: int = 0):
+def build_layer_inputs(w, device, cap: int = 0, allocate: bool = True):
     """Seeded inputs of workload `w` on `device` (only the first `cap` experts when cap > 0).
 
     X rows are the generated token activations gathered in expert-sorted row order;
@@ -114,7 +114,8 @@ def build_layer_inputs(w, device, cap: int = 0):
     W2 = wl.gen_matrix(wl.KEY_W2, G * Hd, I, w.w_std, w.seed, device=device).view(G, Hd, I)
     dY = wl.gen_matrix(wl.KEY_DY, M, Hd, 1.0, w.seed, device=device)
     gl = torch.from_numpy(np.ascontiguousarray(lens)).to(device)
-    return lens, row_token, ExpertLayerBuffers(X, W1, W2, dY, gl).allocate()
+    b = ExpertLayerBuffers(X, W1, W2, dY, gl)
+    return lens, row_token, (b.allocate() if allocate else b)
 
 
 def expert_inputs_cpu(w, lens, row_token, e: int):
@@ -126,3 +127,121 @@ def expert_inputs_cpu(w, lens, row_token, e: int):
     W2 = wl.gen_matrix(wl.KEY_W2, w.hidden, w.inter, w.w_std, w.seed, row0=e * w.hidden)
     dY = wl.gen_matrix(wl.KEY_DY, b - a, w.hidden, 1.0, w.seed, row0=a)
     return X, W1, W2, dY, (a, b)
+
+
+# ----------------------------------------------------------------------------
+# MX (MXFP8 / MXFP4) expert layer
+# ----------------------------------------------------------------------------
+
+MX_STEP_NAMES = ("q_x_row", "fc1_fwd_swiglu", "q_a_row", "fc2_fwd", "q_dy_row", "fc2_dgrad_swiglu_bwd",
+                 "q_dy_col", "q_a_col", "fc2_wgrad", "q_dh_row", "fc1_dgrad", "q_dh_col", "q_x_col",
+                 "fc1_wgrad")
+
+
+@dataclasses.dataclass
+class MxLayerBuffers:
+    """Block-scaled expert layer: bf16 activations, MX weights quantized once (the caller's
+    weight cache), and the MX activation / gradient operands each step re-quantizes."""
+    fmt: str
+    X: torch.Tensor
+    dY: torch.Tensor
+    group_lens: torch.Tensor
+    W1q: tuple = None      # row-wise  [G*2I, H]   (fc1 fwd, blocks along H)
+    W1t: tuple = None      # column-wise [H, G*2I] (fc1 dgrad, blocks along 2I)
+    W2q: tuple = None      # row-wise  [G*H, I]    (fc2 fwd, blocks along I)
+    W2t: tuple = None      # column-wise [I, G*H]  (fc2 dgrad, blocks along H)
+    M_pad: int = 0
+    bufs: dict = None
+
+    @staticmethod
+    def build(fmt, X, W1, W2, dY, group_lens):
+        """Quantize the weights (outside any timed region) and allocate every step buffer."""
+        G, I2, Hd = W1.shape
+        I = I2 // 2
+        M = X.shape[0]
+        dev = X.device
+        b = MxLayerBuffers(fmt, X, dY, group_lens)
+        W1f, W2f = W1.reshape(G * I2, Hd), W2.reshape(G * Hd, I)
+        b.W1q = B.mx_quantize_rowwise(W1f, fmt)
+        b.W1t = B.mx_quantize_colwise(W1f, torch.full((G,), I2, dtype=torch.int32, device=dev), fmt, G * I2)
+        b.W2q = B.mx_quantize_rowwise(W2f, fmt)
+        b.W2t = B.mx_quantize_colwise(W2f, torch.full((G,), Hd, dtype=torch.int32, device=dev), fmt, G * Hd)
+        b.M_pad = B.mx_pad_rows(M, G)
+        cb = (lambda c: c) if fmt == "e4m3" else (lambda c: c // 2)
+        u8, bf = torch.uint8, torch.bfloat16
+        Mp = b.M_pad
+        e = lambda *s: torch.empty(s, dtype=u8, device=dev)
+        b.bufs = {
+            "Xq": (e(M, cb(Hd)), e(M, Hd // 32)), "A": torch.empty((M, I), dtype=bf, device=dev),
+            "H": torch.empty((M, I2), dtype=bf, device=dev), "Aq": (e(M, cb(I)), e(M, I // 32)),
+            "Y": torch.empty((M, Hd), dtype=bf, device=dev), "dYq": (e(M, cb(Hd)), e(M, Hd // 32)),
+            "dH": torch.empty((M, I2), dtype=bf, device=dev), "dYc": (e(Hd, cb(Mp)), e(Hd, Mp // 32)),
+            "Ac": (e(I, cb(Mp)), e(I, Mp // 32)), "dW2": torch.empty((G, Hd, I), dtype=bf, device=dev),
+            "dHq": (e(M, cb(I2)), e(M, I2 // 32)), "dX": torch.empty((M, Hd), dtype=bf, device=dev),
+            "dHc": (e(I2, cb(Mp)), e(I2, Mp // 32)), "Xc": (e(Hd, cb(Mp)), e(Hd, Mp // 32)),
+            "dW1": torch.empty((G, I2, Hd), dtype=bf, device=dev),
+            "err": torch.zeros(1, dtype=torch.int32, device=dev),
+        }
+        return b
+
+
+def mx_layer_step(b: MxLayerBuffers, between=None):
+    """One MX expert-layer fwd + bwd: 8 activation quantizations and 6 block-scaled GEMMs."""
+    f, gl, u = b.fmt, b.group_lens, b.bufs
+    err, Mp = u["err"], b.M_pad
+    M, Hd = b.X.shape
+    I = u["A"].shape[1]
+    G = gl.numel()
+    calls = (
+        lambda: B.mx_quantize_rowwise(b.X, f, *u["Xq"]),
+        lambda: B.mx_grouped_gemm(B.MODE_FWD, f, *u["Xq"], *b.W1q, gl, M, 2 * I, Hd, out=u["A"], out2=u["H"],
+                                  epilogue=B.EPI_SWIGLU, err=err),
+        lambda: B.mx_quantize_rowwise(u["A"], f, *u["Aq"]),
+        lambda: B.mx_grouped_gemm(B.MODE_FWD, f, *u["Aq"], *b.W2q, gl, M, Hd, I, out=u["Y"], err=err),
+        lambda: B.mx_quantize_rowwise(b.dY, f, *u["dYq"]),
+        lambda: B.mx_grouped_gemm(B.MODE_DGRAD, f, *u["dYq"], *b.W2t, gl, M, Hd, I, out=u["dH"], H=u["H"],
+                                  epilogue=B.EPI_SWIGLU, err=err),
+        lambda: B.mx_quantize_colwise(b.dY, gl, f, Mp, *u["dYc"], err=err),
+        lambda: B.mx_quantize_colwise(u["A"], gl, f, Mp, *u["Ac"], err=err),
+        lambda: B.mx_grouped_gemm(B.MODE_WGRAD, f, *u["dYc"], *u["Ac"], gl, M, Hd, I, out=u["dW2"], M_pad=Mp,
+                                  err=err),
+        lambda: B.mx_quantize_rowwise(u["dH"], f, *u["dHq"]),
+        lambda: B.mx_grouped_gemm(B.MODE_DGRAD, f, *u["dHq"], *b.W1t, gl, M, 2 * I, Hd, out=u["dX"], err=err),
+        lambda: B.mx_quantize_colwise(u["dH"], gl, f, Mp, *u["dHc"], err=err),
+        lambda: B.mx_quantize_colwise(b.X, gl, f, Mp, *u["Xc"], err=err),
+        lambda: B.mx_grouped_gemm(B.MODE_WGRAD, f, *u["dHc"], *u["Xc"], gl, M, 2 * I, Hd, out=u["dW1"],
+                                  M_pad=Mp, err=err),
+    )
+    assert len(calls) == len(MX_STEP_NAMES) and G > 0
+    for i, c in enumerate(calls):
+        if between:
+            between(i)
+        c()
+    if between:
+        between(len(calls))
+
+
+def mx_layer_work(fmt: str, M: int, G: int, Hd: int, I: int, M_pad: int) -> dict:
+    """Algorithmic flops and bytes of each MX-layer call (codes at 1 or 0.5 B/element,
+    scales at 1/32 B/element, bf16 activations and outputs at 2 B/element)."""
+    c = 1.0 if fmt == "e4m3" else 0.5
+    q = c + 1.0 / 32                          # bytes per quantized element (codes + scale)
+    f1, f2 = 2.0 * M * 2 * I * Hd, 2.0 * M * Hd * I
+    W1, W2 = G * 2 * I * Hd, G * Hd * I       # elements
+    lens = 4 * G
+    return {
+        "q_x_row": (0.0, M * Hd * (2 + q)),
+        "fc1_fwd_swiglu": (f1, M * Hd * q + W1 * q + M * I * 2 + M * 2 * I * 2 + lens),
+        "q_a_row": (0.0, M * I * (2 + q)),
+        "fc2_fwd": (f2, M * I * q + W2 * q + M * Hd * 2 + lens),
+        "q_dy_row": (0.0, M * Hd * (2 + q)),
+        "fc2_dgrad_swiglu_bwd": (f2, M * Hd * q + W2 * q + M * 2 * I * 2 * 2 + lens),
+        "q_dy_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),
+        "q_a_col": (0.0, M * I * 2 + I * M_pad * q + lens),
+        "fc2_wgrad": (f2, (Hd + I) * M_pad * q + W2 * 2 + lens),
+        "q_dh_row": (0.0, M * 2 * I * (2 + q)),
+        "fc1_dgrad": (f1, M * 2 * I * q + W1 * q + M * Hd * 2 + lens),
+        "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M_pad * q + lens),
+        "q_x_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),
+        "fc1_wgrad": (f1, (2 * I + Hd) * M_pad * q + W1 * 2 + lens),
+    }

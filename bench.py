@@ -44,7 +44,7 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="pgg", choices=["pgg", "reference"])
     p.add_argument("--workload", default=wl.DSV4_BF16.name, choices=sorted(wl.WORKLOADS))
-    p.add_argument("--e2e-steps", type=int, default=2)
+    p.add_argument("--e2e-steps", type=int, default=4)
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
@@ -271,30 +271,34 @@ PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}  # dense tensor peak vs bf1
 
 
 def setup_workload(w, device, cap=0):
-    """Inputs and the step function for workload w: (lens, step, names, work, ins, outs, err)."""
+    """Inputs and the step function for workload w.
+
+    Returns (lens, bufs, step, names, work, io, err): step(bufs, between) runs one layer
+    step on a buffer set; io(bufs) gives that set's (inputs, outputs) tensor lists; a
+    second independent set comes from bufs.clone_empty() (for the pipelined e2e run)."""
     from precision_grouped_gemm_gb300.layer import (MX_STEP_NAMES, STEP_NAMES, MxLayerBuffers, build_layer_inputs,
                                                     expert_layer_step, layer_work, mx_layer_step, mx_layer_work)
     lens, _, buf = build_layer_inputs(w, device, cap, allocate=(w.fmt == "bf16"))
     M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
     if w.fmt == "bf16":
         work = layer_work(M, G, Hd, I)
-        ins = [buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens]
-        outs = [buf.Y, buf.dX, buf.dW1, buf.dW2]
-        return lens, (lambda between=None: expert_layer_step(buf, between)), STEP_NAMES, work, ins, outs, buf.err
+        io = lambda b: ([b.X, b.W1, b.W2, b.dY, b.group_lens], [b.Y, b.dX, b.dW1, b.dW2])
+        return lens, buf, expert_layer_step, STEP_NAMES, work, io, buf.err
     mb = MxLayerBuffers.build(w.fmt, buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens)
     del buf
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     work = mx_layer_work(w.fmt, M, G, Hd, I, mb.M_pad)
-    ins = [mb.X, mb.dY, mb.group_lens, *mb.W1q, *mb.W1t, *mb.W2q, *mb.W2t]
-    u = mb.bufs
-    outs = [u["Y"], u["dX"], u["dW1"], u["dW2"]]
-    return lens, (lambda between=None: mx_layer_step(mb, between)), MX_STEP_NAMES, work, ins, outs, u["err"]
+    io = lambda b: ([b.X, b.dY, b.group_lens, *b.W1q, *b.W1t, *b.W2q, *b.W2t],
+                    [b.bufs["Y"], b.bufs["dX"], b.bufs["dW1"], b.bufs["dW2"]])
+    return lens, mb, mx_layer_step, MX_STEP_NAMES, work, io, mb.bufs["err"]
 
 
 def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample_clocks=True):
     import precision_grouped_gemm_gb300 as pgg
-    lens, step, names, work, ins, outs, err = setup_workload(w, device, cap)
+    lens, bufs, step_fn, names, work, io, err = setup_workload(w, device, cap)
+    step = lambda between=None: step_fn(bufs, between)
+    ins, outs = io(bufs)
     flops = layer_flops(lens, w)
     warmup = max(3, warmup)
     for _ in range(warmup):
@@ -361,8 +365,8 @@ def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample
         "weights_gb": sum(t.numel() * t.element_size() for t in ins[1:3]) / 1e9 if w.fmt == "bf16" else None,
     }
     if e2e_steps:
-        res["e2e"] = run_e2e(step, ins, outs, flops, e2e_steps)
-    del ins, outs, step
+        res["e2e"] = run_e2e(step_fn, bufs, io, flops, e2e_steps)
+    del ins, outs, step, bufs
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
@@ -425,34 +429,57 @@ def run_pgg(args, w):
         dist.destroy_process_group()
 
 
-def run_e2e(step, ins, outs, flops, n):
-    """Same metric through the public API with host buffers: H2D of the step's inputs from
-    pinned memory, the layer's calls, D2H of the step's results, all inside the timed region."""
-    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
-    for h, t in zip(h_in, ins):
+def run_e2e(step_fn, bufs, io, flops, n):
+    """The same metric through the public API with host buffers.  Every step copies its
+    inputs from pinned host memory to the device, runs the layer's calls and copies its
+    results back to pinned host memory, all inside the timed region.  Two device buffer
+    sets alternate so that step k's results stream out (D2H stream) while step k+1's
+    inputs stream in (H2D stream) and compute (current stream) runs."""
+    sets = [bufs, bufs.clone_empty()]
+    ins0, outs0 = io(bufs)
+    h_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins0]
+    for h, t in zip(h_in, ins0):
         h.copy_(t)
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    bi = sum(t.numel() * t.element_size() for t in ins)
-    bo = sum(t.numel() * t.element_size() for t in outs)
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs0]
+    bi = sum(t.numel() * t.element_size() for t in ins0)
+    bo = sum(t.numel() * t.element_size() for t in outs0)
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    E = lambda: torch.cuda.Event()
+    done_out = [None, None]  # D2H of a set finished -> its buffers may be overwritten
 
-    def one():
-        for d, h in zip(ins, h_in):
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(h_out, outs):
-            h.copy_(d, non_blocking=True)
+    def one(k):
+        b = sets[k & 1]
+        ins, outs = io(b)
+        with torch.cuda.stream(s_in):
+            if done_out[k & 1] is not None:
+                s_in.wait_event(done_out[k & 1])
+            for d, h in zip(ins, h_in):
+                d.copy_(h, non_blocking=True)
+            e_in = E(); e_in.record(s_in)
+        comp.wait_event(e_in)
+        step_fn(b)
+        e_c = E(); e_c.record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(e_c)
+            for h, d in zip(h_out, outs):
+                h.copy_(d, non_blocking=True)
+            done_out[k & 1] = E(); done_out[k & 1].record(s_out)
 
-    one()
+    for k in range(2):
+        one(k)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for _ in range(n):
-        one()
-    t1.record()
+    t0.record(s_in)
+    for k in range(n):
+        one(k)
+    t1.record(s_out)
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / n
+    del sets[1]
     return {"value": flops / ms / 1e9, "unit": "TFLOP/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
-            "ms_per_step": ms, "steps": n}
+            "ms_per_step": ms, "steps": n,
+            "overlap": "two device buffer sets; H2D, compute and D2H on three streams"}
 
 
 def main():

@@ -78,14 +78,15 @@ template <int MODE, int EPI, int BN>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int32_t* s_off,
                                             const int32_t* s_tile) {
   Tile T;
-  const int ncol = (a.out_cols + tile_cols<MODE, EPI, BN>() - 1) / tile_cols<MODE, EPI, BN>();
   const int g = find_group(s_tile, a.G, t);
   const int local = t - s_tile[g];
   const int off = s_off[g], len = s_off[g + 1] - s_off[g];
   T.g = g;
   if (MODE == kWgrad) {
-    const int nrt = (a.wg_rows + kBM - 1) / kBM;
-    const int rt = local % nrt, ct = local / nrt;
+    // column tiles vary fastest: the CTAs running at one time fill whole rows of dW_g
+    // (contiguous DRAM pages) instead of narrow stripes of many rows
+    const int nct = (a.out_cols + BN - 1) / BN;
+    const int ct = local % nct, rt = local / nct;
     T.row0 = rt * kBM;
     T.rows = min(kBM, a.wg_rows - T.row0);
     T.col0 = ct * BN;
@@ -95,7 +96,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int3
   } else {
     const int nmt = (len + kBM - 1) / kBM;
     const int mt = local % nmt, ct = local / nmt;
-    (void)ncol;
     T.row0 = off + mt * kBM;
     T.rows = min(kBM, len - mt * kBM);
     T.col0 = ct * tile_cols<MODE, EPI, BN>();

@@ -90,10 +90,11 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
   T.g = g;
   T.poff = s_poff[g];
   if (MODE == kWgrad) {
-    const int nrt = (a.wg_rows + kMxBM - 1) / kMxBM;
-    T.row0 = (local % nrt) * kMxBM;
+    // column tiles vary fastest (whole rows of dW_g written by concurrent CTAs)
+    const int nct = (a.out_cols + kMxBN - 1) / kMxBN;
+    T.row0 = (local / nct) * kMxBM;
     T.rows = min(kMxBM, a.wg_rows - T.row0);
-    T.col0 = (local / nrt) * kMxBN;
+    T.col0 = (local % nct) * kMxBN;
     T.nkb = (len + kMxBK - 1) / kMxBK;
   } else {
     const int nmt = (len + kMxBM - 1) / kMxBM;

@@ -111,12 +111,49 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
 // Output column space [0, M_pad) is cut into 32-wide blocks; block j holds
 // rows off_g + 32 b .. of group g for j = pb_g + b with pb_g the prefix of
 // round_up(len_g, 128) / 32, or nothing (pad) -- every output byte is written
-// once.  A CTA tile is one block j x 128 input columns: 32 rows x 128 columns
-// are staged in smem (coalesced 16-byte loads), then thread c quantizes column
-// c down the 32 rows and writes its 32 (e4m3) or 16 (e2m1) code bytes.
-constexpr int kColTile = 128;
-constexpr int kColThreads = 128;
-constexpr int kSmemPitch = kColTile + 8;  // bf16 elements per staged row (bank spread)
+// once.  One warp handles one block j x 64 input columns: lane l reads columns
+// c0 + 2l, c0 + 2l + 1 of the block's rows (32 coalesced 128-byte row loads in
+// flight, no shared memory, no block barrier), takes each column's amax and
+// writes the column's 32 codes (32 bytes e4m3 / 16 bytes e2m1) and its scale.
+// Work items run with j fastest, so the warps writing the 32-byte pieces of one
+// 128-byte line of codes_t run at the same time.
+constexpr int kColSlab = 64;
+constexpr int kColThreads = 256;
+
+template <int FMT>
+__device__ __forceinline__ void colwise_store(const uint32_t (&v)[32], int half, int valid, int c,
+                                              int64_t M_pad, int j, uint8_t* __restrict__ codes_t,
+                                              uint8_t* __restrict__ scales_t) {
+  uint32_t am = 0;
+#pragma unroll
+  for (int r = 0; r < 32; ++r) am = max(am, ((v[r] >> (16 * half)) & 0x7FFFu));
+  uint32_t sc = 0;
+  float mult = 0.0f;
+  const bool fin = valid > 0 ? block_scale<FMT>(am, sc, mult) : true;
+  const bool keep = valid > 0 && fin;
+  float f[32];
+#pragma unroll
+  for (int r = 0; r < 32; ++r) f[r] = keep ? __uint_as_float((v[r] >> (16 * half)) << 16) * mult : 0.0f;
+  if (FMT == kE4M3) {
+    uint4 o[2];
+    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ow[k] = cvt_e4m3x2(f[4 * k], f[4 * k + 1]) | (cvt_e4m3x2(f[4 * k + 2], f[4 * k + 3]) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(codes_t + (int64_t)c * M_pad + (int64_t)j * 32);
+    dst[0] = o[0];
+    dst[1] = o[1];
+  } else {
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      ow[k] = cvt_e2m1x2(f[8 * k], f[8 * k + 1]) | (cvt_e2m1x2(f[8 * k + 2], f[8 * k + 3]) << 8) |
+              (cvt_e2m1x2(f[8 * k + 4], f[8 * k + 5]) << 16) | (cvt_e2m1x2(f[8 * k + 6], f[8 * k + 7]) << 24);
+    *reinterpret_cast<uint4*>(codes_t + (int64_t)c * (M_pad / 2) + (int64_t)j * 16) = o;
+  }
+  scales_t[(int64_t)c * (M_pad / 32) + j] = (uint8_t)(valid > 0 ? sc : 0u);
+}
 
 template <int FMT>
 __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
@@ -126,7 +163,6 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
   extern __shared__ int32_t s_dyn[];
   int32_t* s_off = s_dyn;             // [G+1] row offsets
   int32_t* s_blk = s_dyn + (G + 1);   // [G+1] prefix of 32-blocks in the padded layout
-  __shared__ __align__(16) uint16_t tile[32 * kSmemPitch];
   __shared__ int s_bad;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == 0) {
@@ -145,8 +181,7 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
       __syncwarp();
     }
     if (lane == 0) {
-      int code = bad ? PGG_ERR_BAD_GROUP_LENS
-                     : ((int64_t)s_blk[G] * 32 > M_pad ? PGG_ERR_PAD_OVERFLOW : 0);
+      int code = bad ? kErrBadGroupLens : ((int64_t)s_blk[G] * 32 > M_pad ? kErrPadOverflow : 0);
       s_bad = code;
       if (code && blockIdx.x == 0) set_error(err, code);
     }
@@ -154,66 +189,28 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
   __syncthreads();
   if (s_bad) return;
   const int nblk = (int)(M_pad / 32);
-  const int nct = (C + kColTile - 1) / kColTile;
-  const int64_t total = (int64_t)nblk * nct;
+  const int nslab = (C + kColSlab - 1) / kColSlab;
+  const int64_t total = (int64_t)nblk * nslab;
   const int used = s_blk[G];
-  for (int64_t t = blockIdx.x; t < total; t += gridDim.x) {
-    const int j = (int)(t / nct);
-    const int c0 = (int)(t % nct) * kColTile;
+  const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
+  for (int64_t t = (int64_t)blockIdx.x * (kColThreads / 32) + warp; t < total; t += nwarps) {
+    const int j = (int)(t % nblk);
+    const int c = (int)(t / nblk) * kColSlab + 2 * lane;
     int valid = 0;
     int64_t row0 = 0;
     if (j < used) {
       const int g = find_group(s_blk, G, j);
       const int b = j - s_blk[g];
-      const int len = s_off[g + 1] - s_off[g];
-      valid = min(32, max(0, len - 32 * b));
+      valid = min(32, max(0, s_off[g + 1] - s_off[g] - 32 * b));
       row0 = (int64_t)s_off[g] + 32 * b;
     }
-    __syncthreads();  // previous tile fully consumed
-    // stage rows row0 .. row0+valid-1, columns c0 .. c0+127 (16-byte chunks)
-    for (int q = threadIdx.x; q < 32 * (kColTile / 8); q += kColThreads) {
-      const int r = q / (kColTile / 8), cc = (q % (kColTile / 8)) * 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < valid && c0 + cc < C) v = __ldg(reinterpret_cast<const uint4*>(in + (row0 + r) * C + c0 + cc));
-      *reinterpret_cast<uint4*>(&tile[r * kSmemPitch + cc]) = v;
-    }
-    __syncthreads();
-    const int c = c0 + threadIdx.x;
     if (c >= C) continue;
-    uint32_t am = 0;
-    for (int r = 0; r < valid; ++r) am = max(am, (uint32_t)(tile[r * kSmemPitch + threadIdx.x] & 0x7FFFu));
-    uint32_t sc = 0;
-    float mult = 0.0f;
-    bool fin = true;
-    if (valid > 0) fin = block_scale<FMT>(am, sc, mult);
-    float f[32];
+    uint32_t v[32];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(in + row0 * C + c);
 #pragma unroll
-    for (int r = 0; r < 32; ++r)
-      f[r] = (r < valid && fin) ? __uint_as_float((uint32_t)tile[r * kSmemPitch + threadIdx.x] << 16) * mult : 0.0f;
-    if (valid == 0 || !fin) {
-#pragma unroll
-      for (int r = 0; r < 32; ++r) f[r] = 0.0f;  // pad block or non-finite block: +0 codes
-    }
-    if (FMT == kE4M3) {
-      uint4 o[2];
-      uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        ow[k] = cvt_e4m3x2(f[4 * k], f[4 * k + 1]) | (cvt_e4m3x2(f[4 * k + 2], f[4 * k + 3]) << 16);
-      uint4* dst = reinterpret_cast<uint4*>(codes_t + (int64_t)c * M_pad + (int64_t)j * 32);
-      dst[0] = o[0];
-      dst[1] = o[1];
-    } else {
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        ow[k] = cvt_e2m1x2(f[8 * k], f[8 * k + 1]) | (cvt_e2m1x2(f[8 * k + 2], f[8 * k + 3]) << 8) |
-                (cvt_e2m1x2(f[8 * k + 4], f[8 * k + 5]) << 16) |
-                (cvt_e2m1x2(f[8 * k + 6], f[8 * k + 7]) << 24);
-      *reinterpret_cast<uint4*>(codes_t + (int64_t)c * (M_pad / 2) + (int64_t)j * 16) = o;
-    }
-    scales_t[(int64_t)c * (M_pad / 32) + j] = (uint8_t)(valid > 0 ? sc : 0u);
+    for (int r = 0; r < 32; ++r) v[r] = r < valid ? __ldg(src + (int64_t)r * (C / 2)) : 0u;
+    colwise_store<FMT>(v, 0, valid, c, M_pad, j, codes_t, scales_t);
+    colwise_store<FMT>(v, 1, valid, c + 1, M_pad, j, codes_t, scales_t);
   }
 }
 
@@ -243,8 +240,9 @@ int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != PGG_OK) return st;
-  const int64_t total = (M_pad / 32) * ((C + kColTile - 1) / kColTile);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(total, (int64_t)dev.sms * 8));
+  const int64_t total = (M_pad / 32) * ((C + kColSlab - 1) / kColSlab);  // warp work items
+  const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
   const size_t smem = 8 * (size_t)(G + 1);
   auto* x = static_cast<const __nv_bfloat16*>(in);
   if (fmt == PGG_FMT_E4M3)

@@ -44,6 +44,12 @@ class ExpertLayerBuffers:
     dW2: torch.Tensor = None
     err: torch.Tensor = None
 
+    def clone_empty(self):
+        """An independent buffer set of the same shapes (inputs uninitialised)."""
+        e = lambda t: torch.empty_like(t)
+        return ExpertLayerBuffers(e(self.X), e(self.W1), e(self.W2), e(self.dY),
+                                  self.group_lens.clone()).allocate()
+
     def allocate(self):
         M, Hd = self.X.shape
         G, I2, _ = self.W1.shape
@@ -152,6 +158,17 @@ class MxLayerBuffers:
     W2t: tuple = None      # column-wise [I, G*H]  (fc2 dgrad, blocks along H)
     M_pad: int = 0
     bufs: dict = None
+
+    def clone_empty(self):
+        """An independent buffer set of the same shapes (inputs and weight caches uninitialised)."""
+        e = lambda t: torch.empty_like(t)
+        c = MxLayerBuffers(self.fmt, e(self.X), e(self.dY), self.group_lens.clone())
+        c.W1q, c.W1t = tuple(map(e, self.W1q)), tuple(map(e, self.W1t))
+        c.W2q, c.W2t = tuple(map(e, self.W2q)), tuple(map(e, self.W2t))
+        c.M_pad = self.M_pad
+        c.bufs = {k: (tuple(map(e, v)) if isinstance(v, tuple) else e(v)) for k, v in self.bufs.items()}
+        c.bufs["err"].zero_()
+        return c
 
     @staticmethod
     def build(fmt, X, W1, W2, dY, group_lens):

@@ -178,4 +178,45 @@ __device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8
   }
 }
 
+// Whole-tile store for the 4-D view {64, rows, cols/64, G} of the output (cols a
+// multiple of 64): this warp's 32 rows x BN columns are staged as BN/64 atoms of
+// 32 x 64 bf16 (4 KB each, 128B-swizzled) in its `stg` buffer and leave with one
+// bulk tensor store at (0, row0, col0 / 64, g), clipped at the bounds.  The
+// previous tile's store must have finished reading `stg` before it is rewritten.
+template <int BN>
+__device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8_t* stg,
+                                                   const CUtensorMap* tmC4, int row0, int col0, int g,
+                                                   int rows_total, int lane) {
+  if (row0 >= rows_total) return;  // nothing of this warp's rows exists (warp-uniform)
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+#pragma unroll 1
+  for (int a = 0; a < BN / 64; ++a) {
+    uint32_t v[64];
+    if (!zero) {
+      tmem_ld64(tb + a * 64, v);
+      tmem_ld_wait();
+    } else {
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] = 0u;
+    }
+    uint8_t* sb = stg + a * 4096;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(v[j * 8 + 0]), __uint_as_float(v[j * 8 + 1]));
+      w.y = pack_bf16x2(__uint_as_float(v[j * 8 + 2]), __uint_as_float(v[j * 8 + 3]));
+      w.z = pack_bf16x2(__uint_as_float(v[j * 8 + 4]), __uint_as_float(v[j * 8 + 5]));
+      w.w = pack_bf16x2(__uint_as_float(v[j * 8 + 6]), __uint_as_float(v[j * 8 + 7]));
+      *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_4d(tmC4, smem_u32(stg), 0, row0, col0 / 64, g);
+    bulk_commit();
+  }
+}
+
 }  // namespace pgg

@@ -84,12 +84,11 @@ int launch_bf16(const Bf16Call& c) {
     uint32_t bx[2] = {64, (uint32_t)kBK};
     if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, bx, (CUtensorMapSwizzle)sw))) return st;
     if ((st = encode_tmap(&tb, bf, 2, c.b, db, sb, bx, (CUtensorMapSwizzle)sw))) return st;
-    uint64_t dc[3] = {(uint64_t)c.K, (uint64_t)c.N, (uint64_t)c.G};
-    uint64_t sc[2] = {(uint64_t)c.K * 2, (uint64_t)(c.N * c.K * 2)};
-    uint32_t bc[3] = {64, 32, 1};
-    if ((st = encode_tmap(&tc, bf, 3, c.out, dc, sc, bc, (CUtensorMapSwizzle)sw))) return st;
+    st = encode_wgrad_out(&tc, c.out, c.N, c.K, c.G, kBN, &a.c4d);
+    if (st) return st;
     a.out_cols = (int)c.K;
     a.wg_rows = (int)c.N;
+    a.nct = FastDiv((uint32_t)ceil_div(c.K, kBN));
     tiles_ub = c.G * ceil_div(c.N, kBM) * ceil_div(c.K, kBN);
   }
   if (c.mode != 2) tc = ta;  // unused outside wgrad

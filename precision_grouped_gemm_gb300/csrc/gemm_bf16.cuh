@@ -42,6 +42,8 @@ struct GemmArgs {
   void* out2;       // SwiGLU forward: H (bf16 [M, 2I]) or nullptr
   const void* aux;  // SwiGLU backward: saved H (bf16 [M, 2I])
   int32_t* err;     // device error word or nullptr
+  FastDiv nct;      // wgrad: column tiles per row tile
+  int c4d;          // wgrad: tmC is the 4-D whole-tile view (cols % 64 == 0)
 };
 
 // Shared memory: STAGES x (A tile | B tile), the epilogue staging buffers
@@ -63,7 +65,7 @@ struct GemmSmem {
 
 // Epilogue staging bytes per mode: wgrad stores its full tiles with TMA.
 template <int MODE>
-constexpr int epi_bytes() { return MODE == kWgrad ? 4 * 2 * 4096 : 0; }
+__host__ __device__ constexpr int epi_bytes() { return MODE == kWgrad ? 4 * 16384 : 0; }
 
 struct Tile {
   int g, row0, rows, col0, nkb, red0, red_valid;
@@ -76,17 +78,16 @@ __device__ __forceinline__ int tile_cols() {
 
 template <int MODE, int EPI, int BN>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int32_t* s_off,
-                                            const int32_t* s_tile) {
+                                            const int32_t* s_tile, GroupCursor& cur) {
   Tile T;
-  const int g = find_group(s_tile, a.G, t);
+  const int g = cur.at(s_tile, a.G, t);
   const int local = t - s_tile[g];
   const int off = s_off[g], len = s_off[g + 1] - s_off[g];
   T.g = g;
   if (MODE == kWgrad) {
     // column tiles vary fastest: the CTAs running at one time fill whole rows of dW_g
-    // (contiguous DRAM pages) instead of narrow stripes of many rows
-    const int nct = (a.out_cols + BN - 1) / BN;
-    const int ct = local % nct, rt = local / nct;
+    const int rt = (int)a.nct.div((uint32_t)local);
+    const int ct = local - rt * (int)a.nct.d;
     T.row0 = rt * kBM;
     T.rows = min(kBM, a.wg_rows - T.row0);
     T.col0 = ct * BN;
@@ -187,11 +188,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
+    GroupCursor cur;
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
+      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
         if (lane == 0) {
@@ -236,12 +238,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    GroupCursor cur;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
+      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile, cur);
       if (T.nkb == 0) continue;  // empty wgrad group: the epilogue writes zeros
       if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
       tc_fence_after();
@@ -305,10 +308,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
-    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 8192;  // wgrad: this warp's two 4 KB buffers
+    GroupCursor cur;
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 16384;  // wgrad: this warp's staging buffer
     int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile);
+      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile, cur);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;  // empty group: dW_g = 0, no accumulator
@@ -316,8 +320,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
           tc_fence_after();
         }
-        epi_tma_store_rows<BN>(tmem_base + acc * BN + ((uint32_t)(q * 32) << 16), zero, stg, nstore,
-                               &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, args.out_cols, lane);
+        const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
+        if (args.c4d)
+          epi_tma_store_tile<BN>(tb, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
+        else
+          epi_tma_store_rows<BN>(tb, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                 args.out_cols, lane);
         if (!zero) {
           tc_fence_before();
           mbar_arrive(smem_u32(&tempty[acc]));

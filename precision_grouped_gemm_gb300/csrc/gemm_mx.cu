@@ -49,6 +49,8 @@ struct MxArgs {
   const void* aux;
   int32_t* err;
   int64_t M_pad;
+  FastDiv nct;  // wgrad: column tiles per row tile
+  int c4d;      // wgrad: tmC is the 4-D whole-tile view
 };
 
 template <int FMT>
@@ -82,19 +84,19 @@ __device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? kMxBN
 
 template <int MODE, int EPI>
 __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_t* s_off,
-                                            const int32_t* s_tile, const int32_t* s_poff) {
+                                            const int32_t* s_tile, const int32_t* s_poff, GroupCursor& cur) {
   MxTile T;
-  const int g = find_group(s_tile, a.G, t);
+  const int g = cur.at(s_tile, a.G, t);
   const int local = t - s_tile[g];
   const int len = s_off[g + 1] - s_off[g];
   T.g = g;
   T.poff = s_poff[g];
   if (MODE == kWgrad) {
     // column tiles vary fastest (whole rows of dW_g written by concurrent CTAs)
-    const int nct = (a.out_cols + kMxBN - 1) / kMxBN;
-    T.row0 = (local / nct) * kMxBM;
+    const int rt = (int)a.nct.div((uint32_t)local);
+    T.row0 = rt * kMxBM;
     T.rows = min(kMxBM, a.wg_rows - T.row0);
-    T.col0 = (local % nct) * kMxBN;
+    T.col0 = (local - rt * (int)a.nct.d) * kMxBN;
     T.nkb = (len + kMxBK - 1) / kMxBK;
   } else {
     const int nmt = (len + kMxBM - 1) / kMxBM;
@@ -184,11 +186,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer: TMA codes + cp.async scales
+    GroupCursor cur;
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff);
+      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
         const uint32_t sa = smem0 + stage * L::kStage;
@@ -267,12 +270,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    GroupCursor cur;
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff);
+      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff, cur);
       if (T.nkb == 0) continue;
       if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
       tc_fence_after();
@@ -319,10 +323,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
+    GroupCursor cur;
     uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 8192;
     int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff);
+      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff, cur);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;
@@ -330,8 +335,12 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
           tc_fence_after();
         }
-        epi_tma_store_rows<kMxBN>(tmem_base + acc * kMxBN + ((uint32_t)(q * 32) << 16), zero, stg, nstore,
-                                  &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, args.out_cols, lane);
+        const uint32_t tbw = tmem_base + acc * kMxBN + ((uint32_t)(q * 32) << 16);
+        if (args.c4d)
+          epi_tma_store_tile<kMxBN>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
+        else
+          epi_tma_store_rows<kMxBN>(tbw, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                    args.out_cols, lane);
         if (!zero) {
           tc_fence_before();
           mbar_arrive(smem_u32(&tempty[acc]));
@@ -459,11 +468,8 @@ int launch_mx_gemm(const MxCall& c) {
     uint32_t bx[2] = {rb, 128};
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
     if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bx, sw))) return st;
-    uint64_t dc[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)c.G}, sc[2] = {(uint64_t)K * 2, (uint64_t)(N * K * 2)};
-    uint32_t bc[3] = {64, 32, 1};
-    if ((st = encode_tmap(&tc, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, c.out, dc, sc, bc,
-                          CU_TENSOR_MAP_SWIZZLE_128B)))
-      return st;
+    if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxBN, &a.c4d))) return st;
+    a.nct = FastDiv((uint32_t)cdiv(K, kMxBN));
     a.sa_ld = a.sb_ld = Mp / 32;
     a.a_rows = (int)N;
     a.b_rows = (int)K;

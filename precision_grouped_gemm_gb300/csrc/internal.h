@@ -20,12 +20,16 @@ struct DeviceInfo {
 int current_device(DeviceInfo* info);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
-// dims/strides in elements/bytes as the driver expects; rank 2 or 3.
+// dims/strides in elements/bytes as the driver expects; rank 2 to 5.
 int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                 CUtensorMapSwizzle swizzle);
 
 int cuda_status(cudaError_t e);
+
+// Output map of a wgrad dW [G, N, K] bf16: the 4-D whole-tile view when K % 64 == 0
+// and the driver accepts it (*whole_tile = 1), else the 3-D 32 x 64 box view.
+int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int bn, int* whole_tile);
 
 // BF16 grouped GEMM family (gemm_bf16.cu)
 struct Bf16Call {

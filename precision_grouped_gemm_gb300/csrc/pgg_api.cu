@@ -60,8 +60,8 @@ int current_device(DeviceInfo* info) {
 int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                 const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                 CUtensorMapSwizzle swizzle) {
-  cuuint64_t d[3], s[2];
-  cuuint32_t b[3], e[3] = {1, 1, 1};
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5] = {1, 1, 1, 1, 1};
   for (int i = 0; i < rank; ++i) {
     d[i] = dims[i];
     b[i] = box[i];
@@ -71,6 +71,27 @@ int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? PGG_OK : PGG_ERR_INVALID_ARG;
+}
+
+int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int bn, int* whole_tile) {
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (K % 64 == 0) {
+    // 4-D view {64, N, K/64, G}: one bulk store moves 32 rows x bn columns of a tile
+    uint64_t d[4] = {64, (uint64_t)N, (uint64_t)(K / 64), (uint64_t)G};
+    uint64_t s[3] = {(uint64_t)K * 2, 128, (uint64_t)(N * K * 2)};
+    uint32_t b[4] = {64, 32, (uint32_t)(bn / 64), 1};
+    if (encode_tmap(map, bf, 4, out, d, s, b, sw) == PGG_OK) {
+      *whole_tile = 1;
+      return PGG_OK;
+    }
+  }
+  // 3-D view {K, N, G}: stores of 32 x 64 boxes
+  uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
+  uint64_t s[2] = {(uint64_t)K * 2, (uint64_t)(N * K * 2)};
+  uint32_t b[3] = {64, 32, 1};
+  *whole_tile = 0;
+  return encode_tmap(map, bf, 3, out, d, s, b, sw);
 }
 
 }  // namespace pgg

@@ -81,6 +81,20 @@ __device__ __forceinline__ bool scan_groups(const int32_t* __restrict__ lens, in
   return bad;
 }
 
+// Division by a divisor fixed for the launch (Granlund-Montgomery: n / d =
+// (umulhi(n, m) + n) >> s for 0 <= n < 2^31, with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1), so per-tile index math needs no divide.
+struct FastDiv {
+  uint32_t d, m, s;
+  __host__ __device__ FastDiv() : d(1), m(0), s(0) {}
+  __host__ __device__ explicit FastDiv(uint32_t div) : d(div) {
+    s = 0;
+    while ((1u << s) < d) ++s;
+    m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << s) - d)) / d + 1);
+  }
+  __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> s; }
+};
+
 // Group owning linear tile t: the largest g with s_tile[g] <= t (empty groups
 // have s_tile[g] == s_tile[g+1] and are skipped).
 __device__ __forceinline__ int find_group(const int32_t* s_tile, int G, int t) {
@@ -91,5 +105,16 @@ __device__ __forceinline__ int find_group(const int32_t* s_tile, int G, int t) {
   }
   return lo;
 }
+
+// The group of a CTA's tiles, tracked as t grows (t, t + gridDim.x, ...): a
+// binary search for the first tile, then a short forward walk.
+struct GroupCursor {
+  int g = -1;
+  __device__ __forceinline__ int at(const int32_t* s_tile, int G, int t) {
+    if (g < 0) g = find_group(s_tile, G, t);
+    while (g + 1 < G && s_tile[g + 1] <= t) ++g;
+    return g;
+  }
+};
 
 }  // namespace pgg

@@ -322,12 +322,7 @@ def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max_time(t0.elapsed_time(t1), world, device)
     if pgg.read_error(err) != 0:
         raise RuntimeError(f"{w.name}: device error word set during the timed region")
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -350,7 +345,7 @@ def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample
                                          if w.fmt != "bf16" else "")
     attain = sum(max(work[n][1] / (hbm * 1e9), work[n][0] / (tc * 1e12)) for n in names)
     res = {
-        "value": world * flops / (ms / K) / 1e9, "unit": "TFLOP/s", "ms_per_step": ms / K, "steps": K,
+        "value": job_value(world, flops, ms, K), "unit": "TFLOP/s", "ms_per_step": ms / K, "steps": K,
         "warmup": warmup, "dtype": w.fmt, "rows_M": int(lens.sum()), "group_lens_min": int(lens.min()),
         "group_lens_max": int(lens.max()), "groups_under_128": int((lens < 128).sum()),
         "empty_groups": int((lens == 0).sum()),
@@ -370,6 +365,21 @@ def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
+
+
+def reduce_max_time(ms, world, device):
+    """The timed region's length as the slowest rank saw it (all ranks get the max)."""
+    if world <= 1:
+        return ms
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world, flops_per_step, ms_total, steps):
+    """Whole-job TFLOP/s: every rank runs its own replica of the step (weak scaling)."""
+    return world * flops_per_step / (ms_total / steps) / 1e9
 
 
 def barrier(world):

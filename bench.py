@@ -284,7 +284,7 @@ def setup_workload(w, device, cap=0):
         work = layer_work(M, G, Hd, I)
         io = lambda b: ([b.X, b.W1, b.W2, b.dY, b.group_lens], [b.Y, b.dX, b.dW1, b.dW2])
         return lens, buf, expert_layer_step, STEP_NAMES, work, io, buf.err
-    mb = MxLayerBuffers.build(w.fmt, buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens)
+    mb = MxLayerBuffers.build(w.fmt, buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens, host_lens=lens)
     del buf
     torch.cuda.synchronize()
     torch.cuda.empty_cache()

@@ -70,20 +70,42 @@ int launch_bf16(const Bf16Call& c) {
   } else if (c.mode == 1) {  // dgrad (optionally FC2 dgrad + SwiGLU bwd): A = dY [M, N]
     uint64_t da[2] = {(uint64_t)c.N, (uint64_t)c.M}, sa[1] = {(uint64_t)c.N * 2};
     uint32_t ba[2] = {64, 128};
-    uint64_t db[3] = {(uint64_t)c.K, (uint64_t)c.N, (uint64_t)c.G};
-    uint64_t sb[2] = {(uint64_t)c.K * 2, (uint64_t)(c.N * c.K * 2)};
-    uint32_t bb[3] = {64, 64, 1};
     if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, ba, (CUtensorMapSwizzle)sw))) return st;
-    if ((st = encode_tmap(&tb, bf, 3, c.b, db, sb, bb, (CUtensorMapSwizzle)sw))) return st;
+    a.b_multi = 0;
+    if (c.K % 64 == 0) {  // W as {64, N, K/64, G}: all BN/64 k-atoms of a k-block in one load
+      uint64_t d4[4] = {64, (uint64_t)c.N, (uint64_t)(c.K / 64), (uint64_t)c.G};
+      uint64_t s4[3] = {(uint64_t)c.K * 2, 128, (uint64_t)(c.N * c.K * 2)};
+      uint32_t b4[4] = {64, (uint32_t)kBK, (uint32_t)(kBN / 64), 1};
+      a.b_multi = encode_tmap(&tb, bf, 4, c.b, d4, s4, b4, (CUtensorMapSwizzle)sw) == PGG_OK;
+    }
+    if (!a.b_multi) {
+      uint64_t db[3] = {(uint64_t)c.K, (uint64_t)c.N, (uint64_t)c.G};
+      uint64_t sb[2] = {(uint64_t)c.K * 2, (uint64_t)(c.N * c.K * 2)};
+      uint32_t bb[3] = {64, 64, 1};
+      if ((st = encode_tmap(&tb, bf, 3, c.b, db, sb, bb, (CUtensorMapSwizzle)sw))) return st;
+    }
     a.out_cols = (int)c.K;
     a.red = (int)c.N;
     tiles_ub = (ceil_div(c.M, kBM) + c.G) * ceil_div(c.K, kBN);
   } else {  // wgrad: A = dY [M, N] MN-major, B = X [M, K] MN-major
-    uint64_t da[2] = {(uint64_t)c.N, (uint64_t)c.M}, sa[1] = {(uint64_t)c.N * 2};
-    uint64_t db[2] = {(uint64_t)c.K, (uint64_t)c.M}, sb[1] = {(uint64_t)c.K * 2};
-    uint32_t bx[2] = {64, (uint32_t)kBK};
-    if ((st = encode_tmap(&ta, bf, 2, c.a, da, sa, bx, (CUtensorMapSwizzle)sw))) return st;
-    if ((st = encode_tmap(&tb, bf, 2, c.b, db, sb, bx, (CUtensorMapSwizzle)sw))) return st;
+    // operands as atom views {64, M, cols/64} (one load per k-block) when cols % 64 == 0,
+    // else 64-column boxes
+    auto enc = [&](CUtensorMap* m, const void* base, int64_t cols, uint32_t atoms, int* multi) {
+      *multi = 0;
+      if (cols % 64 == 0) {
+        uint64_t d3[3] = {64, (uint64_t)c.M, (uint64_t)(cols / 64)}, s3[2] = {(uint64_t)cols * 2, 128};
+        uint32_t b3[3] = {64, (uint32_t)kBK, atoms};
+        if (encode_tmap(m, bf, 3, base, d3, s3, b3, (CUtensorMapSwizzle)sw) == PGG_OK) {
+          *multi = 1;
+          return (int)PGG_OK;
+        }
+      }
+      uint64_t d2[2] = {(uint64_t)cols, (uint64_t)c.M}, s2[1] = {(uint64_t)cols * 2};
+      uint32_t b2[2] = {64, (uint32_t)kBK};
+      return encode_tmap(m, bf, 2, base, d2, s2, b2, (CUtensorMapSwizzle)sw);
+    };
+    if ((st = enc(&ta, c.a, c.N, kBM / 64, &a.a_multi))) return st;
+    if ((st = enc(&tb, c.b, c.K, kBN / 64, &a.b_multi))) return st;
     st = encode_wgrad_out(&tc, c.out, c.N, c.K, c.G, kBN, &a.c4d);
     if (st) return st;
     a.out_cols = (int)c.K;

@@ -44,6 +44,8 @@ struct GemmArgs {
   int32_t* err;     // device error word or nullptr
   FastDiv nct;      // wgrad: column tiles per row tile
   int c4d;          // wgrad: tmC is the 4-D whole-tile view (cols % 64 == 0)
+  int a_multi;      // wgrad: tmA is the atom view {64, M, N/64} (one load per k-block)
+  int b_multi;      // wgrad / dgrad: tmB is the atom view of X {64, M, K/64} / W {64, N, K/64, G}
 };
 
 // Shared memory: STAGES x (A tile | B tile), the epilogue staging buffers
@@ -212,13 +214,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           } else if (MODE == kDgrad) {
             tma_load_2d(sa, &tmA, fb, kr, T.row0);
+            if (args.b_multi) {
+              // BN/64 atoms of 64 k-columns x kBK n-rows in one copy: smem [atom][row][64]
+              tma_load_4d(sb, &tmB, fb, 0, kr, T.col0 / 64, T.g);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, kr, T.g);
+              for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, kr, T.g);
+            }
           } else {
+            if (args.a_multi) {
+              tma_load_3d(sa, &tmA, fb, 0, T.red0 + kr, T.row0 / 64);
+            } else {
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kBK * 128, &tmA, fb, T.row0 + 64 * j, T.red0 + kr);
+              for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kBK * 128, &tmA, fb, T.row0 + 64 * j, T.red0 + kr);
+            }
+            if (args.b_multi) {
+              tma_load_3d(sb, &tmB, fb, 0, T.red0 + kr, T.col0 / 64);
+            } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, T.red0 + kr);
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, T.red0 + kr);
+            }
           }
         }
         __syncwarp();

@@ -171,8 +171,12 @@ class MxLayerBuffers:
         return c
 
     @staticmethod
-    def build(fmt, X, W1, W2, dY, group_lens):
-        """Quantize the weights (outside any timed region) and allocate every step buffer."""
+    def build(fmt, X, W1, W2, dY, group_lens, host_lens=None):
+        """Quantize the weights (outside any timed region) and allocate every step buffer.
+
+        host_lens (optional, numpy): the group lengths as the host knows them after
+        routing; the column-wise operands then take exactly sum(round_up(len, 128))
+        padded columns instead of the worst case for M rows in G groups."""
         G, I2, Hd = W1.shape
         I = I2 // 2
         M = X.shape[0]
@@ -183,7 +187,10 @@ class MxLayerBuffers:
         b.W1t = B.mx_quantize_colwise(W1f, torch.full((G,), I2, dtype=torch.int32, device=dev), fmt, G * I2)
         b.W2q = B.mx_quantize_rowwise(W2f, fmt)
         b.W2t = B.mx_quantize_colwise(W2f, torch.full((G,), Hd, dtype=torch.int32, device=dev), fmt, G * Hd)
-        b.M_pad = B.mx_pad_rows(M, G)
+        if host_lens is not None:
+            b.M_pad = max(B.PAD, int(sum(-(-int(n) // B.PAD) * B.PAD for n in host_lens)))
+        else:
+            b.M_pad = B.mx_pad_rows(M, G)
         cb = (lambda c: c) if fmt == "e4m3" else (lambda c: c // 2)
         u8, bf = torch.uint8, torch.bfloat16
         Mp = b.M_pad

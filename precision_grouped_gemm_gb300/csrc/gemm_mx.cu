@@ -76,7 +76,7 @@ struct MxSmem {
 };
 
 struct MxTile {
-  int g, row0, rows, col0, nkb, poff;
+  int g, row0, rows, col0, nkb, poff, len;
 };
 
 template <int MODE, int EPI>
@@ -91,6 +91,7 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
   const int len = s_off[g + 1] - s_off[g];
   T.g = g;
   T.poff = s_poff[g];
+  T.len = len;
   if (MODE == kWgrad) {
     // column tiles vary fastest (whole rows of dW_g written by concurrent CTAs)
     const int rt = (int)a.nct.div((uint32_t)local);
@@ -293,8 +294,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           fence_proxy_async_smem();  // cp.async-written scales -> async proxy
           tmem_cp_32x128b_x4(sfa_t, smem_desc(ssf, 0, 128, kSwizzleNone));
           tmem_cp_32x128b_x4(sfb_t, smem_desc(ssf + 512, 0, 128, kSwizzleNone));
+          // wgrad: k-steps that cover only a group's zero padding are skipped (exact)
+          int nmma = C::kMmas;
+          if (MODE == kWgrad) {
+            const int valid = T.len - kb * kMxBK;
+            const int per = kMxBK / C::kMmas;  // elements per MMA
+            if (valid < kMxBK) nmma = (valid + per - 1) / per;
+          }
 #pragma unroll
           for (int j = 0; j < C::kMmas; ++j) {
+            if (j >= nmma) break;
             const uint64_t ad = smem_desc(sa + j * 32, 16, C::kSbo, C::kSwizzle);
             const uint64_t bd = smem_desc(sb + j * 32, 16, C::kSbo, C::kSwizzle);
             const uint32_t sfid = FMT == kE4M3 ? (uint32_t)j : (uint32_t)(2 * j);

@@ -391,6 +391,44 @@ def barrier(world):
 EXTRA = [wl.DSV4_MXFP8, wl.GPTOSS_BF16, wl.ZIPF_MXFP4]
 
 
+def measure_wgrad_accumulate(device, peaks, steps):
+    """FC1 wgrad of the DeepSeek-shaped layer accumulated into an fp32 main_grad
+    [256, 4096, 4096]: algorithmic bytes = X + dH + fp32 read + write of main_grad."""
+    import precision_grouped_gemm_gb300 as pgg
+    from precision_grouped_gemm_gb300.layer import build_layer_inputs
+    w = wl.DSV4_BF16
+    lens, _, b = build_layer_inputs(w, device, allocate=False)
+    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
+    del b.W1, b.W2
+    dH = wl.gen_matrix(wl.KEY_DH, M, 2 * I, 0.25, w.seed, device=device)
+    acc = torch.zeros((G, 2 * I, Hd), dtype=torch.float32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    call = lambda: pgg.grouped_gemm_wgrad_accumulate(b.X, dH, b.group_lens, acc, err=err)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        call()
+    t1.record()
+    torch.cuda.synchronize()
+    if pgg.read_error(err) != 0:
+        raise RuntimeError("device error word set in the wgrad accumulate run")
+    ms = t0.elapsed_time(t1) / steps
+    flops = 2.0 * M * 2 * I * Hd
+    nbytes = 2.0 * M * Hd + 2.0 * M * 2 * I + 8.0 * G * 2 * I * Hd
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    res = {"call": "pgg_grouped_gemm_wgrad_accumulate (fc1 shape: dW_f32[256, 4096, 4096] += dH_g^T X_g)",
+           "ms": ms, "tflops": flops / ms / 1e9, "gbs": nbytes / ms / 1e6,
+           "roofline": {"bound": "hbm", "achieved": nbytes / ms / 1e6, "peak": hbm, "unit": "GB/s",
+                        "frac": nbytes / ms / 1e6 / hbm, "algo_bytes_per_launch": nbytes}}
+    del acc, dH, b
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_pgg(args, w):
     import precision_grouped_gemm_gb300 as pgg
     world, rank, local = dist_env()
@@ -413,6 +451,7 @@ def run_pgg(args, w):
                                                     "group_lens_min", "group_lens_max", "groups_under_128",
                                                     "empty_groups", "steps")}
                 extra[ew.name]["kernels_ms"] = {k: round(v["ms"], 4) for k, v in r["kernels"].items()}
+        extra["wgrad_accumulate_fp32"] = measure_wgrad_accumulate(device, peaks, args.extra_steps)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)

@@ -102,6 +102,20 @@ int pgg_grouped_gemm_dgrad(const void* dY, const void* W, const int32_t* group_l
 int pgg_grouped_gemm_wgrad(const void* X, const void* dY, const int32_t* group_lens, void* dW,
                            int64_t M, int64_t N, int64_t K, int G, int32_t* err, void* stream);
 
+/* Variable-K wgrad accumulated into an fp32 gradient buffer ("main_grad"):
+ *   dW_f32[g] += dY_g^T . X_g  for every group (an empty group adds nothing).
+ * The weight-gradient bridge of "[Megatron-LM] feat: add grouped gemm fp4
+ * support ... Pull Request #891", "Changes": the weight gradient is always
+ * accumulated into weight.main_grad.  fp32 accumulation in tensor memory; the
+ * add into dW_f32 is done by bulk tensor reduce-adds, one add per element per
+ * call, so repeated calls (gradient accumulation over micro-batches) are
+ * deterministic.
+ *   X [M, K] bf16, dY [M, N] bf16, dW_f32 [G, N, K] fp32 (in/out).
+ *   N % 8 == 0, K % 8 == 0.  Calls that overlap on the same dW_f32 race. */
+int pgg_grouped_gemm_wgrad_accumulate(const void* X, const void* dY, const int32_t* group_lens,
+                                      float* dW_f32, int64_t M, int64_t N, int64_t K, int G,
+                                      int32_t* err, void* stream);
+
 /* FC1 with SwiGLU folded into the epilogue ("Primus-Turbo" README, "What's
  * New": fused GroupedMLP with SwiGLU folded into the grouped GEMM; weight
  * layout w1 [g, 2I, H] "gate + up" from the MegaMoE section).

@@ -97,6 +97,12 @@ def grouped_gemm_wgrad(X: np.ndarray, dY: np.ndarray, group_lens) -> np.ndarray:
     return dW
 
 
+def grouped_gemm_wgrad_accumulate(dW0: np.ndarray, X: np.ndarray, dY: np.ndarray, group_lens) -> np.ndarray:
+    """main_grad accumulation: dW0[g] + dY_g^T . X_g (the weight-gradient bridge of
+    Pull Request #891, "Changes": the gradient is always added into weight.main_grad)."""
+    return np.asarray(dW0, dtype=np.float64) + grouped_gemm_wgrad(X, dY, group_lens)
+
+
 def sigmoid(x: np.ndarray) -> np.ndarray:
     return 1.0 / (1.0 + np.exp(-x))
 

@@ -9,13 +9,15 @@ there is no fallback path.
 from ._binding import (PggError, PAD, FMT_E4M3, FMT_E2M1, MODE_FWD, MODE_DGRAD, MODE_WGRAD,
                        EPI_NONE, EPI_SWIGLU, lib, library_path, init, version, read_error,
                        grouped_gemm_fwd, grouped_gemm_dgrad, grouped_gemm_wgrad,
+                       grouped_gemm_wgrad_accumulate,
                        grouped_fc1_swiglu, grouped_fc2_dgrad_swiglu_bwd,
                        mx_quantize_rowwise, mx_quantize_colwise, mx_grouped_gemm, mx_pad_rows)
 
 __all__ = [
     "PggError", "PAD", "FMT_E4M3", "FMT_E2M1", "MODE_FWD", "MODE_DGRAD", "MODE_WGRAD",
     "EPI_NONE", "EPI_SWIGLU", "lib", "library_path", "init", "version", "read_error",
-    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "grouped_fc1_swiglu",
+    "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "grouped_gemm_wgrad_accumulate",
+    "grouped_fc1_swiglu",
     "grouped_fc2_dgrad_swiglu_bwd", "mx_quantize_rowwise", "mx_quantize_colwise",
     "mx_grouped_gemm", "mx_pad_rows",
 ]

@@ -25,6 +25,7 @@ SIGNATURES = {
     "pgg_grouped_gemm_fwd": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_gemm_dgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_gemm_wgrad": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_grouped_gemm_wgrad_accumulate": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_fc1_swiglu": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_fc2_dgrad_swiglu_bwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_mx_quantize_rowwise": [_P, _I64, _I64, _I32, _P, _P, _P],
@@ -142,6 +143,20 @@ def grouped_gemm_wgrad(X, dY, group_lens, dW=None, err=None, stream=None):
     _check(lib().pgg_grouped_gemm_wgrad(_ptr(X), _ptr(dY), _ptr(_lens(group_lens)), _ptr(dW), M, N, K,
                                         G, _ptr(err), _stream(stream)), "pgg_grouped_gemm_wgrad")
     return dW
+
+
+def grouped_gemm_wgrad_accumulate(X, dY, group_lens, dW_f32, err=None, stream=None):
+    """dW_f32[g] += dY_g^T . X_g in place (fp32 main_grad accumulation); returns dW_f32."""
+    M, K = X.shape
+    N = dY.shape[1]
+    G = group_lens.numel()
+    if dW_f32.dtype != torch.float32 or tuple(dW_f32.shape) != (G, N, K):
+        raise ValueError("dW_f32 must be float32 [G, N, K]")
+    _dev(X, dY, group_lens, dW_f32, err)
+    _check(lib().pgg_grouped_gemm_wgrad_accumulate(_ptr(X), _ptr(dY), _ptr(_lens(group_lens)), _ptr(dW_f32), M, N,
+                                                   K, G, _ptr(err), _stream(stream)),
+           "pgg_grouped_gemm_wgrad_accumulate")
+    return dW_f32
 
 
 def grouped_fc1_swiglu(X, W1, group_lens, A=None, H=None, save_h=True, err=None, stream=None):

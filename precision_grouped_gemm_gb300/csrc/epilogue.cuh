@@ -219,4 +219,50 @@ __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8
   }
 }
 
+// fp32 accumulate: this warp's 32 rows x BN columns are added to an fp32 output
+// with bulk tensor reduce-adds, 64 columns at a time.  Each 64-column piece is
+// staged as two 32 x 32 fp32 atoms (4 KB each, 128B-swizzled) in one of two
+// alternating 8 KB halves of `stg` and leaves with one reduce-add of the 4-D
+// view {32, rows, cols/32, G} at (0, row0, (col0 + 64 p) / 32, g) (r4d), or two
+// of the 3-D view {cols, rows, G} (cols not a multiple of 32).  Every element
+// gets exactly one add per call, so the result is deterministic.
+template <int BN>
+__device__ __forceinline__ void epi_tma_reduce_f32(uint32_t tb, uint8_t* stg, int& nstore,
+                                                   const CUtensorMap* tmC, int row0, int col0, int g,
+                                                   int rows_total, int cols_total, bool r4d, int lane) {
+  if (row0 >= rows_total) return;
+#pragma unroll 1
+  for (int p = 0; p < BN / 64; ++p) {
+    const int c0 = col0 + p * 64;
+    if (c0 >= cols_total) break;
+    uint32_t v[64];
+    tmem_ld64(tb + p * 64, v);
+    tmem_ld_wait();
+    uint8_t* sb = stg + (nstore & 1) * 8192;
+    if (lane == 0) bulk_wait_read<1>();  // the reduce that last read this half is done
+    __syncwarp();
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint4 w = make_uint4(v[a * 32 + j * 4 + 0], v[a * 32 + j * 4 + 1], v[a * 32 + j * 4 + 2],
+                             v[a * 32 + j * 4 + 3]);
+        *reinterpret_cast<uint4*>(sb + a * 4096 + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+      }
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (r4d) {
+        tma_reduce_add_4d(tmC, smem_u32(sb), 0, row0, c0 / 32, g);
+      } else {
+        tma_reduce_add_3d(tmC, smem_u32(sb), c0, row0, g);
+        if (c0 + 32 < cols_total) tma_reduce_add_3d(tmC, smem_u32(sb) + 4096, c0 + 32, row0, g);
+      }
+      bulk_commit();
+    }
+    ++nstore;
+  }
+}
+
 }  // namespace pgg

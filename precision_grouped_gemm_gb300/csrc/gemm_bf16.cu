@@ -106,7 +106,8 @@ int launch_bf16(const Bf16Call& c) {
     };
     if ((st = enc(&ta, c.a, c.N, kBM / 64, &a.a_multi))) return st;
     if ((st = enc(&tb, c.b, c.K, kBN / 64, &a.b_multi))) return st;
-    st = encode_wgrad_out(&tc, c.out, c.N, c.K, c.G, kBN, &a.c4d);
+    if (c.epi == 3) st = encode_wgrad_accum_f32(&tc, c.out, c.N, c.K, c.G, &a.c4d);
+    else st = encode_wgrad_out(&tc, c.out, c.N, c.K, c.G, kBN, &a.c4d);
     if (st) return st;
     a.out_cols = (int)c.K;
     a.wg_rows = (int)c.N;
@@ -120,6 +121,7 @@ int launch_bf16(const Bf16Call& c) {
   if (c.mode == 1 && c.epi == 0) return run<kDgrad, kEpiStore>(ta, tb, tc, a, grid, c.stream);
   if (c.mode == 1 && c.epi == 2) return run<kDgrad, kEpiSwiGLUBwd>(ta, tb, tc, a, grid, c.stream);
   if (c.mode == 2 && c.epi == 0) return run<kWgrad, kEpiStore>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 2 && c.epi == 3) return run<kWgrad, kEpiAccumF32>(ta, tb, tc, a, grid, c.stream);
   return PGG_ERR_INVALID_ARG;
 }
 

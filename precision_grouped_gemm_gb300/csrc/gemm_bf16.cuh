@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != kEpiSwiGLU || (MODE == kFwd && BN == 256), "SwiGLU fwd tile");
   static_assert(EPI != kEpiSwiGLUBwd || MODE == kDgrad, "SwiGLU bwd tile");
+  static_assert(EPI != kEpiAccumF32 || MODE == kWgrad, "fp32 accumulation is a wgrad epilogue");
   constexpr uint32_t kTmemCols = 2 * BN <= 32 ? 32 : (2 * BN <= 64 ? 64 : (2 * BN <= 128 ? 128 : (2 * BN <= 256 ? 256 : 512)));
   constexpr bool kAmn = (MODE == kWgrad);
   constexpr bool kBmn = (MODE != kFwd);
@@ -343,11 +344,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tc_fence_after();
         }
         const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-        if (args.c4d)
+        if (EPI == kEpiAccumF32) {
+          // main_grad += dW_g: an empty group adds nothing
+          if (!zero)
+            epi_tma_reduce_f32<BN>(tb, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                   args.out_cols, args.c4d != 0, lane);
+        } else if (args.c4d) {
           epi_tma_store_tile<BN>(tb, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
-        else
+        } else {
           epi_tma_store_rows<BN>(tb, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
                                  args.out_cols, lane);
+        }
         if (!zero) {
           tc_fence_before();
           mbar_arrive(smem_u32(&tempty[acc]));

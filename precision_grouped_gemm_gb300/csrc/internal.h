@@ -31,10 +31,14 @@ int cuda_status(cudaError_t e);
 // and the driver accepts it (*whole_tile = 1), else the 3-D 32 x 64 box view.
 int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int bn, int* whole_tile);
 
+// Reduce-add map of an fp32 wgrad accumulator [G, N, K]: the 4-D view {32, N, K/32, G}
+// (*four_d = 1) when K % 32 == 0 and accepted, else the 3-D view {K, N, G}.
+int encode_wgrad_accum_f32(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int* four_d);
+
 // BF16 grouped GEMM family (gemm_bf16.cu)
 struct Bf16Call {
   int mode;      // 0 fwd, 1 dgrad, 2 wgrad
-  int epi;       // 0 store, 1 swiglu fwd, 2 swiglu bwd
+  int epi;       // 0 store, 1 swiglu fwd, 2 swiglu bwd, 3 fp32 accumulate (wgrad)
   const void* a; // fwd: X; dgrad: dY; wgrad: dY
   const void* b; // fwd/dgrad: W; wgrad: X
   const int32_t* group_lens;

@@ -94,6 +94,26 @@ int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, i
   return encode_tmap(map, bf, 3, out, d, s, b, sw);
 }
 
+int encode_wgrad_accum_f32(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int* four_d) {
+  const auto f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (K % 32 == 0) {
+    // 4-D view {32, N, K/32, G}: one reduce-add covers 32 rows x 64 fp32 columns
+    uint64_t d[4] = {32, (uint64_t)N, (uint64_t)(K / 32), (uint64_t)G};
+    uint64_t s[3] = {(uint64_t)K * 4, 128, (uint64_t)(N * K * 4)};
+    uint32_t b[4] = {32, 32, 2, 1};
+    if (encode_tmap(map, f32, 4, out, d, s, b, sw) == PGG_OK) {
+      *four_d = 1;
+      return PGG_OK;
+    }
+  }
+  uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
+  uint64_t s[2] = {(uint64_t)K * 4, (uint64_t)(N * K * 4)};
+  uint32_t b[3] = {32, 32, 1};
+  *four_d = 0;
+  return encode_tmap(map, f32, 3, out, d, s, b, sw);
+}
+
 }  // namespace pgg
 
 using namespace pgg;
@@ -186,6 +206,21 @@ int pgg_grouped_gemm_wgrad(const void* X, const void* dY, const int32_t* group_l
   if (!X || !dY) return PGG_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(dY)) return PGG_ERR_ALIGNMENT;
   Bf16Call c{2, 0, dY, X, group_lens, dW, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
+  return launch_bf16(c);
+}
+
+int pgg_grouped_gemm_wgrad_accumulate(const void* X, const void* dY, const int32_t* group_lens,
+                                      float* dW_f32, int64_t M, int64_t N, int64_t K, int G, int32_t* err,
+                                      void* stream) {
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (!dW_f32) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(dW_f32)) return PGG_ERR_ALIGNMENT;
+  if (M == 0) return PGG_OK;  // every group is empty: nothing to add
+  if (!X || !dY) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(dY)) return PGG_ERR_ALIGNMENT;
+  Bf16Call c{2, 3, dY, X, group_lens, dW_f32, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
   return launch_bf16(c);
 }
 

@@ -15,7 +15,7 @@ constexpr int kMaxGroups = 1024;
 
 // GEMM modes and epilogues shared by the BF16 and block-scaled kernels.
 enum GemmMode : int { kFwd = 0, kDgrad = 1, kWgrad = 2 };
-enum GemmEpi : int { kEpiStore = 0, kEpiSwiGLU = 1, kEpiSwiGLUBwd = 2 };
+enum GemmEpi : int { kEpiStore = 0, kEpiSwiGLU = 1, kEpiSwiGLUBwd = 2, kEpiAccumF32 = 3 };
 
 // Device error-word codes (the public values of pgg_status).
 constexpr int kErrBadGroupLens = 16;

@@ -422,3 +422,14 @@ def test_layer_chain_matches_step_by_step():
     _, dXb, dW1b = _brute(X, W1, dH16, lens)
     np.testing.assert_allclose(out["dX"], dXb, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(out["dW1"], dW1b, rtol=1e-12, atol=1e-12)
+
+
+def test_wgrad_accumulate_adds_to_main_grad():
+    rng = np.random.default_rng(23)
+    lens = np.array([3, 0, 5], dtype=np.int32)
+    X, dY = rng.standard_normal((8, 4)), rng.standard_normal((8, 6))
+    dW0 = rng.standard_normal((3, 6, 4))
+    out = og.grouped_gemm_wgrad_accumulate(dW0, X, dY, lens)
+    _, _, dWb = _brute(X, np.zeros((3, 6, 4)), dY, lens)
+    np.testing.assert_allclose(out, dW0 + dWb, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(out[1], dW0[1])  # empty group: main_grad unchanged

@@ -9,16 +9,16 @@ namespace {
 
 constexpr int kBN = 256;
 
-// stages per mode: fwd/dgrad stream W through 4 stages; wgrad's short reductions
-// need fewer and leave room for the TMA-store staging buffers
+// stages per mode: fwd/dgrad stream W through 4 x 48 KB; wgrad runs 6 x 24 KB (32-row
+// k-blocks) and keeps 64 KB for the TMA-store staging buffers
 template <int MODE>
-constexpr int stages() { return MODE == kWgrad ? 3 : 4; }
+constexpr int stages() { return MODE == kWgrad ? 6 : 4; }
 
 template <int MODE, int EPI>
 int run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
         int grid, cudaStream_t s) {
   constexpr int S = stages<MODE>();
-  using L = GemmSmem<kBN, S, epi_bytes<MODE>()>;
+  using L = GemmSmem<kBN, kblock<MODE>(), S, epi_bytes<MODE>()>;
   auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, S>;
   const size_t smem = L::bytes(args.G);
   static bool attr_done = false;  // per instantiation; the attribute is per device function
@@ -75,7 +75,7 @@ int launch_bf16(const Bf16Call& c) {
     if (c.K % 64 == 0) {  // W as {64, N, K/64, G}: all BN/64 k-atoms of a k-block in one load
       uint64_t d4[4] = {64, (uint64_t)c.N, (uint64_t)(c.K / 64), (uint64_t)c.G};
       uint64_t s4[3] = {(uint64_t)c.K * 2, 128, (uint64_t)(c.N * c.K * 2)};
-      uint32_t b4[4] = {64, (uint32_t)kBK, (uint32_t)(kBN / 64), 1};
+      uint32_t b4[4] = {64, (uint32_t)kblock<kDgrad>(), (uint32_t)(kBN / 64), 1};
       a.b_multi = encode_tmap(&tb, bf, 4, c.b, d4, s4, b4, (CUtensorMapSwizzle)sw) == PGG_OK;
     }
     if (!a.b_multi) {
@@ -94,14 +94,14 @@ int launch_bf16(const Bf16Call& c) {
       *multi = 0;
       if (cols % 64 == 0) {
         uint64_t d3[3] = {64, (uint64_t)c.M, (uint64_t)(cols / 64)}, s3[2] = {(uint64_t)cols * 2, 128};
-        uint32_t b3[3] = {64, (uint32_t)kBK, atoms};
+        uint32_t b3[3] = {64, (uint32_t)kblock<kWgrad>(), atoms};
         if (encode_tmap(m, bf, 3, base, d3, s3, b3, (CUtensorMapSwizzle)sw) == PGG_OK) {
           *multi = 1;
           return (int)PGG_OK;
         }
       }
       uint64_t d2[2] = {(uint64_t)cols, (uint64_t)c.M}, s2[1] = {(uint64_t)cols * 2};
-      uint32_t b2[2] = {64, (uint32_t)kBK};
+      uint32_t b2[2] = {64, (uint32_t)kblock<kWgrad>()};
       return encode_tmap(m, bf, 2, base, d2, s2, b2, (CUtensorMapSwizzle)sw);
     };
     if ((st = enc(&ta, c.a, c.N, kBM / 64, &a.a_multi))) return st;

@@ -27,7 +27,12 @@
 namespace pgg {
 
 constexpr int kBM = 128;          // MMA M (TMEM lanes)
-constexpr int kBK = 64;           // reduction step per stage: one 128-byte swizzle atom of bf16
+// Reduction rows per pipeline stage: 64 (one 128-byte swizzle atom of bf16) for the
+// K-major fwd / dgrad operands; 32 for wgrad, whose reductions are a group's few
+// rows -- twice the stages in the same shared memory keep more of the short k-loop
+// in flight (measured 4% faster on the DeepSeek-shaped fc1 wgrad than 64).
+template <int MODE>
+__host__ __device__ constexpr int kblock() { return MODE == kWgrad ? 32 : 64; }
 constexpr int kGemmThreads = 192;
 
 struct GemmArgs {
@@ -51,10 +56,10 @@ struct GemmArgs {
 // Shared memory: STAGES x (A tile | B tile), the epilogue staging buffers
 // (wgrad: 4 warps x 2 x 4 KB, 1024-byte aligned for the 128-byte swizzle), the
 // mbarriers and the group scan arrays.
-template <int BN, int STAGES, int EPI_BYTES>
+template <int BN, int BK, int STAGES, int EPI_BYTES>
 struct GemmSmem {
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kABytes = kBM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiOff = STAGES * kStageBytes;
   static constexpr int kBarOff = kEpiOff + EPI_BYTES;
@@ -93,7 +98,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int3
     T.row0 = rt * kBM;
     T.rows = min(kBM, a.wg_rows - T.row0);
     T.col0 = ct * BN;
-    T.nkb = (len + kBK - 1) / kBK;
+    T.nkb = (len + kblock<MODE>() - 1) / kblock<MODE>();
     T.red0 = off;
     T.red_valid = len;
   } else {
@@ -102,7 +107,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int3
     T.row0 = off + mt * kBM;
     T.rows = min(kBM, len - mt * kBM);
     T.col0 = ct * tile_cols<MODE, EPI, BN>();
-    T.nkb = (a.red + kBK - 1) / kBK;
+    T.nkb = (a.red + kblock<MODE>() - 1) / kblock<MODE>();
     T.red0 = 0;
     T.red_valid = a.red;
   }
@@ -114,7 +119,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  using L = GemmSmem<BN, STAGES, epi_bytes<MODE>()>;
+  constexpr int BK = kblock<MODE>();
+  using L = GemmSmem<BN, BK, STAGES, epi_bytes<MODE>()>;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != kEpiSwiGLU || (MODE == kFwd && BN == 256), "SwiGLU fwd tile");
   static_assert(EPI != kEpiSwiGLUBwd || MODE == kDgrad, "SwiGLU bwd tile");
@@ -204,7 +210,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t sa = smem_a0 + stage * L::kABytes;
           const uint32_t sb = smem_b0 + stage * L::kBBytes;
           mbar_arrive_expect_tx(fb, L::kStageBytes);
-          const int kr = kb * kBK;
+          const int kr = kb * BK;
           if (MODE == kFwd) {
             tma_load_2d(sa, &tmA, fb, kr, T.row0);
             if (EPI == kEpiSwiGLU) {
@@ -216,24 +222,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           } else if (MODE == kDgrad) {
             tma_load_2d(sa, &tmA, fb, kr, T.row0);
             if (args.b_multi) {
-              // BN/64 atoms of 64 k-columns x kBK n-rows in one copy: smem [atom][row][64]
+              // BN/64 atoms of 64 k-columns x BK n-rows in one copy: smem [atom][row][64]
               tma_load_4d(sb, &tmB, fb, 0, kr, T.col0 / 64, T.g);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, kr, T.g);
+              for (int j = 0; j < BN / 64; ++j) tma_load_3d(sb + j * BK * 128, &tmB, fb, T.col0 + 64 * j, kr, T.g);
             }
           } else {
             if (args.a_multi) {
               tma_load_3d(sa, &tmA, fb, 0, T.red0 + kr, T.row0 / 64);
             } else {
 #pragma unroll
-              for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kBK * 128, &tmA, fb, T.row0 + 64 * j, T.red0 + kr);
+              for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * BK * 128, &tmA, fb, T.row0 + 64 * j, T.red0 + kr);
             }
             if (args.b_multi) {
               tma_load_3d(sb, &tmB, fb, 0, T.red0 + kr, T.col0 / 64);
             } else {
 #pragma unroll
-              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * kBK * 128, &tmB, fb, T.col0 + 64 * j, T.red0 + kr);
+              for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * BK * 128, &tmB, fb, T.col0 + 64 * j, T.red0 + kr);
             }
           }
         }
@@ -275,21 +281,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // K=16 steps that hold group rows measured 4% slower on the DeepSeek-shaped fc1
         // wgrad than zeroing the rest of the k-block and running all four.)
         if (MODE == kWgrad) {
-          const int valid = T.red_valid - kb * kBK;
-          if (valid < kBK) {
+          const int valid = T.red_valid - kb * BK;
+          if (valid < BK) {
             const uint4 z = make_uint4(0, 0, 0, 0);
             uint8_t* pa = smem + (sa - smem_a0);
             uint8_t* pb = smem + (sb - smem_a0);
-            // each atom column is [kBK rows][128 B]; lane writes 16-byte chunk (lane & 7)
+            // each atom column is [BK rows][128 B]; lane writes 16-byte chunk (lane & 7)
             // of rows valid + (lane >> 3), +4, ... (the swizzle stays inside a row)
             const int c16 = (lane & 7) * 16;
-            for (int row = valid + (lane >> 3); row < kBK; row += 4) {
+            for (int row = valid + (lane >> 3); row < BK; row += 4) {
 #pragma unroll
               for (int atom = 0; atom < kBM / 64; ++atom)
-                *reinterpret_cast<uint4*>(pa + atom * kBK * 128 + row * 128 + c16) = z;
+                *reinterpret_cast<uint4*>(pa + atom * BK * 128 + row * 128 + c16) = z;
 #pragma unroll
               for (int atom = 0; atom < BN / 64; ++atom)
-                *reinterpret_cast<uint4*>(pb + atom * kBK * 128 + row * 128 + c16) = z;
+                *reinterpret_cast<uint4*>(pb + atom * BK * 128 + row * 128 + c16) = z;
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -297,11 +303,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         if (lane == 0) {
 #pragma unroll
-          for (int ks = 0; ks < kBK / 16; ++ks) {
+          for (int ks = 0; ks < BK / 16; ++ks) {
             uint64_t ad, bd;
-            if (kAmn) ad = smem_desc(sa + ks * 2048, kBK * 128, 1024, kSwizzle128B);
+            if (kAmn) ad = smem_desc(sa + ks * 2048, BK * 128, 1024, kSwizzle128B);
             else ad = smem_desc(sa + ks * 32, 16, 1024, kSwizzle128B);
-            if (kBmn) bd = smem_desc(sb + ks * 2048, kBK * 128, 1024, kSwizzle128B);
+            if (kBmn) bd = smem_desc(sb + ks * 2048, BK * 128, 1024, kSwizzle128B);
             else bd = smem_desc(sb + ks * 32, 16, 1024, kSwizzle128B);
             mma_f16(d_tmem, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }

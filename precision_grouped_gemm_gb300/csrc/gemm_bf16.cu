@@ -9,17 +9,17 @@ namespace {
 
 constexpr int kBN = 256;
 
-// stages per mode: fwd/dgrad stream W through 4 x 48 KB; wgrad runs 6 x 24 KB (32-row
-// k-blocks) and keeps 64 KB for the TMA-store staging buffers
-template <int MODE>
-constexpr int stages() { return MODE == kWgrad ? 6 : 4; }
+// stages: fwd/dgrad stream W through 4 x 48 KB (BK 64); wgrad keeps 64 KB for the
+// TMA-store staging and runs 6 x 24 KB (BK 32) or 3 x 48 KB (BK 64)
+template <int MODE, int BK>
+constexpr int stages() { return MODE == kWgrad ? (BK == 32 ? 6 : 3) : 4; }
 
-template <int MODE, int EPI>
+template <int MODE, int EPI, int BK = 64>
 int run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
         int grid, cudaStream_t s) {
-  constexpr int S = stages<MODE>();
-  using L = GemmSmem<kBN, kblock<MODE>(), S, epi_bytes<MODE>()>;
-  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, S>;
+  constexpr int S = stages<MODE, BK>();
+  using L = GemmSmem<kBN, BK, S, epi_bytes<MODE>()>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, S, BK>;
   const size_t smem = L::bytes(args.G);
   static bool attr_done = false;  // per instantiation; the attribute is per device function
   if (!attr_done) {
@@ -53,6 +53,7 @@ int launch_bf16(const Bf16Call& c) {
   a.err = c.err;
   a.I = (int)c.I;
   int tiles_ub = 0;
+  int wbk = 64;
 
   if (c.mode == 0) {  // forward (optionally FC1 + SwiGLU): B = W [G, Nw, K]
     const int64_t Nw = c.epi == 1 ? 2 * c.I : c.N;
@@ -75,7 +76,7 @@ int launch_bf16(const Bf16Call& c) {
     if (c.K % 64 == 0) {  // W as {64, N, K/64, G}: all BN/64 k-atoms of a k-block in one load
       uint64_t d4[4] = {64, (uint64_t)c.N, (uint64_t)(c.K / 64), (uint64_t)c.G};
       uint64_t s4[3] = {(uint64_t)c.K * 2, 128, (uint64_t)(c.N * c.K * 2)};
-      uint32_t b4[4] = {64, (uint32_t)kblock<kDgrad>(), (uint32_t)(kBN / 64), 1};
+      uint32_t b4[4] = {64, 64, (uint32_t)(kBN / 64), 1};
       a.b_multi = encode_tmap(&tb, bf, 4, c.b, d4, s4, b4, (CUtensorMapSwizzle)sw) == PGG_OK;
     }
     if (!a.b_multi) {
@@ -88,20 +89,21 @@ int launch_bf16(const Bf16Call& c) {
     a.red = (int)c.N;
     tiles_ub = (ceil_div(c.M, kBM) + c.G) * ceil_div(c.K, kBN);
   } else {  // wgrad: A = dY [M, N] MN-major, B = X [M, K] MN-major
+    wbk = (c.M <= 256 * (int64_t)c.G) ? 32 : 64;  // short groups: smaller, deeper k-blocks
     // operands as atom views {64, M, cols/64} (one load per k-block) when cols % 64 == 0,
     // else 64-column boxes
     auto enc = [&](CUtensorMap* m, const void* base, int64_t cols, uint32_t atoms, int* multi) {
       *multi = 0;
       if (cols % 64 == 0) {
         uint64_t d3[3] = {64, (uint64_t)c.M, (uint64_t)(cols / 64)}, s3[2] = {(uint64_t)cols * 2, 128};
-        uint32_t b3[3] = {64, (uint32_t)kblock<kWgrad>(), atoms};
+        uint32_t b3[3] = {64, (uint32_t)wbk, atoms};
         if (encode_tmap(m, bf, 3, base, d3, s3, b3, (CUtensorMapSwizzle)sw) == PGG_OK) {
           *multi = 1;
           return (int)PGG_OK;
         }
       }
       uint64_t d2[2] = {(uint64_t)cols, (uint64_t)c.M}, s2[1] = {(uint64_t)cols * 2};
-      uint32_t b2[2] = {64, (uint32_t)kblock<kWgrad>()};
+      uint32_t b2[2] = {64, (uint32_t)wbk};
       return encode_tmap(m, bf, 2, base, d2, s2, b2, (CUtensorMapSwizzle)sw);
     };
     if ((st = enc(&ta, c.a, c.N, kBM / 64, &a.a_multi))) return st;
@@ -120,8 +122,12 @@ int launch_bf16(const Bf16Call& c) {
   if (c.mode == 0 && c.epi == 1) return run<kFwd, kEpiSwiGLU>(ta, tb, tc, a, grid, c.stream);
   if (c.mode == 1 && c.epi == 0) return run<kDgrad, kEpiStore>(ta, tb, tc, a, grid, c.stream);
   if (c.mode == 1 && c.epi == 2) return run<kDgrad, kEpiSwiGLUBwd>(ta, tb, tc, a, grid, c.stream);
-  if (c.mode == 2 && c.epi == 0) return run<kWgrad, kEpiStore>(ta, tb, tc, a, grid, c.stream);
-  if (c.mode == 2 && c.epi == 3) return run<kWgrad, kEpiAccumF32>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 2 && c.epi == 0)
+    return wbk == 32 ? run<kWgrad, kEpiStore, 32>(ta, tb, tc, a, grid, c.stream)
+                     : run<kWgrad, kEpiStore, 64>(ta, tb, tc, a, grid, c.stream);
+  if (c.mode == 2 && c.epi == 3)
+    return wbk == 32 ? run<kWgrad, kEpiAccumF32, 32>(ta, tb, tc, a, grid, c.stream)
+                     : run<kWgrad, kEpiAccumF32, 64>(ta, tb, tc, a, grid, c.stream);
   return PGG_ERR_INVALID_ARG;
 }
 

@@ -27,12 +27,11 @@
 namespace pgg {
 
 constexpr int kBM = 128;          // MMA M (TMEM lanes)
-// Reduction rows per pipeline stage: 64 (one 128-byte swizzle atom of bf16) for the
-// K-major fwd / dgrad operands; 32 for wgrad, whose reductions are a group's few
-// rows -- twice the stages in the same shared memory keep more of the short k-loop
-// in flight (measured 4% faster on the DeepSeek-shaped fc1 wgrad than 64).
-template <int MODE>
-__host__ __device__ constexpr int kblock() { return MODE == kWgrad ? 32 : 64; }
+// Reduction rows per pipeline stage (BK): 64 (one 128-byte swizzle atom of bf16) for
+// the K-major fwd / dgrad operands.  wgrad runs 32 when groups are short (a few
+// hundred rows): twice the stages in the same shared memory keep more of the short
+// k-loop in flight (4% faster on the DeepSeek-shaped fc1 wgrad); long reductions
+// keep 64 (fewer, larger steps; 10% faster on the GPT-OSS-shaped wgrad).
 constexpr int kGemmThreads = 192;
 
 struct GemmArgs {
@@ -83,7 +82,7 @@ __device__ __forceinline__ int tile_cols() {
   return EPI == kEpiSwiGLU ? BN / 2 : BN;
 }
 
-template <int MODE, int EPI, int BN>
+template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int32_t* s_off,
                                             const int32_t* s_tile, GroupCursor& cur) {
   Tile T;
@@ -98,7 +97,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int3
     T.row0 = rt * kBM;
     T.rows = min(kBM, a.wg_rows - T.row0);
     T.col0 = ct * BN;
-    T.nkb = (len + kblock<MODE>() - 1) / kblock<MODE>();
+    T.nkb = (len + BK - 1) / BK;
     T.red0 = off;
     T.red_valid = len;
   } else {
@@ -107,19 +106,19 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int3
     T.row0 = off + mt * kBM;
     T.rows = min(kBM, len - mt * kBM);
     T.col0 = ct * tile_cols<MODE, EPI, BN>();
-    T.nkb = (a.red + kblock<MODE>() - 1) / kblock<MODE>();
+    T.nkb = (a.red + BK - 1) / BK;
     T.red0 = 0;
     T.red_valid = a.red;
   }
   return T;
 }
 
-template <int MODE, int EPI, int BN, int STAGES>
+template <int MODE, int EPI, int BN, int STAGES, int BK>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
-  constexpr int BK = kblock<MODE>();
+  static_assert(BK == 64 || (MODE == kWgrad && BK == 32), "k-block");
   using L = GemmSmem<BN, BK, STAGES, epi_bytes<MODE>()>;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != kEpiSwiGLU || (MODE == kFwd && BN == 256), "SwiGLU fwd tile");
@@ -202,7 +201,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     long long issued = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile, cur);
+      const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
         if (lane == 0) {
@@ -266,7 +265,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile, cur);
+      const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
       if (T.nkb == 0) continue;  // empty wgrad group: the epilogue writes zeros
       if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
       tc_fence_after();
@@ -336,7 +335,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 16384;  // wgrad: this warp's staging buffer
     int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const Tile T = decode_tile<MODE, EPI, BN>(t, args, s_off, s_tile, cur);
+      const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;  // empty group: dW_g = 0, no accumulator

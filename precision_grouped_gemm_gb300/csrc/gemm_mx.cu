@@ -28,6 +28,7 @@ namespace pgg {
 namespace {
 
 constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
+constexpr int kMxWgradBN = 256;                        // wgrad tiles are 128 x 256
 constexpr int kMxThreads = 192;
 constexpr int kE4M3 = 1;
 
@@ -63,11 +64,13 @@ struct MxCfg {
   static constexpr int kTileBytes = 128 * kRowBytes;
 };
 
-template <int FMT, int STAGES, int EPI_BYTES>
+// BN = 128 (two accumulators, double-buffered) or 256 (wgrad: one accumulator;
+// TMEM cannot hold two 256-column accumulators next to the scale factors).
+template <int FMT, int BN, int STAGES, int EPI_BYTES>
 struct MxSmem {
   static constexpr int kA = MxCfg<FMT>::kTileBytes;
-  static constexpr int kB = MxCfg<FMT>::kTileBytes;
-  static constexpr int kSF = 1024;  // SFA atom (512 B) + SFB atom (512 B)
+  static constexpr int kB = MxCfg<FMT>::kRowBytes * BN;
+  static constexpr int kSF = BN == 256 ? 2048 : 1024;  // SFA atom + BN/128 SFB atoms (512 B each), padded
   static constexpr int kStage = kA + kB + kSF;
   static constexpr int kEpiOff = STAGES * kStage;
   static constexpr int kBarOff = kEpiOff + EPI_BYTES;
@@ -82,7 +85,7 @@ struct MxTile {
 template <int MODE, int EPI>
 __device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? kMxBN / 2 : kMxBN; }
 
-template <int MODE, int EPI>
+template <int MODE, int EPI, int BN>
 __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_t* s_off,
                                             const int32_t* s_tile, const int32_t* s_poff, GroupCursor& cur) {
   MxTile T;
@@ -97,7 +100,7 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
     const int rt = (int)a.nct.div((uint32_t)local);
     T.row0 = rt * kMxBM;
     T.rows = min(kMxBM, a.wg_rows - T.row0);
-    T.col0 = (local - rt * (int)a.nct.d) * kMxBN;
+    T.col0 = (local - rt * (int)a.nct.d) * BN;
     T.nkb = (len + kMxBK - 1) / kMxBK;
   } else {
     const int nmt = (len + kMxBM - 1) / kMxBM;
@@ -110,15 +113,19 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
   return T;
 }
 
-template <int FMT, int MODE, int EPI, int STAGES>
+template <int FMT, int MODE, int EPI, int STAGES, int BN>
 __global__ void __launch_bounds__(kMxThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
   using C = MxCfg<FMT>;
-  using L = MxSmem<FMT, STAGES, MODE == kWgrad ? 32768 : 0>;
-  constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, kMxBN);
+  static_assert(BN == 128 || (BN == 256 && MODE == kWgrad), "BN");
+  using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
+  constexpr int NACC = BN == 256 ? 1 : 2;                // accumulator buffers
+  constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
   constexpr uint32_t kTmemCols = 512;
-  constexpr uint32_t kSfCol0 = 2 * kMxBN;  // scale-factor columns after the two accumulators
+  constexpr uint32_t kSfCol0 = NACC * BN;                 // scale-factor columns after the accumulators
+  constexpr uint32_t kSfPer = 4 + 4 * (BN / 128);         // per stage: SFA 4 + SFB 4 per 128 rows
+  static_assert(kSfCol0 + STAGES * kSfPer <= kTmemCols, "TMEM columns");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     TileCount tc;
     if (MODE == kWgrad) {
       tc.bm = 0;
-      tc.per_row_tile = ((args.wg_rows + kMxBM - 1) / kMxBM) * ((args.out_cols + kMxBN - 1) / kMxBN);
+      tc.per_row_tile = ((args.wg_rows + kMxBM - 1) / kMxBM) * ((args.out_cols + BN - 1) / BN);
     } else {
       constexpr int tcw = EPI == kEpiSwiGLU ? kMxBN / 2 : kMxBN;
       tc.bm = kMxBM;
@@ -192,7 +199,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint32_t phase = 0;
     long long issued = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff, cur);
+      const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
         const uint32_t sa = smem0 + stage * L::kStage;
@@ -231,13 +238,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           sfa_col = sfb_col = kb * 4;
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < BN / 32; ++i) {
           const int m = lane + 32 * i;
           // A rows: fwd/dgrad token rows; wgrad rows of dY^T (n)
-          const int ar = T.row0 + m;
-          const bool aok = ar < args.a_rows;
-          cp_async_4(ssf + (lane * 4 + i) * 4, args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0),
-                     aok ? 4u : 0u);
+          if (i < 4) {
+            const int ar = T.row0 + m;
+            const bool aok = ar < args.a_rows;
+            cp_async_4(ssf + (lane * 4 + i) * 4, args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0),
+                       aok ? 4u : 0u);
+          }
           // B rows
           int br;
           bool bok;
@@ -251,8 +260,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             br = T.col0 + m;
             bok = br < args.b_rows;
           }
-          cp_async_4(ssf + 512 + (lane * 4 + i) * 4, args.SB + (bok ? (int64_t)br * args.sb_ld + sfb_col : 0),
-                     bok ? 4u : 0u);
+          // B row m goes to atom m / 128, word 4 (m % 32) + (m % 128) / 32
+          cp_async_4(ssf + 512 + (i / 4) * 512 + (lane * 4 + (i % 4)) * 4,
+                     args.SB + (bok ? (int64_t)br * args.sb_ld + sfb_col : 0), bok ? 4u : 0u);
         }
         cp_async_arrive_noinc(fb);
         __syncwarp();
@@ -277,11 +287,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff, cur);
+      const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       if (T.nkb == 0) continue;
       if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + acc * kMxBN;
+      const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!warp_wait(smem_u32(&full[stage]), phase, s_abort)) { aborted = true; break; }
         tc_fence_after();
@@ -289,11 +299,13 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sa = smem0 + stage * L::kStage;
           const uint32_t sb = sa + L::kA;
           const uint32_t ssf = sb + L::kB;
-          const uint32_t sfa_t = tmem_base + kSfCol0 + stage * 8;
+          const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;
           const uint32_t sfb_t = sfa_t + 4;
           fence_proxy_async_smem();  // cp.async-written scales -> async proxy
           tmem_cp_32x128b_x4(sfa_t, smem_desc(ssf, 0, 128, kSwizzleNone));
-          tmem_cp_32x128b_x4(sfb_t, smem_desc(ssf + 512, 0, 128, kSwizzleNone));
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32: 4 columns per 128 rows
+            tmem_cp_32x128b_x4(sfb_t + 4 * h, smem_desc(ssf + 512 + 512 * h, 0, 128, kSwizzleNone));
           // wgrad: k-steps that cover only a group's zero padding are skipped (exact)
           int nmma = C::kMmas;
           if (MODE == kWgrad) {
@@ -319,7 +331,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       if (aborted) break;
       if (lane == 0) mma_commit(smem_u32(&tfull[acc]));
       __syncwarp();
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
     }
     if (aborted && lane == 0) {
       mma_commit(smem_u32(drain));
@@ -333,10 +345,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
     GroupCursor cur;
-    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 8192;
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (32 * BN * 2);
     int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI>(t, args, s_off, s_tile, s_poff, cur);
+      const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;
@@ -344,34 +356,34 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
           tc_fence_after();
         }
-        const uint32_t tbw = tmem_base + acc * kMxBN + ((uint32_t)(q * 32) << 16);
+        const uint32_t tbw = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
         if (args.c4d)
-          epi_tma_store_tile<kMxBN>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
+          epi_tma_store_tile<BN>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
         else
-          epi_tma_store_rows<kMxBN>(tbw, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
-                                    args.out_cols, lane);
+          epi_tma_store_rows<BN>(tbw, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                 args.out_cols, lane);
         if (!zero) {
           tc_fence_before();
           mbar_arrive(smem_u32(&tempty[acc]));
-          if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+          if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
         }
         continue;
       }
       if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
       tc_fence_after();
-      const uint32_t tb = tmem_base + acc * kMxBN + ((uint32_t)(q * 32) << 16);
+      const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       const size_t grow = (size_t)T.row0 + r;
       if (EPI == kEpiSwiGLU) {
-        epi_swiglu<kMxBN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
+        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
       } else if (EPI == kEpiSwiGLUBwd) {
-        epi_swiglu_bwd<kMxBN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
+        epi_swiglu_bwd<BN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
                               args.I);
       } else {
-        epi_store<kMxBN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
+        epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
     }
   }
 
@@ -385,32 +397,32 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-template <int FMT, int MODE, int EPI, int STAGES>
+template <int FMT, int MODE, int EPI, int STAGES, int BN = kMxBN>
 int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a, int grid,
            cudaStream_t s) {
-  using L = MxSmem<FMT, STAGES, MODE == kWgrad ? 32768 : 0>;
-  auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES>;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::bytes(kMaxGroups));
-    if (e != cudaSuccess) return cuda_status(e);
-    attr_done = true;
+  using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
+  auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES, BN>;
+  const size_t smem = L::bytes(a.G);
+  static size_t attr_bytes = 0;  // per instantiation: raised to the largest G seen
+  if (smem > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e == cudaErrorInvalidValue ? PGG_ERR_UNSUPPORTED : cuda_status(e);
+    attr_bytes = smem;
   }
-  kern<<<grid, kMxThreads, L::bytes(a.G), s>>>(ta, tb, tc, a);
+  kern<<<grid, kMxThreads, smem, s>>>(ta, tb, tc, a);
   return cuda_status(cudaGetLastError());
 }
 
 template <int FMT>
 int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
-  constexpr int kS = FMT == kE4M3 ? 6 : 8;       // stages for fwd / dgrad
-  constexpr int kSw = FMT == kE4M3 ? 5 : 8;      // wgrad keeps 32 KB for its TMA-store staging
+  constexpr int kS = FMT == kE4M3 ? 6 : 8;       // stages for fwd / dgrad (128 x 128 tiles)
+  constexpr int kSw = FMT == kE4M3 ? 3 : 5;      // wgrad: 128 x 256 tiles, 64 KB of TMA-store staging
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS>(ta, tb, tc, a, grid, s);
-  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw>(ta, tb, tc, a, grid, s);
+  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, 256>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
 
@@ -474,17 +486,17 @@ int launch_mx_gemm(const MxCall& c) {
     const int64_t N = c.N, K = c.K, Mp = c.M_pad;
     uint64_t da[2] = {bytes(Mp), (uint64_t)N}, sa[1] = {bytes(Mp)};
     uint64_t db[2] = {bytes(Mp), (uint64_t)K}, sb[1] = {bytes(Mp)};
-    uint32_t bx[2] = {rb, 128};
+    uint32_t bx[2] = {rb, 128}, bw[2] = {rb, (uint32_t)kMxWgradBN};
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
-    if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bx, sw))) return st;
-    if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxBN, &a.c4d))) return st;
-    a.nct = FastDiv((uint32_t)cdiv(K, kMxBN));
+    if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bw, sw))) return st;
+    if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxWgradBN, &a.c4d))) return st;
+    a.nct = FastDiv((uint32_t)cdiv(K, kMxWgradBN));
     a.sa_ld = a.sb_ld = Mp / 32;
     a.a_rows = (int)N;
     a.b_rows = (int)K;
     a.out_cols = (int)K;
     a.wg_rows = (int)N;
-    tiles_ub = c.G * cdiv(N, kMxBM) * cdiv(K, kMxBN);
+    tiles_ub = c.G * cdiv(N, kMxBM) * cdiv(K, kMxWgradBN);
   }
   if (c.mode != 2) tc = ta;  // unused outside wgrad
   const int grid = std::max(1, std::min(dev.sms, tiles_ub));

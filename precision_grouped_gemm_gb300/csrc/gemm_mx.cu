@@ -28,7 +28,10 @@ namespace pgg {
 namespace {
 
 constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
-constexpr int kMxWgradBN = 256;                        // wgrad tiles are 128 x 256
+// wgrad tiles: 128 x 128 with a double-buffered accumulator.  (128 x 256 with one
+// accumulator -- TMEM cannot hold two next to the scale factors -- measured 12%
+// slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
+constexpr int kMxWgradBN = 128;
 constexpr int kMxThreads = 192;
 constexpr int kE4M3 = 1;
 
@@ -417,12 +420,12 @@ template <int FMT>
 int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kS = FMT == kE4M3 ? 6 : 8;       // stages for fwd / dgrad (128 x 128 tiles)
-  constexpr int kSw = FMT == kE4M3 ? 3 : 5;      // wgrad: 128 x 256 tiles, 64 KB of TMA-store staging
+  constexpr int kSw = FMT == kE4M3 ? 5 : 8;      // wgrad keeps 32 KB for its TMA-store staging
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS>(ta, tb, tc, a, grid, s);
-  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, 256>(ta, tb, tc, a, grid, s);
+  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kMxWgradBN>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
 

@@ -186,13 +186,20 @@ int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t*
  *                   deq(A)[:, r] deq(B)[:, r]^T with A = dY column-wise
  *                   codes [N, M_pad], B = X column-wise codes [K, M_pad]
  *                   (pgg_mx_quantize_colwise); empty groups give 0.
+ * Fused MX output (SwiGLU epilogues only; both NULL to skip): out_codes /
+ * out_scales receive the row-wise MX quantization, in `fmt`, of the bf16 tensor
+ * written to `out` (A of the forward, dH of the dgrad) -- bit-identical to
+ * pgg_mx_quantize_rowwise(out) -- so the next GEMM's operand needs no separate
+ * quantize pass ("Primus-Turbo" README, "What's New": fused GroupedMLP in
+ * FP8 / MXFP8).  The width of `out` (I) must be a multiple of 32.
  * Sizes: the reduction axis is a multiple of 128 (fwd K, dgrad N); the other
  * dimensions are multiples of 8 (N of a SwiGLU forward a multiple of 16); e2m1
  * codes are packed two per byte.  fp32 accumulation, bf16 output. */
 int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const uint8_t* SA,
                         const uint8_t* B, const uint8_t* SB, const void* H,
-                        const int32_t* group_lens, void* out, void* out2, int64_t M, int64_t N,
-                        int64_t K, int G, int64_t M_pad, int32_t* err, void* stream);
+                        const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
+                        uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G,
+                        int64_t M_pad, int32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

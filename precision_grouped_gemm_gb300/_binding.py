@@ -30,8 +30,8 @@ SIGNATURES = {
     "pgg_grouped_fc2_dgrad_swiglu_bwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_mx_quantize_rowwise": [_P, _I64, _I64, _I32, _P, _P, _P],
     "pgg_mx_quantize_colwise": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P],
-    "pgg_mx_grouped_gemm": [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64,
-                            _I32, _I64, _P, _P],
+    "pgg_mx_grouped_gemm": [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
+                            _I64, _I32, _I64, _P, _P],
 }
 
 
@@ -226,8 +226,11 @@ def mx_quantize_colwise(x, group_lens, fmt, M_pad=None, codes_t=None, scales_t=N
 
 
 def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2=None, H=None,
-                    epilogue=EPI_NONE, M_pad=0, err=None, stream=None):
-    """Block-scaled grouped GEMM on MX operands (see pgg.h for the per-mode layouts)."""
+                    epilogue=EPI_NONE, M_pad=0, err=None, stream=None, out_q=None):
+    """Block-scaled grouped GEMM on MX operands (see pgg.h for the per-mode layouts).
+
+    out_q: optional (codes, scales) receiving the row-wise MX quantization of `out`
+    (SwiGLU epilogues only)."""
     f = _FMT[fmt]
     G = group_lens.numel()
     dev = A.device
@@ -239,8 +242,9 @@ def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2
         else:
             shape = (G, N, K)
         out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
-    _dev(A, SA, B, SB, group_lens, out, out2, H, err)
+    qc, qs = out_q if out_q is not None else (None, None)
+    _dev(A, SA, B, SB, group_lens, out, out2, H, err, qc, qs)
     _check(lib().pgg_mx_grouped_gemm(mode, f, epilogue, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(H),
-                                     _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), M, N, K, G, M_pad,
-                                     _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
+                                     _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), _ptr(qc), _ptr(qs), M, N,
+                                     K, G, M_pad, _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
     return out

@@ -4,6 +4,7 @@
 // Thread (warp quarter q, lane) owns accumulator row q*32 + lane; `tb` is the
 // TMEM address of that warp's lane quarter at the tile's first column.
 #pragma once
+#include "mx_codec.cuh"
 #include "ptx.cuh"
 
 namespace pgg {
@@ -73,12 +74,34 @@ __device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* dst_row, b
   }
 }
 
+// bf16 bit patterns of 32 fp32 values (round to nearest even, as store_row32).
+__device__ __forceinline__ void bf16_bits32(const float* v, uint32_t (&b)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) b[j] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+}
+
+// Optional fused MX output (QF = kE4M3 / kE2M1): the 32 bf16 values just stored at
+// columns c0..c0+31 of row `grow` of a [rows, ld] tensor form one row-wise MX block;
+// its codes and scale go to codes[grow, c0 ..] / scales[grow, c0 / 32] exactly as
+// the row-wise quantize kernel would write them for the stored tensor.
+template <int QF>
+__device__ __forceinline__ void mx_emit(const float* v, uint8_t* codes, uint8_t* scales, size_t grow, int ld,
+                                        int c0) {
+  uint32_t b[32];
+  bf16_bits32(v, b);
+  const size_t cb = QF == kE4M3 ? (size_t)ld : (size_t)ld / 2;  // code bytes per row
+  const uint32_t sc = quantize_block32<QF>(b, codes + grow * cb + (QF == kE4M3 ? c0 : c0 / 2));
+  scales[grow * (size_t)(ld / 32) + c0 / 32] = (uint8_t)sc;
+}
+
 // FC1 SwiGLU: accumulator columns [0, BN/2) are gate columns col0.., [BN/2, BN)
 // the matching up columns.  A[row, col0 + c] = silu(gate) * up (fp32), and the
 // pre-activation H[row, col0 + c] = gate, H[row, I + col0 + c] = up when H != null.
-template <int BN>
+// QF != 0 and qcodes != null: A is also emitted MX-quantized (row-wise, I % 32 == 0).
+template <int BN, int QF = 0>
 __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t grow,
-                                           bool row_ok, int col0, int I) {
+                                           bool row_ok, int col0, int I, uint8_t* qcodes = nullptr,
+                                           uint8_t* qscales = nullptr) {
 #pragma unroll 1
   for (int c = 0; c < BN / 64; ++c) {
     uint32_t rg[32], ru[32];
@@ -96,6 +119,7 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
       }
       const int nc = min(32, I - c0);
       store_row32(A + grow * I + c0, a, nc);
+      if (QF != 0 && qcodes) mx_emit<QF == 0 ? 1 : QF>(a, qcodes, qscales, grow, I, c0);
       if (H) {
         store_row32(H + grow * (2 * (size_t)I) + c0, g, nc);
         store_row32(H + grow * (2 * (size_t)I) + I + c0, u, nc);
@@ -106,9 +130,11 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
 
 // FC2 dgrad + SwiGLU backward: accumulator = dA[row, col0 ..]; with g, u from
 // the saved H: dH[:, c] = dA u s (1 + g (1 - s)), dH[:, I + c] = dA g s, s = sigmoid(g).
-template <int BN>
+// QF != 0 and qcodes != null: dH [rows, 2I] is also emitted MX-quantized (row-wise).
+template <int BN, int QF = 0>
 __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
-                                               size_t grow, bool row_ok, int col0, int I) {
+                                               size_t grow, bool row_ok, int col0, int I,
+                                               uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t rd[32];
@@ -129,6 +155,10 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
       }
       store_row32(dH + grow * (2 * (size_t)I) + c0, dg, nc);
       store_row32(dH + grow * (2 * (size_t)I) + I + c0, du, nc);
+      if (QF != 0 && qcodes) {
+        mx_emit<QF == 0 ? 1 : QF>(dg, qcodes, qscales, grow, 2 * I, c0);
+        mx_emit<QF == 0 ? 1 : QF>(du, qcodes, qscales, grow, 2 * I, I + c0);
+      }
     }
   }
 }

@@ -21,6 +21,7 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "mx_codec.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
@@ -33,7 +34,6 @@ constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
 // slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
 constexpr int kMxWgradBN = 128;
 constexpr int kMxThreads = 192;
-constexpr int kE4M3 = 1;
 
 struct MxArgs {
   const int32_t* group_lens;
@@ -53,6 +53,8 @@ struct MxArgs {
   const void* aux;
   int32_t* err;
   int64_t M_pad;
+  uint8_t* q_codes;   // SwiGLU epilogues: row-wise MX codes of `out` (or nullptr)
+  uint8_t* q_scales;  // and their scales
   FastDiv nct;  // wgrad: column tiles per row tile
   int c4d;      // wgrad: tmC is the 4-D whole-tile view
 };
@@ -377,10 +379,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       const size_t grow = (size_t)T.row0 + r;
       if (EPI == kEpiSwiGLU) {
-        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
+        epi_swiglu<BN, FMT>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I,
+                            args.q_codes, args.q_scales);
       } else if (EPI == kEpiSwiGLUBwd) {
-        epi_swiglu_bwd<BN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
-                              args.I);
+        epi_swiglu_bwd<BN, FMT>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
+                                args.I, args.q_codes, args.q_scales);
       } else {
         epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
       }
@@ -454,6 +457,8 @@ int launch_mx_gemm(const MxCall& c) {
   a.aux = c.H;
   a.err = c.err;
   a.M_pad = c.M_pad;
+  a.q_codes = c.q_codes;
+  a.q_scales = c.q_scales;
   int tiles_ub;
   if (c.mode == 0) {
     const int64_t N = c.N, K = c.K;

@@ -68,6 +68,8 @@ struct MxCall {
   const int32_t* group_lens;
   void* out;
   void* out2;
+  uint8_t* q_codes;   // fused row-wise MX output of `out` (SwiGLU epilogues) or nullptr
+  uint8_t* q_scales;
   int64_t M, N, K, M_pad;
   int G;
   int32_t* err;

@@ -14,50 +14,12 @@
 #include <algorithm>
 
 #include "internal.h"
+#include "mx_codec.cuh"
 #include "ptx.cuh"
 #include "sched.cuh"
 
 namespace pgg {
 namespace {
-
-constexpr int kE4M3 = 1;
-constexpr int kE2M1 = 2;
-
-template <int FMT>
-__device__ __forceinline__ int emax() { return FMT == kE4M3 ? 8 : 2; }
-
-// amax bits (bf16 magnitude bits, ordered as integers) -> (scale code, fp32 multiplier 2^-E);
-// returns false for a non-finite block.
-template <int FMT>
-__device__ __forceinline__ bool block_scale(uint32_t amax_bits, uint32_t& code, float& mult) {
-  if (amax_bits >= 0x7F80u) {
-    code = 0xFFu;
-    mult = 0.0f;
-    return false;
-  }
-  int e = (int)(amax_bits >> 7) - 127 - emax<FMT>();
-  e = max(e, -127);  // upper clamp is never reached from bf16 (max exponent 127)
-  code = (uint32_t)(e + 127);
-  mult = __uint_as_float((uint32_t)(127 - e) << 23);
-  return true;
-}
-
-// two fp32 -> two e4m3 bytes (lo in the low byte)
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
-  uint16_t r;
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-// two fp32 -> one byte of two e2m1 nibbles (lo in the low nibble)
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
-  uint32_t r;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-      "cvt.u32.u8 %0, t;\n\t}"
-      : "=r"(r)
-      : "f"(hi), "f"(lo));
-  return r;
-}
 
 // ------------------------------------------------------------------ row-wise
 // The tensor is a flat run of 32-element blocks (C % 32 == 0), so block i's

@@ -279,8 +279,9 @@ int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t*
 
 int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const uint8_t* SA,
                         const uint8_t* B, const uint8_t* SB, const void* H,
-                        const int32_t* group_lens, void* out, void* out2, int64_t M, int64_t N,
-                        int64_t K, int G, int64_t M_pad, int32_t* err, void* stream) {
+                        const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
+                        uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G, int64_t M_pad,
+                        int32_t* err, void* stream) {
   int st;
   if (mode < 0 || mode > 2) return PGG_ERR_INVALID_ARG;
   if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
@@ -298,9 +299,17 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
   if (mode == PGG_MODE_DGRAD && N % 128) return PGG_ERR_ALIGNMENT;
   if (mode == PGG_MODE_WGRAD && (M_pad <= 0 || M_pad % PGG_MX_PAD || M_pad >= kMaxRows))
     return PGG_ERR_ALIGNMENT;
+  if ((out_codes != nullptr) != (out_scales != nullptr)) return PGG_ERR_INVALID_ARG;
+  if (out_codes) {
+    // fused row-wise MX output of `out`: SwiGLU epilogues only, whole 32-column blocks
+    const int64_t w = mode == PGG_MODE_FWD ? N / 2 : K;
+    if (epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
+    if (w % 32) return PGG_ERR_ALIGNMENT;
+    if (!aligned16(out_codes)) return PGG_ERR_ALIGNMENT;
+  }
   if (M == 0 && mode != PGG_MODE_WGRAD) return PGG_OK;
-  MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, M, N, K, M_pad, G, err,
-           as_stream(stream)};
+  MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales,
+           M, N, K, M_pad, G, err, as_stream(stream)};
   return launch_mx_gemm(c);
 }
 

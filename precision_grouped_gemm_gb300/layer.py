@@ -139,9 +139,8 @@ def expert_inputs_cpu(w, lens, row_token, e: int):
 # MX (MXFP8 / MXFP4) expert layer
 # ----------------------------------------------------------------------------
 
-MX_STEP_NAMES = ("q_x_row", "fc1_fwd_swiglu", "q_a_row", "fc2_fwd", "q_dy_row", "fc2_dgrad_swiglu_bwd",
-                 "q_dy_col", "q_a_col", "fc2_wgrad", "q_dh_row", "fc1_dgrad", "q_dh_col", "q_x_col",
-                 "fc1_wgrad")
+MX_STEP_NAMES = ("q_x_row", "fc1_fwd_swiglu", "fc2_fwd", "q_dy_row", "fc2_dgrad_swiglu_bwd", "q_dy_col",
+                 "q_a_col", "fc2_wgrad", "fc1_dgrad", "q_dh_col", "q_x_col", "fc1_wgrad")
 
 
 @dataclasses.dataclass
@@ -210,7 +209,8 @@ class MxLayerBuffers:
 
 
 def mx_layer_step(b: MxLayerBuffers, between=None):
-    """One MX expert-layer fwd + bwd: 8 activation quantizations and 6 block-scaled GEMMs."""
+    """One MX expert-layer fwd + bwd: 6 activation quantizations and 6 block-scaled GEMMs; the
+    FC1 and FC2-dgrad epilogues emit A and dH already MX-quantized for the next GEMM."""
     f, gl, u = b.fmt, b.group_lens, b.bufs
     err, Mp = u["err"], b.M_pad
     M, Hd = b.X.shape
@@ -219,17 +219,15 @@ def mx_layer_step(b: MxLayerBuffers, between=None):
     calls = (
         lambda: B.mx_quantize_rowwise(b.X, f, *u["Xq"]),
         lambda: B.mx_grouped_gemm(B.MODE_FWD, f, *u["Xq"], *b.W1q, gl, M, 2 * I, Hd, out=u["A"], out2=u["H"],
-                                  epilogue=B.EPI_SWIGLU, err=err),
-        lambda: B.mx_quantize_rowwise(u["A"], f, *u["Aq"]),
+                                  epilogue=B.EPI_SWIGLU, err=err, out_q=u["Aq"]),
         lambda: B.mx_grouped_gemm(B.MODE_FWD, f, *u["Aq"], *b.W2q, gl, M, Hd, I, out=u["Y"], err=err),
         lambda: B.mx_quantize_rowwise(b.dY, f, *u["dYq"]),
         lambda: B.mx_grouped_gemm(B.MODE_DGRAD, f, *u["dYq"], *b.W2t, gl, M, Hd, I, out=u["dH"], H=u["H"],
-                                  epilogue=B.EPI_SWIGLU, err=err),
+                                  epilogue=B.EPI_SWIGLU, err=err, out_q=u["dHq"]),
         lambda: B.mx_quantize_colwise(b.dY, gl, f, Mp, *u["dYc"], err=err),
         lambda: B.mx_quantize_colwise(u["A"], gl, f, Mp, *u["Ac"], err=err),
         lambda: B.mx_grouped_gemm(B.MODE_WGRAD, f, *u["dYc"], *u["Ac"], gl, M, Hd, I, out=u["dW2"], M_pad=Mp,
                                   err=err),
-        lambda: B.mx_quantize_rowwise(u["dH"], f, *u["dHq"]),
         lambda: B.mx_grouped_gemm(B.MODE_DGRAD, f, *u["dHq"], *b.W1t, gl, M, 2 * I, Hd, out=u["dX"], err=err),
         lambda: B.mx_quantize_colwise(u["dH"], gl, f, Mp, *u["dHc"], err=err),
         lambda: B.mx_quantize_colwise(b.X, gl, f, Mp, *u["Xc"], err=err),
@@ -255,15 +253,13 @@ def mx_layer_work(fmt: str, M: int, G: int, Hd: int, I: int, M_pad: int) -> dict
     lens = 4 * G
     return {
         "q_x_row": (0.0, M * Hd * (2 + q)),
-        "fc1_fwd_swiglu": (f1, M * Hd * q + W1 * q + M * I * 2 + M * 2 * I * 2 + lens),
-        "q_a_row": (0.0, M * I * (2 + q)),
+        "fc1_fwd_swiglu": (f1, M * Hd * q + W1 * q + M * I * (2 + q) + M * 2 * I * 2 + lens),
         "fc2_fwd": (f2, M * I * q + W2 * q + M * Hd * 2 + lens),
         "q_dy_row": (0.0, M * Hd * (2 + q)),
-        "fc2_dgrad_swiglu_bwd": (f2, M * Hd * q + W2 * q + M * 2 * I * 2 * 2 + lens),
+        "fc2_dgrad_swiglu_bwd": (f2, M * Hd * q + W2 * q + M * 2 * I * 2 + M * 2 * I * (2 + q) + lens),
         "q_dy_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),
         "q_a_col": (0.0, M * I * 2 + I * M_pad * q + lens),
         "fc2_wgrad": (f2, (Hd + I) * M_pad * q + W2 * 2 + lens),
-        "q_dh_row": (0.0, M * 2 * I * (2 + q)),
         "fc1_dgrad": (f1, M * 2 * I * q + W1 * q + M * Hd * 2 + lens),
         "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M_pad * q + lens),
         "q_x_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),

@@ -161,3 +161,35 @@ def test_mx_pad_overflow_and_bad_lens():
     pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, torch.tensor([100, 99], dtype=torch.int32, device=DEV),
                         M, N, K, err=err)
     assert pgg.read_error(err) == 16
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mx_fused_quantized_outputs(fmt):
+    # the SwiGLU epilogues' fused MX outputs equal the row-wise quantizer applied to the
+    # bf16 tensor they stored (the quantizer itself is bit-exact against the oracle)
+    lens = np.array([70, 0, 190], dtype=np.int32)
+    G, M, I, K = 3, 260, 192, 256
+    X, W1 = _bf16(wl.KEY_X, M, K, 1.0, 37), _bf16(wl.KEY_W1, G * 2 * I, K, 0.1, 37)
+    gl = torch.from_numpy(lens).to(DEV)
+    A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise(W1.to(DEV), fmt)
+    cb = I if fmt == "e4m3" else I // 2
+    qc = torch.empty((M, cb), dtype=torch.uint8, device=DEV)
+    qs = torch.empty((M, I // 32), dtype=torch.uint8, device=DEV)
+    Aout = pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, gl, M, 2 * I, K, epilogue=pgg.EPI_SWIGLU,
+                               out_q=(qc, qs))
+    rc, rs = pgg.mx_quantize_rowwise(Aout, fmt)
+    assert torch.equal(qc, rc) and torch.equal(qs, rs)
+    Hd = 256
+    dY, W2, Hs = _bf16(wl.KEY_DY, M, Hd, 1.0, 38), _bf16(wl.KEY_W2, G * Hd, I, 0.1, 38), _bf16(wl.KEY_H, M, 2 * I, 1.0, 38)
+    Ad, SAd = pgg.mx_quantize_rowwise(dY.to(DEV), fmt)
+    Bt, SBt = pgg.mx_quantize_colwise(W2.to(DEV), torch.full((G,), Hd, dtype=torch.int32, device=DEV), fmt, G * Hd)
+    qc2 = torch.empty((M, 2 * cb), dtype=torch.uint8, device=DEV)
+    qs2 = torch.empty((M, 2 * I // 32), dtype=torch.uint8, device=DEV)
+    dH = pgg.mx_grouped_gemm(pgg.MODE_DGRAD, fmt, Ad, SAd, Bt, SBt, gl, M, Hd, I, H=Hs.to(DEV),
+                             epilogue=pgg.EPI_SWIGLU, out_q=(qc2, qs2))
+    rc2, rs2 = pgg.mx_quantize_rowwise(dH, fmt)
+    assert torch.equal(qc2, rc2) and torch.equal(qs2, rs2)
+    # fused outputs exist only for the SwiGLU epilogues
+    with pytest.raises(pgg.PggError):
+        pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, gl, M, 2 * I, K, out_q=(qc, qs))

@@ -9,11 +9,13 @@ A plain, slow, obviously correct fp64 restatement of what the pages define:
   forward/backward and the fused FC1 / FC2-dgrad compositions;
 * mx.py -- E8M0 / e4m3 / e2m1 decode, MX block quantization (row- and
   group-aware column-wise), dequantization, and the block-scaled grouped GEMM
-  as "dequantize, then the fp64 grouped GEMM".
+  as "dequantize, then the fp64 grouped GEMM";
+* moe_glue.py -- the single-GPU token permute / combine around the grouped
+  GEMM and their backward passes.
 
 It shares no code with the CUDA path and imports nothing from it.  Inputs are
 bf16 bit patterns (numpy uint16) or MX byte codes; everything is computed in
 fp64.  Every function is pinned by a `-m "not gpu"` test against brute force,
 closed forms, invariants or hand-derived format values.
 """
-from . import grouped_gemm, mx  # noqa: F401
+from . import grouped_gemm, moe_glue, mx  # noqa: F401

@@ -433,3 +433,61 @@ def test_wgrad_accumulate_adds_to_main_grad():
     _, _, dWb = _brute(X, np.zeros((3, 6, 4)), dY, lens)
     np.testing.assert_allclose(out, dW0 + dWb, rtol=1e-12, atol=1e-12)
     np.testing.assert_array_equal(out[1], dW0[1])  # empty group: main_grad unchanged
+
+
+# ---------------------------------------------------------------------------
+# MoE glue: permute / combine
+# ---------------------------------------------------------------------------
+
+from oracle import moe_glue as omg  # noqa: E402
+
+
+def _topk_ids(rng, T, E, k):
+    return np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)])
+
+
+def test_permute_is_stable_expert_sort():
+    rng = np.random.default_rng(24)
+    T, E, k = 37, 9, 3
+    ids = _topk_ids(rng, T, E, k)
+    pos, lens, row_token = omg.permute(ids, E)
+    assert sorted(pos.reshape(-1).tolist()) == list(range(T * k))  # a bijection onto the rows
+    np.testing.assert_array_equal(lens, np.bincount(ids.reshape(-1), minlength=E))
+    # brute force: walk experts, then tokens, assigning rows in order
+    r = 0
+    for e in range(E):
+        for t in range(T):
+            for j in range(k):
+                if ids[t, j] == e:
+                    assert pos[t, j] == r and row_token[r] == t
+                    r += 1
+    X = rng.standard_normal((T, 5))
+    Xs = omg.permute_rows(X, pos)
+    np.testing.assert_array_equal(Xs, X[row_token])
+
+
+def test_combine_and_backward():
+    rng = np.random.default_rng(25)
+    T, E, k, H = 20, 6, 2, 7
+    ids = _topk_ids(rng, T, E, k)
+    pos, lens, row_token = omg.permute(ids, E)
+    Ys = rng.standard_normal((T * k, H))
+    w = rng.random((T, k))
+    out = omg.combine(Ys, pos, w)
+    for t in range(T):
+        np.testing.assert_allclose(out[t], sum(w[t, j] * Ys[pos[t, j]] for j in range(k)), rtol=1e-12)
+    # one-hot weights pick a row; unit weights of the permute round trip give k * X
+    X = rng.standard_normal((T, H))
+    np.testing.assert_allclose(omg.combine(omg.permute_rows(X, pos), pos), k * X, rtol=1e-12)
+    dOut = rng.standard_normal((T, H))
+    dYs, dw = omg.combine_bwd(dOut, Ys, pos, w)
+    # adjoint in Ys: <combine(Ys), dOut> = <Ys, dYs>; derivative in w by finite differences
+    assert np.sum(out * dOut) == pytest.approx(np.sum(Ys * dYs), rel=1e-12)
+    eps = 1e-6
+    for t, j in [(0, 0), (7, 1), (19, 0)]:
+        wp, wm = w.copy(), w.copy()
+        wp[t, j] += eps; wm[t, j] -= eps
+        num = (np.sum(omg.combine(Ys, pos, wp) * dOut) - np.sum(omg.combine(Ys, pos, wm) * dOut)) / (2 * eps)
+        assert dw[t, j] == pytest.approx(num, rel=1e-6)
+    with pytest.raises(ValueError):
+        omg.permute(np.array([[0, E]]), E)

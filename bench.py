@@ -429,6 +429,55 @@ def measure_wgrad_accumulate(device, peaks, steps):
     return res
 
 
+def measure_moe_glue(device, peaks, steps):
+    """The single-GPU MoE glue on the DeepSeek-shaped routing (4096 tokens, top-6 of
+    256 experts, hidden 4096): permute, weighted combine and combine backward, each
+    timed over `steps` back-to-back calls.  Algorithmic bytes: permute = X read once
+    + Xs written + ids/pos; combine = Ys read + out written; backward = dOut + Ys
+    read + dYs written."""
+    import precision_grouped_gemm_gb300 as pgg
+    w = wl.DSV4_BF16
+    T, k, E, H = w.tokens, w.topk, w.experts, w.hidden
+    ids = torch.from_numpy(w.topk_ids().astype(np.int32)).to(device)
+    X = wl.gen_matrix(wl.KEY_X, T, H, 1.0, w.seed, device=device)
+    wts = wl.gen_f32(wl.KEY_LOGITS, torch.arange(T, device=device), k, 1.0, w.seed + 7).abs().contiguous()
+    Xs, lens, pos = pgg.moe_permute(ids, X, E)
+    ws = torch.empty(pgg.moe_permute_workspace_size(T, E) // 4, dtype=torch.int32, device=device)
+    dOut = wl.gen_matrix(wl.KEY_DY, T, H, 1.0, w.seed, device=device)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    dYs, dw = torch.empty_like(Xs), torch.empty((T, k), dtype=torch.float32, device=device)
+    err = torch.zeros(1, dtype=torch.int32, device=device)
+    R = T * k
+    calls = {
+        "permute": (lambda: pgg.moe_permute(ids, X, E, Xs, lens, pos, ws, err),
+                    2.0 * T * H + 2.0 * R * H + 8.0 * R + 4.0 * E, 4),
+        "combine": (lambda: pgg.moe_combine(Xs, pos, wts, out), 2.0 * R * H + 2.0 * T * H + 8.0 * R, 1),
+        "combine_bwd": (lambda: pgg.moe_combine_bwd(dOut, Xs, pos, wts, dYs, dw),
+                        2.0 * T * H + 4.0 * R * H + 12.0 * R, 1),
+    }
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    res = {"workload": f"tokens {T}, top-{k} of {E} experts, hidden {H}, bf16 rows, fp32 weights"}
+    for name, (call, nbytes, launches) in calls.items():
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for _ in range(steps):
+            call()
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1) / steps
+        res[name] = {"ms": ms, "launches": launches, "algo_bytes": nbytes, "gbs": nbytes / ms / 1e6,
+                     "frac_of_measured_hbm": nbytes / ms / 1e6 / hbm}
+    if pgg.read_error(err) != 0:
+        raise RuntimeError("device error word set in the MoE glue run")
+    del X, Xs, dOut, out, dYs
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_pgg(args, w):
     import precision_grouped_gemm_gb300 as pgg
     world, rank, local = dist_env()
@@ -452,6 +501,7 @@ def run_pgg(args, w):
                                                     "empty_groups", "steps")}
                 extra[ew.name]["kernels_ms"] = {k: round(v["ms"], 4) for k, v in r["kernels"].items()}
         extra["wgrad_accumulate_fp32"] = measure_wgrad_accumulate(device, peaks, args.extra_steps)
+        extra["moe_glue"] = measure_moe_glue(device, peaks, args.extra_steps)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.cpu_seconds)

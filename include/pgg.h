@@ -29,7 +29,7 @@
  *    M, a bounded wait that expired) write a code to *err (a device int32,
  *    first error wins; may be NULL) and the kernel still terminates, writing
  *    no output for bad group_lens.  Clear *err to 0 before the call.
- *  - Results are deterministic: no atomics in any reduction.
+ *  - Results are deterministic: no floating-point atomics in any reduction.
  */
 #ifndef PGG_H_
 #define PGG_H_
@@ -51,7 +51,8 @@ typedef enum {
   /* codes written to the device error word */
   PGG_ERR_BAD_GROUP_LENS = 16, /* some len < 0, or sum(len) != M */
   PGG_ERR_TIMEOUT = 17,        /* a bounded pipeline wait expired; output incomplete */
-  PGG_ERR_PAD_OVERFLOW = 18    /* column-wise MX: sum(round_up(len, 128)) > M_pad */
+  PGG_ERR_PAD_OVERFLOW = 18,   /* column-wise MX: sum(round_up(len, 128)) > M_pad */
+  PGG_ERR_BAD_EXPERT = 19      /* MoE permute: an expert id outside [0, E) */
 } pgg_status;
 
 typedef enum { PGG_FMT_E4M3 = 1, PGG_FMT_E2M1 = 2 } pgg_mx_fmt;
@@ -200,6 +201,49 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
                         const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
                         uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G,
                         int64_t M_pad, int32_t* err, void* stream);
+
+/* ---------------------------------------------------------------- MoE glue (one GPU) */
+
+/* Bytes of the scratch table pgg_moe_permute needs: ceil(T / 32) * E * 4. */
+size_t pgg_moe_permute_workspace_size(int64_t T, int E);
+
+/* Token permute into the expert-sorted layout the grouped GEMM consumes
+ * ("Enabling DeepSeek-V4-Flash ...", section "Expert parallelism: DeepEP and
+ * the grouped GEMM": the dispatch lays tokens out for the grouped GEMM; on one
+ * GPU it has no communication).  Entry (t, j) -- token t's j-th routed expert
+ * e = topk_ids[t, j] -- becomes row pos[t, j] of Xs; rows are ordered by expert,
+ * then token, then choice (a stable sort of the flattened entries by expert),
+ * so group g's rows are [sum_{h<g} len_h, sum_{h<=g} len_h).
+ *   topk_ids [T, k] int32 in [0, E); X [T, H] bf16 (may be NULL: routing only);
+ *   Xs [T * k, H] bf16 (out; rows past sum(group_lens) untouched);
+ *   group_lens [E] int32 (out); pos [T, k] int32 (out);
+ *   ws: device scratch of at least pgg_moe_permute_workspace_size(T, E) bytes,
+ *   owned by the caller, 4-byte aligned, clobbered.
+ *   1 <= k <= 32, 1 <= E <= 1024, T * k < 2^31, H % 8 == 0.
+ * An id outside [0, E) sets *err = PGG_ERR_BAD_EXPERT; that entry gets
+ * pos = -1, is not counted and not copied.  The result is deterministic. */
+int pgg_moe_permute(const int32_t* topk_ids, const void* X, int64_t T, int k, int64_t H, int E,
+                    void* Xs, int32_t* group_lens, int32_t* pos, void* ws, size_t ws_bytes,
+                    int32_t* err, void* stream);
+
+/* Combine ("Enabling DeepSeek-V4-Flash ...", section "MegaMoE": the second
+ * grouped GEMM is followed by the combine and the weighted reduce):
+ *   out[t] = sum_j w[t, j] * Ys[pos[t, j]], fp32 accumulation in choice order,
+ *   bf16 output.  w NULL means weight 1, which makes this also the permute's
+ *   backward: dX[t] = sum_j dXs[pos[t, j]].  Entries with pos < 0 are skipped.
+ *   Ys [R, H] bf16 (R >= max pos + 1); pos [T, k] int32; w [T, k] fp32 or NULL;
+ *   out [T, H] bf16.  1 <= k <= 32, H % 8 == 0. */
+int pgg_moe_combine(const void* Ys, const int32_t* pos, const float* w, void* out, int64_t T, int k,
+                    int64_t H, void* stream);
+
+/* Backward of the weighted combine:
+ *   dYs[pos[t, j]] = bf16(w[t, j] * dOut[t]);  dw[t, j] = <dOut[t], Ys[pos[t, j]]>
+ *   (fp32 dot product in a fixed order: deterministic).  Entries with pos < 0
+ *   get dw = 0 and leave dYs untouched.
+ *   dOut [T, H] bf16, Ys [R, H] bf16, pos [T, k] int32, w [T, k] fp32,
+ *   dYs [R, H] bf16 (out), dw [T, k] fp32 (out).  1 <= k <= 32, H % 8 == 0. */
+int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, const float* w,
+                        void* dYs, float* dw, int64_t T, int k, int64_t H, void* stream);
 
 #ifdef __cplusplus
 }

@@ -32,6 +32,9 @@ SIGNATURES = {
     "pgg_mx_quantize_colwise": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P],
     "pgg_mx_grouped_gemm": [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                             _I64, _I32, _I64, _P, _P],
+    "pgg_moe_permute": [_P, _P, _I64, _I32, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
+    "pgg_moe_combine": [_P, _P, _P, _P, _I64, _I32, _I64, _P],
+    "pgg_moe_combine_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I32, _I64, _P],
 }
 
 
@@ -60,6 +63,8 @@ def lib():
             f.restype = ctypes.c_int
         L.pgg_status_string.argtypes = [ctypes.c_int]
         L.pgg_status_string.restype = ctypes.c_char_p
+        L.pgg_moe_permute_workspace_size.argtypes = [_I64, _I32]
+        L.pgg_moe_permute_workspace_size.restype = ctypes.c_size_t
         _LIB = L
     return _LIB
 
@@ -248,3 +253,60 @@ def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2
                                      _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), _ptr(qc), _ptr(qs), M, N,
                                      K, G, M_pad, _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
     return out
+
+
+def moe_permute_workspace_size(T: int, E: int) -> int:
+    return int(lib().pgg_moe_permute_workspace_size(T, E))
+
+
+def moe_permute(topk_ids, X, E, Xs=None, group_lens=None, pos=None, ws=None, err=None, stream=None):
+    """topk_ids [T,k] int32 (+ X [T,H] bf16 or None) -> (Xs [T*k,H], group_lens [E], pos [T,k])."""
+    T, k = topk_ids.shape
+    if topk_ids.dtype != torch.int32:
+        raise ValueError("topk_ids must be int32")
+    dev = topk_ids.device
+    H = 0 if X is None else X.shape[1]
+    if X is not None and Xs is None:
+        Xs = torch.empty((T * k, H), dtype=torch.bfloat16, device=dev)
+    if group_lens is None:
+        group_lens = torch.empty(E, dtype=torch.int32, device=dev)
+    if pos is None:
+        pos = torch.empty((T, k), dtype=torch.int32, device=dev)
+    nbytes = moe_permute_workspace_size(T, E)
+    if ws is None:
+        ws = torch.empty(max(1, nbytes // 4), dtype=torch.int32, device=dev)
+    _dev(topk_ids, X, Xs, group_lens, pos, ws, err)
+    _check(lib().pgg_moe_permute(_ptr(topk_ids), _ptr(X), T, k, H, E, _ptr(Xs), _ptr(group_lens), _ptr(pos),
+                                 _ptr(ws), ws.numel() * ws.element_size(), _ptr(err), _stream(stream)),
+           "pgg_moe_permute")
+    return Xs, group_lens, pos
+
+
+def moe_combine(Ys, pos, w=None, out=None, stream=None):
+    """out[t] = sum_j w[t,j] * Ys[pos[t,j]] (w None: weight 1, the permute backward)."""
+    T, k = pos.shape
+    H = Ys.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=Ys.device)
+    if w is not None and w.dtype != torch.float32:
+        raise ValueError("w must be float32")
+    _dev(Ys, pos, w, out)
+    _check(lib().pgg_moe_combine(_ptr(Ys), _ptr(pos), _ptr(w), _ptr(out), T, k, H, _stream(stream)),
+           "pgg_moe_combine")
+    return out
+
+
+def moe_combine_bwd(dOut, Ys, pos, w, dYs=None, dw=None, stream=None):
+    """-> (dYs [R,H] bf16 with dYs[pos[t,j]] = w[t,j] dOut[t], dw [T,k] fp32)."""
+    T, k = pos.shape
+    H = dOut.shape[1]
+    if dYs is None:
+        dYs = torch.empty_like(Ys)
+    if dw is None:
+        dw = torch.empty((T, k), dtype=torch.float32, device=dOut.device)
+    if w.dtype != torch.float32:
+        raise ValueError("w must be float32")
+    _dev(dOut, Ys, pos, w, dYs, dw)
+    _check(lib().pgg_moe_combine_bwd(_ptr(dOut), _ptr(Ys), _ptr(pos), _ptr(w), _ptr(dYs), _ptr(dw), T, k, H,
+                                     _stream(stream)), "pgg_moe_combine_bwd")
+    return dYs, dw

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libpgg.so")
-SOURCES = ["pgg_api.cu", "gemm_bf16.cu", "mx_quant.cu", "gemm_mx.cu"]
+SOURCES = ["pgg_api.cu", "gemm_bf16.cu", "mx_quant.cu", "gemm_mx.cu", "moe_glue.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

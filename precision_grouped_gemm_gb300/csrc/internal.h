@@ -77,4 +77,13 @@ struct MxCall {
 };
 int launch_mx_gemm(const MxCall& c);
 
+// MoE glue (moe_glue.cu)
+size_t moe_permute_ws_bytes(int64_t T, int E);
+int launch_moe_permute(const int32_t* ids, const void* X, int64_t T, int k, int64_t H, int E, void* Xs,
+                       int32_t* group_lens, int32_t* pos, int32_t* ws, int32_t* err, cudaStream_t s);
+int launch_moe_combine(const void* Ys, const int32_t* pos, const float* w, int64_t T, int k, int64_t H,
+                       void* out, cudaStream_t s);
+int launch_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, const float* w, int64_t T, int k,
+                           int64_t H, void* dYs, float* dw, cudaStream_t s);
+
 }  // namespace pgg

@@ -158,6 +158,7 @@ const char* pgg_status_string(int s) {
     case PGG_ERR_BAD_GROUP_LENS: return "bad group_lens (negative length or sum != M)";
     case PGG_ERR_TIMEOUT: return "bounded pipeline wait expired";
     case PGG_ERR_PAD_OVERFLOW: return "padded column-wise layout exceeds M_pad";
+    case PGG_ERR_BAD_EXPERT: return "expert id out of range";
     default: return "unknown status";
   }
 }
@@ -311,6 +312,58 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
   MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales,
            M, N, K, M_pad, G, err, as_stream(stream)};
   return launch_mx_gemm(c);
+}
+
+size_t pgg_moe_permute_workspace_size(int64_t T, int E) {
+  if (T < 0 || E < 1) return 0;
+  return moe_permute_ws_bytes(T, E);
+}
+
+int pgg_moe_permute(const int32_t* topk_ids, const void* X, int64_t T, int k, int64_t H, int E,
+                    void* Xs, int32_t* group_lens, int32_t* pos, void* ws, size_t ws_bytes,
+                    int32_t* err, void* stream) {
+  if (k < 1 || k > 32 || E < 1 || E > kMaxGroups || T < 0 || T * k >= kMaxRows) return PGG_ERR_INVALID_ARG;
+  if (!group_lens) return PGG_ERR_INVALID_ARG;
+  if (X) {
+    int st = check_dim(H, 8);
+    if (st) return st;
+    if (!Xs) return PGG_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(Xs)) return PGG_ERR_ALIGNMENT;
+  }
+  if (T > 0) {
+    if (!topk_ids || !pos || !ws) return PGG_ERR_INVALID_ARG;
+    if (ws_bytes < moe_permute_ws_bytes(T, E)) return PGG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 3u) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+        (reinterpret_cast<uintptr_t>(pos) & 3u))
+      return PGG_ERR_ALIGNMENT;
+  }
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  return launch_moe_permute(topk_ids, X, T, k, H, E, Xs, group_lens, pos, static_cast<int32_t*>(ws), err,
+                            as_stream(stream));
+}
+
+int pgg_moe_combine(const void* Ys, const int32_t* pos, const float* w, void* out, int64_t T, int k,
+                    int64_t H, void* stream) {
+  if (k < 1 || k > 32 || T < 0 || T * k >= kMaxRows) return PGG_ERR_INVALID_ARG;
+  int st = check_dim(H, 8);
+  if (st) return st;
+  if (T == 0) return PGG_OK;
+  if (!Ys || !pos || !out) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(Ys) || !aligned16(out)) return PGG_ERR_ALIGNMENT;
+  return launch_moe_combine(Ys, pos, w, T, k, H, out, as_stream(stream));
+}
+
+int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, const float* w,
+                        void* dYs, float* dw, int64_t T, int k, int64_t H, void* stream) {
+  if (k < 1 || k > 32 || T < 0 || T * k >= kMaxRows) return PGG_ERR_INVALID_ARG;
+  int st = check_dim(H, 8);
+  if (st) return st;
+  if (T == 0) return PGG_OK;
+  if (!dOut || !Ys || !pos || !w || !dYs || !dw) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(dOut) || !aligned16(Ys) || !aligned16(dYs)) return PGG_ERR_ALIGNMENT;
+  return launch_moe_combine_bwd(dOut, Ys, pos, w, T, k, H, dYs, dw, as_stream(stream));
 }
 
 }  // extern "C"

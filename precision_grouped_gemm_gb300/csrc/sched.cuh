@@ -21,6 +21,7 @@ enum GemmEpi : int { kEpiStore = 0, kEpiSwiGLU = 1, kEpiSwiGLUBwd = 2, kEpiAccum
 constexpr int kErrBadGroupLens = 16;
 constexpr int kErrTimeout = 17;
 constexpr int kErrPadOverflow = 18;
+constexpr int kErrBadExpert = 19;
 
 // Tiles of one group as a function of its length.
 struct TileCount {

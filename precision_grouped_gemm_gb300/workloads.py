@@ -101,24 +101,32 @@ def gen_matrix(key: int, nrows: int, cols: int, std: float, seed: int = 0,
 # routing -> group_lens
 # ----------------------------------------------------------------------------
 
-def route_softmax_topk(T: int, E: int, k: int, seed: int, blocked=()) -> tuple[np.ndarray, np.ndarray]:
-    """Top-k of softmax over generator logits [T, E]; returns (group_lens[E], row_token[M])."""
+def topk_softmax(T: int, E: int, k: int, seed: int, blocked=()) -> np.ndarray:
+    """Top-k expert ids [T, k] of softmax over generator logits [T, E], best first."""
     logits = gen_f32(KEY_LOGITS, torch.arange(T), E, 1.0, seed).numpy().astype(np.float64)
     for e in blocked:
         logits[:, e] = -np.inf
     # stable sort on -logit: equal logits keep ascending expert order
-    order = np.argsort(-logits, axis=1, kind="stable")[:, :k]
-    return _rows_from_choice(order, T, E)
+    return np.argsort(-logits, axis=1, kind="stable")[:, :k]
 
 
-def route_zipf(T: int, E: int, k: int, s: float, seed: int) -> tuple[np.ndarray, np.ndarray]:
-    """Top-k without replacement, p_e ~ (e+1)^-s, by Gumbel-top-k (numpy PCG64)."""
+def topk_zipf(T: int, E: int, k: int, s: float, seed: int) -> np.ndarray:
+    """Top-k ids [T, k] without replacement, p_e ~ (e+1)^-s, by Gumbel-top-k (numpy PCG64)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     logp = -s * np.log(np.arange(1, E + 1, dtype=np.float64))
     u = rng.random((T, E))
     keys = logp[None, :] - np.log(-np.log(u))
-    order = np.argsort(-keys, axis=1, kind="stable")[:, :k]
-    return _rows_from_choice(order, T, E)
+    return np.argsort(-keys, axis=1, kind="stable")[:, :k]
+
+
+def route_softmax_topk(T: int, E: int, k: int, seed: int, blocked=()) -> tuple[np.ndarray, np.ndarray]:
+    """Softmax top-k routing; returns (group_lens[E], row_token[M])."""
+    return _rows_from_choice(topk_softmax(T, E, k, seed, blocked), T, E)
+
+
+def route_zipf(T: int, E: int, k: int, s: float, seed: int) -> tuple[np.ndarray, np.ndarray]:
+    """Zipf top-k routing; returns (group_lens[E], row_token[M])."""
+    return _rows_from_choice(topk_zipf(T, E, k, s, seed), T, E)
 
 
 def _rows_from_choice(order: np.ndarray, T: int, E: int):
@@ -169,6 +177,14 @@ class Workload:
         if self.routing == "zipf":
             return route_zipf(self.tokens, self.experts, self.topk, self.zipf_s, self.seed)
         raise ValueError(self.routing)
+
+    def topk_ids(self) -> np.ndarray:
+        """The routing's expert ids [tokens, topk] (group_lens / row_token are their stable sort)."""
+        if self.routing == "softmax":
+            return topk_softmax(self.tokens, self.experts, self.topk, self.seed, self.blocked)
+        if self.routing == "zipf":
+            return topk_zipf(self.tokens, self.experts, self.topk, self.zipf_s, self.seed)
+        raise ValueError(f"routing {self.routing!r} has no top-k ids")
 
 
 def _gptoss_blocked(seed: int, E: int = 32) -> tuple:

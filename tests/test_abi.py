@@ -27,7 +27,9 @@ def test_header_declares_the_hot_path():
     syms = declared_symbols()
     for name in ["pgg_grouped_gemm_fwd", "pgg_grouped_gemm_dgrad", "pgg_grouped_gemm_wgrad",
                  "pgg_grouped_fc1_swiglu", "pgg_grouped_fc2_dgrad_swiglu_bwd",
-                 "pgg_mx_quantize_rowwise", "pgg_mx_quantize_colwise", "pgg_mx_grouped_gemm"]:
+                 "pgg_mx_quantize_rowwise", "pgg_mx_quantize_colwise", "pgg_mx_grouped_gemm",
+                 "pgg_grouped_gemm_wgrad_accumulate", "pgg_moe_permute", "pgg_moe_combine",
+                 "pgg_moe_combine_bwd"]:
         assert name in syms
 
 
@@ -39,7 +41,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_binding_signatures_cover_header():
     from precision_grouped_gemm_gb300 import _binding
     for s in declared_symbols():
-        if s != "pgg_status_string":
+        if s not in ("pgg_status_string", "pgg_moe_permute_workspace_size"):  # non-int returns
             assert s in _binding.SIGNATURES, s
 
 
@@ -65,3 +67,30 @@ def test_host_validation_without_gpu(lib):
     q.argtypes = [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, P, P, P]
     assert q(good, 4, 48, 1, good, good, None) == 3                        # C % 32
     assert q(good, 4, 64, 7, good, good, None) == 1                        # bad format
+
+
+def test_moe_glue_host_validation_without_gpu(lib):
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    ws = lib.pgg_moe_permute_workspace_size
+    ws.argtypes, ws.restype = [I64, I32], ctypes.c_size_t
+    assert ws(4096, 256) == 128 * 256 * 4            # ceil(T / 32) chunks x E experts x int32
+    assert ws(33, 3) == 2 * 3 * 4
+    f = lib.pgg_moe_permute
+    f.argtypes = [P, P, I64, I32, I64, I32, P, P, P, P, ctypes.c_size_t, P, P]
+    g = 1 << 20
+    assert f(g, g, 100, 0, 64, 8, g, g, g, g, 1 << 20, None, None) == 1        # k < 1
+    assert f(g, g, 100, 33, 64, 8, g, g, g, g, 1 << 20, None, None) == 1       # k > 32
+    assert f(g, g, 100, 4, 64, 2000, g, g, g, g, 1 << 20, None, None) == 1     # E > 1024
+    assert f(g, g, 100, 4, 60, 8, g, g, g, g, 1 << 20, None, None) == 3        # H % 8
+    assert f(g, g, 100, 4, 64, 8, g, g, g, g, 16, None, None) == 1             # workspace too small
+    assert f(g, g, 100, 4, 64, 8, g + 8, g, g, g, 1 << 20, None, None) == 3    # misaligned Xs
+    assert f(g, g, 100, 4, 64, 8, g, None, g, g, 1 << 20, None, None) == 1     # null group_lens
+    c = lib.pgg_moe_combine
+    c.argtypes = [P, P, P, P, I64, I32, I64, P]
+    assert c(None, None, None, None, 0, 4, 64, None) == 0                      # T == 0 is a no-op
+    assert c(g, g, None, None, 8, 4, 64, None) == 1                            # null out
+    assert c(g, g, None, g, 8, 4, 12, None) == 3                               # H % 8
+    b = lib.pgg_moe_combine_bwd
+    b.argtypes = [P, P, P, P, P, P, I64, I32, I64, P]
+    assert b(g, g, g, None, g, g, 8, 4, 64, None) == 1                         # w required
+    assert b(g, g, g, g, g + 4, g, 8, 4, 64, None) == 3                        # misaligned dYs

@@ -48,6 +48,7 @@ typedef enum {
   PGG_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned, or a dimension off its multiple */
   PGG_ERR_NOT_INITIALIZED = 4,
   PGG_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  PGG_ERR_TOO_LARGE = 6,     /* the problem does not fit a no-alloc entry point's fixed scratch */
   /* codes written to the device error word */
   PGG_ERR_BAD_GROUP_LENS = 16, /* some len < 0, or sum(len) != M */
   PGG_ERR_TIMEOUT = 17,        /* a bounded pipeline wait expired; output incomplete */
@@ -244,6 +245,31 @@ int pgg_moe_combine(const void* Ys, const int32_t* pos, const float* w, void* ou
  *   dYs [R, H] bf16 (out), dw [T, k] fp32 (out).  1 <= k <= 32, H % 8 == 0. */
 int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, const float* w,
                         void* dYs, float* dw, int64_t T, int k, int64_t H, void* stream);
+
+/* Capacity of pgg_moe_permute_noalloc's fixed scratch, in int32 entries
+ * (4 MiB of device memory in the library's module): ceil(T / 32) * E must not
+ * exceed it, e.g. 131072 tokens over 256 experts or 32768 over 1024. */
+#define PGG_MOE_NOALLOC_MAX_WS_INTS (1 << 20)
+
+/* pgg_moe_permute without a caller workspace.  The pages have no counterpart:
+ * it exists for callers that cannot provide device scratch -- a C or real-time
+ * component without access to the framework's allocator and with a fixed
+ * memory budget, or code that must not call cudaMalloc because it
+ * synchronises the device.  The count table lives instead in a statically
+ * sized array of the library's own module (PGG_MOE_NOALLOC_MAX_WS_INTS int32
+ * entries per device), and the call allocates nothing.
+ *   Arguments, layouts and results are those of pgg_moe_permute without ws /
+ *   ws_bytes.  ceil(T / 32) * E > PGG_MOE_NOALLOC_MAX_WS_INTS returns
+ *   PGG_ERR_TOO_LARGE and launches nothing.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.
+ *   All calls on one device share the one array: calls that may overlap on
+ *   the GPU (different streams without ordering between them) race and give
+ *   wrong results.  Calls ordered on one stream are safe. */
+int pgg_moe_permute_noalloc(const int32_t* topk_ids, const void* X, int64_t T, int k, int64_t H,
+                            int E, void* Xs, int32_t* group_lens, int32_t* pos, int32_t* err,
+                            void* stream);
 
 #ifdef __cplusplus
 }

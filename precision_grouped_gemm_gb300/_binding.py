@@ -33,6 +33,7 @@ SIGNATURES = {
     "pgg_mx_grouped_gemm": [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                             _I64, _I32, _I64, _P, _P],
     "pgg_moe_permute": [_P, _P, _I64, _I32, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
+    "pgg_moe_permute_noalloc": [_P, _P, _I64, _I32, _I64, _I32, _P, _P, _P, _P, _P],
     "pgg_moe_combine": [_P, _P, _P, _P, _I64, _I32, _I64, _P],
     "pgg_moe_combine_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I32, _I64, _P],
 }

@@ -18,6 +18,7 @@
 //   gather  one warp per entry, Xs[pos[t, j]] = X[t] with 16-byte copies
 // All integer work is exact, so pos and group_lens are deterministic.
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -300,4 +301,72 @@ int launch_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos,
   return cuda_status(cudaGetLastError());
 }
 
+// ---------------------------------------------------------------- permute without a caller workspace
+//
+// Some callers cannot hand the permute a scratch buffer: a C or real-time host
+// component with no access to the framework's caching allocator and a fixed
+// device-memory budget, or code that must not call cudaMalloc because it
+// implicitly synchronises the device in the middle of a pipelined stream
+// schedule.  For them the count table lives in a statically sized module
+// array instead, and the call allocates nothing.
+namespace {
+
+constexpr int64_t kNoAllocScratchInts = PGG_MOE_NOALLOC_MAX_WS_INTS;
+
+// The count table of pgg_moe_permute_noalloc.  In host code this name is only
+// a stand-in for the symbol; its device address comes from cudaGetSymbolAddress.
+__device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
+
+constexpr int kScratchDevices = 64;
+int32_t* g_scratch_ptr[kScratchDevices] = {};
+std::mutex g_scratch_mu;
+
+// Device address of g_permute_scratch on `device` (the current device),
+// looked up on the first call per device and cached.
+int scratch_for(int device, int32_t** out) {
+  if (device < 0 || device >= kScratchDevices) return PGG_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[device]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    if (e != cudaSuccess || p == nullptr) return PGG_ERR_CUDA;
+    g_scratch_ptr[device] = static_cast<int32_t*>(p);
+  }
+  *out = g_scratch_ptr[device];
+  return PGG_OK;
+}
+
+}  // namespace
 }  // namespace pgg
+
+extern "C" int pgg_moe_permute_noalloc(const int32_t* topk_ids, const void* X, int64_t T, int k, int64_t H,
+                                       int E, void* Xs, int32_t* group_lens, int32_t* pos, int32_t* err,
+                                       void* stream) {
+  using namespace pgg;
+  if (k < 1 || k > 32 || E < 1 || E > kMaxGroups || T < 0 || T * k >= ((int64_t)1 << 31))
+    return PGG_ERR_INVALID_ARG;
+  if (!group_lens) return PGG_ERR_INVALID_ARG;
+  if (X) {
+    if (H < 8 || H >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+    if (H % 8) return PGG_ERR_ALIGNMENT;
+    if (!Xs) return PGG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(X) & 15u) || (reinterpret_cast<uintptr_t>(Xs) & 15u))
+      return PGG_ERR_ALIGNMENT;
+  }
+  if ((int64_t)moe_permute_ws_bytes(T, E) > kNoAllocScratchInts * (int64_t)sizeof(int32_t))
+    return PGG_ERR_TOO_LARGE;
+  if (T > 0) {
+    if (!topk_ids || !pos) return PGG_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+      return PGG_ERR_ALIGNMENT;
+  }
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  int32_t* ws = nullptr;
+  if ((st = scratch_for(dev.device, &ws)) != PGG_OK) return st;
+  // The count kernel writes every table entry that the scan and rank kernels
+  // read, so the scratch needs no clearing between calls.
+  return launch_moe_permute(topk_ids, X, T, k, H, E, Xs, group_lens, pos, ws, err,
+                            reinterpret_cast<cudaStream_t>(stream));
+}

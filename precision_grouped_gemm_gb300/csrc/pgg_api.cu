@@ -155,6 +155,7 @@ const char* pgg_status_string(int s) {
     case PGG_ERR_ALIGNMENT: return "misaligned pointer or dimension";
     case PGG_ERR_NOT_INITIALIZED: return "not initialized";
     case PGG_ERR_CUDA: return "CUDA runtime error";
+    case PGG_ERR_TOO_LARGE: return "problem exceeds the fixed scratch of a no-alloc entry point";
     case PGG_ERR_BAD_GROUP_LENS: return "bad group_lens (negative length or sum != M)";
     case PGG_ERR_TIMEOUT: return "bounded pipeline wait expired";
     case PGG_ERR_PAD_OVERFLOW: return "padded column-wise layout exceeds M_pad";

@@ -208,44 +208,57 @@ __device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8
   }
 }
 
-// Whole-tile store for the 4-D view {64, rows, cols/64, G} of the output (cols a
+// Store through the 4-D view {64, rows, cols/64, G} of the output (cols a
 // multiple of 64): this warp's 32 rows x BN columns are staged as BN/64 atoms of
-// 32 x 64 bf16 (4 KB each, 128B-swizzled) in its `stg` buffer and leave with one
-// bulk tensor store at (0, row0, col0 / 64, g), clipped at the bounds.  The
-// previous tile's store must have finished reading `stg` before it is rewritten.
-template <int BN>
+// 32 x 64 bf16 (4 KB each, 128B-swizzled) in its `stg` buffer and leave in
+// BN/64/SA bulk tensor stores of SA atoms each, at (0, row0, col0 / 64 + s SA, g),
+// clipped at the bounds, one bulk group per store.  Before a store's atoms are
+// rewritten only the store that last read them -- BN/64/SA groups back -- has to
+// be done reading, so with SA < BN/64 one tile's stores drain while the next
+// tile's atoms are filled.  Stores that start past `cols_total` are skipped but
+// still commit an (empty) group, which keeps that count exact.
+template <int BN, int SA>
 __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8_t* stg,
                                                    const CUtensorMap* tmC4, int row0, int col0, int g,
-                                                   int rows_total, int lane) {
+                                                   int rows_total, int cols_total, int lane) {
+  static_assert(SA >= 1 && (BN / 64) % SA == 0, "atoms per store");
+  constexpr int NS = BN / 64 / SA;
   if (row0 >= rows_total) return;  // nothing of this warp's rows exists (warp-uniform)
-  if (lane == 0) bulk_wait_read<0>();
-  __syncwarp();
 #pragma unroll 1
-  for (int a = 0; a < BN / 64; ++a) {
-    uint32_t v[64];
-    if (!zero) {
-      tmem_ld64(tb + a * 64, v);
-      tmem_ld_wait();
-    } else {
+  for (int st = 0; st < NS; ++st) {
+#pragma unroll 1
+    for (int i = 0; i < SA; ++i) {
+      const int a = st * SA + i;
+      uint32_t v[64];
+      if (!zero) {
+        tmem_ld64(tb + a * 64, v);
+        tmem_ld_wait();
+      } else {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) v[j] = 0u;
-    }
-    uint8_t* sb = stg + a * 4096;
+        for (int j = 0; j < 64; ++j) v[j] = 0u;
+      }
+      if (i == 0) {
+        if (lane == 0) bulk_wait_read<NS - 1>();  // the store that last read these atoms
+        __syncwarp();
+      }
+      uint8_t* sb = stg + a * 4096;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(v[j * 8 + 0]), __uint_as_float(v[j * 8 + 1]));
-      w.y = pack_bf16x2(__uint_as_float(v[j * 8 + 2]), __uint_as_float(v[j * 8 + 3]));
-      w.z = pack_bf16x2(__uint_as_float(v[j * 8 + 4]), __uint_as_float(v[j * 8 + 5]));
-      w.w = pack_bf16x2(__uint_as_float(v[j * 8 + 6]), __uint_as_float(v[j * 8 + 7]));
-      *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+      for (int j = 0; j < 8; ++j) {
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(v[j * 8 + 0]), __uint_as_float(v[j * 8 + 1]));
+        w.y = pack_bf16x2(__uint_as_float(v[j * 8 + 2]), __uint_as_float(v[j * 8 + 3]));
+        w.z = pack_bf16x2(__uint_as_float(v[j * 8 + 4]), __uint_as_float(v[j * 8 + 5]));
+        w.w = pack_bf16x2(__uint_as_float(v[j * 8 + 6]), __uint_as_float(v[j * 8 + 7]));
+        *reinterpret_cast<uint4*>(sb + lane * 128 + ((j ^ (lane & 7)) << 4)) = w;
+      }
     }
-  }
-  fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
-    tma_store_4d(tmC4, smem_u32(stg), 0, row0, col0 / 64, g);
-    bulk_commit();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (col0 + st * SA * 64 < cols_total)
+        tma_store_4d(tmC4, smem_u32(stg + st * SA * 4096), 0, row0, col0 / 64 + st * SA, g);
+      bulk_commit();
+    }
   }
 }
 

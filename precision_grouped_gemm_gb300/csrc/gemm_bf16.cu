@@ -109,7 +109,7 @@ int launch_bf16(const Bf16Call& c) {
     if ((st = enc(&ta, c.a, c.N, kBM / 64, &a.a_multi))) return st;
     if ((st = enc(&tb, c.b, c.K, kBN / 64, &a.b_multi))) return st;
     if (c.epi == 3) st = encode_wgrad_accum_f32(&tc, c.out, c.N, c.K, c.G, &a.c4d);
-    else st = encode_wgrad_out(&tc, c.out, c.N, c.K, c.G, kBN, &a.c4d);
+    else st = encode_wgrad_out(&tc, c.out, c.N, c.K, c.G, kWgradStoreAtoms, &a.c4d);
     if (st) return st;
     a.out_cols = (int)c.K;
     a.wg_rows = (int)c.N;

@@ -33,6 +33,9 @@ constexpr int kBM = 128;          // MMA M (TMEM lanes)
 // k-loop in flight (4% faster on the DeepSeek-shaped fc1 wgrad); long reductions
 // keep 64 (fewer, larger steps; 10% faster on the GPT-OSS-shaped wgrad).
 constexpr int kGemmThreads = 192;
+// 64-column atoms per bulk store of a wgrad output tile: one atom per store lets a
+// tile's stores drain while the next tile is staged.
+constexpr int kWgradStoreAtoms = 1;
 
 struct GemmArgs {
   const int32_t* group_lens;
@@ -47,7 +50,7 @@ struct GemmArgs {
   const void* aux;  // SwiGLU backward: saved H (bf16 [M, 2I])
   int32_t* err;     // device error word or nullptr
   FastDiv nct;      // wgrad: column tiles per row tile
-  int c4d;          // wgrad: tmC is the 4-D whole-tile view (cols % 64 == 0)
+  int c4d;          // wgrad: tmC is the 4-D atom view (cols % 64 == 0)
   int a_multi;      // wgrad: tmA is the atom view {64, M, N/64} (one load per k-block)
   int b_multi;      // wgrad / dgrad: tmB is the atom view of X {64, M, K/64} / W {64, N, K/64, G}
 };
@@ -350,7 +353,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             epi_tma_reduce_f32<BN>(tb, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
                                    args.out_cols, args.c4d != 0, lane);
         } else if (args.c4d) {
-          epi_tma_store_tile<BN>(tb, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
+          epi_tma_store_tile<BN, kWgradStoreAtoms>(tb, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                 args.out_cols, lane);
         } else {
           epi_tma_store_rows<BN>(tb, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
                                  args.out_cols, lane);

@@ -33,6 +33,7 @@ constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
 // accumulator -- TMEM cannot hold two next to the scale factors -- measured 12%
 // slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
 constexpr int kMxWgradBN = 128;
+constexpr int kMxWgradStoreAtoms = 2;  // 64-column atoms per bulk store of a wgrad tile
 constexpr int kMxThreads = 192;
 
 struct MxArgs {
@@ -56,7 +57,7 @@ struct MxArgs {
   uint8_t* q_codes;   // SwiGLU epilogues: row-wise MX codes of `out` (or nullptr)
   uint8_t* q_scales;  // and their scales
   FastDiv nct;  // wgrad: column tiles per row tile
-  int c4d;      // wgrad: tmC is the 4-D whole-tile view
+  int c4d;      // wgrad: tmC is the 4-D atom view
 };
 
 template <int FMT>
@@ -363,7 +364,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         const uint32_t tbw = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
         if (args.c4d)
-          epi_tma_store_tile<BN>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows, lane);
+          epi_tma_store_tile<BN, kMxWgradStoreAtoms>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                 args.out_cols, lane);
         else
           epi_tma_store_rows<BN>(tbw, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
                                  args.out_cols, lane);
@@ -497,7 +499,7 @@ int launch_mx_gemm(const MxCall& c) {
     uint32_t bx[2] = {rb, 128}, bw[2] = {rb, (uint32_t)kMxWgradBN};
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
     if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bw, sw))) return st;
-    if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxWgradBN, &a.c4d))) return st;
+    if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxWgradStoreAtoms, &a.c4d))) return st;
     a.nct = FastDiv((uint32_t)cdiv(K, kMxWgradBN));
     a.sa_ld = a.sb_ld = Mp / 32;
     a.a_rows = (int)N;

@@ -27,9 +27,10 @@ int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
 
 int cuda_status(cudaError_t e);
 
-// Output map of a wgrad dW [G, N, K] bf16: the 4-D whole-tile view when K % 64 == 0
-// and the driver accepts it (*whole_tile = 1), else the 3-D 32 x 64 box view.
-int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int bn, int* whole_tile);
+// Output map of a wgrad dW [G, N, K] bf16: the 4-D view {64, N, K/64, G} with
+// `atoms` 32 x 64 atoms per store when K % 64 == 0 and the driver accepts it
+// (*four_d = 1), else the 3-D {K, N, G} view with 32 x 64 boxes.
+int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int atoms, int* four_d);
 
 // Reduce-add map of an fp32 wgrad accumulator [G, N, K]: the 4-D view {32, N, K/32, G}
 // (*four_d = 1) when K % 32 == 0 and accepted, else the 3-D view {K, N, G}.

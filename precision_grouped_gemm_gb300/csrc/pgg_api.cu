@@ -73,16 +73,16 @@ int encode_tmap(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const voi
   return r == CUDA_SUCCESS ? PGG_OK : PGG_ERR_INVALID_ARG;
 }
 
-int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int bn, int* whole_tile) {
+int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, int atoms, int* four_d) {
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   if (K % 64 == 0) {
-    // 4-D view {64, N, K/64, G}: one bulk store moves 32 rows x bn columns of a tile
+    // 4-D view {64, N, K/64, G}: one bulk store moves `atoms` 32-row x 64-column atoms
     uint64_t d[4] = {64, (uint64_t)N, (uint64_t)(K / 64), (uint64_t)G};
     uint64_t s[3] = {(uint64_t)K * 2, 128, (uint64_t)(N * K * 2)};
-    uint32_t b[4] = {64, 32, (uint32_t)(bn / 64), 1};
+    uint32_t b[4] = {64, 32, (uint32_t)atoms, 1};
     if (encode_tmap(map, bf, 4, out, d, s, b, sw) == PGG_OK) {
-      *whole_tile = 1;
+      *four_d = 1;
       return PGG_OK;
     }
   }
@@ -90,7 +90,7 @@ int encode_wgrad_out(CUtensorMap* map, void* out, int64_t N, int64_t K, int G, i
   uint64_t d[3] = {(uint64_t)K, (uint64_t)N, (uint64_t)G};
   uint64_t s[2] = {(uint64_t)K * 2, (uint64_t)(N * K * 2)};
   uint32_t b[3] = {64, 32, 1};
-  *whole_tile = 0;
+  *four_d = 0;
   return encode_tmap(map, bf, 3, out, d, s, b, sw);
 }
 

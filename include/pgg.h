@@ -161,7 +161,12 @@ int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8
  * prefix sum of round_up(len_h, PGG_MX_PAD).  Tail positions and everything
  * past the last group up to M_pad hold code 0 and scale 0.
  *   in [M, C] bf16; group_lens may be NULL for one group of M rows.
- *   codes_t [C, M_pad] u8 (e4m3) or [C, M_pad/2] (e2m1); scales_t [C, M_pad/32].
+ *   codes_t [C, M_pad] u8 (e4m3) or [C, M_pad/2] (e2m1).
+ *   scales_t: round_up(C, 128) * M_pad / 32 bytes in the blocked layout the
+ *   block-scaled MMA reads: one 512-byte atom per 128-row block rb of C and
+ *   per 128-column k-block p of [0, M_pad), at byte (rb * M_pad / 128 + p) * 512;
+ *   inside it the scale of row 128 rb + m, 32-block 4 p + q sits at byte
+ *   16 (m % 32) + 4 (m / 32) + q.  Rows past C hold scale 0.
  *   M_pad % PGG_MX_PAD == 0 and M_pad >= sum(round_up(len_g, PGG_MX_PAD))
  *   (else *err = PGG_ERR_PAD_OVERFLOW and nothing is written);
  *   M + G * (PGG_MX_PAD - 1) rounded up to PGG_MX_PAD always suffices. */
@@ -179,21 +184,25 @@ int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t*
  *                   out2 = H [M, 2I] or NULL (as pgg_grouped_fc1_swiglu).
  *   PGG_MODE_DGRAD: out[M, K] = deq(A)_g . W_g with A = dY [M, N] row-wise
  *                   codes (blocks along N), SA [M, N/32]; B = W quantized
- *                   along N and stored transposed, [K, G*N] codes, SB
- *                   [K, G*N/32] (pgg_mx_quantize_colwise of W viewed as
- *                   [G*N, K] with G groups of N rows produces exactly this).
+ *                   along N and stored transposed, [K, G*N] codes, SB in the
+ *                   blocked layout of pgg_mx_quantize_colwise (that call on W
+ *                   viewed as [G*N, K] with G groups of N rows and M_pad =
+ *                   G*N produces exactly this).
  *                   epilogue PGG_EPI_SWIGLU: the SwiGLU backward with the
  *                   saved bf16 H [M, 2K]; out = dH [M, 2K].
  *   PGG_MODE_WGRAD: out[G, N, K] = sum over group g's padded columns of
  *                   deq(A)[:, r] deq(B)[:, r]^T with A = dY column-wise
- *                   codes [N, M_pad], B = X column-wise codes [K, M_pad]
- *                   (pgg_mx_quantize_colwise); empty groups give 0.
+ *                   codes [N, M_pad], B = X column-wise codes [K, M_pad],
+ *                   SA / SB their blocked scales (pgg_mx_quantize_colwise);
+ *                   empty groups give 0.
  * Fused MX output (SwiGLU epilogues only; both NULL to skip): out_codes /
  * out_scales receive the row-wise MX quantization, in `fmt`, of the bf16 tensor
  * written to `out` (A of the forward, dH of the dgrad) -- bit-identical to
  * pgg_mx_quantize_rowwise(out) -- so the next GEMM's operand needs no separate
  * quantize pass ("Primus-Turbo" README, "What's New": fused GroupedMLP in
  * FP8 / MXFP8).  The width of `out` (I) must be a multiple of 32.
+ * Row-major scales (fwd SA / SB, dgrad SA) need 4-byte alignment, blocked ones
+ * (dgrad SB, wgrad SA / SB) 16-byte alignment.
  * Sizes: the reduction axis is a multiple of 128 (fwd K, dgrad N); the other
  * dimensions are multiples of 8 (N of a SwiGLU forward a multiple of 16); e2m1
  * codes are packed two per byte.  fp32 accumulation, bf16 output. */

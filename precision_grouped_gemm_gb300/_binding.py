@@ -214,7 +214,8 @@ def mx_pad_rows(M: int, G: int) -> int:
 
 def mx_quantize_colwise(x, group_lens, fmt, M_pad=None, codes_t=None, scales_t=None, err=None,
                         stream=None):
-    """bf16 [M,C] + group_lens -> transposed (codes_t [C,M_pad] or [C,M_pad/2], scales_t [C,M_pad/32])."""
+    """bf16 [M,C] + group_lens -> transposed codes_t [C,M_pad] (or [C,M_pad/2]) and scales_t
+    [round_up(C,128), M_pad/32] bytes in the blocked atom layout (see pgg.h)."""
     M, C = x.shape
     f = _FMT[fmt]
     G = 1 if group_lens is None else group_lens.numel()
@@ -222,8 +223,8 @@ def mx_quantize_colwise(x, group_lens, fmt, M_pad=None, codes_t=None, scales_t=N
         M_pad = mx_pad_rows(M, G)
     if codes_t is None:
         codes_t = torch.empty((C, M_pad if f == FMT_E4M3 else M_pad // 2), dtype=torch.uint8, device=x.device)
-    if scales_t is None:
-        scales_t = torch.empty((C, M_pad // 32), dtype=torch.uint8, device=x.device)
+    if scales_t is None:  # blocked atom layout, rows padded to a multiple of 128
+        scales_t = torch.empty((-(-C // 128) * 128, M_pad // 32), dtype=torch.uint8, device=x.device)
     _dev(x, group_lens, codes_t, scales_t, err)
     lens = None if group_lens is None else _lens(group_lens)
     _check(lib().pgg_mx_quantize_colwise(_ptr(x), M, C, _ptr(lens), G, f, _ptr(codes_t), _ptr(scales_t),

@@ -89,10 +89,10 @@ template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmArgs& a, const int32_t* s_off,
                                             const int32_t* s_tile, GroupCursor& cur) {
   Tile T;
-  const int g = cur.at(s_tile, a.G, t);
-  const int local = t - s_tile[g];
-  const int off = s_off[g], len = s_off[g + 1] - s_off[g];
-  T.g = g;
+  cur.at(s_tile, s_off, nullptr, a.G, t);
+  const int local = t - cur.t_lo;
+  const int off = cur.off, len = cur.len;
+  T.g = cur.g;
   if (MODE == kWgrad) {
     // column tiles vary fastest: the CTAs running at one time fill whole rows of dW_g
     const int rt = (int)a.nct.div((uint32_t)local);

@@ -34,6 +34,10 @@ constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
 // slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
 constexpr int kMxWgradBN = 128;
 constexpr int kMxWgradStoreAtoms = 2;  // 64-column atoms per bulk store of a wgrad tile
+// TMEM accumulator buffers of a 128-column tile.  Three let the MMA for tile t+2
+// start before the epilogue has drained tile t: a wgrad tile has a single k-block,
+// so the accumulator hand-off round trip is as long as the epilogue itself.
+constexpr int kMxAccBufs = 3;
 constexpr int kMxThreads = 192;
 
 struct MxArgs {
@@ -70,8 +74,8 @@ struct MxCfg {
   static constexpr int kTileBytes = 128 * kRowBytes;
 };
 
-// BN = 128 (two accumulators, double-buffered) or 256 (wgrad: one accumulator;
-// TMEM cannot hold two 256-column accumulators next to the scale factors).
+// BN = 128 (kMxAccBufs accumulators) or 256 (wgrad: one accumulator; TMEM
+// cannot hold two 256-column accumulators next to the scale factors).
 template <int FMT, int BN, int STAGES, int EPI_BYTES>
 struct MxSmem {
   static constexpr int kA = MxCfg<FMT>::kTileBytes;
@@ -95,11 +99,11 @@ template <int MODE, int EPI, int BN>
 __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_t* s_off,
                                             const int32_t* s_tile, const int32_t* s_poff, GroupCursor& cur) {
   MxTile T;
-  const int g = cur.at(s_tile, a.G, t);
-  const int local = t - s_tile[g];
-  const int len = s_off[g + 1] - s_off[g];
-  T.g = g;
-  T.poff = s_poff[g];
+  cur.at(s_tile, s_off, s_poff, a.G, t);
+  const int local = t - cur.t_lo;
+  const int len = cur.len;
+  T.g = cur.g;
+  T.poff = cur.poff;
   T.len = len;
   if (MODE == kWgrad) {
     // column tiles vary fastest (whole rows of dW_g written by concurrent CTAs)
@@ -111,7 +115,7 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
   } else {
     const int nmt = (len + kMxBM - 1) / kMxBM;
     const int mt = local % nmt;
-    T.row0 = s_off[g] + mt * kMxBM;
+    T.row0 = cur.off + mt * kMxBM;
     T.rows = min(kMxBM, len - mt * kMxBM);
     T.col0 = (local / nmt) * mx_tile_cols<MODE, EPI>();
     T.nkb = (a.red + kMxBK - 1) / kMxBK;
@@ -126,12 +130,20 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   using C = MxCfg<FMT>;
   static_assert(BN == 128 || (BN == 256 && MODE == kWgrad), "BN");
   using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
-  constexpr int NACC = BN == 256 ? 1 : 2;                // accumulator buffers
+  constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
   constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kSfCol0 = NACC * BN;                 // scale-factor columns after the accumulators
   constexpr uint32_t kSfPer = 4 + 4 * (BN / 128);         // per stage: SFA 4 + SFB 4 per 128 rows
   static_assert(kSfCol0 + STAGES * kSfPer <= kTmemCols, "TMEM columns");
+  static_assert((2 * STAGES + 2 * NACC + 1) * 8 + 12 <= L::kGroupOff - L::kBarOff, "barrier area");
+  // Scale factors of an operand either sit in the blocked layout of the column-wise
+  // quantizer (wgrad A and B, dgrad B: 128-row aligned tiles), fetched as whole
+  // 512-byte atoms by bulk copy, or are row-major [rows, K/32] (ragged token rows),
+  // gathered 4 bytes per row by cp.async into the atom.
+  constexpr bool kGatherA = MODE != kWgrad;
+  constexpr bool kGatherB = MODE == kFwd;
+  constexpr uint32_t kSfBulk = (kGatherA ? 0u : 512u) + (kGatherB ? 0u : 512u * (BN / 128));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -139,8 +151,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + NACC;
+  uint64_t* drain = tempty + NACC;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
@@ -151,10 +163,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), 1 + 32);  // expect_tx arrive + 32 cp.async arrives
+      mbar_init(smem_u32(&full[s]), (kGatherA || kGatherB) ? 1 + 32 : 1);  // expect_tx arrive (+ 32 cp.async arrives)
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int a = 0; a < 2; ++a) {
+    for (int a = 0; a < NACC; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
       mbar_init(smem_u32(&tempty[a]), 128);
     }
@@ -214,7 +226,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const uint32_t fb = smem_u32(&full[stage]);
         const int kbyte = kb * C::kRowBytes;  // byte offset of this k-block along a row
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, L::kA + L::kB);
+          mbar_arrive_expect_tx(fb, L::kA + L::kB + kSfBulk);
           if (MODE == kFwd) {
             tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
             if (EPI == kEpiSwiGLU) {
@@ -231,9 +243,21 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             tma_load_2d(sa, &tmA, fb, pb, T.row0);
             tma_load_2d(sb, &tmB, fb, pb, T.col0);
           }
+          // blocked scale atoms: ((row block) * atoms-per-row-block + k-block) * 512
+          if (!kGatherA)
+            bulk_load(ssf, args.SA + ((int64_t)(T.row0 >> 7) * (args.sa_ld >> 2) + (T.poff >> 7) + kb) * 512, 512,
+                      fb);
+          if (!kGatherB) {
+            const int p = MODE == kWgrad ? (T.poff >> 7) + kb : T.g * (args.red >> 7) + kb;
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              bulk_load(ssf + 512 + 512 * h,
+                        args.SB + ((int64_t)((T.col0 >> 7) + h) * (args.sb_ld >> 2) + p) * 512, 512, fb);
+          }
         }
-        // scale factors: lane l fetches rows l, l+32, l+64, l+96 of each operand tile
-        // (4 bytes = the k-block's 4 block scales) into word 4 l + i of the atom
+        // gathered scale factors (row-major operands): lane l fetches rows l, l+32, l+64,
+        // l+96 of the operand tile (4 bytes = the k-block's 4 block scales) into word
+        // 4 l + i of the atom
         int sfa_col, sfb_col;  // byte column of this k-block in the scale tensors
         if (MODE == kWgrad) {
           sfa_col = sfb_col = T.poff / 32 + kb * 4;
@@ -246,8 +270,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 #pragma unroll
         for (int i = 0; i < BN / 32; ++i) {
           const int m = lane + 32 * i;
-          // A rows: fwd/dgrad token rows; wgrad rows of dY^T (n)
-          if (i < 4) {
+          // A rows: fwd/dgrad token rows
+          if (kGatherA && i < 4) {
             const int ar = T.row0 + m;
             const bool aok = ar < args.a_rows;
             cp_async_4(ssf + (lane * 4 + i) * 4, args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0),
@@ -267,10 +291,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             bok = br < args.b_rows;
           }
           // B row m goes to atom m / 128, word 4 (m % 32) + (m % 128) / 32
-          cp_async_4(ssf + 512 + (i / 4) * 512 + (lane * 4 + (i % 4)) * 4,
-                     args.SB + (bok ? (int64_t)br * args.sb_ld + sfb_col : 0), bok ? 4u : 0u);
+          if (kGatherB)
+            cp_async_4(ssf + 512 + (i / 4) * 512 + (lane * 4 + (i % 4)) * 4,
+                       args.SB + (bok ? (int64_t)br * args.sb_ld + sfb_col : 0), bok ? 4u : 0u);
         }
-        cp_async_arrive_noinc(fb);
+        if (kGatherA || kGatherB) cp_async_arrive_noinc(fb);
         __syncwarp();
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -307,7 +332,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t ssf = sb + L::kB;
           const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;
           const uint32_t sfb_t = sfa_t + 4;
-          fence_proxy_async_smem();  // cp.async-written scales -> async proxy
+          if (kGatherA || kGatherB) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
           tmem_cp_32x128b_x4(sfa_t, smem_desc(ssf, 0, 128, kSwizzleNone));
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32: 4 columns per 128 rows

@@ -79,7 +79,18 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
 // writes the column's 32 codes (32 bytes e4m3 / 16 bytes e2m1) and its scale.
 // Work items run with j fastest, so the warps writing the 32-byte pieces of one
 // 128-byte line of codes_t run at the same time.
+//
+// Scales go to the blocked layout the block-scaled MMA reads: for every 128-row
+// block rb of the C rows and every 128-column k-block p of [0, M_pad), one 512-byte
+// atom at ((rb * M_pad / 128) + p) * 512 in which row r = 128 rb + m, 32-block
+// j = 4 p + q sits at byte 16 (m % 32) + 4 (m / 32) + q.  Rows past C up to the
+// next multiple of 128 get scale 0.
 constexpr int kColSlab = 64;
+
+__device__ __forceinline__ int64_t blocked_scale_index(int r, int j, int64_t M_pad) {
+  const int m = r & 127;
+  return (((int64_t)(r >> 7) * (M_pad >> 7) + (j >> 2)) << 9) + 16 * (m & 31) + 4 * (m >> 5) + (j & 3);
+}
 constexpr int kColThreads = 256;
 
 template <int FMT>
@@ -114,7 +125,7 @@ __device__ __forceinline__ void colwise_store(const uint32_t (&v)[32], int half,
               (cvt_e2m1x2(f[8 * k + 4], f[8 * k + 5]) << 16) | (cvt_e2m1x2(f[8 * k + 6], f[8 * k + 7]) << 24);
     *reinterpret_cast<uint4*>(codes_t + (int64_t)c * (M_pad / 2) + (int64_t)j * 16) = o;
   }
-  scales_t[(int64_t)c * (M_pad / 32) + j] = (uint8_t)(valid > 0 ? sc : 0u);
+  scales_t[blocked_scale_index(c, j, M_pad)] = (uint8_t)(valid > 0 ? sc : 0u);
 }
 
 template <int FMT>
@@ -151,7 +162,8 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
   __syncthreads();
   if (s_bad) return;
   const int nblk = (int)(M_pad / 32);
-  const int nslab = (C + kColSlab - 1) / kColSlab;
+  const int C128 = (C + 127) & ~127;  // scale rows, padded to whole atoms
+  const int nslab = C128 / kColSlab;
   const int64_t total = (int64_t)nblk * nslab;
   const int used = s_blk[G];
   const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
@@ -166,7 +178,13 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
       valid = min(32, max(0, s_off[g + 1] - s_off[g] - 32 * b));
       row0 = (int64_t)s_off[g] + 32 * b;
     }
-    if (c >= C) continue;
+    if (c >= C) {  // pad rows of the last atom: scale 0, no codes
+      if (c < C128) {
+        scales_t[blocked_scale_index(c, j, M_pad)] = 0;
+        scales_t[blocked_scale_index(c + 1, j, M_pad)] = 0;
+      }
+      continue;
+    }
     uint32_t v[32];
     const uint32_t* src = reinterpret_cast<const uint32_t*>(in + row0 * C + c);
 #pragma unroll
@@ -202,7 +220,7 @@ int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != PGG_OK) return st;
-  const int64_t total = (M_pad / 32) * ((C + kColSlab - 1) / kColSlab);  // warp work items
+  const int64_t total = (M_pad / 32) * (((C + 127) / 128 * 128) / kColSlab);  // warp work items
   const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
   const size_t smem = 8 * (size_t)(G + 1);

@@ -295,6 +295,9 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
   if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
       (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
+  // blocked scale atoms (wgrad SA and SB, dgrad SB) are fetched by 16-byte-aligned bulk copies
+  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || (mode != PGG_MODE_FWD && !aligned16(SB)))
+    return PGG_ERR_ALIGNMENT;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
   if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
     return PGG_ERR_ALIGNMENT;

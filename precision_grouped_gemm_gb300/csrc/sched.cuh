@@ -109,12 +109,26 @@ __device__ __forceinline__ int find_group(const int32_t* s_tile, int G, int t) {
 
 // The group of a CTA's tiles, tracked as t grows (t, t + gridDim.x, ...): a
 // binary search for the first tile, then a short forward walk.
+// The group of a role's current tile with its scan values, held in registers.
+// A CTA's tiles ascend and almost always stay in one group from one tile to
+// the next, so the shared-memory tables are read only when a tile crosses into
+// another group: while the pipeline keeps shared memory busy, each dependent
+// table read costs hundreds of cycles.
 struct GroupCursor {
   int g = -1;
-  __device__ __forceinline__ int at(const int32_t* s_tile, int G, int t) {
-    if (g < 0) g = find_group(s_tile, G, t);
+  int t_lo = 0, t_hi = 0;    // tiles [t_lo, t_hi) belong to group g
+  int off = 0, len = 0;      // rows [off, off + len) of the ragged operand
+  int poff = 0;              // padded column offset (column-wise MX layout), if tracked
+  __device__ __forceinline__ void at(const int32_t* s_tile, const int32_t* s_off, const int32_t* s_poff,
+                                     int G, int t) {
+    if (g >= 0 && t >= t_lo && t < t_hi) return;
+    if (g < 0 || t < t_lo) g = find_group(s_tile, G, t);
     while (g + 1 < G && s_tile[g + 1] <= t) ++g;
-    return g;
+    t_lo = s_tile[g];
+    t_hi = s_tile[g + 1];
+    off = s_off[g];
+    len = s_off[g + 1] - off;
+    if (s_poff) poff = s_poff[g];
   }
 };
 

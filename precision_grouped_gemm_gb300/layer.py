@@ -194,14 +194,15 @@ class MxLayerBuffers:
         u8, bf = torch.uint8, torch.bfloat16
         Mp = b.M_pad
         e = lambda *s: torch.empty(s, dtype=u8, device=dev)
+        r128 = lambda n: -(-n // 128) * 128  # blocked column-wise scales: rows padded to 128
         b.bufs = {
             "Xq": (e(M, cb(Hd)), e(M, Hd // 32)), "A": torch.empty((M, I), dtype=bf, device=dev),
             "H": torch.empty((M, I2), dtype=bf, device=dev), "Aq": (e(M, cb(I)), e(M, I // 32)),
             "Y": torch.empty((M, Hd), dtype=bf, device=dev), "dYq": (e(M, cb(Hd)), e(M, Hd // 32)),
-            "dH": torch.empty((M, I2), dtype=bf, device=dev), "dYc": (e(Hd, cb(Mp)), e(Hd, Mp // 32)),
-            "Ac": (e(I, cb(Mp)), e(I, Mp // 32)), "dW2": torch.empty((G, Hd, I), dtype=bf, device=dev),
+            "dH": torch.empty((M, I2), dtype=bf, device=dev), "dYc": (e(Hd, cb(Mp)), e(r128(Hd), Mp // 32)),
+            "Ac": (e(I, cb(Mp)), e(r128(I), Mp // 32)), "dW2": torch.empty((G, Hd, I), dtype=bf, device=dev),
             "dHq": (e(M, cb(I2)), e(M, I2 // 32)), "dX": torch.empty((M, Hd), dtype=bf, device=dev),
-            "dHc": (e(I2, cb(Mp)), e(I2, Mp // 32)), "Xc": (e(Hd, cb(Mp)), e(Hd, Mp // 32)),
+            "dHc": (e(I2, cb(Mp)), e(r128(I2), Mp // 32)), "Xc": (e(Hd, cb(Mp)), e(r128(Hd), Mp // 32)),
             "dW1": torch.empty((G, I2, Hd), dtype=bf, device=dev),
             "err": torch.zeros(1, dtype=torch.int32, device=dev),
         }

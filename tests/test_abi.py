@@ -94,3 +94,19 @@ def test_moe_glue_host_validation_without_gpu(lib):
     b.argtypes = [P, P, P, P, P, P, I64, I32, I64, P]
     assert b(g, g, g, None, g, g, 8, 4, 64, None) == 1                         # w required
     assert b(g, g, g, g, g + 4, g, 8, 4, 64, None) == 3                        # misaligned dYs
+
+
+def test_blocked_scale_layout_helpers():
+    # the tests' view of the blocked column-wise scale layout (pgg.h): atom (r // 128, j // 4)
+    # of 512 bytes, byte 16 (m % 32) + 4 (m // 32) + j % 4 inside it, m = r % 128
+    import numpy as np
+    import util
+    C, M_pad = 200, 384
+    s = (np.arange(C * (M_pad // 32)) % 251 + 1).astype(np.uint8).reshape(C, M_pad // 32)
+    b = util.block_scales(s, M_pad)
+    assert b.shape == (256, M_pad // 32)
+    flat = b.reshape(-1)
+    assert flat[0] == s[0, 0] and flat[1] == s[0, 1] and flat[4] == s[32, 0] and flat[16] == s[1, 0]
+    assert flat[512] == s[0, 4]                                  # next k-block atom of row block 0
+    assert flat[3 * 512 + 16 * 5 + 4 * 2 + 3] == s[128 + 69, 3]  # row block 1, m = 69
+    np.testing.assert_array_equal(util.unblock_scales(b, C, M_pad), s)

@@ -41,3 +41,32 @@ def assert_close(got: torch.Tensor, ref: np.ndarray, what: str = "", rel: float 
         raise AssertionError(f"{what}: tolerance exceeded, worst err/bound = {ratio:.3g} at {i}: "
                              f"got {g[i]!r} ref {ref[i]!r} bound {bound[i]:.3g} rms {og.rms(ref):.3g}")
     return ratio
+
+
+def _blocked_index(C: int, M_pad: int) -> np.ndarray:
+    """Byte position in the blocked scale layout of column-wise scale (row r, 32-block j):
+    atom (r // 128, j // 4) at ((r // 128) * M_pad / 128 + j // 4) * 512, and inside it
+    byte 16 (m % 32) + 4 (m // 32) + j % 4 with m = r % 128."""
+    r = np.arange(C)[:, None]
+    j = np.arange(M_pad // 32)[None, :]
+    m = r % 128
+    return ((r // 128) * (M_pad // 128) + j // 4) * 512 + 16 * (m % 32) + 4 * (m // 32) + j % 4
+
+
+def block_scales(s: np.ndarray, M_pad: int) -> np.ndarray:
+    """Row-major column-wise scales [C, M_pad/32] -> the blocked layout [round_up(C,128), M_pad/32]."""
+    C = s.shape[0]
+    out = np.zeros(-(-C // 128) * 128 * (M_pad // 32), dtype=np.uint8)
+    out[_blocked_index(C, M_pad)] = s
+    return out.reshape(-1, M_pad // 32)
+
+
+def unblock_scales(b, C: int, M_pad: int) -> np.ndarray:
+    """The blocked layout (any shape, tensor or array) -> row-major [C, M_pad/32]; also
+    checks that the rows past C are zero."""
+    flat = (b.detach().cpu().numpy() if isinstance(b, torch.Tensor) else np.asarray(b)).reshape(-1)
+    idx = _blocked_index(C, M_pad)
+    pad = np.ones(flat.size, dtype=bool)
+    pad[idx.reshape(-1)] = False
+    assert not flat[pad].any(), "blocked scales: rows past C must hold scale 0"
+    return flat[idx]

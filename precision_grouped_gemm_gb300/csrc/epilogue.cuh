@@ -131,27 +131,79 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
 // FC2 dgrad + SwiGLU backward: accumulator = dA[row, col0 ..]; with g, u from
 // the saved H: dH[:, c] = dA u s (1 + g (1 - s)), dH[:, I + c] = dA g s, s = sigmoid(g).
 // QF != 0 and qcodes != null: dH [rows, 2I] is also emitted MX-quantized (row-wise).
+// The saved H is read a chunk ahead of its use (raw bf16 words in registers), so the
+// load latency overlaps the previous chunk's arithmetic; epi_swiglu_bwd_prefetch,
+// called before the accumulator wait, has already pulled the tile's H into L2.
+template <int BN>
+__device__ __forceinline__ void epi_swiglu_bwd_prefetch(const __nv_bfloat16* H, size_t grow, bool row_ok,
+                                                        int col0, int I) {
+  if (!row_ok) return;
+  const __nv_bfloat16* g = H + grow * (2 * (size_t)I) + col0;
+  const int n = min(BN, I - col0);  // columns of this tile in each half
+  if (n <= 0) return;
+#pragma unroll 1
+  for (int b = 0; b < n * 2; b += 128) {  // 128-byte lines of the gate and up segments
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(g) + b));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<const char*>(g + I) + b));
+  }
+}
+
+// 32 bf16 of a row (ncols < 32: the tail, zero-filled) as raw words.
+__device__ __forceinline__ void load_raw32(const __nv_bfloat16* src, uint4 (&w)[4], int ncols) {
+  if (ncols >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = __ldg(s4 + q);
+  } else {
+    const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+    uint32_t* ww = reinterpret_cast<uint32_t*>(w);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t lo = 2 * j < ncols ? s16[2 * j] : 0u, hi = 2 * j + 1 < ncols ? s16[2 * j + 1] : 0u;
+      ww[j] = lo | (hi << 16);
+    }
+  }
+}
+
 template <int BN, int QF = 0>
 __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
                                                size_t grow, bool row_ok, int col0, int I,
                                                uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr) {
+  const __nv_bfloat16* hrow = H + grow * (2 * (size_t)I);
+  uint4 ng[4], nu[4];  // the next chunk's gate / up words
+  if (row_ok && col0 < I) {
+    load_raw32(hrow + col0, ng, I - col0);
+    load_raw32(hrow + I + col0, nu, I - col0);
+  }
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
+    const int c0 = col0 + c * 32;
+    uint4 wg[4], wu[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      wg[q] = ng[q];
+      wu[q] = nu[q];
+    }
+    if (row_ok && c0 + 32 < I && c + 1 < BN / 32) {
+      load_raw32(hrow + c0 + 32, ng, I - c0 - 32);
+      load_raw32(hrow + I + c0 + 32, nu, I - c0 - 32);
+    }
     uint32_t rd[32];
     tmem_ld32(tb + c * 32, rd);
     tmem_ld_wait();
-    const int c0 = col0 + c * 32;
     if (row_ok && c0 < I) {
       const int nc = min(32, I - c0);
-      float hg[32], hu[32], dg[32], du[32];
-      load_row32(H + grow * (2 * (size_t)I) + c0, hg, nc);
-      load_row32(H + grow * (2 * (size_t)I) + I + c0, hu, nc);
+      const uint32_t* pg = reinterpret_cast<const uint32_t*>(wg);
+      const uint32_t* pu = reinterpret_cast<const uint32_t*>(wu);
+      float dg[32], du[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
+        const float hg = (j & 1) ? bf16_hi(pg[j >> 1]) : bf16_lo(pg[j >> 1]);
+        const float hu = (j & 1) ? bf16_hi(pu[j >> 1]) : bf16_lo(pu[j >> 1]);
         const float da = __uint_as_float(rd[j]);
-        const float s = 1.0f / (1.0f + __expf(-hg[j]));
-        dg[j] = da * hu[j] * s * (1.0f + hg[j] * (1.0f - s));
-        du[j] = da * hg[j] * s;
+        const float s = 1.0f / (1.0f + __expf(-hg));
+        dg[j] = da * hu * s * (1.0f + hg * (1.0f - s));
+        du[j] = da * hg * s;
       }
       store_row32(dH + grow * (2 * (size_t)I) + c0, dg, nc);
       store_row32(dH + grow * (2 * (size_t)I) + I + c0, du, nc);

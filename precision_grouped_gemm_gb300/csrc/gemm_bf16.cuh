@@ -366,10 +366,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         continue;
       }
+      const size_t grow = (size_t)T.row0 + r;
+      if (EPI == kEpiSwiGLUBwd)  // the saved H of this tile streams into L2 while the MMAs run
+        epi_swiglu_bwd_prefetch<BN>(reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
+                                    args.I);
       if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      const size_t grow = (size_t)T.row0 + r;
       if (EPI == kEpiSwiGLU) {
         epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
       } else if (EPI == kEpiSwiGLUBwd) {

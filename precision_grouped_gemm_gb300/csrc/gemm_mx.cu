@@ -33,6 +33,14 @@ constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
 // accumulator -- TMEM cannot hold two next to the scale factors -- measured 12%
 // slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
 constexpr int kMxWgradBN = 128;
+// Forward / dgrad tile width per format.  A block-scaled MMA carries little work
+// per instruction (128 x 128 x 64 e2m1 is ~24 ns of tensor time) and the MMA warp
+// pays ~45 ns per MMA and ~36 ns per scale copy, so a 128-wide tile is issue-bound;
+// 256-wide tiles double the work per MMA and per scale copy, at the price of a
+// single TMEM accumulator.  On one GPU: MXFP4 fc2 fwd 1.46 -> 1.07 ms, fc1 dgrad
+// 2.62 -> 1.71 ms; MXFP8 fc2 fwd 0.403 -> 0.368 ms, fc1 dgrad 0.762 -> 0.724 ms.
+constexpr int kMxFwdBNE4M3 = 256;
+constexpr int kMxFwdBNE2M1 = 256;
 constexpr int kMxWgradStoreAtoms = 2;  // 64-column atoms per bulk store of a wgrad tile
 // TMEM accumulator buffers of a 128-column tile.  Three let the MMA for tile t+2
 // start before the epilogue has drained tile t: a wgrad tile has a single k-block,
@@ -74,8 +82,8 @@ struct MxCfg {
   static constexpr int kTileBytes = 128 * kRowBytes;
 };
 
-// BN = 128 (kMxAccBufs accumulators) or 256 (wgrad: one accumulator; TMEM
-// cannot hold two 256-column accumulators next to the scale factors).
+// BN = 128 (kMxAccBufs accumulators) or 256 (one accumulator: TMEM cannot hold
+// two 256-column accumulators next to the scale factors).
 template <int FMT, int BN, int STAGES, int EPI_BYTES>
 struct MxSmem {
   static constexpr int kA = MxCfg<FMT>::kTileBytes;
@@ -92,8 +100,8 @@ struct MxTile {
   int g, row0, rows, col0, nkb, poff, len;
 };
 
-template <int MODE, int EPI>
-__device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? kMxBN / 2 : kMxBN; }
+template <int EPI, int BN>
+__device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? BN / 2 : BN; }
 
 template <int MODE, int EPI, int BN>
 __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_t* s_off,
@@ -117,7 +125,7 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
     const int mt = local % nmt;
     T.row0 = cur.off + mt * kMxBM;
     T.rows = min(kMxBM, len - mt * kMxBM);
-    T.col0 = (local / nmt) * mx_tile_cols<MODE, EPI>();
+    T.col0 = (local / nmt) * mx_tile_cols<EPI, BN>();
     T.nkb = (a.red + kMxBK - 1) / kMxBK;
   }
   return T;
@@ -128,7 +136,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
   using C = MxCfg<FMT>;
-  static_assert(BN == 128 || (BN == 256 && MODE == kWgrad), "BN");
+  static_assert(BN == 128 || BN == 256, "BN");
   using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
   constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
   constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc.bm = 0;
       tc.per_row_tile = ((args.wg_rows + kMxBM - 1) / kMxBM) * ((args.out_cols + BN - 1) / BN);
     } else {
-      constexpr int tcw = EPI == kEpiSwiGLU ? kMxBN / 2 : kMxBN;
+      constexpr int tcw = EPI == kEpiSwiGLU ? BN / 2 : BN;
       tc.bm = kMxBM;
       tc.per_row_tile = (args.out_cols + tcw - 1) / tcw;
     }
@@ -231,7 +239,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
             if (EPI == kEpiSwiGLU) {
               tma_load_3d(sb, &tmB, fb, kbyte, T.col0, T.g);
-              tma_load_3d(sb + 64 * C::kRowBytes, &tmB, fb, kbyte, args.I + T.col0, T.g);
+              tma_load_3d(sb + (BN / 2) * C::kRowBytes, &tmB, fb, kbyte, args.I + T.col0, T.g);
             } else {
               tma_load_3d(sb, &tmB, fb, kbyte, T.col0, T.g);
             }
@@ -281,10 +289,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           int br;
           bool bok;
           if (MODE == kFwd) {
-            const int n = (EPI == kEpiSwiGLU) ? (m < 64 ? T.col0 + m : args.I + T.col0 + (m - 64))
+            constexpr int kHalf = BN / 2;  // SwiGLU: gate rows, then the matching up rows
+            const int n = (EPI == kEpiSwiGLU) ? (m < kHalf ? T.col0 + m : args.I + T.col0 + (m - kHalf))
                                               : T.col0 + m;
-            const int lim = (EPI == kEpiSwiGLU) ? (m < 64 ? args.I : 2 * args.I) : args.nw;
-            bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m & 63) < args.I);
+            const int lim = (EPI == kEpiSwiGLU) ? (m < kHalf ? args.I : 2 * args.I) : args.nw;
+            bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m % kHalf) < args.I);
             br = T.g * args.nw + n;
           } else {
             br = T.col0 + m;
@@ -452,12 +461,14 @@ int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, 
 template <int FMT>
 int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
-  constexpr int kS = FMT == kE4M3 ? 6 : 8;       // stages for fwd / dgrad (128 x 128 tiles)
+  constexpr int kBN = FMT == kE4M3 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;
+  // stages for fwd / dgrad: as many as fit next to the group tables (e4m3 128-wide: 6, e2m1 256-wide: 8)
+  constexpr int kS = FMT == kE4M3 ? (kBN == 128 ? 6 : 4) : (kBN == 128 ? 8 : 8);
   constexpr int kSw = FMT == kE4M3 ? 5 : 8;      // wgrad keeps 32 KB for its TMA-store staging
-  if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS>(ta, tb, tc, a, grid, s);
-  if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kMxWgradBN>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
@@ -489,13 +500,14 @@ int launch_mx_gemm(const MxCall& c) {
   a.M_pad = c.M_pad;
   a.q_codes = c.q_codes;
   a.q_scales = c.q_scales;
+  const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {
     const int64_t N = c.N, K = c.K;
     uint64_t da[2] = {bytes(K), (uint64_t)c.M}, sa[1] = {bytes(K)};
     uint32_t ba[2] = {rb, 128};
     uint64_t db[3] = {bytes(K), (uint64_t)N, (uint64_t)c.G}, sb[2] = {bytes(K), bytes(K) * (uint64_t)N};
-    uint32_t bb[3] = {rb, c.epi ? 64u : 128u, 1};
+    uint32_t bb[3] = {rb, (uint32_t)(c.epi ? fbn / 2 : fbn), 1};
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, ba, sw))) return st;
     if ((st = encode_tmap(&tb, u8, 3, c.B, db, sb, bb, sw))) return st;
     a.sa_ld = a.sb_ld = K / 32;
@@ -504,14 +516,14 @@ int launch_mx_gemm(const MxCall& c) {
     a.I = (int)(N / 2);
     a.out_cols = (int)(c.epi ? N / 2 : N);
     a.red = (int)K;
-    tiles_ub = (cdiv(c.M, kMxBM) + c.G) * cdiv(a.out_cols, c.epi ? kMxBN / 2 : kMxBN);
+    tiles_ub = (cdiv(c.M, kMxBM) + c.G) * cdiv(a.out_cols, c.epi ? fbn / 2 : fbn);
   } else if (c.mode == 1) {
     const int64_t N = c.N, K = c.K;
     uint64_t da[2] = {bytes(N), (uint64_t)c.M}, sa[1] = {bytes(N)};
     uint64_t db[2] = {bytes(N) * (uint64_t)c.G, (uint64_t)K}, sb[1] = {bytes(N) * (uint64_t)c.G};
-    uint32_t bx[2] = {rb, 128};
+    uint32_t bx[2] = {rb, 128}, bwide[2] = {rb, (uint32_t)fbn};
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
-    if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bx, sw))) return st;
+    if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bwide, sw))) return st;
     a.sa_ld = N / 32;
     a.sb_ld = c.G * N / 32;
     a.a_rows = (int)c.M;
@@ -519,7 +531,7 @@ int launch_mx_gemm(const MxCall& c) {
     a.I = (int)K;
     a.out_cols = (int)K;
     a.red = (int)N;
-    tiles_ub = (cdiv(c.M, kMxBM) + c.G) * cdiv(K, kMxBN);
+    tiles_ub = (cdiv(c.M, kMxBM) + c.G) * cdiv(K, fbn);
   } else {
     const int64_t N = c.N, K = c.K, Mp = c.M_pad;
     uint64_t da[2] = {bytes(Mp), (uint64_t)N}, sa[1] = {bytes(Mp)};

@@ -154,6 +154,17 @@ int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void*
 int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
                             uint8_t* scales, void* stream);
 
+/* Row-wise MX quantization with the scales in the blocked atom layout of the
+ * block-scaled MMA -- the weight operand of the forward GEMM, quantized once
+ * into the caller's weight cache.  Codes and the quantization rule are those of
+ * pgg_mx_quantize_rowwise.
+ *   in [R, C] bf16; C % 128 == 0.  codes as pgg_mx_quantize_rowwise.
+ *   scales: round_up(R, 128) * C / 32 bytes; block j of row r sits at byte
+ *   ((r / 128) * (C / 128) + j / 4) * 512 + 16 (r % 32) + 4 ((r % 128) / 32) + j % 4;
+ *   rows past R hold scale 0. */
+int pgg_mx_quantize_rowwise_blocked(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                                    uint8_t* scales, void* stream);
+
 /* Group-aware column-wise MX quantization (the wgrad operands, quantized
  * along the token axis).  Blocks of 32 rows run inside one group, starting at
  * the group's first row; group g is stored transposed in columns
@@ -179,7 +190,8 @@ int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t*
  * bf16 output):
  *   PGG_MODE_FWD:   out[M, N] = deq(A)_g . deq(B)_g^T
  *                   A [M, K] row-wise codes, SA [M, K/32];
- *                   B [G*N, K] row-wise codes (W), SB [G*N, K/32].
+ *                   B [G*N, K] row-wise codes (W) with SB in the blocked layout
+ *                   of pgg_mx_quantize_rowwise_blocked.
  *                   epilogue PGG_EPI_SWIGLU: N = 2I, out = A_act [M, I],
  *                   out2 = H [M, 2I] or NULL (as pgg_grouped_fc1_swiglu).
  *   PGG_MODE_DGRAD: out[M, K] = deq(A)_g . W_g with A = dY [M, N] row-wise
@@ -201,8 +213,8 @@ int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t*
  * pgg_mx_quantize_rowwise(out) -- so the next GEMM's operand needs no separate
  * quantize pass ("Primus-Turbo" README, "What's New": fused GroupedMLP in
  * FP8 / MXFP8).  The width of `out` (I) must be a multiple of 32.
- * Row-major scales (fwd SA / SB, dgrad SA) need 4-byte alignment, blocked ones
- * (dgrad SB, wgrad SA / SB) 16-byte alignment.
+ * Row-major scales (fwd SA, dgrad SA) need 4-byte alignment, blocked ones
+ * (fwd SB, dgrad SB, wgrad SA / SB) 16-byte alignment.
  * Sizes: the reduction axis is a multiple of 128 (fwd K, dgrad N); the other
  * dimensions are multiples of 8 (N of a SwiGLU forward a multiple of 16); e2m1
  * codes are packed two per byte.  fp32 accumulation, bf16 output. */

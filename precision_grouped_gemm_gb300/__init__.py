@@ -11,7 +11,8 @@ from ._binding import (PggError, PAD, FMT_E4M3, FMT_E2M1, MODE_FWD, MODE_DGRAD, 
                        grouped_gemm_fwd, grouped_gemm_dgrad, grouped_gemm_wgrad,
                        grouped_gemm_wgrad_accumulate,
                        grouped_fc1_swiglu, grouped_fc2_dgrad_swiglu_bwd,
-                       mx_quantize_rowwise, mx_quantize_colwise, mx_grouped_gemm, mx_pad_rows,
+                       mx_quantize_rowwise, mx_quantize_rowwise_blocked, mx_quantize_colwise, mx_grouped_gemm,
+                       mx_pad_rows,
                        moe_permute_workspace_size, moe_permute, moe_combine, moe_combine_bwd)
 
 __all__ = [
@@ -19,7 +20,7 @@ __all__ = [
     "EPI_NONE", "EPI_SWIGLU", "lib", "library_path", "init", "version", "read_error",
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "grouped_gemm_wgrad_accumulate",
     "grouped_fc1_swiglu",
-    "grouped_fc2_dgrad_swiglu_bwd", "mx_quantize_rowwise", "mx_quantize_colwise",
+    "grouped_fc2_dgrad_swiglu_bwd", "mx_quantize_rowwise", "mx_quantize_rowwise_blocked", "mx_quantize_colwise",
     "mx_grouped_gemm", "mx_pad_rows", "moe_permute_workspace_size", "moe_permute", "moe_combine",
     "moe_combine_bwd",
 ]

@@ -29,6 +29,7 @@ SIGNATURES = {
     "pgg_grouped_fc1_swiglu": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_fc2_dgrad_swiglu_bwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_mx_quantize_rowwise": [_P, _I64, _I64, _I32, _P, _P, _P],
+    "pgg_mx_quantize_rowwise_blocked": [_P, _I64, _I64, _I32, _P, _P, _P],
     "pgg_mx_quantize_colwise": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P],
     "pgg_mx_grouped_gemm": [_I32, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64,
                             _I64, _I32, _I64, _P, _P],
@@ -204,6 +205,21 @@ def mx_quantize_rowwise(x, fmt, codes=None, scales=None, stream=None):
     _dev(x, codes, scales)
     _check(lib().pgg_mx_quantize_rowwise(_ptr(x), R, C, f, _ptr(codes), _ptr(scales), _stream(stream)),
            "pgg_mx_quantize_rowwise")
+    return codes, scales
+
+
+def mx_quantize_rowwise_blocked(x, fmt, codes=None, scales=None, stream=None):
+    """bf16 [R,C] (C % 128 == 0) -> (codes as mx_quantize_rowwise, scales [round_up(R,128), C/32]
+    bytes in the blocked atom layout): the forward GEMM's weight operand."""
+    R, C = x.shape
+    f = _FMT[fmt]
+    if codes is None:
+        codes = torch.empty((R, C if f == FMT_E4M3 else C // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((-(-R // 128) * 128, C // 32), dtype=torch.uint8, device=x.device)
+    _dev(x, codes, scales)
+    _check(lib().pgg_mx_quantize_rowwise_blocked(_ptr(x), R, C, f, _ptr(codes), _ptr(scales), _stream(stream)),
+           "pgg_mx_quantize_rowwise_blocked")
     return codes, scales
 
 

@@ -52,9 +52,10 @@ struct MxArgs {
   const int32_t* group_lens;
   int G;
   int64_t M;
-  const uint8_t* SA;      // scale tensors, row-major [rows, red/32]
+  const uint8_t* SA;      // scale tensors: row-major [rows, red/32], or blocked atoms (see kGatherA/B)
   const uint8_t* SB;
-  int64_t sa_ld, sb_ld;   // scale row strides (bytes)
+  int64_t sa_ld, sb_ld;   // scale bytes per row (red/32); blocked: 4 x atoms per 128-row block
+  int b_bulk;             // fwd: the tile's B rows start on 128-row atoms (whole-atom copies)
   int a_rows, b_rows;     // rows of the A / B scale tensors that exist (zero-filled beyond)
   int out_cols;           // fwd N (or I with SwiGLU), dgrad K, wgrad K
   int red;                // fwd K / dgrad N (elements)
@@ -145,13 +146,15 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kSfPer = 4 + 4 * (BN / 128);         // per stage: SFA 4 + SFB 4 per 128 rows
   static_assert(kSfCol0 + STAGES * kSfPer <= kTmemCols, "TMEM columns");
   static_assert((2 * STAGES + 2 * NACC + 1) * 8 + 12 <= L::kGroupOff - L::kBarOff, "barrier area");
-  // Scale factors of an operand either sit in the blocked layout of the column-wise
-  // quantizer (wgrad A and B, dgrad B: 128-row aligned tiles), fetched as whole
-  // 512-byte atoms by bulk copy, or are row-major [rows, K/32] (ragged token rows),
-  // gathered 4 bytes per row by cp.async into the atom.
+  // Scale factors of an operand are either row-major [rows, K/32] (activations, whose
+  // tiles start at ragged group offsets), gathered 4 bytes per row by cp.async into
+  // the atom, or in the blocked atom layout (column-wise operands: wgrad A and B,
+  // dgrad B; forward weights B), fetched as whole 512-byte atoms by bulk copy.  A
+  // forward weight tile whose rows do not start on an atom (N, or I for SwiGLU, not
+  // a multiple of 128) is gathered row by row from the blocked layout instead.
   constexpr bool kGatherA = MODE != kWgrad;
-  constexpr bool kGatherB = MODE == kFwd;
-  constexpr uint32_t kSfBulk = (kGatherA ? 0u : 512u) + (kGatherB ? 0u : 512u * (BN / 128));
+  const bool gather_b = MODE == kFwd && (!args.b_bulk || (EPI == kEpiSwiGLU && BN < 256));
+  const uint32_t sf_bulk = (kGatherA ? 0u : 512u) + (gather_b ? 0u : 512u * (BN / 128));
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&full[s]), (kGatherA || kGatherB) ? 1 + 32 : 1);  // expect_tx arrive (+ 32 cp.async arrives)
+      mbar_init(smem_u32(&full[s]), kGatherA ? 1 + 32 : 1);  // expect_tx arrive (+ 32 cp.async arrives)
       mbar_init(smem_u32(&empty[s]), 1);
     }
     for (int a = 0; a < NACC; ++a) {
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const uint32_t fb = smem_u32(&full[stage]);
         const int kbyte = kb * C::kRowBytes;  // byte offset of this k-block along a row
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, L::kA + L::kB + kSfBulk);
+          mbar_arrive_expect_tx(fb, L::kA + L::kB + sf_bulk);
           if (MODE == kFwd) {
             tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
             if (EPI == kEpiSwiGLU) {
@@ -255,26 +258,26 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (!kGatherA)
             bulk_load(ssf, args.SA + ((int64_t)(T.row0 >> 7) * (args.sa_ld >> 2) + (T.poff >> 7) + kb) * 512, 512,
                       fb);
-          if (!kGatherB) {
-            const int p = MODE == kWgrad ? (T.poff >> 7) + kb : T.g * (args.red >> 7) + kb;
+          if (!gather_b) {
+            const int p = MODE == kWgrad ? (T.poff >> 7) + kb : MODE == kDgrad ? T.g * (args.red >> 7) + kb : kb;
 #pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              bulk_load(ssf + 512 + 512 * h,
-                        args.SB + ((int64_t)((T.col0 >> 7) + h) * (args.sb_ld >> 2) + p) * 512, 512, fb);
+            for (int h = 0; h < BN / 128; ++h) {
+              // first B row of this 128-row group: wgrad / dgrad col0 + 128 h; fwd the weight
+              // row g * nw + col0 + 128 h, or with SwiGLU the gate (h = 0) / up (h = 1) half
+              int64_t r0;
+              if (MODE == kFwd)
+                r0 = (int64_t)T.g * args.nw + T.col0 +
+                     (EPI == kEpiSwiGLU ? (h < BN / 256 ? 128 * h : args.I + 128 * (h - BN / 256)) : 128 * h);
+              else
+                r0 = T.col0 + 128 * h;
+              bulk_load(ssf + 512 + 512 * h, args.SB + ((r0 >> 7) * (args.sb_ld >> 2) + p) * 512, 512, fb);
+            }
           }
         }
         // gathered scale factors (row-major operands): lane l fetches rows l, l+32, l+64,
         // l+96 of the operand tile (4 bytes = the k-block's 4 block scales) into word
         // 4 l + i of the atom
-        int sfa_col, sfb_col;  // byte column of this k-block in the scale tensors
-        if (MODE == kWgrad) {
-          sfa_col = sfb_col = T.poff / 32 + kb * 4;
-        } else if (MODE == kDgrad) {
-          sfa_col = kb * 4;
-          sfb_col = T.g * (args.red / 32) + kb * 4;
-        } else {
-          sfa_col = sfb_col = kb * 4;
-        }
+        const int sfa_col = kb * 4;  // byte column of this k-block in the row-major A scales
 #pragma unroll
         for (int i = 0; i < BN / 32; ++i) {
           const int m = lane + 32 * i;
@@ -299,12 +302,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             br = T.col0 + m;
             bok = br < args.b_rows;
           }
-          // B row m goes to atom m / 128, word 4 (m % 32) + (m % 128) / 32
-          if (kGatherB)
+          // B row m goes to atom m / 128, word 4 (m % 32) + (m % 128) / 32; the source is
+          // row br's 4 bytes of k-block kb in the blocked layout
+          if (gather_b)
             cp_async_4(ssf + 512 + (i / 4) * 512 + (lane * 4 + (i % 4)) * 4,
-                       args.SB + (bok ? (int64_t)br * args.sb_ld + sfb_col : 0), bok ? 4u : 0u);
+                       args.SB + (bok ? ((((int64_t)br >> 7) * (args.sb_ld >> 2) + kb) << 9) + 16 * (br & 31) +
+                                            4 * ((br >> 5) & 3)
+                                      : 0),
+                       bok ? 4u : 0u);
         }
-        if (kGatherA || kGatherB) cp_async_arrive_noinc(fb);
+        if (kGatherA || gather_b) cp_async_arrive_noinc(fb);
         __syncwarp();
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -341,7 +348,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t ssf = sb + L::kB;
           const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;
           const uint32_t sfb_t = sfa_t + 4;
-          if (kGatherA || kGatherB) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
+          if (kGatherA) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
           tmem_cp_32x128b_x4(sfa_t, smem_desc(ssf, 0, 128, kSwizzleNone));
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32: 4 columns per 128 rows
@@ -468,7 +475,10 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS, kBN>(ta, tb, tc, a, grid, s);
+  // the SwiGLU-backward epilogue (read H, write dH and its MX codes) is long enough that
+  // overlapping it with the next tile through buffered accumulators matters more than
+  // wide MMAs (MXFP8 fc2 dgrad: 0.50 ms at 128 wide, 0.73 ms at 256)
+  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, FMT == kE4M3 ? 6 : 8, 128>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kMxWgradBN>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
@@ -500,7 +510,7 @@ int launch_mx_gemm(const MxCall& c) {
   a.M_pad = c.M_pad;
   a.q_codes = c.q_codes;
   a.q_scales = c.q_scales;
-  const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
+  const int fbn = (c.mode == 1 && c.epi) ? 128 : (e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1);  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {
     const int64_t N = c.N, K = c.K;
@@ -511,6 +521,9 @@ int launch_mx_gemm(const MxCall& c) {
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, ba, sw))) return st;
     if ((st = encode_tmap(&tb, u8, 3, c.B, db, sb, bb, sw))) return st;
     a.sa_ld = a.sb_ld = K / 32;
+    // weight scales are blocked: whole-atom copies when every B tile (or SwiGLU half)
+    // starts on a 128-row atom
+    a.b_bulk = c.epi ? ((fbn / 2) % 128 == 0 && (N / 2) % 128 == 0) : (N % 128 == 0 && fbn % 128 == 0);
     a.a_rows = (int)c.M;
     a.nw = (int)N;
     a.I = (int)(N / 2);

@@ -57,6 +57,8 @@ int launch_bf16(const Bf16Call& c);
 // MX quantize (mx_quant.cu)
 int launch_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
                                uint8_t* scales, cudaStream_t s);
+int launch_mx_quantize_rowwise_blocked(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                                       uint8_t* scales, cudaStream_t s);
 int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens,
                                int G, int fmt, uint8_t* codes_t, uint8_t* scales_t,
                                int64_t M_pad, int32_t* err, cudaStream_t s);

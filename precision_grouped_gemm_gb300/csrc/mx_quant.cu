@@ -27,11 +27,14 @@ namespace {
 // Four lanes own one block: each loads 8 bf16 (16 B, fully coalesced across the
 // warp), the block amax is a 2-step xor shuffle, each lane writes 8 (e4m3) or
 // 4 (e2m1) bytes and lane%4 == 0 writes the scale byte.
-template <int FMT>
+// BLOCKED: scales go to the atom layout of the block-scaled MMA instead of row-major
+// [R, C/32] (the weight operand of the forward GEMM; C % 128 == 0): block j of row r
+// at ((r / 128) * C / 128 + j / 4) * 512 + 16 (r % 32) + 4 ((r % 128) / 32) + j % 4.
+template <int FMT, bool BLOCKED = false>
 __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __restrict__ in,
                                                                uint8_t* __restrict__ codes,
                                                                uint8_t* __restrict__ scales,
-                                                               int64_t n_chunks) {
+                                                               int64_t n_chunks, uint32_t row_blocks) {
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i - (threadIdx.x & 31) < n_chunks;
        i += stride) {
@@ -65,7 +68,17 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
       if (!fin) o = 0;
       reinterpret_cast<uint32_t*>(codes)[i] = o;
     }
-    if ((threadIdx.x & 3) == 0) scales[i >> 2] = (uint8_t)sc;
+    if ((threadIdx.x & 3) == 0) {
+      const int64_t b = i >> 2;  // block index = r * row_blocks + j
+      if (BLOCKED) {
+        const int64_t r = b / row_blocks;
+        const uint32_t j = (uint32_t)(b - r * row_blocks), m = (uint32_t)(r & 127);
+        scales[(((r >> 7) * (row_blocks >> 2) + (j >> 2)) << 9) + 16 * (m & 31) + 4 * (m >> 5) + (j & 3)] =
+            (uint8_t)sc;
+      } else {
+        scales[b] = (uint8_t)sc;
+      }
+    }
   }
 }
 
@@ -205,12 +218,37 @@ int launch_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, ui
   const int threads = 256;
   const int64_t want = (n_chunks + threads - 1) / threads;
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
+  const uint32_t rb = (uint32_t)(C / 32);
   if (fmt == PGG_FMT_E4M3)
     mx_quant_rowwise_kernel<kE4M3><<<grid, threads, 0, s>>>(static_cast<const uint4*>(in), codes,
-                                                             scales, n_chunks);
+                                                             scales, n_chunks, rb);
   else
     mx_quant_rowwise_kernel<kE2M1><<<grid, threads, 0, s>>>(static_cast<const uint4*>(in), codes,
-                                                             scales, n_chunks);
+                                                             scales, n_chunks, rb);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_mx_quantize_rowwise_blocked(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                                       uint8_t* scales, cudaStream_t s) {
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  if (R % 128) {  // rows past R in the last 128-row block hold scale 0
+    const size_t atoms = (size_t)(C / 128);
+    cudaError_t e = cudaMemsetAsync(scales + (size_t)(R / 128) * atoms * 512, 0, atoms * 512, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  const int64_t n_chunks = R * C / 8;
+  const int threads = 256;
+  const int64_t want = (n_chunks + threads - 1) / threads;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
+  const uint32_t rb = (uint32_t)(C / 32);
+  if (fmt == PGG_FMT_E4M3)
+    mx_quant_rowwise_kernel<kE4M3, true><<<grid, threads, 0, s>>>(static_cast<const uint4*>(in), codes,
+                                                                   scales, n_chunks, rb);
+  else
+    mx_quant_rowwise_kernel<kE2M1, true><<<grid, threads, 0, s>>>(static_cast<const uint4*>(in), codes,
+                                                                   scales, n_chunks, rb);
   return cuda_status(cudaGetLastError());
 }
 

@@ -265,6 +265,17 @@ int pgg_mx_quantize_rowwise(const void* in, int64_t R, int64_t C, int fmt, uint8
   return launch_mx_quantize_rowwise(in, R, C, fmt, codes, scales, as_stream(stream));
 }
 
+int pgg_mx_quantize_rowwise_blocked(const void* in, int64_t R, int64_t C, int fmt, uint8_t* codes,
+                                    uint8_t* scales, void* stream) {
+  if (!in || !codes || !scales) return PGG_ERR_INVALID_ARG;
+  if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
+  if (R < 0 || R >= kMaxRows || C <= 0 || C >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+  if (C % 128) return PGG_ERR_ALIGNMENT;
+  if (!aligned16(in) || !aligned16(codes) || !aligned16(scales)) return PGG_ERR_ALIGNMENT;
+  if (R == 0) return PGG_OK;
+  return launch_mx_quantize_rowwise_blocked(in, R, C, fmt, codes, scales, as_stream(stream));
+}
+
 int pgg_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens,
                             int G, int fmt, uint8_t* codes_t, uint8_t* scales_t, int64_t M_pad,
                             int32_t* err, void* stream) {
@@ -295,9 +306,8 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
   if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
       (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
-  // blocked scale atoms (wgrad SA and SB, dgrad SB) are fetched by 16-byte-aligned bulk copies
-  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || (mode != PGG_MODE_FWD && !aligned16(SB)))
-    return PGG_ERR_ALIGNMENT;
+  // blocked scale atoms (SB always, wgrad SA) are fetched by 16-byte-aligned bulk copies
+  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned16(SB)) return PGG_ERR_ALIGNMENT;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
   if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
     return PGG_ERR_ALIGNMENT;

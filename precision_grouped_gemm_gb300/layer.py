@@ -151,9 +151,9 @@ class MxLayerBuffers:
     X: torch.Tensor
     dY: torch.Tensor
     group_lens: torch.Tensor
-    W1q: tuple = None      # row-wise  [G*2I, H]   (fc1 fwd, blocks along H)
+    W1q: tuple = None      # row-wise  [G*2I, H], blocked scales (fc1 fwd, blocks along H)
     W1t: tuple = None      # column-wise [H, G*2I] (fc1 dgrad, blocks along 2I)
-    W2q: tuple = None      # row-wise  [G*H, I]    (fc2 fwd, blocks along I)
+    W2q: tuple = None      # row-wise  [G*H, I], blocked scales (fc2 fwd, blocks along I)
     W2t: tuple = None      # column-wise [I, G*H]  (fc2 dgrad, blocks along H)
     M_pad: int = 0
     bufs: dict = None
@@ -182,9 +182,9 @@ class MxLayerBuffers:
         dev = X.device
         b = MxLayerBuffers(fmt, X, dY, group_lens)
         W1f, W2f = W1.reshape(G * I2, Hd), W2.reshape(G * Hd, I)
-        b.W1q = B.mx_quantize_rowwise(W1f, fmt)
+        b.W1q = B.mx_quantize_rowwise_blocked(W1f, fmt)
         b.W1t = B.mx_quantize_colwise(W1f, torch.full((G,), I2, dtype=torch.int32, device=dev), fmt, G * I2)
-        b.W2q = B.mx_quantize_rowwise(W2f, fmt)
+        b.W2q = B.mx_quantize_rowwise_blocked(W2f, fmt)
         b.W2t = B.mx_quantize_colwise(W2f, torch.full((G,), Hd, dtype=torch.int32, device=dev), fmt, G * Hd)
         if host_lens is not None:
             b.M_pad = max(B.PAD, int(sum(-(-int(n) // B.PAD) * B.PAD for n in host_lens)))

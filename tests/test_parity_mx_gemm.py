@@ -36,7 +36,7 @@ def test_mx_fwd(fmt, lens, N, K):
     G, M = len(lens), int(lens.sum())
     X, W = _bf16(wl.KEY_X, M, K, 1.0, 31), _bf16(wl.KEY_W1, G * N, K, 0.5, 31)
     A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
-    B, SB = pgg.mx_quantize_rowwise(W.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise_blocked(W.to(DEV), fmt)
     err = _err()
     Y = pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, torch.from_numpy(lens).to(DEV), M, N, K, err=err)
     assert pgg.read_error(err) == 0
@@ -90,7 +90,7 @@ def test_mx_swiglu_fwd_bwd(fmt):
     X, W1 = _bf16(wl.KEY_X, M, K, 1.0, 34), _bf16(wl.KEY_W1, G * 2 * I, K, 0.1, 34)
     gl = torch.from_numpy(lens).to(DEV)
     A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
-    B, SB = pgg.mx_quantize_rowwise(W1.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise_blocked(W1.to(DEV), fmt)
     H = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=DEV)
     err = _err()
     Aout = pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, gl, M, 2 * I, K, out2=H,
@@ -136,7 +136,7 @@ def test_mx_lossless_operands_exact(fmt):
     X, x = grid_tensor(M, K)
     W, w = grid_tensor(G * N, K)
     A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
-    B, SB = pgg.mx_quantize_rowwise(W.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise_blocked(W.to(DEV), fmt)
     Y = pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, torch.from_numpy(lens).to(DEV), M, N, K)
     ref = og.grouped_gemm_fwd(x, w.reshape(G, N, K), lens)
     util.assert_close(Y, ref, f"mx lossless {fmt}")
@@ -172,7 +172,7 @@ def test_mx_fused_quantized_outputs(fmt):
     X, W1 = _bf16(wl.KEY_X, M, K, 1.0, 37), _bf16(wl.KEY_W1, G * 2 * I, K, 0.1, 37)
     gl = torch.from_numpy(lens).to(DEV)
     A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
-    B, SB = pgg.mx_quantize_rowwise(W1.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise_blocked(W1.to(DEV), fmt)
     cb = I if fmt == "e4m3" else I // 2
     qc = torch.empty((M, cb), dtype=torch.uint8, device=DEV)
     qs = torch.empty((M, I // 32), dtype=torch.uint8, device=DEV)

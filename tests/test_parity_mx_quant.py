@@ -71,6 +71,18 @@ def test_rowwise_non_finite_block(fmt):
 
 
 @pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+@pytest.mark.parametrize("R,C", [(200, 256), (128, 128), (1, 384)])
+def test_rowwise_blocked_bit_exact(fmt, R, C):
+    # the weight layout: same codes as the row-wise quantizer, scales in 512-byte atoms
+    x = _mixed(R, C, R + C)
+    codes, scales = pgg.mx_quantize_rowwise_blocked(x.to(DEV), fmt)
+    rc, rs = omx.mx_quantize_rowwise(util.bits(x), fmt)
+    assert tuple(scales.shape) == (-(-R // 128) * 128, C // 32)
+    np.testing.assert_array_equal(codes.cpu().numpy(), rc)
+    np.testing.assert_array_equal(util.unblock_scales(scales, R, C), rs)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
 @pytest.mark.parametrize("lens", [[33, 0, 5, 64, 1, 200], [128, 256], [0, 0, 7]])
 def test_colwise_bit_exact(fmt, lens):
     lens = np.asarray(lens, dtype=np.int32)

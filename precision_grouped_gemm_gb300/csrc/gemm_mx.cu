@@ -32,7 +32,9 @@ constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
 // wgrad tiles: 128 x 128 with a double-buffered accumulator.  (128 x 256 with one
 // accumulator -- TMEM cannot hold two next to the scale factors -- measured 12%
 // slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
-constexpr int kMxWgradBN = 128;
+// wgrad tile width per format (e2m1 reduces long group k-loops with little work per MMA)
+constexpr int kMxWgradBNE4M3 = 128;
+constexpr int kMxWgradBNE2M1 = 256;
 // Forward / dgrad tile width per format.  A block-scaled MMA carries little work
 // per instruction (128 x 128 x 64 e2m1 is ~24 ns of tensor time) and the MMA warp
 // pays ~45 ns per MMA and ~36 ns per scale copy, so a 128-wide tile is issue-bound;
@@ -471,7 +473,9 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   constexpr int kBN = FMT == kE4M3 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;
   // stages for fwd / dgrad: as many as fit next to the group tables (e4m3 128-wide: 6, e2m1 256-wide: 8)
   constexpr int kS = FMT == kE4M3 ? (kBN == 128 ? 6 : 4) : (kBN == 128 ? 8 : 8);
-  constexpr int kSw = FMT == kE4M3 ? 5 : 8;      // wgrad keeps 32 KB for its TMA-store staging
+  constexpr int kWBN = FMT == kE4M3 ? kMxWgradBNE4M3 : kMxWgradBNE2M1;
+  // wgrad keeps 4 x 32 rows x kWBN bf16 of TMA-store staging next to the stages
+  constexpr int kSw = FMT == kE4M3 ? (kWBN == 128 ? 5 : 2) : (kWBN == 128 ? 8 : 5);
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
@@ -479,7 +483,7 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   // overlapping it with the next tile through buffered accumulators matters more than
   // wide MMAs (MXFP8 fc2 dgrad: 0.50 ms at 128 wide, 0.73 ms at 256)
   if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, FMT == kE4M3 ? 6 : 8, 128>(ta, tb, tc, a, grid, s);
-  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kMxWgradBN>(ta, tb, tc, a, grid, s);
+  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kWBN>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
 
@@ -549,17 +553,18 @@ int launch_mx_gemm(const MxCall& c) {
     const int64_t N = c.N, K = c.K, Mp = c.M_pad;
     uint64_t da[2] = {bytes(Mp), (uint64_t)N}, sa[1] = {bytes(Mp)};
     uint64_t db[2] = {bytes(Mp), (uint64_t)K}, sb[1] = {bytes(Mp)};
-    uint32_t bx[2] = {rb, 128}, bw[2] = {rb, (uint32_t)kMxWgradBN};
+    const int wbn = e4 ? kMxWgradBNE4M3 : kMxWgradBNE2M1;
+    uint32_t bx[2] = {rb, 128}, bw[2] = {rb, (uint32_t)wbn};
     if ((st = encode_tmap(&ta, u8, 2, c.A, da, sa, bx, sw))) return st;
     if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bw, sw))) return st;
     if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxWgradStoreAtoms, &a.c4d))) return st;
-    a.nct = FastDiv((uint32_t)cdiv(K, kMxWgradBN));
+    a.nct = FastDiv((uint32_t)cdiv(K, wbn));
     a.sa_ld = a.sb_ld = Mp / 32;
     a.a_rows = (int)N;
     a.b_rows = (int)K;
     a.out_cols = (int)K;
     a.wg_rows = (int)N;
-    tiles_ub = c.G * cdiv(N, kMxBM) * cdiv(K, kMxWgradBN);
+    tiles_ub = c.G * cdiv(N, kMxBM) * cdiv(K, wbn);
   }
   if (c.mode != 2) tc = ta;  // unused outside wgrad
   const int grid = std::max(1, std::min(dev.sms, tiles_ub));

@@ -86,12 +86,14 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
 // Output column space [0, M_pad) is cut into 32-wide blocks; block j holds
 // rows off_g + 32 b .. of group g for j = pb_g + b with pb_g the prefix of
 // round_up(len_g, 128) / 32, or nothing (pad) -- every output byte is written
-// once.  One warp handles one block j x 64 input columns: lane l reads columns
-// c0 + 2l, c0 + 2l + 1 of the block's rows (32 coalesced 128-byte row loads in
-// flight, no shared memory, no block barrier), takes each column's amax and
-// writes the column's 32 codes (32 bytes e4m3 / 16 bytes e2m1) and its scale.
-// Work items run with j fastest, so the warps writing the 32-byte pieces of one
-// 128-byte line of codes_t run at the same time.
+// once.  One warp handles one 128-wide k-block p (blocks j = 4 p .. 4 p + 3, one
+// scale atom; it never straddles groups, whose spans are padded to 128) x 64 input
+// columns: for each block, lane l reads columns c0 + 2l, c0 + 2l + 1 of the
+// block's rows (32 coalesced 128-byte row loads in flight, no shared memory, no
+// block barrier), takes each column's amax and writes the column's 32 codes
+// (32 bytes e4m3 / 16 bytes e2m1).  The column's four scales of the k-block leave
+// together as one 32-bit store: one-byte scale stores were two thirds of the
+// kernel's store sectors.  Work items run with p fastest.
 //
 // Scales go to the blocked layout the block-scaled MMA reads: for every 128-row
 // block rb of the C rows and every 128-column k-block p of [0, M_pad), one 512-byte
@@ -99,17 +101,19 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
 // j = 4 p + q sits at byte 16 (m % 32) + 4 (m / 32) + q.  Rows past C up to the
 // next multiple of 128 get scale 0.
 constexpr int kColSlab = 64;
-
-__device__ __forceinline__ int64_t blocked_scale_index(int r, int j, int64_t M_pad) {
-  const int m = r & 127;
-  return (((int64_t)(r >> 7) * (M_pad >> 7) + (j >> 2)) << 9) + 16 * (m & 31) + 4 * (m >> 5) + (j & 3);
-}
 constexpr int kColThreads = 256;
 
+// Byte offset of row r's four scales of k-block p in the blocked layout.
+__device__ __forceinline__ int64_t blocked_atom_word(int r, int p, int64_t M_pad) {
+  const int m = r & 127;
+  return (((int64_t)(r >> 7) * (M_pad >> 7) + p) << 9) + 16 * (m & 31) + 4 * (m >> 5);
+}
+
+// Quantize column `half` of the packed bf16 pairs v (zero past `valid`) and store its
+// 32 codes at position j; returns the scale byte (0 when the block holds no rows).
 template <int FMT>
-__device__ __forceinline__ void colwise_store(const uint32_t (&v)[32], int half, int valid, int c,
-                                              int64_t M_pad, int j, uint8_t* __restrict__ codes_t,
-                                              uint8_t* __restrict__ scales_t) {
+__device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int half, int valid, int c,
+                                                  int64_t M_pad, int j, uint8_t* __restrict__ codes_t) {
   uint32_t am = 0;
 #pragma unroll
   for (int r = 0; r < 32; ++r) am = max(am, ((v[r] >> (16 * half)) & 0x7FFFu));
@@ -117,15 +121,16 @@ __device__ __forceinline__ void colwise_store(const uint32_t (&v)[32], int half,
   float mult = 0.0f;
   const bool fin = valid > 0 ? block_scale<FMT>(am, sc, mult) : true;
   const bool keep = valid > 0 && fin;
-  float f[32];
-#pragma unroll
-  for (int r = 0; r < 32; ++r) f[r] = keep ? __uint_as_float((v[r] >> (16 * half)) << 16) * mult : 0.0f;
   if (FMT == kE4M3) {
     uint4 o[2];
     uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-      ow[k] = cvt_e4m3x2(f[4 * k], f[4 * k + 1]) | (cvt_e4m3x2(f[4 * k + 2], f[4 * k + 3]) << 16);
+    for (int k = 0; k < 8; ++k) {
+      float f[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f[e] = keep ? __uint_as_float((v[4 * k + e] >> (16 * half)) << 16) * mult : 0.0f;
+      ow[k] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
+    }
     uint4* dst = reinterpret_cast<uint4*>(codes_t + (int64_t)c * M_pad + (int64_t)j * 32);
     dst[0] = o[0];
     dst[1] = o[1];
@@ -133,12 +138,16 @@ __device__ __forceinline__ void colwise_store(const uint32_t (&v)[32], int half,
     uint4 o;
     uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      ow[k] = cvt_e2m1x2(f[8 * k], f[8 * k + 1]) | (cvt_e2m1x2(f[8 * k + 2], f[8 * k + 3]) << 8) |
-              (cvt_e2m1x2(f[8 * k + 4], f[8 * k + 5]) << 16) | (cvt_e2m1x2(f[8 * k + 6], f[8 * k + 7]) << 24);
+    for (int k = 0; k < 4; ++k) {
+      float f[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = keep ? __uint_as_float((v[8 * k + e] >> (16 * half)) << 16) * mult : 0.0f;
+      ow[k] = cvt_e2m1x2(f[0], f[1]) | (cvt_e2m1x2(f[2], f[3]) << 8) | (cvt_e2m1x2(f[4], f[5]) << 16) |
+              (cvt_e2m1x2(f[6], f[7]) << 24);
+    }
     *reinterpret_cast<uint4*>(codes_t + (int64_t)c * (M_pad / 2) + (int64_t)j * 16) = o;
   }
-  scales_t[blocked_scale_index(c, j, M_pad)] = (uint8_t)(valid > 0 ? sc : 0u);
+  return valid > 0 ? sc : 0u;
 }
 
 template <int FMT>
@@ -174,36 +183,43 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
   }
   __syncthreads();
   if (s_bad) return;
-  const int nblk = (int)(M_pad / 32);
-  const int C128 = (C + 127) & ~127;  // scale rows, padded to whole atoms
+  const int nkb = (int)(M_pad / 128);  // k-blocks (scale atoms) along the padded axis
+  const int C128 = (C + 127) & ~127;   // scale rows, padded to whole atoms
   const int nslab = C128 / kColSlab;
-  const int64_t total = (int64_t)nblk * nslab;
+  const int64_t total = (int64_t)nkb * nslab;
   const int used = s_blk[G];
   const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
   for (int64_t t = (int64_t)blockIdx.x * (kColThreads / 32) + warp; t < total; t += nwarps) {
-    const int j = (int)(t % nblk);
-    const int c = (int)(t / nblk) * kColSlab + 2 * lane;
-    int valid = 0;
-    int64_t row0 = 0;
-    if (j < used) {
-      const int g = find_group(s_blk, G, j);
-      const int b = j - s_blk[g];
-      valid = min(32, max(0, s_off[g + 1] - s_off[g] - 32 * b));
-      row0 = (int64_t)s_off[g] + 32 * b;
-    }
+    const int p = (int)(t % nkb);
+    const int c = (int)(t / nkb) * kColSlab + 2 * lane;
     if (c >= C) {  // pad rows of the last atom: scale 0, no codes
       if (c < C128) {
-        scales_t[blocked_scale_index(c, j, M_pad)] = 0;
-        scales_t[blocked_scale_index(c + 1, j, M_pad)] = 0;
+        *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = 0u;
+        *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = 0u;
       }
       continue;
     }
-    uint32_t v[32];
-    const uint32_t* src = reinterpret_cast<const uint32_t*>(in + row0 * C + c);
+    int len = 0, b0 = 0;
+    int64_t grow0 = 0;
+    if (4 * p < used) {
+      const int g = find_group(s_blk, G, 4 * p);
+      b0 = 4 * p - s_blk[g];
+      len = s_off[g + 1] - s_off[g];
+      grow0 = s_off[g];
+    }
+    uint32_t sc0 = 0, sc1 = 0;
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {
+      const int valid = min(32, max(0, len - 32 * (b0 + q)));
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(in + (grow0 + 32 * (b0 + q)) * C + c);
+      uint32_t v[32];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) v[r] = r < valid ? __ldg(src + (int64_t)r * (C / 2)) : 0u;
-    colwise_store<FMT>(v, 0, valid, c, M_pad, j, codes_t, scales_t);
-    colwise_store<FMT>(v, 1, valid, c + 1, M_pad, j, codes_t, scales_t);
+      for (int r = 0; r < 32; ++r) v[r] = r < valid ? __ldg(src + (int64_t)r * (C / 2)) : 0u;
+      sc0 |= colwise_codes<FMT>(v, 0, valid, c, M_pad, 4 * p + q, codes_t) << (8 * q);
+      sc1 |= colwise_codes<FMT>(v, 1, valid, c + 1, M_pad, 4 * p + q, codes_t) << (8 * q);
+    }
+    *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = sc0;
+    *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = sc1;
   }
 }
 
@@ -258,10 +274,15 @@ int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32
   DeviceInfo dev;
   int st = current_device(&dev);
   if (st != PGG_OK) return st;
-  const int64_t total = (M_pad / 32) * (((C + 127) / 128 * 128) / kColSlab);  // warp work items
-  const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
+  const int64_t total = (M_pad / 128) * (((C + 127) / 128 * 128) / kColSlab);  // warp work items
   const size_t smem = 8 * (size_t)(G + 1);
+  int per_sm = 0;  // resident CTAs per SM: the grid-stride loop runs one wave of them
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &per_sm, fmt == PGG_FMT_E4M3 ? mx_quant_colwise_kernel<kE4M3> : mx_quant_colwise_kernel<kE2M1>, kColThreads,
+      smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * std::max(per_sm, 1)));
   auto* x = static_cast<const __nv_bfloat16*>(in);
   if (fmt == PGG_FMT_E4M3)
     mx_quant_colwise_kernel<kE4M3><<<grid, kColThreads, smem, s>>>(x, M, (int)C, group_lens, G,

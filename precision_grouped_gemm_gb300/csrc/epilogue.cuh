@@ -264,17 +264,19 @@ __device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8
 // multiple of 64): this warp's 32 rows x BN columns are staged as BN/64 atoms of
 // 32 x 64 bf16 (4 KB each, 128B-swizzled) in its `stg` buffer and leave in
 // BN/64/SA bulk tensor stores of SA atoms each, at (0, row0, col0 / 64 + s SA, g),
-// clipped at the bounds, one bulk group per store.  Before a store's atoms are
-// rewritten only the store that last read them -- BN/64/SA groups back -- has to
-// be done reading, so with SA < BN/64 one tile's stores drain while the next
-// tile's atoms are filled.  Stores that start past `cols_total` are skipped but
-// still commit an (empty) group, which keeps that count exact.
-template <int BN, int SA>
+// clipped at the bounds, one bulk group per store.  The atoms cycle through RING
+// slots of `stg` (RING a multiple of SA): before a slot is rewritten only the
+// store that last read it -- RING/SA groups back -- has to be done reading, so
+// with RING/SA > 1 stores drain while the next atoms are filled.  Stores that
+// start past `cols_total` are skipped but still commit an (empty) group, which
+// keeps that count exact.
+template <int BN, int SA, int RING = BN / 64>
 __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8_t* stg,
                                                    const CUtensorMap* tmC4, int row0, int col0, int g,
                                                    int rows_total, int cols_total, int lane) {
-  static_assert(SA >= 1 && (BN / 64) % SA == 0, "atoms per store");
+  static_assert(SA >= 1 && (BN / 64) % SA == 0 && RING % SA == 0, "atoms per store");
   constexpr int NS = BN / 64 / SA;
+  constexpr int NW = RING / SA;  // stores sharing the ring
   if (row0 >= rows_total) return;  // nothing of this warp's rows exists (warp-uniform)
 #pragma unroll 1
   for (int st = 0; st < NS; ++st) {
@@ -290,10 +292,10 @@ __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8
         for (int j = 0; j < 64; ++j) v[j] = 0u;
       }
       if (i == 0) {
-        if (lane == 0) bulk_wait_read<NS - 1>();  // the store that last read these atoms
+        if (lane == 0) bulk_wait_read<NW - 1>();  // the store that last read these slots
         __syncwarp();
       }
-      uint8_t* sb = stg + a * 4096;
+      uint8_t* sb = stg + (a % RING) * 4096;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         uint4 w;
@@ -308,7 +310,7 @@ __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8
     __syncwarp();
     if (lane == 0) {
       if (col0 + st * SA * 64 < cols_total)
-        tma_store_4d(tmC4, smem_u32(stg + st * SA * 4096), 0, row0, col0 / 64 + st * SA, g);
+        tma_store_4d(tmC4, smem_u32(stg + ((st * SA) % RING) * 4096), 0, row0, col0 / 64 + st * SA, g);
       bulk_commit();
     }
   }

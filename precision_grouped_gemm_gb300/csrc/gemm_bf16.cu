@@ -9,27 +9,43 @@ namespace {
 
 constexpr int kBN = 256;
 
-// stages: fwd/dgrad stream W through 4 x 48 KB (BK 64); wgrad keeps 64 KB for the
-// TMA-store staging and runs 6 x 24 KB (BK 32) or 3 x 48 KB (BK 64)
-template <int MODE, int BK>
-constexpr int stages() { return MODE == kWgrad ? (BK == 32 ? 6 : 3) : 4; }
+// stages: fwd/dgrad stream W through 4 x 48 KB (BK 64).  The wgrad store keeps a
+// 32 KB staging ring and runs 7 x 24 KB (BK 32) or 4 x 48 KB (BK 64; 3 when the group
+// tables of a large G leave no room); the fp32 accumulate keeps 64 KB and runs 6 x 24 KB
+// or 3 x 48 KB.
+template <int MODE, int EPI, int BK>
+constexpr int stages() {
+  return MODE != kWgrad ? 4 : (EPI == kEpiAccumF32 ? (BK == 32 ? 6 : 3) : (BK == 32 ? 7 : 4));
+}
+
+template <int MODE, int EPI, int BK, int S>
+int run_s(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
+          int grid, cudaStream_t s) {
+  using L = GemmSmem<kBN, BK, S, epi_bytes<MODE, EPI>()>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, S, BK>;
+  const size_t smem = L::bytes(args.G);
+  static size_t attr_bytes = 0;  // per instantiation: raised to the largest G seen
+  if (smem > attr_bytes) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e == cudaErrorInvalidValue ? PGG_ERR_UNSUPPORTED : cuda_status(e);
+    attr_bytes = smem;
+  }
+  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, tc, args);
+  return cuda_status(cudaGetLastError());
+}
 
 template <int MODE, int EPI, int BK = 64>
 int run(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmArgs& args,
         int grid, cudaStream_t s) {
-  constexpr int S = stages<MODE, BK>();
-  using L = GemmSmem<kBN, BK, S, epi_bytes<MODE>()>;
-  auto kern = grouped_gemm_bf16_kernel<MODE, EPI, kBN, S, BK>;
-  const size_t smem = L::bytes(args.G);
-  static bool attr_done = false;  // per instantiation; the attribute is per device function
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)L::bytes(kMaxGroups));
-    if (e != cudaSuccess) return cuda_status(e);
-    attr_done = true;
+  constexpr int S = stages<MODE, EPI, BK>();
+  if constexpr (MODE == kWgrad && EPI != kEpiAccumF32 && BK == 64) {
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != PGG_OK) return st;
+    using L = GemmSmem<kBN, BK, S, epi_bytes<MODE, EPI>()>;
+    if (L::bytes(args.G) > dev.smem_optin) return run_s<MODE, EPI, BK, S - 1>(ta, tb, tc, args, grid, s);
   }
-  kern<<<grid, kGemmThreads, smem, s>>>(ta, tb, tc, args);
-  return cuda_status(cudaGetLastError());
+  return run_s<MODE, EPI, BK, S>(ta, tb, tc, args, grid, s);
 }
 
 int ceil_div(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }

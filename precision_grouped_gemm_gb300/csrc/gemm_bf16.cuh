@@ -72,9 +72,13 @@ struct GemmSmem {
   }
 };
 
-// Epilogue staging bytes per mode: wgrad stores its full tiles with TMA.
-template <int MODE>
-__host__ __device__ constexpr int epi_bytes() { return MODE == kWgrad ? 4 * 16384 : 0; }
+// Epilogue staging bytes: the wgrad store keeps a ring of kWgradRing 4 KB atoms per
+// epilogue warp; the fp32 accumulate two 8 KB halves per warp.
+constexpr int kWgradRing = 2;
+template <int MODE, int EPI>
+__host__ __device__ constexpr int epi_bytes() {
+  return MODE != kWgrad ? 0 : (EPI == kEpiAccumF32 ? 4 * 16384 : 4 * kWgradRing * 4096);
+}
 
 struct Tile {
   int g, row0, rows, col0, nkb, red0, red_valid;
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                              const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
   static_assert(BK == 64 || (MODE == kWgrad && BK == 32), "k-block");
-  using L = GemmSmem<BN, BK, STAGES, epi_bytes<MODE>()>;
+  using L = GemmSmem<BN, BK, STAGES, epi_bytes<MODE, EPI>()>;
   static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(EPI != kEpiSwiGLU || (MODE == kFwd && BN == 256), "SwiGLU fwd tile");
   static_assert(EPI != kEpiSwiGLUBwd || MODE == kDgrad, "SwiGLU bwd tile");
@@ -335,7 +339,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
     GroupCursor cur;
-    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * 16384;  // wgrad: this warp's staging buffer
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (epi_bytes<MODE, EPI>() / 4);  // wgrad: this warp's staging
     int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
@@ -353,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             epi_tma_reduce_f32<BN>(tb, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
                                    args.out_cols, args.c4d != 0, lane);
         } else if (args.c4d) {
-          epi_tma_store_tile<BN, kWgradStoreAtoms>(tb, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+          epi_tma_store_tile<BN, kWgradStoreAtoms, kWgradRing>(tb, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
                                  args.out_cols, lane);
         } else {
           epi_tma_store_rows<BN>(tb, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,

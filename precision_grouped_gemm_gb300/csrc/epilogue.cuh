@@ -14,7 +14,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+// silu(x) = x sigmoid(x) with the fast exponential and division intrinsics: a few
+// ulp of fp32, far inside the bf16 output's rounding, and short enough not to hold
+// up the producer and MMA warps that share issue slots with the epilogue warps.
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // Store 32 consecutive fp32 values of one row as bf16 at dst[0..31], columns
 // limited to ncols (<= 32).  16-byte vector stores when the chunk is whole.
@@ -201,7 +204,7 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
         const float hg = (j & 1) ? bf16_hi(pg[j >> 1]) : bf16_lo(pg[j >> 1]);
         const float hu = (j & 1) ? bf16_hi(pu[j >> 1]) : bf16_lo(pu[j >> 1]);
         const float da = __uint_as_float(rd[j]);
-        const float s = 1.0f / (1.0f + __expf(-hg));
+        const float s = __fdividef(1.0f, 1.0f + __expf(-hg));
         dg[j] = da * hu * s * (1.0f + hg * (1.0f - s));
         du[j] = da * hg * s;
       }

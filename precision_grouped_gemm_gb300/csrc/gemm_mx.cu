@@ -479,10 +479,7 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
-  // the SwiGLU-backward epilogue (read H, write dH and its MX codes) is long enough that
-  // overlapping it with the next tile through buffered accumulators matters more than
-  // wide MMAs (MXFP8 fc2 dgrad: 0.50 ms at 128 wide, 0.73 ms at 256)
-  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, FMT == kE4M3 ? 6 : 8, 128>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kWBN>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
@@ -514,7 +511,7 @@ int launch_mx_gemm(const MxCall& c) {
   a.M_pad = c.M_pad;
   a.q_codes = c.q_codes;
   a.q_scales = c.q_scales;
-  const int fbn = (c.mode == 1 && c.epi) ? 128 : (e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1);  // fwd / dgrad tile width
+  const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {
     const int64_t N = c.N, K = c.K;

@@ -107,33 +107,45 @@ def sigmoid(x: np.ndarray) -> np.ndarray:
     return 1.0 / (1.0 + np.exp(-x))
 
 
-def swiglu_fwd(H: np.ndarray) -> np.ndarray:
-    """A = silu(gate) * up with gate = H[:, :I], up = H[:, I:] (H [M, 2I])."""
+def _clamp_gate_up(g: np.ndarray, u: np.ndarray, limit):
+    """The swiglu_limit clamp ("Enabling DeepSeek-V4-Flash ...", model-config table names the
+    knob without a formula; read here as gate <- min(gate, L), up <- clip(up, -L, L)).
+    Returns the clamped values and the masks where each clamp is inactive (boundaries
+    included), which is where the gradient passes."""
+    if limit is None or limit <= 0:
+        return g, u, np.ones_like(g, dtype=bool), np.ones_like(u, dtype=bool)
+    return np.minimum(g, limit), np.clip(u, -limit, limit), g <= limit, np.abs(u) <= limit
+
+
+def swiglu_fwd(H: np.ndarray, limit=None) -> np.ndarray:
+    """A = silu(gate) * up with gate = H[:, :I], up = H[:, I:] (H [M, 2I]); with a limit L > 0
+    the gate and up are clamped first (see _clamp_gate_up)."""
     I = H.shape[1] // 2
-    g, u = H[:, :I], H[:, I:]
+    g, u, _, _ = _clamp_gate_up(H[:, :I], H[:, I:], limit)
     return g * sigmoid(g) * u
 
 
-def swiglu_bwd(dA: np.ndarray, H: np.ndarray) -> np.ndarray:
-    """dH = [dA*u*sigma(g)*(1 + g*(1-sigma(g))) | dA*g*sigma(g)] (derivative of swiglu_fwd)."""
+def swiglu_bwd(dA: np.ndarray, H: np.ndarray, limit=None) -> np.ndarray:
+    """dH = [dA*u*sigma(g)*(1 + g*(1-sigma(g))) | dA*g*sigma(g)] (derivative of swiglu_fwd),
+    on the clamped g, u and zero where a clamp is active."""
     I = H.shape[1] // 2
-    g, u = H[:, :I], H[:, I:]
+    g, u, mg, mu = _clamp_gate_up(H[:, :I], H[:, I:], limit)
     s = sigmoid(g)
-    dgate = dA * u * s * (1.0 + g * (1.0 - s))
-    dup = dA * g * s
+    dgate = np.where(mg, dA * u * s * (1.0 + g * (1.0 - s)), 0.0)
+    dup = np.where(mu, dA * g * s, 0.0)
     return np.concatenate([dgate, dup], axis=1)
 
 
-def grouped_fc1_swiglu(X: np.ndarray, W1: np.ndarray, group_lens):
+def grouped_fc1_swiglu(X: np.ndarray, W1: np.ndarray, group_lens, limit=None):
     """FC1 with SwiGLU folded in: H = grouped fwd(X, W1) [M, 2I]; A = swiglu(H) [M, I]."""
     H = grouped_gemm_fwd(X, W1, group_lens)
-    return swiglu_fwd(H), H
+    return swiglu_fwd(H, limit), H
 
 
-def grouped_fc2_dgrad_swiglu_bwd(dY: np.ndarray, W2: np.ndarray, H: np.ndarray, group_lens):
+def grouped_fc2_dgrad_swiglu_bwd(dY: np.ndarray, W2: np.ndarray, H: np.ndarray, group_lens, limit=None):
     """FC2 dgrad followed by the SwiGLU backward: dA = dgrad(dY, W2); dH = swiglu_bwd(dA, H)."""
     dA = grouped_gemm_dgrad(dY, W2, group_lens)
-    return swiglu_bwd(dA, H)
+    return swiglu_bwd(dA, H, limit)
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:

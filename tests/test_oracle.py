@@ -171,6 +171,51 @@ def test_swiglu_bwd_finite_difference():
     np.testing.assert_allclose(dH, num, rtol=1e-7, atol=1e-8)
 
 
+def test_clamped_swiglu_closed_forms_and_special_cases():
+    # limit L: gate -> min(gate, L), up -> clip(up, -L, L) before silu(gate) * up
+    L = 2.0
+    H = np.array([[5.0, -1.0, 7.0, 0.5],      # gate 5 -> 2; up 7 -> 2 | gate -1, up 0.5 untouched
+                  [1.0, -30.0, -9.0, 3.0]])   # up -9 -> -2 | gate -30 (below: no clamp), up 3 -> 2
+    A = og.swiglu_fwd(H, L)
+    silu = lambda x: x / (1.0 + math.exp(-x))
+    assert A[0, 0] == pytest.approx(silu(2.0) * 2.0, rel=1e-15)
+    assert A[0, 1] == pytest.approx(silu(-1.0) * 0.5, rel=1e-15)
+    assert A[1, 0] == pytest.approx(silu(1.0) * -2.0, rel=1e-15)
+    assert A[1, 1] == pytest.approx(silu(-30.0) * 2.0, rel=1e-15)
+    # no limit (None or 0) and a limit above every value both reduce to the plain SwiGLU
+    rng = np.random.default_rng(21)
+    Hr = rng.standard_normal((5, 8))
+    for lim in (None, 0.0, 1e9):
+        np.testing.assert_array_equal(og.swiglu_fwd(Hr, lim), og.swiglu_fwd(Hr))
+        np.testing.assert_array_equal(og.swiglu_bwd(Hr[:, :4], Hr, lim), og.swiglu_bwd(Hr[:, :4], Hr))
+    # clamped entries get no gradient; unclamped ones match the plain derivative at the clamped values
+    dA = np.ones((2, 2))
+    dH = og.swiglu_bwd(dA, H, L)
+    assert dH[0, 0] == 0.0 and dH[0, 2] == 0.0      # gate 5 > L, up 7 > L
+    assert dH[1, 2] == 0.0 and dH[1, 3] == 0.0      # up -9 < -L, up 3 > L
+    s1 = 1.0 / (1.0 + math.exp(1.0))                # sigma(-1)
+    assert dH[0, 1] == pytest.approx(0.5 * s1 * (1.0 - 1.0 * (1.0 - s1)), rel=1e-14)
+
+
+def test_clamped_swiglu_bwd_finite_difference():
+    # away from the clamp boundaries the clamped backward is the derivative of the clamped forward
+    rng = np.random.default_rng(22)
+    L = 1.5
+    H = rng.standard_normal((6, 8)) * 2
+    H[np.abs(np.abs(H) - L) < 0.05] += 0.2   # keep every entry clear of a kink
+    dA = rng.standard_normal((6, 4))
+    dH = og.swiglu_bwd(dA, H, L)
+    eps = 1e-6
+    num = np.zeros_like(H)
+    for i in range(H.shape[0]):
+        for j in range(H.shape[1]):
+            Hp, Hm = H.copy(), H.copy()
+            Hp[i, j] += eps; Hm[i, j] -= eps
+            num[i, j] = np.sum(dA * (og.swiglu_fwd(Hp, L) - og.swiglu_fwd(Hm, L))) / (2 * eps)
+    np.testing.assert_allclose(dH, num, rtol=1e-7, atol=1e-8)
+    assert (dH == 0).any() and (dH != 0).any()
+
+
 def test_fc1_fc2_compositions():
     rng = np.random.default_rng(12)
     G, M, I, K = 3, 20, 4, 6

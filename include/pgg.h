@@ -139,6 +139,22 @@ int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void*
                                      const int32_t* group_lens, void* dH, int64_t M, int64_t Hd,
                                      int64_t I, int G, int32_t* err, void* stream);
 
+/* Clamped SwiGLU (the `swiglu_limit` knob of "Enabling DeepSeek-V4-Flash ...",
+ * model-config table; the pages give no formula -- read here as): with L =
+ * swiglu_limit > 0, gate <- min(gate, L) and up <- clamp(up, -L, L) before
+ * A = silu(gate) * up.  H keeps the values before the clamp; the backward
+ * applies the clamp to them again and passes no gradient where a clamp is
+ * active (gate > L, |up| > L).  swiglu_limit == 0 is the plain SwiGLU (the two
+ * calls above); a negative or non-finite limit returns PGG_ERR_INVALID_ARG.
+ * Arguments otherwise as pgg_grouped_fc1_swiglu / pgg_grouped_fc2_dgrad_swiglu_bwd. */
+int pgg_grouped_fc1_swiglu_clamped(const void* X, const void* W1, const int32_t* group_lens, void* A,
+                                   void* H, int64_t M, int64_t I, int64_t K, int G, float swiglu_limit,
+                                   int32_t* err, void* stream);
+int pgg_grouped_fc2_dgrad_swiglu_bwd_clamped(const void* dY, const void* W2, const void* H,
+                                             const int32_t* group_lens, void* dH, int64_t M, int64_t Hd,
+                                             int64_t I, int G, float swiglu_limit, int32_t* err,
+                                             void* stream);
+
 /* ---------------------------------------------------------------- MX (microscaling) */
 
 /* Row-wise MX quantization: one E8M0 scale per block of 32 consecutive
@@ -291,6 +307,15 @@ int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, co
 int pgg_moe_permute_noalloc(const int32_t* topk_ids, const void* X, int64_t T, int k, int64_t H,
                             int E, void* Xs, int32_t* group_lens, int32_t* pos, int32_t* err,
                             void* stream);
+
+/* The block-scaled grouped GEMM with the clamped SwiGLU epilogue (see
+ * pgg_grouped_fc1_swiglu_clamped): mode PGG_MODE_FWD (FC1) or PGG_MODE_DGRAD
+ * (FC2 dgrad + SwiGLU backward); the other arguments as pgg_mx_grouped_gemm
+ * with epilogue PGG_EPI_SWIGLU. */
+int pgg_mx_grouped_gemm_clamped(int mode, int fmt, const uint8_t* A, const uint8_t* SA, const uint8_t* B,
+                                const uint8_t* SB, const void* H, const int32_t* group_lens, void* out,
+                                void* out2, uint8_t* out_codes, uint8_t* out_scales, int64_t M, int64_t N,
+                                int64_t K, int G, float swiglu_limit, int32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -243,11 +243,11 @@ def mx_grouped_gemm_wgrad(fmt, At, SAt, Bt, SBt, group_lens, P: int = 128):
     return dW
 
 
-def mx_grouped_fc1_swiglu(fmt, A, SA, B, SB, group_lens, G: int):
+def mx_grouped_fc1_swiglu(fmt, A, SA, B, SB, group_lens, G: int, limit=None):
     H = mx_grouped_gemm_fwd(fmt, A, SA, B, SB, group_lens, G)
-    return swiglu_fwd(H), H
+    return swiglu_fwd(H, limit), H
 
 
-def mx_grouped_fc2_dgrad_swiglu_bwd(fmt, A, SA, Bt, SBt, H, group_lens, G: int):
+def mx_grouped_fc2_dgrad_swiglu_bwd(fmt, A, SA, Bt, SBt, H, group_lens, G: int, limit=None):
     dA = mx_grouped_gemm_dgrad(fmt, A, SA, Bt, SBt, group_lens, G)
-    return swiglu_bwd(dA, H)
+    return swiglu_bwd(dA, H, limit)

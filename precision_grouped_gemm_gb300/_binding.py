@@ -15,7 +15,7 @@ MODE_FWD, MODE_DGRAD, MODE_WGRAD = 0, 1, 2
 EPI_NONE, EPI_SWIGLU = 0, 1
 _FMT = {"e4m3": FMT_E4M3, "e2m1": FMT_E2M1, FMT_E4M3: FMT_E4M3, FMT_E2M1: FMT_E2M1}
 
-_P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+_P, _I64, _I32, _F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
 
 # name -> argument types (all return int status)
 SIGNATURES = {
@@ -28,6 +28,10 @@ SIGNATURES = {
     "pgg_grouped_gemm_wgrad_accumulate": [_P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_fc1_swiglu": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
     "pgg_grouped_fc2_dgrad_swiglu_bwd": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _P, _P],
+    "pgg_grouped_fc1_swiglu_clamped": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _F32, _P, _P],
+    "pgg_grouped_fc2_dgrad_swiglu_bwd_clamped": [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _F32, _P, _P],
+    "pgg_mx_grouped_gemm_clamped": [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32,
+                                    _F32, _P, _P],
     "pgg_mx_quantize_rowwise": [_P, _I64, _I64, _I32, _P, _P, _P],
     "pgg_mx_quantize_rowwise_blocked": [_P, _I64, _I64, _I32, _P, _P, _P],
     "pgg_mx_quantize_colwise": [_P, _I64, _I64, _P, _I32, _I32, _P, _P, _I64, _P, _P],
@@ -166,8 +170,9 @@ def grouped_gemm_wgrad_accumulate(X, dY, group_lens, dW_f32, err=None, stream=No
     return dW_f32
 
 
-def grouped_fc1_swiglu(X, W1, group_lens, A=None, H=None, save_h=True, err=None, stream=None):
-    """FC1 + SwiGLU: W1 [G,2I,K] (gate | up) -> A [M,I] and (optionally) H [M,2I]."""
+def grouped_fc1_swiglu(X, W1, group_lens, A=None, H=None, save_h=True, err=None, stream=None, swiglu_limit=0.0):
+    """FC1 + SwiGLU: W1 [G,2I,K] (gate | up) -> A [M,I] and (optionally) H [M,2I];
+    swiglu_limit > 0 selects the clamped SwiGLU."""
     M, K = X.shape
     G, I2, _ = W1.shape
     I = I2 // 2
@@ -176,21 +181,33 @@ def grouped_fc1_swiglu(X, W1, group_lens, A=None, H=None, save_h=True, err=None,
     if H is None and save_h:
         H = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=X.device)
     _dev(X, W1, group_lens, A, H, err)
-    _check(lib().pgg_grouped_fc1_swiglu(_ptr(X), _ptr(W1), _ptr(_lens(group_lens)), _ptr(A), _ptr(H),
-                                        M, I, K, G, _ptr(err), _stream(stream)), "pgg_grouped_fc1_swiglu")
+    if swiglu_limit:
+        _check(lib().pgg_grouped_fc1_swiglu_clamped(_ptr(X), _ptr(W1), _ptr(_lens(group_lens)), _ptr(A), _ptr(H),
+                                                    M, I, K, G, swiglu_limit, _ptr(err), _stream(stream)),
+               "pgg_grouped_fc1_swiglu_clamped")
+    else:
+        _check(lib().pgg_grouped_fc1_swiglu(_ptr(X), _ptr(W1), _ptr(_lens(group_lens)), _ptr(A), _ptr(H),
+                                            M, I, K, G, _ptr(err), _stream(stream)), "pgg_grouped_fc1_swiglu")
     return A, H
 
 
-def grouped_fc2_dgrad_swiglu_bwd(dY, W2, H, group_lens, dH=None, err=None, stream=None):
-    """dA = dY . W2_g (W2 [G,Hd,I]); dH [M,2I] = SwiGLU backward of dA at the saved H."""
+def grouped_fc2_dgrad_swiglu_bwd(dY, W2, H, group_lens, dH=None, err=None, stream=None, swiglu_limit=0.0):
+    """dA = dY . W2_g (W2 [G,Hd,I]); dH [M,2I] = SwiGLU backward of dA at the saved H
+    (swiglu_limit > 0: of the clamped SwiGLU)."""
     M, Hd = dY.shape
     G, _, I = W2.shape
     if dH is None:
         dH = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=dY.device)
     _dev(dY, W2, H, group_lens, dH, err)
-    _check(lib().pgg_grouped_fc2_dgrad_swiglu_bwd(_ptr(dY), _ptr(W2), _ptr(H), _ptr(_lens(group_lens)),
-                                                  _ptr(dH), M, Hd, I, G, _ptr(err), _stream(stream)),
-           "pgg_grouped_fc2_dgrad_swiglu_bwd")
+    if swiglu_limit:
+        _check(lib().pgg_grouped_fc2_dgrad_swiglu_bwd_clamped(_ptr(dY), _ptr(W2), _ptr(H), _ptr(_lens(group_lens)),
+                                                              _ptr(dH), M, Hd, I, G, swiglu_limit, _ptr(err),
+                                                              _stream(stream)),
+               "pgg_grouped_fc2_dgrad_swiglu_bwd_clamped")
+    else:
+        _check(lib().pgg_grouped_fc2_dgrad_swiglu_bwd(_ptr(dY), _ptr(W2), _ptr(H), _ptr(_lens(group_lens)),
+                                                      _ptr(dH), M, Hd, I, G, _ptr(err), _stream(stream)),
+               "pgg_grouped_fc2_dgrad_swiglu_bwd")
     return dH
 
 
@@ -249,11 +266,11 @@ def mx_quantize_colwise(x, group_lens, fmt, M_pad=None, codes_t=None, scales_t=N
 
 
 def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2=None, H=None,
-                    epilogue=EPI_NONE, M_pad=0, err=None, stream=None, out_q=None):
+                    epilogue=EPI_NONE, M_pad=0, err=None, stream=None, out_q=None, swiglu_limit=0.0):
     """Block-scaled grouped GEMM on MX operands (see pgg.h for the per-mode layouts).
 
     out_q: optional (codes, scales) receiving the row-wise MX quantization of `out`
-    (SwiGLU epilogues only)."""
+    (SwiGLU epilogues only); swiglu_limit > 0 (SwiGLU epilogues) clamps the SwiGLU."""
     f = _FMT[fmt]
     G = group_lens.numel()
     dev = A.device
@@ -267,9 +284,17 @@ def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2
         out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     qc, qs = out_q if out_q is not None else (None, None)
     _dev(A, SA, B, SB, group_lens, out, out2, H, err, qc, qs)
-    _check(lib().pgg_mx_grouped_gemm(mode, f, epilogue, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(H),
-                                     _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), _ptr(qc), _ptr(qs), M, N,
-                                     K, G, M_pad, _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
+    if swiglu_limit:
+        if epilogue != EPI_SWIGLU:
+            raise ValueError("swiglu_limit needs the SwiGLU epilogue")
+        _check(lib().pgg_mx_grouped_gemm_clamped(mode, f, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(H),
+                                                 _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), _ptr(qc), _ptr(qs),
+                                                 M, N, K, G, swiglu_limit, _ptr(err), _stream(stream)),
+               "pgg_mx_grouped_gemm_clamped")
+    else:
+        _check(lib().pgg_mx_grouped_gemm(mode, f, epilogue, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(H),
+                                         _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), _ptr(qc), _ptr(qs), M, N,
+                                         K, G, M_pad, _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
     return out
 
 

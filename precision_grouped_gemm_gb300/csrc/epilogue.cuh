@@ -101,10 +101,12 @@ __device__ __forceinline__ void mx_emit(const float* v, uint8_t* codes, uint8_t*
 // the matching up columns.  A[row, col0 + c] = silu(gate) * up (fp32), and the
 // pre-activation H[row, col0 + c] = gate, H[row, I + col0 + c] = up when H != null.
 // QF != 0 and qcodes != null: A is also emitted MX-quantized (row-wise, I % 32 == 0).
+// limit > 0 clamps first: gate <- min(gate, limit), up <- clamp(up, -limit, limit); H
+// keeps the values before the clamp.
 template <int BN, int QF = 0>
 __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t grow,
                                            bool row_ok, int col0, int I, uint8_t* qcodes = nullptr,
-                                           uint8_t* qscales = nullptr) {
+                                           uint8_t* qscales = nullptr, float limit = 0.0f) {
 #pragma unroll 1
   for (int c = 0; c < BN / 64; ++c) {
     uint32_t rg[32], ru[32];
@@ -118,7 +120,9 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
       for (int j = 0; j < 32; ++j) {
         g[j] = __uint_as_float(rg[j]);
         u[j] = __uint_as_float(ru[j]);
-        a[j] = silu_f(g[j]) * u[j];
+        const float gc = limit > 0.0f ? fminf(g[j], limit) : g[j];
+        const float uc = limit > 0.0f ? fminf(fmaxf(u[j], -limit), limit) : u[j];
+        a[j] = silu_f(gc) * uc;
       }
       const int nc = min(32, I - c0);
       store_row32(A + grow * I + c0, a, nc);
@@ -168,10 +172,13 @@ __device__ __forceinline__ void load_raw32(const __nv_bfloat16* src, uint4 (&w)[
   }
 }
 
+// limit > 0: the forward's clamp is applied to the saved g, u again, and the gradient
+// is zero where a clamp was active (g > limit, |u| > limit).
 template <int BN, int QF = 0>
 __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
                                                size_t grow, bool row_ok, int col0, int I,
-                                               uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr) {
+                                               uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr,
+                                               float limit = 0.0f) {
   const __nv_bfloat16* hrow = H + grow * (2 * (size_t)I);
   uint4 ng[4], nu[4];  // the next chunk's gate / up words
   if (row_ok && col0 < I) {
@@ -201,12 +208,19 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
       float dg[32], du[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float hg = (j & 1) ? bf16_hi(pg[j >> 1]) : bf16_lo(pg[j >> 1]);
-        const float hu = (j & 1) ? bf16_hi(pu[j >> 1]) : bf16_lo(pu[j >> 1]);
+        float hg = (j & 1) ? bf16_hi(pg[j >> 1]) : bf16_lo(pg[j >> 1]);
+        float hu = (j & 1) ? bf16_hi(pu[j >> 1]) : bf16_lo(pu[j >> 1]);
         const float da = __uint_as_float(rd[j]);
+        bool pass_g = true, pass_u = true;
+        if (limit > 0.0f) {
+          pass_g = hg <= limit;
+          pass_u = fabsf(hu) <= limit;
+          hg = fminf(hg, limit);
+          hu = fminf(fmaxf(hu, -limit), limit);
+        }
         const float s = __fdividef(1.0f, 1.0f + __expf(-hg));
-        dg[j] = da * hu * s * (1.0f + hg * (1.0f - s));
-        du[j] = da * hg * s;
+        dg[j] = pass_g ? da * hu * s * (1.0f + hg * (1.0f - s)) : 0.0f;
+        du[j] = pass_u ? da * hg * s : 0.0f;
       }
       store_row32(dH + grow * (2 * (size_t)I) + c0, dg, nc);
       store_row32(dH + grow * (2 * (size_t)I) + I + c0, du, nc);

@@ -68,6 +68,7 @@ int launch_bf16(const Bf16Call& c) {
   a.aux = c.aux;
   a.err = c.err;
   a.I = (int)c.I;
+  a.swiglu_limit = c.limit;
   int tiles_ub = 0;
   int wbk = 64;
 

@@ -44,6 +44,7 @@ struct GemmArgs {
   int out_cols;     // columns of the accumulator space: fwd N, dgrad K, wgrad K, swiglu I
   int red;          // reduction length for fwd / dgrad (K resp. N)
   int wg_rows;      // wgrad: N (rows of dW_g)
+  float swiglu_limit;  // SwiGLU epilogues: clamp limit (0: none)
   int I;            // SwiGLU width (gate/up halves)
   void* out;        // Y, dX, dW, A or dH (bf16)
   void* out2;       // SwiGLU forward: H (bf16 [M, 2I]) or nullptr
@@ -378,10 +379,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
-        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I);
+        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I, nullptr,
+                       nullptr, args.swiglu_limit);
       } else if (EPI == kEpiSwiGLUBwd) {
         epi_swiglu_bwd<BN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
-                           args.I);
+                           args.I, nullptr, nullptr, args.swiglu_limit);
       } else {
         epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
       }

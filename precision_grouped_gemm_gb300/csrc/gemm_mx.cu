@@ -58,6 +58,7 @@ struct MxArgs {
   const uint8_t* SB;
   int64_t sa_ld, sb_ld;   // scale bytes per row (red/32); blocked: 4 x atoms per 128-row block
   int b_bulk;             // fwd: the tile's B rows start on 128-row atoms (whole-atom copies)
+  float swiglu_limit;     // SwiGLU epilogues: clamp limit (0: none)
   int a_rows, b_rows;     // rows of the A / B scale tensors that exist (zero-filled beyond)
   int out_cols;           // fwd N (or I with SwiGLU), dgrad K, wgrad K
   int red;                // fwd K / dgrad N (elements)
@@ -428,10 +429,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
         epi_swiglu<BN, FMT>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I,
-                            args.q_codes, args.q_scales);
+                            args.q_codes, args.q_scales, args.swiglu_limit);
       } else if (EPI == kEpiSwiGLUBwd) {
         epi_swiglu_bwd<BN, FMT>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
-                                args.I, args.q_codes, args.q_scales);
+                                args.I, args.q_codes, args.q_scales, args.swiglu_limit);
       } else {
         epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
       }
@@ -511,6 +512,7 @@ int launch_mx_gemm(const MxCall& c) {
   a.M_pad = c.M_pad;
   a.q_codes = c.q_codes;
   a.q_scales = c.q_scales;
+  a.swiglu_limit = c.limit;
   const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {

@@ -51,6 +51,7 @@ struct Bf16Call {
   int G;
   int32_t* err;
   cudaStream_t stream;
+  float limit = 0.0f;  // SwiGLU clamp limit (0: none)
 };
 int launch_bf16(const Bf16Call& c);
 
@@ -77,6 +78,7 @@ struct MxCall {
   int G;
   int32_t* err;
   cudaStream_t stream;
+  float limit = 0.0f;  // SwiGLU clamp limit (0: none)
 };
 int launch_mx_gemm(const MxCall& c);
 

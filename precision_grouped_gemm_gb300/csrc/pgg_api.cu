@@ -137,6 +137,45 @@ int check_dim(int64_t x, int mult) {
 }
 }  // namespace
 
+static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const uint8_t* SA,
+                        const uint8_t* B, const uint8_t* SB, const void* H,
+                        const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
+                        uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G, int64_t M_pad,
+                        float limit, int32_t* err, void* stream) {
+  int st;
+  if (mode < 0 || mode > 2) return PGG_ERR_INVALID_ARG;
+  if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
+  if (epilogue != PGG_EPI_NONE && epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
+  if (epilogue == PGG_EPI_SWIGLU && mode == PGG_MODE_WGRAD) return PGG_ERR_INVALID_ARG;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if (!A || !SA || !B || !SB || !out) return PGG_ERR_INVALID_ARG;
+  if (mode == PGG_MODE_DGRAD && epilogue == PGG_EPI_SWIGLU && !H) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
+      (H && !aligned16(H)))
+    return PGG_ERR_ALIGNMENT;
+  // blocked scale atoms (SB always, wgrad SA) are fetched by 16-byte-aligned bulk copies
+  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned16(SB)) return PGG_ERR_ALIGNMENT;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
+    return PGG_ERR_ALIGNMENT;
+  if (mode == PGG_MODE_DGRAD && N % 128) return PGG_ERR_ALIGNMENT;
+  if (mode == PGG_MODE_WGRAD && (M_pad <= 0 || M_pad % PGG_MX_PAD || M_pad >= kMaxRows))
+    return PGG_ERR_ALIGNMENT;
+  if ((out_codes != nullptr) != (out_scales != nullptr)) return PGG_ERR_INVALID_ARG;
+  if (out_codes) {
+    // fused row-wise MX output of `out`: SwiGLU epilogues only, whole 32-column blocks
+    const int64_t w = mode == PGG_MODE_FWD ? N / 2 : K;
+    if (epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
+    if (w % 32) return PGG_ERR_ALIGNMENT;
+    if (!aligned16(out_codes)) return PGG_ERR_ALIGNMENT;
+  }
+  if (M == 0 && mode != PGG_MODE_WGRAD) return PGG_OK;
+  MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales,
+           M, N, K, M_pad, G, err, as_stream(stream)};
+  c.limit = limit;
+  return launch_mx_gemm(c);
+}
+
 extern "C" {
 
 int pgg_version(void) { return 100; }
@@ -229,7 +268,14 @@ int pgg_grouped_gemm_wgrad_accumulate(const void* X, const void* dY, const int32
 int pgg_grouped_fc1_swiglu(const void* X, const void* W1, const int32_t* group_lens, void* A,
                            void* H, int64_t M, int64_t I, int64_t K, int G, int32_t* err,
                            void* stream) {
+  return pgg_grouped_fc1_swiglu_clamped(X, W1, group_lens, A, H, M, I, K, G, 0.0f, err, stream);
+}
+
+int pgg_grouped_fc1_swiglu_clamped(const void* X, const void* W1, const int32_t* group_lens, void* A,
+                                   void* H, int64_t M, int64_t I, int64_t K, int G, float swiglu_limit,
+                                   int32_t* err, void* stream) {
   int st;
+  if (!(swiglu_limit >= 0.0f) || swiglu_limit > 3.0e38f) return PGG_ERR_INVALID_ARG;
   if ((st = check_common(M, G, group_lens))) return st;
   if ((st = check_dim(I, 8)) || (st = check_dim(K, 8))) return st;
   if (M == 0) return PGG_OK;
@@ -237,13 +283,22 @@ int pgg_grouped_fc1_swiglu(const void* X, const void* W1, const int32_t* group_l
   if (!aligned16(X) || !aligned16(W1) || !aligned16(A) || (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
   Bf16Call c{0, 1, X, W1, group_lens, A, H, nullptr, M, 2 * I, K, I, G, err, as_stream(stream)};
+  c.limit = swiglu_limit;
   return launch_bf16(c);
 }
 
 int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void* H,
                                      const int32_t* group_lens, void* dH, int64_t M, int64_t Hd,
                                      int64_t I, int G, int32_t* err, void* stream) {
+  return pgg_grouped_fc2_dgrad_swiglu_bwd_clamped(dY, W2, H, group_lens, dH, M, Hd, I, G, 0.0f, err, stream);
+}
+
+int pgg_grouped_fc2_dgrad_swiglu_bwd_clamped(const void* dY, const void* W2, const void* H,
+                                             const int32_t* group_lens, void* dH, int64_t M, int64_t Hd,
+                                             int64_t I, int G, float swiglu_limit, int32_t* err,
+                                             void* stream) {
   int st;
+  if (!(swiglu_limit >= 0.0f) || swiglu_limit > 3.0e38f) return PGG_ERR_INVALID_ARG;
   if ((st = check_common(M, G, group_lens))) return st;
   if ((st = check_dim(Hd, 8)) || (st = check_dim(I, 8))) return st;
   if (M == 0) return PGG_OK;
@@ -251,6 +306,7 @@ int pgg_grouped_fc2_dgrad_swiglu_bwd(const void* dY, const void* W2, const void*
   if (!aligned16(dY) || !aligned16(W2) || !aligned16(H) || !aligned16(dH))
     return PGG_ERR_ALIGNMENT;
   Bf16Call c{1, 2, dY, W2, group_lens, dH, nullptr, H, M, Hd, I, I, G, err, as_stream(stream)};
+  c.limit = swiglu_limit;
   return launch_bf16(c);
 }
 
@@ -295,37 +351,18 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
                         const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
                         uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G, int64_t M_pad,
                         int32_t* err, void* stream) {
-  int st;
-  if (mode < 0 || mode > 2) return PGG_ERR_INVALID_ARG;
-  if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
-  if (epilogue != PGG_EPI_NONE && epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
-  if (epilogue == PGG_EPI_SWIGLU && mode == PGG_MODE_WGRAD) return PGG_ERR_INVALID_ARG;
-  if ((st = check_common(M, G, group_lens))) return st;
-  if (!A || !SA || !B || !SB || !out) return PGG_ERR_INVALID_ARG;
-  if (mode == PGG_MODE_DGRAD && epilogue == PGG_EPI_SWIGLU && !H) return PGG_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
-      (H && !aligned16(H)))
-    return PGG_ERR_ALIGNMENT;
-  // blocked scale atoms (SB always, wgrad SA) are fetched by 16-byte-aligned bulk copies
-  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned16(SB)) return PGG_ERR_ALIGNMENT;
-  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
-  if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
-    return PGG_ERR_ALIGNMENT;
-  if (mode == PGG_MODE_DGRAD && N % 128) return PGG_ERR_ALIGNMENT;
-  if (mode == PGG_MODE_WGRAD && (M_pad <= 0 || M_pad % PGG_MX_PAD || M_pad >= kMaxRows))
-    return PGG_ERR_ALIGNMENT;
-  if ((out_codes != nullptr) != (out_scales != nullptr)) return PGG_ERR_INVALID_ARG;
-  if (out_codes) {
-    // fused row-wise MX output of `out`: SwiGLU epilogues only, whole 32-column blocks
-    const int64_t w = mode == PGG_MODE_FWD ? N / 2 : K;
-    if (epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
-    if (w % 32) return PGG_ERR_ALIGNMENT;
-    if (!aligned16(out_codes)) return PGG_ERR_ALIGNMENT;
-  }
-  if (M == 0 && mode != PGG_MODE_WGRAD) return PGG_OK;
-  MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales,
-           M, N, K, M_pad, G, err, as_stream(stream)};
-  return launch_mx_gemm(c);
+  return mx_gemm_impl(mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales, M, N,
+                      K, G, M_pad, 0.0f, err, stream);
+}
+
+int pgg_mx_grouped_gemm_clamped(int mode, int fmt, const uint8_t* A, const uint8_t* SA, const uint8_t* B,
+                                const uint8_t* SB, const void* H, const int32_t* group_lens, void* out,
+                                void* out2, uint8_t* out_codes, uint8_t* out_scales, int64_t M, int64_t N,
+                                int64_t K, int G, float swiglu_limit, int32_t* err, void* stream) {
+  if (mode != PGG_MODE_FWD && mode != PGG_MODE_DGRAD) return PGG_ERR_INVALID_ARG;
+  if (!(swiglu_limit >= 0.0f) || swiglu_limit > 3.0e38f) return PGG_ERR_INVALID_ARG;
+  return mx_gemm_impl(mode, fmt, PGG_EPI_SWIGLU, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales,
+                      M, N, K, G, 0, swiglu_limit, err, stream);
 }
 
 size_t pgg_moe_permute_workspace_size(int64_t T, int E) {

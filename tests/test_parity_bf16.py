@@ -85,6 +85,36 @@ def test_fc1_swiglu_and_fc2_bwd(lens, I, K):
     util.assert_close(dH, ref, "fc2 dgrad swiglu bwd")
 
 
+@pytest.mark.parametrize("limit", [1.0, 0.375])
+def test_fc1_fc2_swiglu_clamped(limit):
+    # the swiglu_limit variant: many gate / up values lie beyond the limit
+    lens = np.array([70, 0, 190, 33], dtype=np.int32)
+    M, G, I, K = int(lens.sum()), 4, 192, 256
+    X = util.gen(wl.KEY_X, M, K, 1.0, 15)
+    W1 = util.gen(wl.KEY_W1, G * 2 * I, K, 0.1, 15).view(G, 2 * I, K)
+    gl = torch.from_numpy(lens).to(DEV)
+    err = _err()
+    A, H = pgg.grouped_fc1_swiglu(X.to(DEV), W1.to(DEV), gl, err=err, swiglu_limit=limit)
+    refA, refH = og.grouped_fc1_swiglu(util.f64(X), util.f64(W1), lens, limit)
+    util.assert_close(H, refH, "clamped fc1 H (pre-clamp)")
+    util.assert_close(A, refA, "clamped fc1 A")
+    assert np.mean(np.abs(refH) > limit) > 0.2
+    Hd = K
+    Hs = util.gen(wl.KEY_H, M, 2 * I, 1.0, 16)
+    W2 = util.gen(wl.KEY_W2, G * Hd, I, 0.1, 16).view(G, Hd, I)
+    dY = util.gen(wl.KEY_DY, M, Hd, 1.0, 16)
+    dH = pgg.grouped_fc2_dgrad_swiglu_bwd(dY.to(DEV), W2.to(DEV), Hs.to(DEV), gl, err=err, swiglu_limit=limit)
+    assert pgg.read_error(err) == 0
+    ref = og.grouped_fc2_dgrad_swiglu_bwd(util.f64(dY), util.f64(W2), util.f64(Hs), lens, limit)
+    util.assert_close(dH, ref, "clamped fc2 dgrad swiglu bwd")
+    # the clamped entries' gradients are exactly zero
+    hs = util.f64(Hs)
+    dh = util.f64(dH)
+    assert np.all(dh[:, :I][hs[:, :I] > limit] == 0) and np.all(dh[:, I:][np.abs(hs[:, I:]) > limit] == 0)
+    with pytest.raises(pgg.PggError):
+        pgg.grouped_fc1_swiglu(X.to(DEV), W1.to(DEV), gl, swiglu_limit=-1.0)
+
+
 def test_bad_group_lens_sets_error_and_writes_nothing():
     lens = np.array([10, -2, 8], dtype=np.int32)
     M, N, K = 16, 64, 64

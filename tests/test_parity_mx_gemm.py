@@ -117,6 +117,37 @@ def test_mx_swiglu_fwd_bwd(fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+def test_mx_swiglu_clamped(fmt):
+    limit = 0.75
+    lens = np.array([70, 0, 190], dtype=np.int32)
+    G, M, I, K = 3, 260, 256, 256
+    X, W1 = _bf16(wl.KEY_X, M, K, 1.0, 39), _bf16(wl.KEY_W1, G * 2 * I, K, 0.1, 39)
+    gl = torch.from_numpy(lens).to(DEV)
+    A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise_blocked(W1.to(DEV), fmt)
+    H = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=DEV)
+    err = _err()
+    Aout = pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, gl, M, 2 * I, K, out2=H,
+                               epilogue=pgg.EPI_SWIGLU, err=err, swiglu_limit=limit)
+    oA, oSA = omx.mx_quantize_rowwise(util.bits(X), fmt)
+    oB, oSB = omx.mx_quantize_rowwise(util.bits(W1), fmt)
+    refA, refH = omx.mx_grouped_fc1_swiglu(fmt, oA, oSA, oB, oSB, lens, G, limit)
+    util.assert_close(H, refH, f"clamped mx fc1 H {fmt}")
+    util.assert_close(Aout, refA, f"clamped mx fc1 A {fmt}")
+    Hd = 256
+    dY, W2, Hs = _bf16(wl.KEY_DY, M, Hd, 1.0, 40), _bf16(wl.KEY_W2, G * Hd, I, 0.1, 40), _bf16(wl.KEY_H, M, 2 * I, 1.0, 40)
+    Ad, SAd = pgg.mx_quantize_rowwise(dY.to(DEV), fmt)
+    Bt, SBt = pgg.mx_quantize_colwise(W2.to(DEV), torch.full((G,), Hd, dtype=torch.int32, device=DEV), fmt, G * Hd)
+    dH = pgg.mx_grouped_gemm(pgg.MODE_DGRAD, fmt, Ad, SAd, Bt, SBt, gl, M, Hd, I, H=Hs.to(DEV),
+                             epilogue=pgg.EPI_SWIGLU, err=err, swiglu_limit=limit)
+    assert pgg.read_error(err) == 0
+    oAd, oSAd = omx.mx_quantize_rowwise(util.bits(dY), fmt)
+    oBt, oSBt = omx.mx_quantize_colwise(util.bits(W2), [Hd] * G, fmt, G * Hd)
+    ref = omx.mx_grouped_fc2_dgrad_swiglu_bwd(fmt, oAd, oSAd, oBt, oSBt, util.f64(Hs), lens, G, limit)
+    util.assert_close(dH, ref, f"clamped mx fc2 dgrad swiglu bwd {fmt}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 def test_mx_lossless_operands_exact(fmt):
     # operands on the MX grid with power-of-two-friendly values: the block-scaled GEMM must
     # match the fp64 GEMM of the original values to fp32 accumulation accuracy

@@ -511,6 +511,17 @@ def test_permute_is_stable_expert_sort():
     np.testing.assert_array_equal(Xs, X[row_token])
 
 
+def test_permute_reproduces_the_workload_layout():
+    # the generator builds each workload's expert-sorted rows (group_lens, row_token) with its own
+    # lexsort; the oracle permute of the same top-k ids must give exactly that layout
+    from precision_grouped_gemm_gb300 import workloads as wl
+    for w in (wl.DSV4_BF16, wl.GPTOSS_BF16):
+        lens, row_token = w.group_lens()
+        pos, glens, rtok = omg.permute(w.topk_ids(), w.experts)
+        np.testing.assert_array_equal(glens, lens)
+        np.testing.assert_array_equal(rtok, row_token)
+
+
 def test_combine_and_backward():
     rng = np.random.default_rng(25)
     T, E, k, H = 20, 6, 2, 7

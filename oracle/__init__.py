@@ -11,11 +11,12 @@ A plain, slow, obviously correct fp64 restatement of what the pages define:
   group-aware column-wise), dequantization, and the block-scaled grouped GEMM
   as "dequantize, then the fp64 grouped GEMM";
 * moe_glue.py -- the single-GPU token permute / combine around the grouped
-  GEMM and their backward passes.
+  GEMM and their backward passes;
+* fp8.py -- e4m3 tensor-wise current scaling and the FP8 grouped GEMMs.
 
 It shares no code with the CUDA path and imports nothing from it.  Inputs are
 bf16 bit patterns (numpy uint16) or MX byte codes; everything is computed in
 fp64.  Every function is pinned by a `-m "not gpu"` test against brute force,
 closed forms, invariants or hand-derived format values.
 """
-from . import grouped_gemm, moe_glue, mx  # noqa: F401
+from . import fp8, grouped_gemm, moe_glue, mx  # noqa: F401

@@ -547,3 +547,77 @@ def test_combine_and_backward():
         assert dw[t, j] == pytest.approx(num, rel=1e-6)
     with pytest.raises(ValueError):
         omg.permute(np.array([[0, E]]), E)
+
+
+# ---------------------------------------------------------------------------
+# FP8 (e4m3) tensor-wise current scaling
+# ---------------------------------------------------------------------------
+from oracle import fp8 as of8  # noqa: E402
+
+
+def test_fp8_tensorwise_hand_values():
+    # amax 2 -> s = 224: 1 -> 224 = 1.75 * 2^7 (0x76), -2 -> -448 (0xFE), 0.5 -> 112 (0x6E), 0 -> 0
+    codes, s = of8.fp8_quantize_tensorwise(np.array([1.0, -2.0, 0.5, 0.0, -0.0]))
+    assert s == np.float32(224.0)
+    assert codes.tolist() == [0x76, 0xFE, 0x6E, 0x00, 0x80]
+    np.testing.assert_array_equal(of8.fp8_dequantize(codes, s), [1.0, -2.0, 0.5, 0.0, -0.0])
+    # an all-zero tensor keeps scale 1
+    z, sz = of8.fp8_quantize_tensorwise(np.zeros(5))
+    assert sz == np.float32(1.0) and not z.any()
+
+
+def test_fp8_tensorwise_amax_maps_to_448_and_ties_round_to_even():
+    rng = np.random.default_rng(31)
+    x = rng.standard_normal(1000) * 3.0
+    codes, s = of8.fp8_quantize_tensorwise(x)
+    i = int(np.argmax(np.abs(x)))
+    assert codes[i] & 0x7F == 0x7E                      # |448|
+    assert np.all(np.abs(omx.decode_e4m3(codes)) <= 448.0)
+    # a power-of-two scale makes x * s exact: 1.0625 lies halfway between 1.0 and 1.125 -> 1.0
+    # (even mantissa); 1.1875 halfway between 1.125 and 1.25 -> 1.25
+    c, _ = of8.fp8_quantize_tensorwise(np.array([1.0625, 1.1875, 448.0 / 64]), scale=64.0)
+    assert omx.decode_e4m3(c).tolist() == [64.0 * 1.0, 64.0 * 1.25, 448.0]
+
+
+def test_fp8_tensorwise_monotone_and_non_finite():
+    x = np.linspace(-5, 5, 2001)
+    codes, _ = of8.fp8_quantize_tensorwise(x)
+    assert np.all(np.diff(omx.decode_e4m3(codes)) >= 0)
+    c, s = of8.fp8_quantize_tensorwise(np.array([1.0, np.nan, np.inf, -np.inf, -4.0]))
+    assert s == np.float32(448.0 / 4.0)                 # amax over the finite values
+    assert c[1] & 0x7F == 0x7F and c[2] == 0x7E and c[3] == 0xFE and c[4] == 0xFE
+
+
+def test_fp8_grouped_gemms_lossless_operands():
+    # operands on the e4m3 grid times 2^-3 with amax 448 * 2^-3: s = 8 exactly, quantization
+    # is lossless, so the FP8 GEMMs equal the fp64 GEMMs of the original values (brute force)
+    rng = np.random.default_rng(32)
+    grid = omx.decode_e4m3(np.arange(0x7F))
+
+    def on_grid(shape):
+        v = grid[rng.integers(0, len(grid), size=shape)] * np.where(rng.random(shape) < 0.5, -1, 1) / 8.0
+        v.flat[0] = 448.0 / 8.0
+        return v
+
+    G, N, K = 3, 5, 7
+    lens = np.array([4, 0, 6], dtype=np.int32)
+    M = int(lens.sum())
+    X, W, dY = on_grid((M, K)), on_grid((G * N, K)), on_grid((M, N))
+    (cx, sx), (cw, sw), (cd, sd) = (of8.fp8_quantize_tensorwise(t) for t in (X, W, dY))
+    assert sx == sw == sd == np.float32(8.0)
+    off = np.concatenate([[0], np.cumsum(lens)])
+    Y = of8.fp8_grouped_gemm_fwd(cx, sx, cw, sw, lens, G)
+    dX = of8.fp8_grouped_gemm_dgrad(cd, sd, cw, sw, lens, G)
+    dW = of8.fp8_grouped_gemm_wgrad(cx, sx, cd, sd, lens)
+    Wg = W.reshape(G, N, K)
+    for g in range(G):
+        for r in range(off[g], off[g + 1]):
+            for n in range(N):
+                assert Y[r, n] == pytest.approx(sum(X[r, k] * Wg[g, n, k] for k in range(K)), abs=1e-12)
+            for k in range(K):
+                assert dX[r, k] == pytest.approx(sum(dY[r, n] * Wg[g, n, k] for n in range(N)), abs=1e-12)
+        for n in range(N):
+            for k in range(K):
+                ref = sum(dY[r, n] * X[r, k] for r in range(off[g], off[g + 1]))
+                assert dW[g, n, k] == pytest.approx(ref, abs=1e-12)
+    assert not dW[1].any()

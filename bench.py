@@ -103,26 +103,31 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
         with open(self.path) as f:
-            for line in f:
-                p = [x.strip() for x in line.split(",")]
-                if len(p) >= 9:
-                    rows.append(p)
+            text = f.read()
         os.unlink(self.path)
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = set()
-        sm, mx, pw = [], [], []
-        for p in rows:
-            try:
-                sm.append(float(p[1])); mx.append(float(p[2])); pw.append(float(p[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, p[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(text)
+
+
+def parse_clock_samples(text: str) -> dict:
+    """Summarise `nvidia-smi --query-gpu=<ClockSampler.Q> --format=csv,noheader,nounits` lines:
+    median SM clock, max clock, max power, and every throttle reason seen active."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    reasons = set()
+    sm, mx, pw = [], [], []
+    for line in text.splitlines():
+        p = [x.strip() for x in line.split(",")]
+        if len(p) < 9:
+            continue
+        try:
+            sm.append(float(p[1])); mx.append(float(p[2])); pw.append(float(p[3]))
+        except ValueError:
+            continue
+        for n, v in zip(names, p[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "power_w_max": max(pw) if pw else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ----------------------------------------------------------------------------

@@ -1,0 +1,77 @@
+"""CPU checks of the benchmark's host-side arithmetic: the per-call flop and byte
+counts behind `value` and `roofline`, the traffic digest guard, and the clock
+record parsing that decides whether a run is kept."""
+import json
+import os
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from precision_grouped_gemm_gb300 import workloads as wl  # noqa: E402
+from precision_grouped_gemm_gb300.layer import layer_work, mx_layer_work  # noqa: E402
+
+
+def test_bf16_layer_work_deepseek_shape():
+    # M = 24576 rows, H = 4096, I = 2048, G = 256: every tensor moved once, bf16
+    M, G, Hd, I = 24576, 256, 4096, 2048
+    w = layer_work(M, G, Hd, I)
+    W1 = G * 2 * I * Hd * 2
+    assert w["fc1_fwd_swiglu"][0] == 2.0 * M * 2 * I * Hd
+    assert w["fc1_fwd_swiglu"][1] == M * Hd * 2 + W1 + M * I * 2 + M * 2 * I * 2 + 4 * G
+    assert w["fc1_wgrad"][1] == M * Hd * 2 + M * 2 * I * 2 + W1 + 4 * G
+    total_flops = sum(v[0] for v in w.values())
+    assert total_flops == pytest.approx(18.0 * M * I * Hd)               # the metric's flop count
+    assert total_flops / 1e12 == pytest.approx(3.711, abs=1e-3)
+    assert sum(v[1] for v in w.values()) / 1e9 == pytest.approx(41.2, abs=0.05)
+    lens, _ = wl.DSV4_BF16.group_lens()
+    assert bench.layer_flops(lens, wl.DSV4_BF16) == pytest.approx(total_flops)
+
+
+@pytest.mark.parametrize("fmt,c", [("e4m3", 1.0), ("e2m1", 0.5)])
+def test_mx_layer_work_matches_bf16_flops_and_scales_bytes(fmt, c):
+    M, G, Hd, I = 24576, 256, 4096, 2048
+    M_pad = G * 128
+    bf, mx = layer_work(M, G, Hd, I), mx_layer_work(fmt, M, G, Hd, I, M_pad)
+    assert sum(v[0] for v in mx.values()) == pytest.approx(sum(v[0] for v in bf.values()))
+    q = c + 1.0 / 32
+    # the weight stream of the forward GEMMs shrinks from 2 B to q B per element
+    W1 = G * 2 * I * Hd
+    assert mx["fc1_fwd_swiglu"][1] - bf["fc1_fwd_swiglu"][1] == pytest.approx(
+        (M * Hd + W1) * (q - 2) + M * I * q)
+    # the column-wise quantizers read bf16 and write the padded transposed codes
+    assert mx["q_x_col"][1] == M * Hd * 2 + Hd * M_pad * q + 4 * G
+
+
+def test_kernel_traffic_only_for_matching_sources(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic.json").write_text(json.dumps(
+        {"source_digest": "abc", "workloads": {"W": {"fc1_wgrad": {"dram_bytes_per_launch": 123.0}}}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    import precision_grouped_gemm_gb300.build as build
+    monkeypatch.setattr(build, "source_digest", lambda: "abc")
+    assert bench.kernel_traffic("W", "fc1_wgrad") == 123.0
+    assert bench.kernel_traffic("W", "fc2_wgrad") is None
+    monkeypatch.setattr(build, "source_digest", lambda: "changed")
+    assert bench.kernel_traffic("W", "fc1_wgrad") is None   # counters of other kernels are not reported
+
+
+def test_clock_samples_parse_reasons_and_median():
+    lines = [
+        "0, 2062, 2070, 1003.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1995, 2070, 1398.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 640.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+    ]
+    r = bench.parse_clock_samples("\n".join(lines))
+    assert r["samples"] == 3 and r["sm_mhz"] == 2062.0 and r["sm_max_mhz"] == 2070.0
+    assert r["power_w_max"] == 1398.0 and r["reasons"] == ["sw_power_cap"]
+    bad = bench.parse_clock_samples("0, 1400, 2070, 900, 0x8, Active, Not Active, Not Active, Not Active")
+    assert bad["reasons"] == ["hw_slowdown"]
+    assert bench.parse_clock_samples("")["sm_mhz"] is None

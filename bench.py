@@ -10,6 +10,9 @@ backward, fc2 wgrad, fc1 dgrad, fc1 wgrad).
 
 Prints one JSON line.  `value` counts 2*M*N*K flops per GEMM (padding rows the
 MMA wastes are not counted) over all ranks divided by the slowest rank's time.
+`extra` adds the same measurement for the MXFP8 DeepSeek-shaped, GPT-OSS-shaped
+BF16 and Zipf-routed MXFP4 layers (--workload makes any of them the main line),
+the fp32 main_grad accumulation and the single-GPU MoE permute / combine.
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload instead (the only other code path this file runs).
 """

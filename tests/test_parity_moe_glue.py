@@ -151,3 +151,28 @@ def test_permute_gemm_combine_chain():
     # Ys is rounded to bf16 before the combine: allow its propagated rounding
     extra = 2.0 ** -8 * mg.combine(np.abs(ys), rpos, w.double().numpy())
     util.assert_close(out, mg.combine(ys, rpos, w.double().numpy()), "permute-gemm-combine", extra=extra)
+
+
+def test_combine_full_size_sample():
+    # the DeepSeek-shaped routing at full size: 4096 tokens, top-6 of 256 experts, hidden 4096;
+    # sampled tokens checked against the oracle, combine and its backward
+    w = wl.DSV4_BF16
+    T, k, E, H = w.tokens, w.topk, w.experts, w.hidden
+    rpos, _, _ = mg.permute(w.topk_ids(), E)
+    pos = torch.from_numpy(rpos.astype(np.int32)).to(DEV)
+    Ys = wl.gen_matrix(wl.KEY_H, T * k, H, 1.0, w.seed, device=DEV)
+    dOut = wl.gen_matrix(wl.KEY_DY, T, H, 1.0, w.seed, device=DEV)
+    wts = _weights(T, k, w.seed).to(DEV)
+    out = pgg.moe_combine(Ys, pos, wts)
+    dYs, dw = pgg.moe_combine_bwd(dOut, Ys, pos, wts)
+    torch.cuda.synchronize()
+    toks = np.random.Generator(np.random.PCG64(6)).choice(T, 48, replace=False)
+    for t in toks:
+        rows = rpos[t]
+        ys = util.f64(Ys[torch.from_numpy(rows.astype(np.int64)).to(DEV)])
+        wt = wts[t].double().cpu().numpy()
+        util.assert_close(out[t], mg.combine(ys, np.arange(k)[None, :], wt[None, :])[0], f"combine token {t}")
+        g = util.f64(dOut[t:t + 1])
+        rdys, rdw = mg.combine_bwd(g, ys, np.arange(k)[None, :], wt[None, :])
+        util.assert_close(dYs[torch.from_numpy(rows.astype(np.int64)).to(DEV)], rdys, f"combine bwd dYs token {t}")
+        util.assert_close(dw[t], rdw[0], f"combine bwd dw token {t}")

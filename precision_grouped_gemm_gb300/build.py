@@ -73,12 +73,18 @@ if __name__ == "__main__":
     print(build(verbose=True))
 
 
+# Translation units whose kernels have no DRAM counters in profiles/traffic.json: editing them
+# leaves the recorded grouped-GEMM and quantizer counters valid.
+DIGEST_EXCLUDE = ("moe_glue.cu",)
+
+
 def source_digest() -> str:
-    """sha256 over the CUDA sources and headers (identifies the kernels a profile was taken on)."""
+    """sha256 over the CUDA sources and headers of the kernels whose DRAM counters are recorded
+    (identifies the kernels a profile was taken on)."""
     import hashlib
     h = hashlib.sha256()
     for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name not in DIGEST_EXCLUDE:
             with open(os.path.join(CSRC, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

@@ -14,7 +14,8 @@
 //           chunks, group_lens[e] its total
 //   rank    one warp per chunk: pos[t, j] = (rows of experts < e) + ws[e, c] +
 //           (earlier entries of expert e inside the chunk, in (token, choice)
-//           order) -- exactly the stable sort's position
+//           order) -- exactly the stable sort's position; the chunk's tokens are
+//           walked in order, a token's k choices ranked in parallel across lanes
 //   gather  one warp per entry, Xs[pos[t, j]] = X[t] with 16-byte copies
 // All integer work is exact, so pos and group_lens are deterministic.
 #include <algorithm>
@@ -123,11 +124,22 @@ __global__ void __launch_bounds__(kRankWarps * 32) moe_rank_kernel(const int32_t
   const int n = (int)min((int64_t)kChunk, T - t0) * k;  // entries of this chunk, contiguous in ids
   for (int i = lane; i < n; i += 32) sid[i] = __ldg(ids + t0 * k + i);
   __syncwarp();
-  if (lane == 0) {
-    // (token, choice) order is the flat order of ids: the stable order within each expert
-    for (int i = 0; i < n; ++i) {
-      const int e = sid[i];
-      sid[i] = (e < 0 || e >= E) ? -1 : base[e]++;
+  if (lane < k) {
+    // tokens in order; lane j takes choice j.  Choices of one token that name the same
+    // expert are ordered by j, so positions follow the (token, choice) order: the stable
+    // order within each expert.
+    const unsigned km = k == 32 ? 0xffffffffu : ((1u << k) - 1u);
+    const int nt = n / k;
+    for (int i = 0; i < nt; ++i) {
+      const int e = sid[i * k + lane];
+      const bool ok = e >= 0 && e < E;
+      const unsigned peers = __match_any_sync(km, ok ? e : -1);
+      const int before = __popc(peers & ((1u << lane) - 1u));
+      const int p = ok ? base[e] + before : -1;
+      __syncwarp(km);
+      if (ok && before == 0) base[e] += __popc(peers);
+      __syncwarp(km);
+      sid[i * k + lane] = p;
     }
   }
   __syncwarp();
@@ -160,11 +172,29 @@ __global__ void __launch_bounds__(kCopyThreads) moe_gather_kernel(const __nv_bfl
   }
 }
 
-__device__ __forceinline__ void fma8(float* acc, float w, const uint4& y) {
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& y) {
   acc[0] += w * bf16_lo(y.x); acc[1] += w * bf16_hi(y.x);
   acc[2] += w * bf16_lo(y.y); acc[3] += w * bf16_hi(y.y);
   acc[4] += w * bf16_lo(y.z); acc[5] += w * bf16_hi(y.z);
   acc[6] += w * bf16_lo(y.w); acc[7] += w * bf16_hi(y.w);
+}
+
+// Choice j of the token whose positions / weights lanes hold in (my_p, my_w): its weight
+// and the 16-byte piece v of its row (not loaded when j >= k, the entry is dropped, or v is
+// past the row).  Every lane takes part in the shuffles.
+struct Choice {
+  uint4 y;
+  float w;
+  bool use;
+};
+__device__ __forceinline__ Choice load_choice(const __nv_bfloat16* __restrict__ Ys, int32_t my_p, float my_w, int j,
+                                              int k, int64_t H, int64_t v, int64_t nvec) {
+  Choice c;
+  const int32_t p = __shfl_sync(0xffffffffu, my_p, j & 31);
+  c.w = __shfl_sync(0xffffffffu, my_w, j & 31);
+  c.use = j < k && p >= 0 && v < nvec;
+  c.y = c.use ? __ldg(reinterpret_cast<const uint4*>(Ys + (int64_t)p * H) + v) : make_uint4(0, 0, 0, 0);
+  return c;
 }
 
 // out[t] = sum_j w[t, j] * Ys[pos[t, j]] (w = 1 when w == nullptr), fp32 accumulation in
@@ -183,10 +213,12 @@ __global__ void __launch_bounds__(kCopyThreads) moe_combine_kernel(const __nv_bf
     for (int64_t v0 = 0; v0 < nvec; v0 += 32) {
       const int64_t v = v0 + lane;
       float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      for (int j = 0; j < k; ++j) {
-        const int32_t p = __shfl_sync(0xffffffffu, my_p, j);
-        const float wj = __shfl_sync(0xffffffffu, my_w, j);
-        if (p >= 0 && v < nvec) fma8(acc, wj, __ldg(reinterpret_cast<const uint4*>(Ys + (int64_t)p * H) + v));
+      // two choices' rows in flight at a time, summed in choice order (four spilled)
+      for (int j0 = 0; j0 < k; j0 += 2) {
+        const Choice c0 = load_choice(Ys, my_p, my_w, j0, k, H, v, nvec);
+        const Choice c1 = load_choice(Ys, my_p, my_w, j0 + 1, k, H, v, nvec);
+        if (c0.use) fma8(acc, c0.w, c0.y);
+        if (c1.use) fma8(acc, c1.w, c1.y);
       }
       if (v >= nvec) continue;
       uint4 o;

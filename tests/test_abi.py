@@ -110,3 +110,27 @@ def test_blocked_scale_layout_helpers():
     assert flat[512] == s[0, 4]                                  # next k-block atom of row block 0
     assert flat[3 * 512 + 16 * 5 + 4 * 2 + 3] == s[128 + 69, 3]  # row block 1, m = 69
     np.testing.assert_array_equal(util.unblock_scales(b, C, M_pad), s)
+
+
+def test_new_entry_points_host_validation_without_gpu(lib):
+    P, I64, I32, F32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+    lib.pgg_status_string.restype = ctypes.c_char_p
+    assert b"expert" in lib.pgg_status_string(19)
+    assert b"scratch" in lib.pgg_status_string(6)
+    g = 1 << 20
+    fc1 = lib.pgg_grouped_fc1_swiglu_clamped
+    fc1.argtypes = [P, P, P, P, P, I64, I64, I64, I32, F32, P, P]
+    assert fc1(g, g, g, g, g, 64, 64, 64, 2, -1.0, None, None) == 1           # negative limit
+    assert fc1(g, g, g, g, g, 64, 64, 64, 2, float("nan"), None, None) == 1   # NaN limit
+    assert fc1(g, g, g, g, g, 0, 64, 64, 2, 1.0, None, None) == 0             # M == 0 is a no-op
+    fc2 = lib.pgg_grouped_fc2_dgrad_swiglu_bwd_clamped
+    fc2.argtypes = [P, P, P, P, P, I64, I64, I64, I32, F32, P, P]
+    assert fc2(g, g, g, g, g, 64, 64, 64, 2, float("inf"), None, None) == 1   # non-finite limit
+    mxc = lib.pgg_mx_grouped_gemm_clamped
+    mxc.argtypes = [I32, I32, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, F32, P, P]
+    assert mxc(2, 1, g, g, g, g, None, g, g, None, None, None, 64, 128, 128, 1, 1.0, None, None) == 1  # wgrad
+    q = lib.pgg_mx_quantize_rowwise_blocked
+    q.argtypes = [P, I64, I64, I32, P, P, P]
+    assert q(g, 4, 96, 1, g, g, None) == 3          # C % 128
+    assert q(g, 4, 128, 7, g, g, None) == 1         # bad format
+    assert q(g, 0, 128, 1, g, g, None) == 0         # R == 0 is a no-op

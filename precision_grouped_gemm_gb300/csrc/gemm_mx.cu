@@ -58,6 +58,7 @@ struct MxArgs {
   const uint8_t* SB;
   int64_t sa_ld, sb_ld;   // scale bytes per row (red/32); blocked: 4 x atoms per 128-row block
   int b_bulk;             // fwd: the tile's B rows start on 128-row atoms (whole-atom copies)
+  int64_t sb_blocks;      // 128-row blocks of the blocked B scales (atom copies stay inside them)
   float swiglu_limit;     // SwiGLU epilogues: clamp limit (0: none)
   int a_rows, b_rows;     // rows of the A / B scale tensors that exist (zero-filled beyond)
   int out_cols;           // fwd N (or I with SwiGLU), dgrad K, wgrad K
@@ -273,7 +274,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                      (EPI == kEpiSwiGLU ? (h < BN / 256 ? 128 * h : args.I + 128 * (h - BN / 256)) : 128 * h);
               else
                 r0 = T.col0 + 128 * h;
-              bulk_load(ssf + 512 + 512 * h, args.SB + ((r0 >> 7) * (args.sb_ld >> 2) + p) * 512, 512, fb);
+              // a tile's second half may lie past the operand's last row (N or K not a multiple
+              // of 256): its scales only feed outputs that are not stored, so the copy reads the
+              // last existing atom row instead of running past the buffer
+              const int64_t rb = min(r0 >> 7, args.sb_blocks - 1);
+              bulk_load(ssf + 512 + 512 * h, args.SB + (rb * (args.sb_ld >> 2) + p) * 512, 512, fb);
             }
           }
         }
@@ -527,6 +532,7 @@ int launch_mx_gemm(const MxCall& c) {
     // weight scales are blocked: whole-atom copies when every B tile (or SwiGLU half)
     // starts on a 128-row atom
     a.b_bulk = c.epi ? ((fbn / 2) % 128 == 0 && (N / 2) % 128 == 0) : (N % 128 == 0 && fbn % 128 == 0);
+    a.sb_blocks = cdiv((int64_t)c.G * N, 128);
     a.a_rows = (int)c.M;
     a.nw = (int)N;
     a.I = (int)(N / 2);
@@ -542,6 +548,7 @@ int launch_mx_gemm(const MxCall& c) {
     if ((st = encode_tmap(&tb, u8, 2, c.B, db, sb, bwide, sw))) return st;
     a.sa_ld = N / 32;
     a.sb_ld = c.G * N / 32;
+    a.sb_blocks = cdiv(K, 128);
     a.a_rows = (int)c.M;
     a.b_rows = (int)K;
     a.I = (int)K;
@@ -559,6 +566,7 @@ int launch_mx_gemm(const MxCall& c) {
     if ((st = encode_wgrad_out(&tc, c.out, N, K, c.G, kMxWgradStoreAtoms, &a.c4d))) return st;
     a.nct = FastDiv((uint32_t)cdiv(K, wbn));
     a.sa_ld = a.sb_ld = Mp / 32;
+    a.sb_blocks = cdiv(K, 128);
     a.a_rows = (int)N;
     a.b_rows = (int)K;
     a.out_cols = (int)K;

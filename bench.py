@@ -261,7 +261,8 @@ def run_reference(args, w):
 # ----------------------------------------------------------------------------
 
 def kernel_traffic(workload, name):
-    """DRAM bytes per launch from the committed ncu summary, if the kernel sources still match."""
+    """DRAM bytes per launch from the committed ncu summary, if the sources of the kernel's
+    family still match the ones the counters were taken on."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -269,10 +270,13 @@ def kernel_traffic(workload, name):
     except (OSError, ValueError):
         return None
     from precision_grouped_gemm_gb300.build import source_digest
-    if d.get("source_digest") != source_digest():
-        return None
     k = d.get("workloads", {}).get(workload, {}).get(name)
-    return None if k is None else k.get("dram_bytes_per_launch")
+    if k is None:
+        return None
+    family = k.get("family")
+    if family is None or d.get("source_digests", {}).get(family) != source_digest(family):
+        return None
+    return k.get("dram_bytes_per_launch")
 
 
 PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}  # dense tensor peak vs bf16 (nominal ratios)

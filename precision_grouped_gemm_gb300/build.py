@@ -73,18 +73,22 @@ if __name__ == "__main__":
     print(build(verbose=True))
 
 
-# Translation units whose kernels have no DRAM counters in profiles/traffic.json: editing them
-# leaves the recorded grouped-GEMM and quantizer counters valid.
-DIGEST_EXCLUDE = ("moe_glue.cu",)
+# Kernel families with DRAM counters in profiles/traffic.json, and the sources each one's
+# kernels cannot depend on (separate translation units): a family's counters stay valid
+# while the sources it is built from are unchanged.
+DIGEST_EXCLUDE = {
+    "bf16": ("gemm_mx.cu", "mx_quant.cu", "moe_glue.cu"),    # BF16 grouped GEMM family
+    "mx": ("gemm_bf16.cu", "gemm_bf16.cuh", "moe_glue.cu"),  # block-scaled GEMM + MX quantizers
+}
 
 
-def source_digest() -> str:
-    """sha256 over the CUDA sources and headers of the kernels whose DRAM counters are recorded
-    (identifies the kernels a profile was taken on)."""
+def source_digest(family: str) -> str:
+    """sha256 over the CUDA sources and headers a kernel family is built from (identifies the
+    kernels a profile was taken on)."""
     import hashlib
     h = hashlib.sha256()
     for name in sorted(os.listdir(CSRC)):
-        if name.endswith((".cu", ".cuh", ".h")) and name not in DIGEST_EXCLUDE:
+        if name.endswith((".cu", ".cuh", ".h")) and name not in DIGEST_EXCLUDE[family]:
             with open(os.path.join(CSRC, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

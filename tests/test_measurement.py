@@ -52,14 +52,35 @@ def test_kernel_traffic_only_for_matching_sources(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "traffic.json").write_text(json.dumps(
-        {"source_digest": "abc", "workloads": {"W": {"fc1_wgrad": {"dram_bytes_per_launch": 123.0}}}}))
+        {"source_digests": {"bf16": "abc", "mx": "def"},
+         "workloads": {"W": {"fc1_wgrad": {"dram_bytes_per_launch": 123.0, "family": "bf16"}},
+                       "Q": {"fc1_wgrad": {"dram_bytes_per_launch": 456.0, "family": "mx"},
+                             "fc2_fwd": {"dram_bytes_per_launch": 789.0}}}}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     import precision_grouped_gemm_gb300.build as build
-    monkeypatch.setattr(build, "source_digest", lambda: "abc")
+    now = {"bf16": "abc", "mx": "def"}
+    monkeypatch.setattr(build, "source_digest", lambda family: now[family])
     assert bench.kernel_traffic("W", "fc1_wgrad") == 123.0
+    assert bench.kernel_traffic("Q", "fc1_wgrad") == 456.0
     assert bench.kernel_traffic("W", "fc2_wgrad") is None
-    monkeypatch.setattr(build, "source_digest", lambda: "changed")
-    assert bench.kernel_traffic("W", "fc1_wgrad") is None   # counters of other kernels are not reported
+    assert bench.kernel_traffic("Q", "fc2_fwd") is None       # no family recorded: not trusted
+    now["mx"] = "changed"                                     # only the MX sources changed
+    assert bench.kernel_traffic("W", "fc1_wgrad") == 123.0
+    assert bench.kernel_traffic("Q", "fc1_wgrad") is None
+    now["bf16"] = "changed"
+    assert bench.kernel_traffic("W", "fc1_wgrad") is None
+
+
+def test_digest_families_cover_the_kernels():
+    # each family's digest changes with its own kernel sources and ignores the other family's
+    import precision_grouped_gemm_gb300.build as build
+    srcs = {n for n in os.listdir(build.CSRC) if n.endswith((".cu", ".cuh", ".h"))}
+    assert {"gemm_bf16.cu", "gemm_bf16.cuh"} <= srcs - set(build.DIGEST_EXCLUDE["bf16"])
+    assert {"gemm_mx.cu", "mx_quant.cu"} <= srcs - set(build.DIGEST_EXCLUDE["mx"])
+    for fam in build.DIGEST_EXCLUDE:
+        assert set(build.DIGEST_EXCLUDE[fam]) <= srcs
+        assert len(build.source_digest(fam)) == 16
+    assert build.source_digest("bf16") != build.source_digest("mx")
 
 
 def test_clock_samples_parse_reasons_and_median():

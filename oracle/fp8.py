@@ -10,13 +10,20 @@ this oracle takes the usual per-tensor current scaling as the plainest reading:
 
 * amax = max |x| over the tensor's finite values;
 * scale s = 448 / amax in fp32 (s = 1 when amax is 0), 448 being e4m3's
-  largest finite value, so the tensor's largest element maps to +-448;
+  largest finite value, so the tensor's largest element maps to +-448; a
+  quotient that overflows fp32 (amax below 448 / 2^128, a subnormal amax) is
+  clamped to the largest finite fp32, so that s stays finite and 0 * s = 0;
 * code = e4m3 round-to-nearest-even of x * s, saturating at +-448, sign of zero
   kept; NaN gives the NaN code 0x7F (with its sign), +-Inf saturates.  x * s is
   formed in fp32: the product decides an integer code, so it is taken in the
   precision a kernel uses;
 * dequantized value = decode(code) / s;
-* the grouped GEMMs reduce decoded codes in fp64 and divide by s_A * s_B.
+* the grouped GEMMs reduce decoded codes in fp64 and divide by s_A * s_B;
+* the column-wise (wgrad) operand is the same codes transposed into the
+  group-padded layout of the MX column-wise operand: group g's rows become
+  columns poff_g .. poff_g + len_g - 1 of [C, M_pad], poff the prefix sum of
+  round_up(len, 128), and pad columns hold code 0 (one tensor scale, so no
+  per-block scales exist).
 """
 from __future__ import annotations
 
@@ -36,7 +43,9 @@ def fp8_tensor_scale(x: np.ndarray) -> np.float32:
     amax = float(np.max(np.abs(v[fin]))) if fin.any() else 0.0
     if amax == 0.0:
         return np.float32(1.0)
-    return np.float32(E4M3_MAX) / np.float32(amax)
+    with np.errstate(over="ignore"):
+        s = np.float32(E4M3_MAX) / np.float32(amax)
+    return s if np.isfinite(s) else np.float32(np.finfo(np.float32).max)
 
 
 def fp8_quantize_tensorwise(x: np.ndarray, scale=None):
@@ -73,3 +82,19 @@ def fp8_grouped_gemm_wgrad(X, sX, dY, sdY, group_lens):
     """out[g] = deq(dY)_g^T . deq(X)_g; X [M, K], dY [M, N] codes (one scale per tensor)."""
     return og.grouped_gemm_wgrad(omx.decode_e4m3(X), omx.decode_e4m3(dY), group_lens) / (
         float(np.float32(sX)) * float(np.float32(sdY)))
+
+
+def fp8_quantize_colwise(x: np.ndarray, group_lens, M_pad: int, scale=None, P: int = 128):
+    """fp64 / bf16-valued x [M, C] -> (codes_t [C, M_pad] u8, fp32 scale): group g's row i
+    goes to column poff_g + i, pad columns are code 0; scale None computes it over x."""
+    v = np.asarray(x, dtype=np.float64)
+    M, C = v.shape
+    codes, s = fp8_quantize_tensorwise(v, scale)
+    off = og.group_offsets(group_lens, M)
+    poff = omx.padded_offsets(group_lens, P)
+    assert M_pad % P == 0 and poff[-1] <= M_pad
+    codes_t = np.zeros((C, M_pad), dtype=np.uint8)
+    for g in range(len(group_lens)):
+        n = int(off[g + 1] - off[g])
+        codes_t[:, poff[g]:poff[g] + n] = codes[off[g]:off[g + 1]].T
+    return codes_t, s

@@ -621,3 +621,37 @@ def test_fp8_grouped_gemms_lossless_operands():
                 ref = sum(dY[r, n] * X[r, k] for r in range(off[g], off[g + 1]))
                 assert dW[g, n, k] == pytest.approx(ref, abs=1e-12)
     assert not dW[1].any()
+
+
+def test_fp8_tensorwise_scale_overflow_is_clamped():
+    # amax = 2^-133 (the smallest bf16 subnormal): 448 / amax overflows fp32, so s is the largest
+    # finite fp32, (2 - 2^-23) 2^127; x * s = (2 - 2^-23) 2^-6 rounds up to 2^-5 (code 0x10)
+    tiny = 2.0 ** -133
+    codes, s = of8.fp8_quantize_tensorwise(np.array([tiny, 0.0, -tiny]))
+    assert s == np.finfo(np.float32).max
+    assert codes.tolist() == [0x10, 0x00, 0x90]
+    # amax = 2^-119 still gives a finite quotient, 448 * 2^119 = 1.75 * 2^127: no clamp
+    c2, s2 = of8.fp8_quantize_tensorwise(np.array([2.0 ** -119]))
+    assert s2 == np.float32(1.75 * 2.0 ** 127) and c2.tolist() == [0x7E]
+
+
+def test_fp8_colwise_is_the_group_padded_transpose():
+    # brute force on a tiny ragged case: every code of the column-wise operand is the row-wise
+    # code of the same element (one tensor scale), pad columns are 0, and the scale is shared
+    rng = np.random.default_rng(33)
+    lens = np.array([5, 0, 130, 1], dtype=np.int32)
+    M, C = int(lens.sum()), 6
+    x = rng.standard_normal((M, C))
+    codes, s = of8.fp8_quantize_tensorwise(x)
+    M_pad = 512
+    ct, sc = of8.fp8_quantize_colwise(x, lens, M_pad)
+    assert sc == s and ct.shape == (C, M_pad)
+    poff = [0, 128, 128, 384, 512]
+    off = [0, 5, 5, 135, 136]
+    used = np.zeros(M_pad, dtype=bool)
+    for g in range(len(lens)):
+        for i in range(int(lens[g])):
+            used[poff[g] + i] = True
+            for c in range(C):
+                assert ct[c, poff[g] + i] == codes[off[g] + i, c]
+    assert not ct[:, ~used].any()

@@ -240,6 +240,66 @@ int pgg_mx_grouped_gemm(int mode, int fmt, int epilogue, const uint8_t* A, const
                         uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G,
                         int64_t M_pad, int32_t* err, void* stream);
 
+/* ---------------------------------------------------------------- FP8 tensor-wise */
+
+/* FP8 (e4m3) with one fp32 scale per tensor, computed from the tensor itself
+ * ("current scaling": "[Megatron-LM] feat: add grouped gemm fp4 support ...
+ * Pull Request #891", description and "Changes": the grouped linear layer's
+ * FP8 path is the plain grouped_gemm_fp8 call, and under current scaling a
+ * cached transposed weight must not be reused; "Primus-Turbo" README: FP8
+ * GroupedGEMM).  The pages give no formula; the library takes the usual
+ * per-tensor recipe:
+ *   amax = max |x| over the tensor's finite elements;
+ *   s = 448 / amax in fp32 (1 when amax is 0; clamped to the largest finite
+ *       fp32 if the quotient overflows), so the largest element maps to +-448;
+ *   code = e4m3 round-to-nearest-even of the fp32 product x * s, saturating
+ *       at +-448 (+-Inf saturates too);
+ *   deq(code) = decode(code) / s.
+ * amax_scale is a device float[2] = {s, amax}, 16-byte aligned.  Every tensor
+ * that the GEMM below reads takes its own amax_scale. */
+
+/* amax and s of a bf16 tensor of n elements (n % 8 == 0; n == 0 gives s = 1,
+ * amax = 0).  Writes amax_scale[0..1]; two small kernels and a 4-byte memset. */
+int pgg_fp8_tensor_scale(const void* in, int64_t n, float* amax_scale, void* stream);
+
+/* Row-major e4m3 codes [R, C] of bf16 in [R, C] with the scale amax_scale[0]
+ * (from pgg_fp8_tensor_scale on the same tensor).  C % 8 == 0. */
+int pgg_fp8_quantize_rowwise(const void* in, int64_t R, int64_t C, const float* amax_scale, uint8_t* codes,
+                             void* stream);
+
+/* Column-wise e4m3 codes for the wgrad GEMM: codes_t [C, M_pad], where group
+ * g's row i of in [M, C] lands in column poff_g + i, poff the prefix sum of
+ * round_up(len_g, PGG_MX_PAD), and every other column holds code 0 (the same
+ * layout as pgg_mx_quantize_colwise's codes, with no scales).  group_lens NULL
+ * means one group of M rows (G 0 or 1).  C % 8 == 0; M_pad a multiple of
+ * PGG_MX_PAD; a layout past M_pad sets *err = PGG_ERR_PAD_OVERFLOW and writes
+ * nothing.  W [G, N, K] for the dgrad GEMM is the same call on W viewed as
+ * [G*N, K] with G groups of N rows and M_pad = G*N: codes_t = W^T [K, G*N]. */
+int pgg_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens, int G,
+                             const float* amax_scale, uint8_t* codes_t, int64_t M_pad, int32_t* err,
+                             void* stream);
+
+/* Bytes of the workspace pgg_fp8_grouped_gemm needs: 4 * max(K, G*N, M_pad)
+ * rounded up to 512 (pass M_pad = 0 outside wgrad). */
+size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad);
+
+/* FP8 tensor-wise grouped GEMM (grouped_gemm_fp8): the operands and shapes of
+ * pgg_mx_grouped_gemm with fmt e4m3 and no epilogue, each operand carrying one
+ * scale instead of per-block scales:
+ *   FWD    out[M, N]    = deq(A)_g . deq(B)_g^T   A = X codes [M, K], B = W codes [G*N, K]
+ *   DGRAD  out[M, K]    = deq(A)_g . W_g          A = dY codes [M, N], B = W^T codes [K, G*N]
+ *   WGRAD  out[G, N, K] = sum over group g's padded columns of deq(A)[:, r] deq(B)[:, r]^T
+ *                         A = dY^T codes [N, M_pad], B = X^T codes [K, M_pad] (column-wise)
+ * i.e. out = (sum of code products) / (s_A s_B), fp32 accumulation, bf16 out.
+ * scale_a / scale_b point at each operand's s (its amax_scale).  ws: device
+ * scratch of pgg_fp8_workspace_size bytes, 16-byte aligned, owned by the
+ * caller and overwritten on the stream by each call (it holds the unit block
+ * scales the tensor cores read).  The size rules, errors and group semantics
+ * are pgg_mx_grouped_gemm's (fwd K and dgrad N multiples of 128). */
+int pgg_fp8_grouped_gemm(int mode, const uint8_t* A, const float* scale_a, const uint8_t* B, const float* scale_b,
+                         const int32_t* group_lens, void* out, int64_t M, int64_t N, int64_t K, int G,
+                         int64_t M_pad, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+
 /* ---------------------------------------------------------------- MoE glue (one GPU) */
 
 /* Bytes of the scratch table pgg_moe_permute needs: ceil(T / 32) * E * 4. */

@@ -13,6 +13,8 @@ from ._binding import (PggError, PAD, FMT_E4M3, FMT_E2M1, MODE_FWD, MODE_DGRAD, 
                        grouped_fc1_swiglu, grouped_fc2_dgrad_swiglu_bwd,
                        mx_quantize_rowwise, mx_quantize_rowwise_blocked, mx_quantize_colwise, mx_grouped_gemm,
                        mx_pad_rows,
+                       fp8_tensor_scale, fp8_quantize_rowwise, fp8_quantize_colwise, fp8_workspace_size,
+                       fp8_grouped_gemm,
                        moe_permute_workspace_size, moe_permute, moe_combine, moe_combine_bwd)
 
 __all__ = [
@@ -21,6 +23,7 @@ __all__ = [
     "grouped_gemm_fwd", "grouped_gemm_dgrad", "grouped_gemm_wgrad", "grouped_gemm_wgrad_accumulate",
     "grouped_fc1_swiglu",
     "grouped_fc2_dgrad_swiglu_bwd", "mx_quantize_rowwise", "mx_quantize_rowwise_blocked", "mx_quantize_colwise",
-    "mx_grouped_gemm", "mx_pad_rows", "moe_permute_workspace_size", "moe_permute", "moe_combine",
+    "mx_grouped_gemm", "mx_pad_rows", "fp8_tensor_scale", "fp8_quantize_rowwise", "fp8_quantize_colwise",
+    "fp8_workspace_size", "fp8_grouped_gemm", "moe_permute_workspace_size", "moe_permute", "moe_combine",
     "moe_combine_bwd",
 ]

@@ -40,6 +40,11 @@ SIGNATURES = {
     "pgg_moe_permute": [_P, _P, _I64, _I32, _I64, _I32, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
     "pgg_moe_permute_noalloc": [_P, _P, _I64, _I32, _I64, _I32, _P, _P, _P, _P, _P],
     "pgg_moe_combine": [_P, _P, _P, _P, _I64, _I32, _I64, _P],
+    "pgg_fp8_tensor_scale": [_P, _I64, _P, _P],
+    "pgg_fp8_quantize_rowwise": [_P, _I64, _I64, _P, _P, _P],
+    "pgg_fp8_quantize_colwise": [_P, _I64, _I64, _P, _I32, _P, _P, _I64, _P, _P],
+    "pgg_fp8_grouped_gemm": [_I32, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, _P, ctypes.c_size_t,
+                             _P, _P],
     "pgg_moe_combine_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I32, _I64, _P],
 }
 
@@ -71,6 +76,8 @@ def lib():
         L.pgg_status_string.restype = ctypes.c_char_p
         L.pgg_moe_permute_workspace_size.argtypes = [_I64, _I32]
         L.pgg_moe_permute_workspace_size.restype = ctypes.c_size_t
+        L.pgg_fp8_workspace_size.argtypes = [_I64, _I64, _I32, _I64]
+        L.pgg_fp8_workspace_size.restype = ctypes.c_size_t
         _LIB = L
     return _LIB
 
@@ -295,6 +302,68 @@ def mx_grouped_gemm(mode, fmt, A, SA, B, SB, group_lens, M, N, K, out=None, out2
         _check(lib().pgg_mx_grouped_gemm(mode, f, epilogue, _ptr(A), _ptr(SA), _ptr(B), _ptr(SB), _ptr(H),
                                          _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), _ptr(qc), _ptr(qs), M, N,
                                          K, G, M_pad, _ptr(err), _stream(stream)), "pgg_mx_grouped_gemm")
+    return out
+
+
+def fp8_tensor_scale(x, amax_scale=None, stream=None):
+    """bf16 tensor (numel % 8 == 0) -> device float32[2] = (s, amax): amax over the finite
+    elements, s = 448 / amax (current scaling, see pgg.h)."""
+    if amax_scale is None:
+        amax_scale = torch.empty(2, dtype=torch.float32, device=x.device)
+    _dev(x, amax_scale)
+    _check(lib().pgg_fp8_tensor_scale(_ptr(x), x.numel(), _ptr(amax_scale), _stream(stream)),
+           "pgg_fp8_tensor_scale")
+    return amax_scale
+
+
+def fp8_quantize_rowwise(x, amax_scale, codes=None, stream=None):
+    """bf16 [R, C] -> e4m3 codes [R, C] (u8) with the tensor scale amax_scale[0]."""
+    R, C = x.shape
+    if codes is None:
+        codes = torch.empty((R, C), dtype=torch.uint8, device=x.device)
+    _dev(x, amax_scale, codes)
+    _check(lib().pgg_fp8_quantize_rowwise(_ptr(x), R, C, _ptr(amax_scale), _ptr(codes), _stream(stream)),
+           "pgg_fp8_quantize_rowwise")
+    return codes
+
+
+def fp8_quantize_colwise(x, group_lens, amax_scale, M_pad=None, codes_t=None, err=None, stream=None):
+    """bf16 [M, C] + group_lens -> e4m3 codes_t [C, M_pad] in the group-padded column-wise
+    layout (the wgrad operand), with the tensor scale amax_scale[0]."""
+    M, C = x.shape
+    G = 1 if group_lens is None else group_lens.numel()
+    if M_pad is None:
+        M_pad = mx_pad_rows(M, G)
+    if codes_t is None:
+        codes_t = torch.empty((C, M_pad), dtype=torch.uint8, device=x.device)
+    _dev(x, group_lens, amax_scale, codes_t, err)
+    lens = None if group_lens is None else _lens(group_lens)
+    _check(lib().pgg_fp8_quantize_colwise(_ptr(x), M, C, _ptr(lens), G, _ptr(amax_scale), _ptr(codes_t), M_pad,
+                                          _ptr(err), _stream(stream)), "pgg_fp8_quantize_colwise")
+    return codes_t
+
+
+def fp8_workspace_size(N: int, K: int, G: int, M_pad: int = 0) -> int:
+    return lib().pgg_fp8_workspace_size(N, K, G, M_pad)
+
+
+def fp8_grouped_gemm(mode, A, scale_a, B, scale_b, group_lens, M, N, K, out=None, M_pad=0, ws=None, err=None,
+                     stream=None):
+    """FP8 tensor-wise grouped GEMM (the MX operand layouts in e4m3, one scale per operand:
+    scale_a / scale_b are the operands' amax_scale tensors; see pgg.h)."""
+    G = group_lens.numel()
+    dev = A.device
+    if out is None:
+        shape = (M, N) if mode == MODE_FWD else (M, K) if mode == MODE_DGRAD else (G, N, K)
+        out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    need = fp8_workspace_size(N, K, G, M_pad if mode == MODE_WGRAD else 0)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    _dev(A, scale_a, B, scale_b, group_lens, out, ws, err)
+    _check(lib().pgg_fp8_grouped_gemm(mode, _ptr(A), _ptr(scale_a), _ptr(B), _ptr(scale_b),
+                                      _ptr(_lens(group_lens)), _ptr(out), M, N, K, G, M_pad, _ptr(ws),
+                                      ws.numel() * ws.element_size(), _ptr(err), _stream(stream)),
+           "pgg_fp8_grouped_gemm")
     return out
 
 

@@ -59,9 +59,10 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v, i
 
 // Plain store: row `dst_row` (already offset to this thread's output row),
 // accumulator columns 0..BN-1 -> output columns col0.., bounded by ncols.
-template <int BN>
+// SCALED: every accumulator is multiplied by alpha first (per-tensor operand scales).
+template <int BN, bool SCALED = false>
 __device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* dst_row, bool row_ok, int col0,
-                                          int ncols) {
+                                          int ncols, float alpha = 1.0f) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t rv[32];
@@ -71,7 +72,10 @@ __device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* dst_row, b
     if (row_ok && c0 < ncols) {
       float v[32];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(rv[j]);
+      for (int j = 0; j < 32; ++j) {
+        v[j] = __uint_as_float(rv[j]);
+        if constexpr (SCALED) v[j] *= alpha;
+      }
       store_row32(dst_row + c0, v, min(32, ncols - c0));
     }
   }
@@ -238,10 +242,12 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
 // (col0 + 64 c, row0, g) that clip at the tensor bounds.  zero: write zeros
 // without touching TMEM.  A box starting past rows_total / cols_total is
 // skipped (warp-uniform), keeping one committed store per used buffer.
-template <int BN>
+// SCALED: values are multiplied by alpha before the bf16 rounding.
+template <int BN, bool SCALED = false>
 __device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8_t* stg, int& nstore,
                                                    const CUtensorMap* tmC, int row0, int col0, int g,
-                                                   int rows_total, int cols_total, int lane) {
+                                                   int rows_total, int cols_total, int lane,
+                                                   float alpha = 1.0f) {
 #pragma unroll 1
   for (int c = 0; c < BN / 64; ++c) {
     if (row0 >= rows_total || col0 + c * 64 >= cols_total) continue;
@@ -253,6 +259,13 @@ __device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) { ra[j] = 0u; rb[j] = 0u; }
+    }
+    if constexpr (SCALED) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        ra[j] = __float_as_uint(__uint_as_float(ra[j]) * alpha);
+        rb[j] = __float_as_uint(__uint_as_float(rb[j]) * alpha);
+      }
     }
     uint8_t* sb = stg + (nstore & 1) * 4096;
     if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer is done
@@ -286,11 +299,12 @@ __device__ __forceinline__ void epi_tma_store_rows(uint32_t tb, bool zero, uint8
 // store that last read it -- RING/SA groups back -- has to be done reading, so
 // with RING/SA > 1 stores drain while the next atoms are filled.  Stores that
 // start past `cols_total` are skipped but still commit an (empty) group, which
-// keeps that count exact.
-template <int BN, int SA, int RING = BN / 64>
+// keeps that count exact.  SCALED: values are multiplied by alpha before the bf16 rounding.
+template <int BN, int SA, int RING = BN / 64, bool SCALED = false>
 __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8_t* stg,
                                                    const CUtensorMap* tmC4, int row0, int col0, int g,
-                                                   int rows_total, int cols_total, int lane) {
+                                                   int rows_total, int cols_total, int lane,
+                                                   float alpha = 1.0f) {
   static_assert(SA >= 1 && (BN / 64) % SA == 0 && RING % SA == 0, "atoms per store");
   constexpr int NS = BN / 64 / SA;
   constexpr int NW = RING / SA;  // stores sharing the ring
@@ -307,6 +321,10 @@ __device__ __forceinline__ void epi_tma_store_tile(uint32_t tb, bool zero, uint8
       } else {
 #pragma unroll
         for (int j = 0; j < 64; ++j) v[j] = 0u;
+      }
+      if constexpr (SCALED) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha);
       }
       if (i == 0) {
         if (lane == 0) bulk_wait_read<NW - 1>();  // the store that last read these slots

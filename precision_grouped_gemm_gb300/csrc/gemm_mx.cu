@@ -17,6 +17,11 @@
 //   dgrad  out[M, K]    = A[M, N] . Bt_g[K, N]^T    Bt = W^T [K, G*N] (blocks along N)
 //   wgrad  out[G, N, K] = At_g[N, .] . Bt_g[K, .]^T over group g's padded columns of
 //                         the column-wise operands At = dY^T [N, M_pad], Bt = X^T [K, M_pad]
+//
+// FP8 tensor-wise operands (one fp32 scale s per tensor, codes = e4m3(x s)) run the
+// e4m3 instantiations with TS = true: every block scale is 1 (E8M0 127), read from a
+// small constant buffer through zero row strides (each tile reads the same atoms), and
+// the epilogue multiplies the accumulator by 1 / (s_A s_B).
 #include <algorithm>
 
 #include "epilogue.cuh"
@@ -73,6 +78,8 @@ struct MxArgs {
   int64_t M_pad;
   uint8_t* q_codes;   // SwiGLU epilogues: row-wise MX codes of `out` (or nullptr)
   uint8_t* q_scales;  // and their scales
+  const float* ts_a;  // TS kernels: the operands' per-tensor fp32 scales s_A, s_B
+  const float* ts_b;
   FastDiv nct;  // wgrad: column tiles per row tile
   int c4d;      // wgrad: tmC is the 4-D atom view
 };
@@ -136,12 +143,13 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
   return T;
 }
 
-template <int FMT, int MODE, int EPI, int STAGES, int BN>
+template <int FMT, int MODE, int EPI, int STAGES, int BN, bool TS = false>
 __global__ void __launch_bounds__(kMxThreads, 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
   using C = MxCfg<FMT>;
   static_assert(BN == 128 || BN == 256, "BN");
+  static_assert(!TS || (FMT == kE4M3 && EPI == kEpiStore), "per-tensor scales: e4m3, plain store");
   using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
   constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
   constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
@@ -402,6 +410,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     GroupCursor cur;
     uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (32 * BN * 2);
     int nstore = 0;
+    float alpha = 1.0f;  // TS: 1 / (s_A s_B), written by the quantizers earlier on the stream
+    if constexpr (TS) alpha = 1.0f / (__ldg(args.ts_a) * __ldg(args.ts_b));
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       const bool row_ok = r < T.rows;
@@ -413,11 +423,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         }
         const uint32_t tbw = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
         if (args.c4d)
-          epi_tma_store_tile<BN, kMxWgradStoreAtoms>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
-                                 args.out_cols, lane);
+          epi_tma_store_tile<BN, kMxWgradStoreAtoms, BN / 64, TS>(tbw, zero, stg, &tmC, T.row0 + q * 32, T.col0,
+                                                                 T.g, args.wg_rows, args.out_cols, lane, alpha);
         else
-          epi_tma_store_rows<BN>(tbw, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
-                                 args.out_cols, lane);
+          epi_tma_store_rows<BN, TS>(tbw, zero, stg, nstore, &tmC, T.row0 + q * 32, T.col0, T.g, args.wg_rows,
+                                     args.out_cols, lane, alpha);
         if (!zero) {
           tc_fence_before();
           mbar_arrive(smem_u32(&tempty[acc]));
@@ -439,7 +449,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         epi_swiglu_bwd<BN, FMT>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
                                 args.I, args.q_codes, args.q_scales, args.swiglu_limit);
       } else {
-        epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
+        epi_store<BN, TS>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols, alpha);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));
@@ -457,11 +467,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-template <int FMT, int MODE, int EPI, int STAGES, int BN = kMxBN>
+template <int FMT, int MODE, int EPI, int STAGES, int BN = kMxBN, bool TS = false>
 int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a, int grid,
            cudaStream_t s) {
   using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
-  auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES, BN>;
+  auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES, BN, TS>;
   const size_t smem = L::bytes(a.G);
   static size_t attr_bytes = 0;  // per instantiation: raised to the largest G seen
   if (smem > attr_bytes) {
@@ -487,6 +497,18 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kWBN>(ta, tb, tc, a, grid, s);
+  return PGG_ERR_INVALID_ARG;
+}
+
+// FP8 tensor-wise operands: the e4m3 tiles and stage counts of dispatch_mx, plain store.
+int dispatch_ts(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a,
+                int grid, cudaStream_t s) {
+  constexpr int kBN = kMxFwdBNE4M3, kWBN = kMxWgradBNE4M3;
+  constexpr int kS = kBN == 128 ? 6 : 4;
+  constexpr int kSw = kWBN == 128 ? 5 : 2;
+  if (mode == 0) return run_mx<kE4M3, kFwd, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 1) return run_mx<kE4M3, kDgrad, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 2) return run_mx<kE4M3, kWgrad, kEpiStore, kSw, kWBN, true>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
 
@@ -518,6 +540,10 @@ int launch_mx_gemm(const MxCall& c) {
   a.q_codes = c.q_codes;
   a.q_scales = c.q_scales;
   a.swiglu_limit = c.limit;
+  a.ts_a = c.ts_a;
+  a.ts_b = c.ts_b;
+  const bool ts = c.ts_a != nullptr;
+  if (ts && (!e4 || c.epi != 0 || !c.ts_b)) return PGG_ERR_INVALID_ARG;
   const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {
@@ -575,6 +601,18 @@ int launch_mx_gemm(const MxCall& c) {
   }
   if (c.mode != 2) tc = ta;  // unused outside wgrad
   const int grid = std::max(1, std::min(dev.sms, tiles_ub));
+  if (ts) {
+    // unit block scales: zero row strides make every row (block) of SA and SB read the
+    // first row block's atoms, so SA = SB = one buffer of mx_unit_scale_bytes() bytes of 127
+    // (largest offset read: fwd K / 128, dgrad G N / 128, wgrad M_pad / 128 atoms of 512 B),
+    // written here on the stream ahead of the kernel
+    const size_t ub = mx_unit_scale_bytes(c.N, c.K, c.G, c.mode == 2 ? c.M_pad : 0);
+    cudaError_t e = cudaMemsetAsync(const_cast<uint8_t*>(c.SA), 127, ub, c.stream);
+    if (e != cudaSuccess) return cuda_status(e);
+    a.SA = a.SB = c.SA;
+    a.sa_ld = a.sb_ld = 0;
+    return dispatch_ts(c.mode, ta, tb, tc, a, grid, c.stream);
+  }
   return e4 ? dispatch_mx<kE4M3>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream)
             : dispatch_mx<2>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream);
 }

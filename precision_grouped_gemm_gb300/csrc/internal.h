@@ -79,8 +79,29 @@ struct MxCall {
   int32_t* err;
   cudaStream_t stream;
   float limit = 0.0f;  // SwiGLU clamp limit (0: none)
+  // FP8 tensor-wise operands (e4m3, plain store): device fp32 scales s_A, s_B; SA = SB =
+  // a buffer of mx_unit_scale_bytes() bytes of 127 (unit block scales)
+  const float* ts_a = nullptr;
+  const float* ts_b = nullptr;
 };
 int launch_mx_gemm(const MxCall& c);
+
+// Bytes of unit block scales a tensor-scaled MX GEMM reads (any mode): 512-byte atoms for
+// the longest scale row, 4 max(K, G N, M_pad) rounded up to 512.
+inline size_t mx_unit_scale_bytes(int64_t N, int64_t K, int G, int64_t M_pad) {
+  int64_t m = K;
+  if ((int64_t)G * N > m) m = (int64_t)G * N;
+  if (M_pad > m) m = M_pad;
+  return (size_t)((4 * m + 511) / 512 * 512);
+}
+
+// FP8 tensor-wise current scaling (mx_quant.cu): amax_scale = device float[2] {s, amax}
+int launch_fp8_tensor_scale(const void* in, int64_t n, float* amax_scale, cudaStream_t s);
+int launch_fp8_quantize_rowwise(const void* in, int64_t n, const float* amax_scale, uint8_t* codes,
+                                cudaStream_t s);
+int launch_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens, int G,
+                                const float* amax_scale, uint8_t* codes_t, int64_t M_pad, int32_t* err,
+                                cudaStream_t s);
 
 // MoE glue (moe_glue.cu)
 size_t moe_permute_ws_bytes(int64_t T, int E);

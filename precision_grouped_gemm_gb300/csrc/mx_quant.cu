@@ -111,16 +111,25 @@ __device__ __forceinline__ int64_t blocked_atom_word(int r, int p, int64_t M_pad
 
 // Quantize column `half` of the packed bf16 pairs v (zero past `valid`) and store its
 // 32 codes at position j; returns the scale byte (0 when the block holds no rows).
-template <int FMT>
+// TENSOR (FP8 tensor-wise, e4m3): the multiplier is the tensor scale ts for every
+// block and no scale byte exists (a non-finite element converts on its own).
+template <int FMT, bool TENSOR = false>
 __device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int half, int valid, int c,
-                                                  int64_t M_pad, int j, uint8_t* __restrict__ codes_t) {
-  uint32_t am = 0;
-#pragma unroll
-  for (int r = 0; r < 32; ++r) am = max(am, ((v[r] >> (16 * half)) & 0x7FFFu));
+                                                  int64_t M_pad, int j, uint8_t* __restrict__ codes_t,
+                                                  float ts = 0.0f) {
   uint32_t sc = 0;
   float mult = 0.0f;
-  const bool fin = valid > 0 ? block_scale<FMT>(am, sc, mult) : true;
-  const bool keep = valid > 0 && fin;
+  bool keep;
+  if constexpr (TENSOR) {
+    mult = ts;
+    keep = valid > 0;
+  } else {
+    uint32_t am = 0;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) am = max(am, ((v[r] >> (16 * half)) & 0x7FFFu));
+    const bool fin = valid > 0 ? block_scale<FMT>(am, sc, mult) : true;
+    keep = valid > 0 && fin;
+  }
   if (FMT == kE4M3) {
     uint4 o[2];
     uint32_t* ow = reinterpret_cast<uint32_t*>(o);
@@ -150,11 +159,13 @@ __device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int h
   return valid > 0 ? sc : 0u;
 }
 
-template <int FMT>
+// TENSOR: FP8 tensor-wise codes (multiplier amax_scale[0] for every element), no scales.
+template <int FMT, bool TENSOR = false>
 __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
     const __nv_bfloat16* __restrict__ in, int64_t M, int C, const int32_t* __restrict__ lens,
     int G, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int64_t M_pad,
-    int32_t* err) {
+    int32_t* err, const float* __restrict__ amax_scale = nullptr) {
+  static_assert(!TENSOR || FMT == kE4M3, "tensor-wise scaling is e4m3");
   extern __shared__ int32_t s_dyn[];
   int32_t* s_off = s_dyn;             // [G+1] row offsets
   int32_t* s_blk = s_dyn + (G + 1);   // [G+1] prefix of 32-blocks in the padded layout
@@ -183,6 +194,7 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
   }
   __syncthreads();
   if (s_bad) return;
+  const float ts = TENSOR ? __ldg(amax_scale) : 0.0f;
   const int nkb = (int)(M_pad / 128);  // k-blocks (scale atoms) along the padded axis
   const int C128 = (C + 127) & ~127;   // scale rows, padded to whole atoms
   const int nslab = C128 / kColSlab;
@@ -193,7 +205,7 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
     const int p = (int)(t % nkb);
     const int c = (int)(t / nkb) * kColSlab + 2 * lane;
     if (c >= C) {  // pad rows of the last atom: scale 0, no codes
-      if (c < C128) {
+      if (!TENSOR && c < C128) {
         *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = 0u;
         *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = 0u;
       }
@@ -215,12 +227,75 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
       uint32_t v[32];
 #pragma unroll
       for (int r = 0; r < 32; ++r) v[r] = r < valid ? __ldg(src + (int64_t)r * (C / 2)) : 0u;
-      sc0 |= colwise_codes<FMT>(v, 0, valid, c, M_pad, 4 * p + q, codes_t) << (8 * q);
-      sc1 |= colwise_codes<FMT>(v, 1, valid, c + 1, M_pad, 4 * p + q, codes_t) << (8 * q);
+      sc0 |= colwise_codes<FMT, TENSOR>(v, 0, valid, c, M_pad, 4 * p + q, codes_t, ts) << (8 * q);
+      sc1 |= colwise_codes<FMT, TENSOR>(v, 1, valid, c + 1, M_pad, 4 * p + q, codes_t, ts) << (8 * q);
     }
-    *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = sc0;
-    *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = sc1;
+    if (!TENSOR) {
+      *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = sc0;
+      *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = sc1;
+    }
   }
+}
+
+// ------------------------------------------------------------------ FP8 tensor-wise
+// Current scaling ("[Megatron-LM] feat: add grouped gemm fp4 support ... Pull Request
+// #891", review: the FP8 grouped GEMM under current scaling): amax over the tensor's
+// finite values, s = 448 / amax in fp32 (1 for amax 0; a quotient that overflows fp32
+// is clamped to the largest finite fp32), codes = e4m3 RNE of the fp32 product x s,
+// saturating.  amax_scale is a device float[2] = {s, amax}; while the amax kernel runs,
+// word 1 holds the largest finite bf16 magnitude as bits (their integer order is the
+// values' order), one atomicMax per warp.
+__global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ in, int64_t n_chunks,
+                                                       uint32_t* __restrict__ amax_bits) {
+  uint32_t am = 0;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
+    const uint4 v = __ldg(in + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+      if (lo < 0x7F80u) am = max(am, lo);  // Inf / NaN excluded
+      if (hi < 0x7F80u) am = max(am, hi);
+    }
+  }
+  am = __reduce_max_sync(0xffffffffu, am);
+  if ((threadIdx.x & 31) == 0 && am != 0u) atomicMax(amax_bits, am);
+}
+
+__global__ void fp8_scale_kernel(float* amax_scale) {
+  const uint32_t bits = reinterpret_cast<const uint32_t*>(amax_scale)[1];
+  const float amax = __uint_as_float(bits << 16);
+  float s = 1.0f;
+  if (bits != 0u) {
+    const float fmax = __uint_as_float(0x7F7FFFFFu);
+    s = __fdiv_rn(448.0f, amax);
+    if (!(s <= fmax)) s = fmax;
+  }
+  amax_scale[0] = s;
+  amax_scale[1] = amax;
+}
+
+// codes[i] = e4m3(x[i] s), eight elements (one 16-byte load, one 8-byte store) per chunk
+__global__ void __launch_bounds__(256) fp8_quant_rowwise_kernel(const uint4* __restrict__ in,
+                                                                uint2* __restrict__ codes, int64_t n_chunks,
+                                                                const float* __restrict__ amax_scale) {
+  const float s = __ldg(amax_scale);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
+    const uint4 v = __ldg(in + i);
+    uint2 o;
+    o.x = cvt_e4m3x2(bf16_lo(v.x) * s, bf16_hi(v.x) * s) | (cvt_e4m3x2(bf16_lo(v.y) * s, bf16_hi(v.y) * s) << 16);
+    o.y = cvt_e4m3x2(bf16_lo(v.z) * s, bf16_hi(v.z) * s) | (cvt_e4m3x2(bf16_lo(v.w) * s, bf16_hi(v.w) * s) << 16);
+    codes[i] = o;
+  }
+}
+
+int stream_grid(int64_t n_chunks) {
+  DeviceInfo dev;
+  if (current_device(&dev) != PGG_OK) return 0;
+  const int64_t want = (n_chunks + 255) / 256;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * 8));
 }
 
 }  // namespace
@@ -290,6 +365,48 @@ int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32
   else
     mx_quant_colwise_kernel<kE2M1><<<grid, kColThreads, smem, s>>>(x, M, (int)C, group_lens, G,
                                                                    codes_t, scales_t, M_pad, err);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_fp8_tensor_scale(const void* in, int64_t n, float* amax_scale, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(amax_scale + 1, 0, sizeof(float), s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (n > 0) {
+    const int grid = stream_grid(n / 8);
+    if (grid == 0) return PGG_ERR_CUDA;
+    fp8_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(in), n / 8,
+                                         reinterpret_cast<uint32_t*>(amax_scale) + 1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
+  }
+  fp8_scale_kernel<<<1, 1, 0, s>>>(amax_scale);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_fp8_quantize_rowwise(const void* in, int64_t n, const float* amax_scale, uint8_t* codes,
+                                cudaStream_t s) {
+  const int grid = stream_grid(n / 8);
+  if (grid == 0) return PGG_ERR_CUDA;
+  fp8_quant_rowwise_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(in), reinterpret_cast<uint2*>(codes),
+                                                n / 8, amax_scale);
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens, int G,
+                                const float* amax_scale, uint8_t* codes_t, int64_t M_pad, int32_t* err,
+                                cudaStream_t s) {
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  const int64_t total = (M_pad / 128) * (((C + 127) / 128 * 128) / kColSlab);  // warp work items
+  const size_t smem = 8 * (size_t)(G + 1);
+  auto kern = mx_quant_colwise_kernel<kE4M3, true>;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kColThreads, smem);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * std::max(per_sm, 1)));
+  kern<<<grid, kColThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(in), M, (int)C, group_lens, G, codes_t,
+                                       nullptr, M_pad, err, amax_scale);
   return cuda_status(cudaGetLastError());
 }
 

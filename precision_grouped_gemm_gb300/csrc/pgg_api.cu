@@ -120,6 +120,7 @@ using namespace pgg;
 
 namespace {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 constexpr int64_t kMaxRows = (int64_t)1 << 31;
 
@@ -127,6 +128,7 @@ int check_common(int64_t M, int G, const int32_t* lens) {
   if (G < 1 || G > kMaxGroups) return PGG_ERR_INVALID_ARG;
   if (M < 0 || M >= kMaxRows) return PGG_ERR_INVALID_ARG;
   if (!lens) return PGG_ERR_INVALID_ARG;
+  if (!aligned4(lens)) return PGG_ERR_ALIGNMENT;
   return PGG_OK;
 }
 
@@ -141,7 +143,8 @@ static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const
                         const uint8_t* B, const uint8_t* SB, const void* H,
                         const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
                         uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G, int64_t M_pad,
-                        float limit, int32_t* err, void* stream) {
+                        float limit, int32_t* err, void* stream, const float* ts_a = nullptr,
+                        const float* ts_b = nullptr) {
   int st;
   if (mode < 0 || mode > 2) return PGG_ERR_INVALID_ARG;
   if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
@@ -153,8 +156,10 @@ static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const
   if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
       (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
-  // blocked scale atoms (SB always, wgrad SA) are fetched by 16-byte-aligned bulk copies
-  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned16(SB)) return PGG_ERR_ALIGNMENT;
+  // blocked scale atoms (SB always, wgrad SA) are fetched by 16-byte-aligned bulk copies,
+  // row-major scales (fwd / dgrad SA) by 4-byte copies
+  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned4(SA) || !aligned16(SB)) return PGG_ERR_ALIGNMENT;
+  if (err && !aligned4(err)) return PGG_ERR_ALIGNMENT;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
   if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
     return PGG_ERR_ALIGNMENT;
@@ -173,12 +178,14 @@ static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const
   MxCall c{mode, fmt, epilogue, A, SA, B, SB, H, group_lens, out, out2, out_codes, out_scales,
            M, N, K, M_pad, G, err, as_stream(stream)};
   c.limit = limit;
+  c.ts_a = ts_a;
+  c.ts_b = ts_b;
   return launch_mx_gemm(c);
 }
 
 extern "C" {
 
-int pgg_version(void) { return 100; }
+int pgg_version(void) { return 101; }
 
 int pgg_init(int device) {
   if (cudaSetDevice(device) != cudaSuccess) return PGG_ERR_CUDA;
@@ -365,6 +372,59 @@ int pgg_mx_grouped_gemm_clamped(int mode, int fmt, const uint8_t* A, const uint8
                       M, N, K, G, 0, swiglu_limit, err, stream);
 }
 
+int pgg_fp8_tensor_scale(const void* in, int64_t n, float* amax_scale, void* stream) {
+  if (!amax_scale || (n > 0 && !in)) return PGG_ERR_INVALID_ARG;
+  if (n < 0 || n >= ((int64_t)1 << 40)) return PGG_ERR_INVALID_ARG;
+  if (n % 8) return PGG_ERR_ALIGNMENT;
+  if ((n > 0 && !aligned16(in)) || !aligned16(amax_scale)) return PGG_ERR_ALIGNMENT;
+  return launch_fp8_tensor_scale(in, n, amax_scale, as_stream(stream));
+}
+
+int pgg_fp8_quantize_rowwise(const void* in, int64_t R, int64_t C, const float* amax_scale, uint8_t* codes,
+                             void* stream) {
+  if (!in || !amax_scale || !codes) return PGG_ERR_INVALID_ARG;
+  if (R < 0 || R >= kMaxRows || C <= 0 || C >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+  if (C % 8) return PGG_ERR_ALIGNMENT;
+  if (!aligned16(in) || !aligned16(codes) || !aligned16(amax_scale)) return PGG_ERR_ALIGNMENT;
+  if (R == 0) return PGG_OK;
+  return launch_fp8_quantize_rowwise(in, R * C, amax_scale, codes, as_stream(stream));
+}
+
+int pgg_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t* group_lens, int G,
+                             const float* amax_scale, uint8_t* codes_t, int64_t M_pad, int32_t* err,
+                             void* stream) {
+  // M == 0 (every group empty) is valid without an input: all M_pad columns get code 0
+  if ((M > 0 && !in) || !amax_scale || !codes_t) return PGG_ERR_INVALID_ARG;
+  if (group_lens ? (G < 1 || G > kMaxGroups) : (G != 1 && G != 0)) return PGG_ERR_INVALID_ARG;
+  if (M < 0 || M >= kMaxRows || C <= 0 || C >= ((int64_t)1 << 30)) return PGG_ERR_INVALID_ARG;
+  if (M_pad <= 0 || M_pad >= kMaxRows || M_pad % PGG_MX_PAD) return PGG_ERR_ALIGNMENT;
+  if (C % 8) return PGG_ERR_ALIGNMENT;
+  if ((M > 0 && !aligned16(in)) || !aligned16(codes_t) || !aligned16(amax_scale)) return PGG_ERR_ALIGNMENT;
+  if ((group_lens && !aligned4(group_lens)) || (err && !aligned4(err))) return PGG_ERR_ALIGNMENT;
+  return launch_fp8_quantize_colwise(in, M, C, group_lens, group_lens ? G : 1, amax_scale, codes_t, M_pad, err,
+                                     as_stream(stream));
+}
+
+size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad) {
+  if (N < 0 || K < 0 || G < 1 || M_pad < 0) return 0;
+  return mx_unit_scale_bytes(N, K, G, M_pad);
+}
+
+int pgg_fp8_grouped_gemm(int mode, const uint8_t* A, const float* scale_a, const uint8_t* B, const float* scale_b,
+                         const int32_t* group_lens, void* out, int64_t M, int64_t N, int64_t K, int G,
+                         int64_t M_pad, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+  if (!scale_a || !scale_b || !ws) return PGG_ERR_INVALID_ARG;
+  if (!aligned4(scale_a) || !aligned4(scale_b) || !aligned16(ws)) return PGG_ERR_ALIGNMENT;
+  if (N < 0 || K < 0 || M_pad < 0 || G < 1 || G > kMaxGroups) return PGG_ERR_INVALID_ARG;
+  const size_t need = mx_unit_scale_bytes(N, K, G, mode == PGG_MODE_WGRAD ? M_pad : 0);
+  if (ws_bytes < need) return PGG_ERR_INVALID_ARG;
+  // ws receives the unit block scales (E8M0 127 = 2^0) on the stream before each launch:
+  // the caller owns it and may have reused it since the last call
+  return mx_gemm_impl(mode, PGG_FMT_E4M3, PGG_EPI_NONE, A, static_cast<const uint8_t*>(ws), B,
+                      static_cast<const uint8_t*>(ws), nullptr, group_lens, out, nullptr, nullptr, nullptr, M, N, K,
+                      G, M_pad, 0.0f, err, stream, scale_a, scale_b);
+}
+
 size_t pgg_moe_permute_workspace_size(int64_t T, int E) {
   if (T < 0 || E < 1) return 0;
   return moe_permute_ws_bytes(T, E);
@@ -402,7 +462,7 @@ int pgg_moe_combine(const void* Ys, const int32_t* pos, const float* w, void* ou
   if (st) return st;
   if (T == 0) return PGG_OK;
   if (!Ys || !pos || !out) return PGG_ERR_INVALID_ARG;
-  if (!aligned16(Ys) || !aligned16(out)) return PGG_ERR_ALIGNMENT;
+  if (!aligned16(Ys) || !aligned16(out) || !aligned4(pos) || (w && !aligned4(w))) return PGG_ERR_ALIGNMENT;
   return launch_moe_combine(Ys, pos, w, T, k, H, out, as_stream(stream));
 }
 
@@ -413,7 +473,8 @@ int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, co
   if (st) return st;
   if (T == 0) return PGG_OK;
   if (!dOut || !Ys || !pos || !w || !dYs || !dw) return PGG_ERR_INVALID_ARG;
-  if (!aligned16(dOut) || !aligned16(Ys) || !aligned16(dYs)) return PGG_ERR_ALIGNMENT;
+  if (!aligned16(dOut) || !aligned16(Ys) || !aligned16(dYs) || !aligned4(pos) || !aligned4(w) || !aligned4(dw))
+    return PGG_ERR_ALIGNMENT;
   return launch_moe_combine_bwd(dOut, Ys, pos, w, T, k, H, dYs, dw, as_stream(stream));
 }
 

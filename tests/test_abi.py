@@ -41,7 +41,8 @@ def test_library_exports_every_declared_symbol(lib):
 def test_binding_signatures_cover_header():
     from precision_grouped_gemm_gb300 import _binding
     for s in declared_symbols():
-        if s not in ("pgg_status_string", "pgg_moe_permute_workspace_size"):  # non-int returns
+        if s not in ("pgg_status_string", "pgg_moe_permute_workspace_size",
+                     "pgg_fp8_workspace_size"):  # non-int returns
             assert s in _binding.SIGNATURES, s
 
 
@@ -134,3 +135,58 @@ def test_new_entry_points_host_validation_without_gpu(lib):
     assert q(g, 4, 96, 1, g, g, None) == 3          # C % 128
     assert q(g, 4, 128, 7, g, g, None) == 1         # bad format
     assert q(g, 0, 128, 1, g, g, None) == 0         # R == 0 is a no-op
+
+
+def test_fp8_entry_points_host_validation_without_gpu(lib):
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    g = 1 << 20
+    ws = lib.pgg_fp8_workspace_size
+    ws.argtypes, ws.restype = [I64, I64, I32, I64], ctypes.c_size_t
+    assert ws(4096, 4096, 256, 0) == 4 * 256 * 4096      # dgrad: G*N/128 atoms of 512 B
+    assert ws(64, 2048, 1, 0) == 4 * 2048                # fwd: K/128 atoms
+    assert ws(8, 100, 1, 0) == 512                       # rounded up to one atom
+    assert ws(64, 64, 2, 24576 + 256) == 4 * (24576 + 256)  # wgrad: M_pad/128 atoms
+    t = lib.pgg_fp8_tensor_scale
+    t.argtypes = [P, I64, P, P]
+    assert t(g, 12, g, None) == 3                        # n % 8
+    assert t(g, 16, None, None) == 1                     # no output
+    assert t(g, 16, g + 4, None) == 3                    # misaligned {s, amax}
+    r = lib.pgg_fp8_quantize_rowwise
+    r.argtypes = [P, I64, I64, P, P, P]
+    assert r(g, 4, 12, g, g, None) == 3                  # C % 8
+    assert r(g, 4, 16, None, g, None) == 1               # no scale
+    assert r(g, 0, 16, g, g, None) == 0                  # R == 0 is a no-op
+    c = lib.pgg_fp8_quantize_colwise
+    c.argtypes = [P, I64, I64, P, I32, P, P, I64, P, P]
+    assert c(g, 64, 16, g, 2, g, g, 100, None, None) == 3    # M_pad % 128
+    assert c(g, 64, 16, g + 2, 2, g, g, 128, None, None) == 3  # misaligned group_lens
+    assert c(g, 64, 16, None, 3, g, g, 128, None, None) == 1  # G > 1 without group_lens
+    f = lib.pgg_fp8_grouped_gemm
+    f.argtypes = [I32, P, P, P, P, P, P, I64, I64, I64, I32, I64, P, ctypes.c_size_t, P, P]
+    assert f(0, g, None, g, g, g, g, 64, 128, 256, 2, 0, g, 1 << 20, None, None) == 1   # no scale_a
+    assert f(0, g, g, g, g, g, g, 64, 128, 256, 2, 0, g + 8, 1 << 20, None, None) == 3  # misaligned ws
+    assert f(1, g, g, g, g, g, g, 64, 128, 256, 2, 0, g, 512, None, None) == 1        # ws < 4 G N
+    assert f(0, g, g, g, g, g, g, 64, 128, 200, 2, 0, g, 1 << 20, None, None) == 3    # fwd K % 128
+    assert f(0, g, g, g, g, g, g, 0, 128, 256, 2, 0, g, 1 << 20, None, None) == 0     # M == 0 is a no-op
+    assert f(3, g, g, g, g, g, g, 64, 128, 256, 2, 0, g, 1 << 20, None, None) == 1    # bad mode
+
+
+def test_scalar_operand_alignment_is_checked(lib):
+    # 4-byte operands read by scalar or 4-byte copies: group_lens, the row-major MX scales,
+    # the combine's positions and weights
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    g = 1 << 20
+    f = lib.pgg_grouped_gemm_fwd
+    f.argtypes = [P, P, P, P, I64, I64, I64, I32, P, P]
+    assert f(g, g, g + 2, g, 8, 64, 64, 1, None, None) == 3           # group_lens
+    mx = lib.pgg_mx_grouped_gemm
+    mx.argtypes = [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, I64, I64, I64, I32, I64, P, P]
+    assert mx(0, 1, 0, g, g + 2, g, g, None, g, g, None, None, None, 8, 64, 128, 1, 0, None, None) == 3  # SA
+    assert mx(0, 1, 0, g, g, g, g, None, g, g, None, None, None, 8, 64, 128, 1, 0, g + 1, None) == 3  # err
+    c = lib.pgg_moe_combine
+    c.argtypes = [P, P, P, P, I64, I32, I64, P]
+    assert c(g, g + 2, None, g, 8, 4, 64, None) == 3                  # pos
+    assert c(g, g, g + 1, g, 8, 4, 64, None) == 3                     # w
+    b = lib.pgg_moe_combine_bwd
+    b.argtypes = [P, P, P, P, P, P, I64, I32, I64, P]
+    assert b(g, g, g, g, g, g + 2, 8, 4, 64, None) == 3               # dw

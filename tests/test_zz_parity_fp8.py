@@ -1,0 +1,158 @@
+"""GPU FP8 tensor-wise (current scaling) path vs the oracle.
+
+The tensor scale {s, amax} and every e4m3 code are integers or decided in the
+same fp32 arithmetic on both sides: bit-exact.  The grouped GEMMs compare
+against the fp64 GEMM of the oracle's own dequantized codes at
+|gpu - ref| <= 1e-2 |ref| + 1e-2 rms(ref).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import fp8 as of8
+from precision_grouped_gemm_gb300 import workloads as wl
+import util
+
+pgg = pytest.importorskip("precision_grouped_gemm_gb300")
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _err():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _scale_pair(x_cpu):
+    """The oracle's (s, amax) of a bf16 tensor."""
+    v = util.f64(x_cpu)
+    fin = np.isfinite(v)
+    amax = float(np.max(np.abs(v[fin]))) if fin.any() else 0.0
+    return of8.fp8_tensor_scale(v), np.float32(amax)
+
+
+@pytest.mark.parametrize("R,C,std", [(1, 8, 1.0), (37, 24, 3.0), (1000, 520, 0.02), (4096, 4096, 1.0)])
+def test_fp8_tensor_scale_and_rowwise_codes(R, C, std):
+    x = util.gen(wl.KEY_X, R, C, std, R + C)
+    sc = pgg.fp8_tensor_scale(x.to(DEV))
+    s, amax = _scale_pair(x)
+    got = sc.cpu().numpy()
+    assert got[0] == s and got[1] == amax, (got, s, amax)
+    codes = pgg.fp8_quantize_rowwise(x.to(DEV), sc)
+    ref, _ = of8.fp8_quantize_tensorwise(util.f64(x), scale=s)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref)
+
+
+def test_fp8_scale_special_tensors():
+    # all zeros: s = 1, amax = 0, codes 0 (and -0 keeps its sign bit)
+    z = torch.zeros((4, 16), dtype=torch.bfloat16)
+    z[1, 3] = -0.0
+    sc = pgg.fp8_tensor_scale(z.to(DEV))
+    assert sc.cpu().tolist() == [1.0, 0.0]
+    codes = pgg.fp8_quantize_rowwise(z.to(DEV), sc).cpu().numpy()
+    assert codes[1, 3] == 0x80 and np.count_nonzero(codes) == 1
+    # Inf and NaN are left out of amax; Inf saturates to +-448 (codes compared off the NaNs)
+    x = util.gen(wl.KEY_X, 8, 32, 1.0, 5)
+    x[2, 7], x[5, 0], x[6, 31] = float("inf"), float("-inf"), float("nan")
+    sc = pgg.fp8_tensor_scale(x.to(DEV))
+    s, amax = _scale_pair(x)
+    assert sc.cpu().tolist() == [float(s), float(amax)]
+    codes = pgg.fp8_quantize_rowwise(x.to(DEV), sc).cpu().numpy()
+    ref, _ = of8.fp8_quantize_tensorwise(util.f64(x), scale=s)
+    keep = ~np.isnan(util.f64(x))
+    np.testing.assert_array_equal(codes[keep], ref[keep])
+    assert codes[2, 7] == 0x7E and codes[5, 0] == 0xFE
+    # the smallest bf16 subnormal as amax: 448 / amax overflows, s = the largest finite fp32
+    t = torch.zeros((1, 8), dtype=torch.bfloat16)
+    t[0, 0], t[0, 5] = 2.0 ** -133, -(2.0 ** -133)
+    sc = pgg.fp8_tensor_scale(t.to(DEV))
+    assert sc.cpu()[0].item() == float(np.finfo(np.float32).max)
+    assert pgg.fp8_quantize_rowwise(t.to(DEV), sc).cpu().numpy().tolist() == [[0x10, 0, 0, 0, 0, 0x90, 0, 0]]
+
+
+@pytest.mark.parametrize("lens,C,M_pad_extra", [([5, 0, 130, 1], 24, 0), ([40, 0, 157, 300, 0, 77], 520, 256),
+                                                ([128, 256], 64, 128), ([3], 8, 0)])
+def test_fp8_quantize_colwise(lens, C, M_pad_extra):
+    lens = np.asarray(lens, dtype=np.int32)
+    G, M = len(lens), int(lens.sum())
+    x = util.gen(wl.KEY_DY, M, C, 1.0, M + C)
+    gl = torch.from_numpy(lens).to(DEV)
+    M_pad = int(sum(-(-int(n) // 128) * 128 for n in lens)) + M_pad_extra
+    err = _err()
+    sc = pgg.fp8_tensor_scale(x.to(DEV))
+    ct = pgg.fp8_quantize_colwise(x.to(DEV), gl, sc, M_pad, err=err)
+    assert pgg.read_error(err) == 0
+    ref, s = of8.fp8_quantize_colwise(util.f64(x), lens, M_pad)
+    assert sc.cpu()[0].item() == float(s)
+    np.testing.assert_array_equal(ct.cpu().numpy(), ref)
+
+
+def test_fp8_colwise_pad_overflow_is_flagged():
+    lens = np.array([100, 100], dtype=np.int32)
+    x = util.gen(wl.KEY_DY, 200, 16, 1.0, 9).to(DEV)
+    err = _err()
+    sc = pgg.fp8_tensor_scale(x)
+    pgg.fp8_quantize_colwise(x, torch.from_numpy(lens).to(DEV), sc, 128, err=err)  # needs 256
+    assert pgg.read_error(err) == 18
+
+
+def _q_row(x):
+    sc = pgg.fp8_tensor_scale(x)
+    return pgg.fp8_quantize_rowwise(x, sc), sc
+
+
+@pytest.mark.parametrize("lens,N,K", [([40, 0, 157], 256, 256), ([129, 1, 300, 0, 77], 384, 512), ([5], 128, 128),
+                                      ([40, 0, 157], 328, 256),  # N off the 128-row scale atoms
+                                      ([300, 0, 129, 1, 517, 64, 1000, 3], 512, 1024)])
+def test_fp8_fwd(lens, N, K):
+    lens = np.asarray(lens, dtype=np.int32)
+    G, M = len(lens), int(lens.sum())
+    X, W = util.gen(wl.KEY_X, M, K, 1.0, 41), util.gen(wl.KEY_W1, G * N, K, 0.05, 41)
+    A, sa = _q_row(X.to(DEV))
+    B, sb = _q_row(W.to(DEV))
+    err = _err()
+    Y = pgg.fp8_grouped_gemm(pgg.MODE_FWD, A, sa, B, sb, torch.from_numpy(lens).to(DEV), M, N, K, err=err)
+    assert pgg.read_error(err) == 0
+    cx, sx = of8.fp8_quantize_tensorwise(util.f64(X))
+    cw, sw = of8.fp8_quantize_tensorwise(util.f64(W))
+    util.assert_close(Y, of8.fp8_grouped_gemm_fwd(cx, sx, cw, sw, lens, G), "fp8 fwd")
+
+
+@pytest.mark.parametrize("lens,N,K", [([40, 0, 157], 256, 256), ([129, 1, 300, 0, 77], 384, 320),
+                                      ([300, 0, 129, 1, 517, 64, 1000, 3], 512, 200)])
+def test_fp8_dgrad(lens, N, K):
+    lens = np.asarray(lens, dtype=np.int32)
+    G, M = len(lens), int(lens.sum())
+    dY, W = util.gen(wl.KEY_DY, M, N, 1.0, 42), util.gen(wl.KEY_W1, G * N, K, 0.05, 42)
+    A, sa = _q_row(dY.to(DEV))
+    Wd = W.to(DEV)
+    sw_d = pgg.fp8_tensor_scale(Wd)
+    Bt = pgg.fp8_quantize_colwise(Wd, torch.full((G,), N, dtype=torch.int32, device=DEV), sw_d, G * N)
+    err = _err()
+    dX = pgg.fp8_grouped_gemm(pgg.MODE_DGRAD, A, sa, Bt, sw_d, torch.from_numpy(lens).to(DEV), M, N, K, err=err)
+    assert pgg.read_error(err) == 0
+    cd, sd = of8.fp8_quantize_tensorwise(util.f64(dY))
+    cw, sw = of8.fp8_quantize_tensorwise(util.f64(W))
+    util.assert_close(dX, of8.fp8_grouped_gemm_dgrad(cd, sd, cw, sw, lens, G), "fp8 dgrad")
+
+
+@pytest.mark.parametrize("lens,N,K", [([40, 0, 157], 256, 256), ([129, 1, 300, 0, 77], 200, 320),
+                                      ([0, 0, 0], 64, 64), ([300, 0, 129, 1, 517, 64, 1000, 3], 512, 384)])
+def test_fp8_wgrad(lens, N, K):
+    lens = np.asarray(lens, dtype=np.int32)
+    G, M = len(lens), int(lens.sum())
+    X, dY = util.gen(wl.KEY_X, max(M, 1), K, 1.0, 43)[:M], util.gen(wl.KEY_DY, max(M, 1), N, 1.0, 43)[:M]
+    gl = torch.from_numpy(lens).to(DEV)
+    M_pad = pgg.mx_pad_rows(M, G)
+    err = _err()
+    Xd, dYd = X.contiguous().to(DEV), dY.contiguous().to(DEV)
+    sx_d, sd_d = pgg.fp8_tensor_scale(Xd), pgg.fp8_tensor_scale(dYd)
+    At = pgg.fp8_quantize_colwise(dYd, gl, sd_d, M_pad, err=err)
+    Bt = pgg.fp8_quantize_colwise(Xd, gl, sx_d, M_pad, err=err)
+    dW = pgg.fp8_grouped_gemm(pgg.MODE_WGRAD, At, sd_d, Bt, sx_d, gl, M, N, K, M_pad=M_pad, err=err)
+    assert pgg.read_error(err) == 0
+    cx, sx = of8.fp8_quantize_tensorwise(util.f64(X))
+    cd, sd = of8.fp8_quantize_tensorwise(util.f64(dY))
+    ref = of8.fp8_grouped_gemm_wgrad(cx, sx, cd, sd, lens)
+    util.assert_close(dW, ref, "fp8 wgrad")
+    for g in np.nonzero(lens == 0)[0]:
+        assert not dW[int(g)].any(), f"empty group {g} must give dW = 0"

@@ -12,7 +12,8 @@ Prints one JSON line.  `value` counts 2*M*N*K flops per GEMM (padding rows the
 MMA wastes are not counted) over all ranks divided by the slowest rank's time.
 `extra` adds the same measurement for the MXFP8 DeepSeek-shaped, GPT-OSS-shaped
 BF16 and Zipf-routed MXFP4 layers (--workload makes any of them the main line),
-the fp32 main_grad accumulation and the single-GPU MoE permute / combine.
+the fp32 main_grad accumulation and the single-GPU MoE permute / combine.  The
+DeepSeek-shaped FP8 tensor-wise layer runs only when --workload names it.
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload instead (the only other code path this file runs).
 """
@@ -279,7 +280,8 @@ def kernel_traffic(workload, name):
     return k.get("dram_bytes_per_launch")
 
 
-PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0}  # dense tensor peak vs bf16 (nominal ratios)
+PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0, "fp8": 2.0}  # dense tensor peak vs bf16 (nominal ratios)
+ARITH = {"fp8": "e4m3"}  # the operand type a layer format computes in, where the names differ
 
 
 def setup_workload(w, device, cap=0):
@@ -288,14 +290,25 @@ def setup_workload(w, device, cap=0):
     Returns (lens, bufs, step, names, work, io, err): step(bufs, between) runs one layer
     step on a buffer set; io(bufs) gives that set's (inputs, outputs) tensor lists; a
     second independent set comes from bufs.clone_empty() (for the pipelined e2e run)."""
-    from precision_grouped_gemm_gb300.layer import (MX_STEP_NAMES, STEP_NAMES, MxLayerBuffers, build_layer_inputs,
-                                                    expert_layer_step, layer_work, mx_layer_step, mx_layer_work)
+    from precision_grouped_gemm_gb300.layer import (FP8_STEP_NAMES, MX_STEP_NAMES, STEP_NAMES, Fp8LayerBuffers,
+                                                    MxLayerBuffers, build_layer_inputs, expert_layer_step,
+                                                    fp8_layer_step, fp8_layer_work, layer_work, mx_layer_step,
+                                                    mx_layer_work)
     lens, _, buf = build_layer_inputs(w, device, cap, allocate=(w.fmt == "bf16"))
     M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
     if w.fmt == "bf16":
         work = layer_work(M, G, Hd, I)
         io = lambda b: ([b.X, b.W1, b.W2, b.dY, b.group_lens], [b.Y, b.dX, b.dW1, b.dW2])
         return lens, buf, expert_layer_step, STEP_NAMES, work, io, buf.err
+    if w.fmt == "fp8":
+        fb = Fp8LayerBuffers.build(buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens, host_lens=lens)
+        del buf
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        work = fp8_layer_work(M, G, Hd, I, fb.M_pad)
+        io = lambda b: ([b.X, b.dY, b.group_lens, b.W1q, b.W1t, b.s_w1, b.W2q, b.W2t, b.s_w2],
+                        [b.bufs["Y"], b.bufs["dX"], b.bufs["dW1"], b.bufs["dW2"]])
+        return lens, fb, fp8_layer_step, FP8_STEP_NAMES, work, io, fb.bufs["err"]
     mb = MxLayerBuffers.build(w.fmt, buf.X, buf.W1, buf.W2, buf.dY, buf.group_lens, host_lens=lens)
     del buf
     torch.cuda.synchronize()
@@ -358,7 +371,7 @@ def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample
     attain = sum(max(work[n][1] / (hbm * 1e9), work[n][0] / (tc * 1e12)) for n in names)
     res = {
         "value": job_value(world, flops, ms, K), "unit": "TFLOP/s", "ms_per_step": ms / K, "steps": K,
-        "warmup": warmup, "dtype": w.fmt, "rows_M": int(lens.sum()), "group_lens_min": int(lens.min()),
+        "warmup": warmup, "dtype": ARITH.get(w.fmt, w.fmt), "rows_M": int(lens.sum()), "group_lens_min": int(lens.min()),
         "group_lens_max": int(lens.max()), "groups_under_128": int((lens < 128).sum()),
         "empty_groups": int((lens == 0).sum()),
         "pct_of_dense_peak": flops / (ms / K) / 1e9 / (peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
@@ -520,7 +533,7 @@ def run_pgg(args, w):
     line = {
         "metric": METRIC, "value": main["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": main["steps"],
         "warmup": main["warmup"], "ms_per_step": main["ms_per_step"], "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.fmt,
+        "scaling": "weak", "vs_baseline": None, "dtype": ARITH.get(w.fmt, w.fmt),
         "data": "synthetic (seeded counter-based generator; routing by top-k of softmax over generated logits)",
         "config": {"workload": w.name + (f"_first{args.experts_cap}experts" if args.experts_cap else ""),
                    "tokens": w.tokens, "experts": args.experts_cap or w.experts, "top_k": w.topk,

@@ -283,22 +283,31 @@ int pgg_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t
  * rounded up to 512 (pass M_pad = 0 outside wgrad). */
 size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad);
 
-/* FP8 tensor-wise grouped GEMM (grouped_gemm_fp8): the operands and shapes of
- * pgg_mx_grouped_gemm with fmt e4m3 and no epilogue, each operand carrying one
+/* FP8 tensor-wise grouped GEMM (grouped_gemm_fp8): the operands, shapes and
+ * epilogues of pgg_mx_grouped_gemm with fmt e4m3, each operand carrying one
  * scale instead of per-block scales:
  *   FWD    out[M, N]    = deq(A)_g . deq(B)_g^T   A = X codes [M, K], B = W codes [G*N, K]
  *   DGRAD  out[M, K]    = deq(A)_g . W_g          A = dY codes [M, N], B = W^T codes [K, G*N]
  *   WGRAD  out[G, N, K] = sum over group g's padded columns of deq(A)[:, r] deq(B)[:, r]^T
  *                         A = dY^T codes [N, M_pad], B = X^T codes [K, M_pad] (column-wise)
- * i.e. out = (sum of code products) / (s_A s_B), fp32 accumulation, bf16 out.
+ * i.e. the sum of code products divided by s_A s_B, fp32 accumulation, bf16 out.
+ * epilogue PGG_EPI_SWIGLU (fwd / dgrad, as pgg_mx_grouped_gemm): the fused
+ * GroupedMLP in FP8 ("Primus-Turbo" README, "What's New": FP8 / MXFP8 expert
+ * MLP with SwiGLU folded into the grouped GEMM).  FWD: N = 2I, out = A_act
+ * [M, I], out2 = H [M, 2I] or NULL; DGRAD: the SwiGLU backward with the saved
+ * bf16 H [M, 2K], out = dH [M, 2K].  swiglu_limit > 0 clamps as in
+ * pgg_grouped_fc1_swiglu_clamped (0: none; SwiGLU epilogue only).  There is no
+ * fused quantized output: a current-scaled operand needs the amax of the whole
+ * tensor before any of its codes.
  * scale_a / scale_b point at each operand's s (its amax_scale).  ws: device
  * scratch of pgg_fp8_workspace_size bytes, 16-byte aligned, owned by the
  * caller and overwritten on the stream by each call (it holds the unit block
  * scales the tensor cores read).  The size rules, errors and group semantics
  * are pgg_mx_grouped_gemm's (fwd K and dgrad N multiples of 128). */
-int pgg_fp8_grouped_gemm(int mode, const uint8_t* A, const float* scale_a, const uint8_t* B, const float* scale_b,
-                         const int32_t* group_lens, void* out, int64_t M, int64_t N, int64_t K, int G,
-                         int64_t M_pad, void* ws, size_t ws_bytes, int32_t* err, void* stream);
+int pgg_fp8_grouped_gemm(int mode, int epilogue, const uint8_t* A, const float* scale_a, const uint8_t* B,
+                         const float* scale_b, const void* H, const int32_t* group_lens, void* out, void* out2,
+                         int64_t M, int64_t N, int64_t K, int G, int64_t M_pad, float swiglu_limit, void* ws,
+                         size_t ws_bytes, int32_t* err, void* stream);
 
 /* ---------------------------------------------------------------- MoE glue (one GPU) */
 

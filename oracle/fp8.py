@@ -98,3 +98,17 @@ def fp8_quantize_colwise(x: np.ndarray, group_lens, M_pad: int, scale=None, P: i
         n = int(off[g + 1] - off[g])
         codes_t[:, poff[g]:poff[g] + n] = codes[off[g]:off[g + 1]].T
     return codes_t, s
+
+
+def fp8_grouped_fc1_swiglu(X, sX, W1, sW1, group_lens, G: int, limit=None):
+    """(A, H): FC1 on FP8 operands (X [M, K], W1 [G*2I, K] codes) with SwiGLU folded in;
+    H = (code products) / (s_X s_W1), A = swiglu(H) (clamped when limit is given)."""
+    H = fp8_grouped_gemm_fwd(X, sX, W1, sW1, group_lens, G)
+    return og.swiglu_fwd(H, limit), H
+
+
+def fp8_grouped_fc2_dgrad_swiglu_bwd(dY, sdY, W2, sW2, H, group_lens, G: int, limit=None):
+    """dH: FC2 dgrad on FP8 operands (dY [M, N], W2 [G*N, K] codes) followed by the SwiGLU
+    backward against the saved fp64 / bf16-valued H [M, 2K]."""
+    dA = fp8_grouped_gemm_dgrad(dY, sdY, W2, sW2, group_lens, G)
+    return og.swiglu_bwd(dA, H, limit)

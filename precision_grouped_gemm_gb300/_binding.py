@@ -43,8 +43,8 @@ SIGNATURES = {
     "pgg_fp8_tensor_scale": [_P, _I64, _P, _P],
     "pgg_fp8_quantize_rowwise": [_P, _I64, _I64, _P, _P, _P],
     "pgg_fp8_quantize_colwise": [_P, _I64, _I64, _P, _I32, _P, _P, _I64, _P, _P],
-    "pgg_fp8_grouped_gemm": [_I32, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, _P, ctypes.c_size_t,
-                             _P, _P],
+    "pgg_fp8_grouped_gemm": [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, _F32, _P,
+                             ctypes.c_size_t, _P, _P],
     "pgg_moe_combine_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I32, _I64, _P],
 }
 
@@ -347,23 +347,28 @@ def fp8_workspace_size(N: int, K: int, G: int, M_pad: int = 0) -> int:
     return lib().pgg_fp8_workspace_size(N, K, G, M_pad)
 
 
-def fp8_grouped_gemm(mode, A, scale_a, B, scale_b, group_lens, M, N, K, out=None, M_pad=0, ws=None, err=None,
-                     stream=None):
-    """FP8 tensor-wise grouped GEMM (the MX operand layouts in e4m3, one scale per operand:
-    scale_a / scale_b are the operands' amax_scale tensors; see pgg.h)."""
+def fp8_grouped_gemm(mode, A, scale_a, B, scale_b, group_lens, M, N, K, out=None, out2=None, H=None,
+                     epilogue=EPI_NONE, M_pad=0, ws=None, err=None, stream=None, swiglu_limit=0.0):
+    """FP8 tensor-wise grouped GEMM: the MX operand layouts and epilogues in e4m3, one scale per
+    operand (scale_a / scale_b are the operands' amax_scale tensors; see pgg.h)."""
     G = group_lens.numel()
     dev = A.device
     if out is None:
-        shape = (M, N) if mode == MODE_FWD else (M, K) if mode == MODE_DGRAD else (G, N, K)
+        if mode == MODE_FWD:
+            shape = (M, N // 2) if epilogue == EPI_SWIGLU else (M, N)
+        elif mode == MODE_DGRAD:
+            shape = (M, 2 * K) if epilogue == EPI_SWIGLU else (M, K)
+        else:
+            shape = (G, N, K)
         out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     need = fp8_workspace_size(N, K, G, M_pad if mode == MODE_WGRAD else 0)
     if ws is None:
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
-    _dev(A, scale_a, B, scale_b, group_lens, out, ws, err)
-    _check(lib().pgg_fp8_grouped_gemm(mode, _ptr(A), _ptr(scale_a), _ptr(B), _ptr(scale_b),
-                                      _ptr(_lens(group_lens)), _ptr(out), M, N, K, G, M_pad, _ptr(ws),
-                                      ws.numel() * ws.element_size(), _ptr(err), _stream(stream)),
-           "pgg_fp8_grouped_gemm")
+    _dev(A, scale_a, B, scale_b, group_lens, out, out2, H, ws, err)
+    _check(lib().pgg_fp8_grouped_gemm(mode, epilogue, _ptr(A), _ptr(scale_a), _ptr(B), _ptr(scale_b), _ptr(H),
+                                      _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), M, N, K, G, M_pad,
+                                      swiglu_limit, _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
+                                      _stream(stream)), "pgg_fp8_grouped_gemm")
     return out
 
 

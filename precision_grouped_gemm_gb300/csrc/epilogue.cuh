@@ -106,11 +106,11 @@ __device__ __forceinline__ void mx_emit(const float* v, uint8_t* codes, uint8_t*
 // pre-activation H[row, col0 + c] = gate, H[row, I + col0 + c] = up when H != null.
 // QF != 0 and qcodes != null: A is also emitted MX-quantized (row-wise, I % 32 == 0).
 // limit > 0 clamps first: gate <- min(gate, limit), up <- clamp(up, -limit, limit); H
-// keeps the values before the clamp.
-template <int BN, int QF = 0>
+// keeps the values before the clamp.  SCALED: gate and up are the accumulators times alpha.
+template <int BN, int QF = 0, bool SCALED = false>
 __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t grow,
                                            bool row_ok, int col0, int I, uint8_t* qcodes = nullptr,
-                                           uint8_t* qscales = nullptr, float limit = 0.0f) {
+                                           uint8_t* qscales = nullptr, float limit = 0.0f, float alpha = 1.0f) {
 #pragma unroll 1
   for (int c = 0; c < BN / 64; ++c) {
     uint32_t rg[32], ru[32];
@@ -124,6 +124,10 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
       for (int j = 0; j < 32; ++j) {
         g[j] = __uint_as_float(rg[j]);
         u[j] = __uint_as_float(ru[j]);
+        if constexpr (SCALED) {
+          g[j] *= alpha;
+          u[j] *= alpha;
+        }
         const float gc = limit > 0.0f ? fminf(g[j], limit) : g[j];
         const float uc = limit > 0.0f ? fminf(fmaxf(u[j], -limit), limit) : u[j];
         a[j] = silu_f(gc) * uc;
@@ -177,12 +181,13 @@ __device__ __forceinline__ void load_raw32(const __nv_bfloat16* src, uint4 (&w)[
 }
 
 // limit > 0: the forward's clamp is applied to the saved g, u again, and the gradient
-// is zero where a clamp was active (g > limit, |u| > limit).
-template <int BN, int QF = 0>
+// is zero where a clamp was active (g > limit, |u| > limit).  SCALED: dA is the
+// accumulator times alpha.
+template <int BN, int QF = 0, bool SCALED = false>
 __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
                                                size_t grow, bool row_ok, int col0, int I,
                                                uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr,
-                                               float limit = 0.0f) {
+                                               float limit = 0.0f, float alpha = 1.0f) {
   const __nv_bfloat16* hrow = H + grow * (2 * (size_t)I);
   uint4 ng[4], nu[4];  // the next chunk's gate / up words
   if (row_ok && col0 < I) {
@@ -214,7 +219,7 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
       for (int j = 0; j < 32; ++j) {
         float hg = (j & 1) ? bf16_hi(pg[j >> 1]) : bf16_lo(pg[j >> 1]);
         float hu = (j & 1) ? bf16_hi(pu[j >> 1]) : bf16_lo(pu[j >> 1]);
-        const float da = __uint_as_float(rd[j]);
+        const float da = SCALED ? __uint_as_float(rd[j]) * alpha : __uint_as_float(rd[j]);
         bool pass_g = true, pass_u = true;
         if (limit > 0.0f) {
           pass_g = hg <= limit;

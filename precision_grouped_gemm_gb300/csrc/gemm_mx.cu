@@ -21,7 +21,8 @@
 // FP8 tensor-wise operands (one fp32 scale s per tensor, codes = e4m3(x s)) run the
 // e4m3 instantiations with TS = true: every block scale is 1 (E8M0 127), read from a
 // small constant buffer through zero row strides (each tile reads the same atoms), and
-// the epilogue multiplies the accumulator by 1 / (s_A s_B).
+// the epilogue multiplies the accumulator by 1 / (s_A s_B) before the store or the
+// SwiGLU (forward) / SwiGLU backward (dgrad).
 #include <algorithm>
 
 #include "epilogue.cuh"
@@ -149,7 +150,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                            const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
   using C = MxCfg<FMT>;
   static_assert(BN == 128 || BN == 256, "BN");
-  static_assert(!TS || (FMT == kE4M3 && EPI == kEpiStore), "per-tensor scales: e4m3, plain store");
+  static_assert(!TS || FMT == kE4M3, "per-tensor scales are e4m3");
   using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
   constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
   constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
@@ -443,11 +444,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
-        epi_swiglu<BN, FMT>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I,
-                            args.q_codes, args.q_scales, args.swiglu_limit);
+        epi_swiglu<BN, FMT, TS>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0,
+                                args.I, args.q_codes, args.q_scales, args.swiglu_limit, alpha);
       } else if (EPI == kEpiSwiGLUBwd) {
-        epi_swiglu_bwd<BN, FMT>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
-                                args.I, args.q_codes, args.q_scales, args.swiglu_limit);
+        epi_swiglu_bwd<BN, FMT, TS>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok,
+                                    T.col0, args.I, args.q_codes, args.q_scales, args.swiglu_limit, alpha);
       } else {
         epi_store<BN, TS>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols, alpha);
       }
@@ -500,15 +501,17 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   return PGG_ERR_INVALID_ARG;
 }
 
-// FP8 tensor-wise operands: the e4m3 tiles and stage counts of dispatch_mx, plain store.
-int dispatch_ts(int mode, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a,
-                int grid, cudaStream_t s) {
+// FP8 tensor-wise operands: the e4m3 tiles, stage counts and epilogues of dispatch_mx.
+int dispatch_ts(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kBN = kMxFwdBNE4M3, kWBN = kMxWgradBNE4M3;
   constexpr int kS = kBN == 128 ? 6 : 4;
   constexpr int kSw = kWBN == 128 ? 5 : 2;
-  if (mode == 0) return run_mx<kE4M3, kFwd, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
-  if (mode == 1) return run_mx<kE4M3, kDgrad, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
-  if (mode == 2) return run_mx<kE4M3, kWgrad, kEpiStore, kSw, kWBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 0) return run_mx<kE4M3, kFwd, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 1) return run_mx<kE4M3, kFwd, kEpiSwiGLU, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 0) return run_mx<kE4M3, kDgrad, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<kE4M3, kDgrad, kEpiSwiGLUBwd, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 2 && epi == 0) return run_mx<kE4M3, kWgrad, kEpiStore, kSw, kWBN, true>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
 
@@ -543,7 +546,7 @@ int launch_mx_gemm(const MxCall& c) {
   a.ts_a = c.ts_a;
   a.ts_b = c.ts_b;
   const bool ts = c.ts_a != nullptr;
-  if (ts && (!e4 || c.epi != 0 || !c.ts_b)) return PGG_ERR_INVALID_ARG;
+  if (ts && (!e4 || !c.ts_b || c.q_codes)) return PGG_ERR_INVALID_ARG;
   const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {
@@ -611,7 +614,7 @@ int launch_mx_gemm(const MxCall& c) {
     if (e != cudaSuccess) return cuda_status(e);
     a.SA = a.SB = c.SA;
     a.sa_ld = a.sb_ld = 0;
-    return dispatch_ts(c.mode, ta, tb, tc, a, grid, c.stream);
+    return dispatch_ts(c.mode, c.epi, ta, tb, tc, a, grid, c.stream);
   }
   return e4 ? dispatch_mx<kE4M3>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream)
             : dispatch_mx<2>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream);

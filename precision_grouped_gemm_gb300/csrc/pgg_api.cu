@@ -410,19 +410,22 @@ size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad) {
   return mx_unit_scale_bytes(N, K, G, M_pad);
 }
 
-int pgg_fp8_grouped_gemm(int mode, const uint8_t* A, const float* scale_a, const uint8_t* B, const float* scale_b,
-                         const int32_t* group_lens, void* out, int64_t M, int64_t N, int64_t K, int G,
-                         int64_t M_pad, void* ws, size_t ws_bytes, int32_t* err, void* stream) {
+int pgg_fp8_grouped_gemm(int mode, int epilogue, const uint8_t* A, const float* scale_a, const uint8_t* B,
+                         const float* scale_b, const void* H, const int32_t* group_lens, void* out, void* out2,
+                         int64_t M, int64_t N, int64_t K, int G, int64_t M_pad, float swiglu_limit, void* ws,
+                         size_t ws_bytes, int32_t* err, void* stream) {
   if (!scale_a || !scale_b || !ws) return PGG_ERR_INVALID_ARG;
   if (!aligned4(scale_a) || !aligned4(scale_b) || !aligned16(ws)) return PGG_ERR_ALIGNMENT;
+  if (!(swiglu_limit >= 0.0f) || swiglu_limit > 3.0e38f) return PGG_ERR_INVALID_ARG;
+  if (swiglu_limit > 0.0f && epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
   if (N < 0 || K < 0 || M_pad < 0 || G < 1 || G > kMaxGroups) return PGG_ERR_INVALID_ARG;
   const size_t need = mx_unit_scale_bytes(N, K, G, mode == PGG_MODE_WGRAD ? M_pad : 0);
   if (ws_bytes < need) return PGG_ERR_INVALID_ARG;
   // ws receives the unit block scales (E8M0 127 = 2^0) on the stream before each launch:
   // the caller owns it and may have reused it since the last call
-  return mx_gemm_impl(mode, PGG_FMT_E4M3, PGG_EPI_NONE, A, static_cast<const uint8_t*>(ws), B,
-                      static_cast<const uint8_t*>(ws), nullptr, group_lens, out, nullptr, nullptr, nullptr, M, N, K,
-                      G, M_pad, 0.0f, err, stream, scale_a, scale_b);
+  return mx_gemm_impl(mode, PGG_FMT_E4M3, epilogue, A, static_cast<const uint8_t*>(ws), B,
+                      static_cast<const uint8_t*>(ws), H, group_lens, out, out2, nullptr, nullptr, M, N, K, G,
+                      M_pad, swiglu_limit, err, stream, scale_a, scale_b);
 }
 
 size_t pgg_moe_permute_workspace_size(int64_t T, int E) {

@@ -266,3 +266,147 @@ def mx_layer_work(fmt: str, M: int, G: int, Hd: int, I: int, M_pad: int) -> dict
         "q_x_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),
         "fc1_wgrad": (f1, (2 * I + Hd) * M_pad * q + W1 * 2 + lens),
     }
+
+
+# ----------------------------------------------------------------------------
+# FP8 tensor-wise (current scaling) expert layer
+# ----------------------------------------------------------------------------
+
+FP8_STEP_NAMES = ("s_x", "q_x_row", "fc1_fwd_swiglu", "s_a", "q_a_row", "fc2_fwd", "s_dy", "q_dy_row",
+                  "fc2_dgrad_swiglu_bwd", "q_dy_col", "q_a_col", "fc2_wgrad", "s_dh", "q_dh_row", "fc1_dgrad",
+                  "q_dh_col", "q_x_col", "fc1_wgrad")
+
+
+@dataclasses.dataclass
+class Fp8LayerBuffers:
+    """FP8 tensor-wise expert layer: bf16 activations; the weights quantized once with their
+    own tensor scales (the caller's weight cache); every activation and gradient operand
+    re-scaled (amax of the whole tensor) and re-quantized each step, as current scaling
+    requires."""
+    X: torch.Tensor
+    dY: torch.Tensor
+    group_lens: torch.Tensor
+    W1q: torch.Tensor = None   # row-wise codes [G*2I, H] (fc1 fwd)
+    W1t: torch.Tensor = None   # column-wise codes [H, G*2I] (fc1 dgrad)
+    s_w1: torch.Tensor = None  # {s, amax} of W1
+    W2q: torch.Tensor = None   # row-wise codes [G*H, I] (fc2 fwd)
+    W2t: torch.Tensor = None   # column-wise codes [I, G*H] (fc2 dgrad)
+    s_w2: torch.Tensor = None
+    M_pad: int = 0
+    bufs: dict = None
+
+    def clone_empty(self):
+        """An independent buffer set of the same shapes (inputs and weight caches uninitialised)."""
+        e = lambda t: torch.empty_like(t)
+        c = Fp8LayerBuffers(e(self.X), e(self.dY), self.group_lens.clone())
+        c.W1q, c.W1t, c.s_w1 = e(self.W1q), e(self.W1t), e(self.s_w1)
+        c.W2q, c.W2t, c.s_w2 = e(self.W2q), e(self.W2t), e(self.s_w2)
+        c.M_pad = self.M_pad
+        c.bufs = {k: e(v) for k, v in self.bufs.items()}
+        c.bufs["err"].zero_()
+        return c
+
+    @staticmethod
+    def build(X, W1, W2, dY, group_lens, host_lens=None):
+        """Quantize the weights (outside any timed region) and allocate every step buffer;
+        host_lens as MxLayerBuffers.build."""
+        G, I2, Hd = W1.shape
+        I = I2 // 2
+        M = X.shape[0]
+        dev = X.device
+        b = Fp8LayerBuffers(X, dY, group_lens)
+        W1f, W2f = W1.reshape(G * I2, Hd), W2.reshape(G * Hd, I)
+        b.s_w1 = B.fp8_tensor_scale(W1f)
+        b.W1q = B.fp8_quantize_rowwise(W1f, b.s_w1)
+        b.W1t = B.fp8_quantize_colwise(W1f, torch.full((G,), I2, dtype=torch.int32, device=dev), b.s_w1, G * I2)
+        b.s_w2 = B.fp8_tensor_scale(W2f)
+        b.W2q = B.fp8_quantize_rowwise(W2f, b.s_w2)
+        b.W2t = B.fp8_quantize_colwise(W2f, torch.full((G,), Hd, dtype=torch.int32, device=dev), b.s_w2, G * Hd)
+        if host_lens is not None:
+            b.M_pad = max(B.PAD, int(sum(-(-int(n) // B.PAD) * B.PAD for n in host_lens)))
+        else:
+            b.M_pad = B.mx_pad_rows(M, G)
+        Mp = b.M_pad
+        ws = max(B.fp8_workspace_size(I2, Hd, G), B.fp8_workspace_size(Hd, I, G),
+                 B.fp8_workspace_size(Hd, I, G, Mp), B.fp8_workspace_size(I2, Hd, G, Mp))
+        u8, bf, f32 = torch.uint8, torch.bfloat16, torch.float32
+        e = lambda *s: torch.empty(s, dtype=u8, device=dev)
+        t = lambda *s: torch.empty(s, dtype=bf, device=dev)
+        sc = lambda: torch.empty(2, dtype=f32, device=dev)
+        b.bufs = {
+            "sx": sc(), "Xq": e(M, Hd), "A": t(M, I), "H": t(M, I2), "sa": sc(), "Aq": e(M, I), "Y": t(M, Hd),
+            "sdy": sc(), "dYq": e(M, Hd), "dH": t(M, I2), "dYc": e(Hd, Mp), "Ac": e(I, Mp), "dW2": t(G, Hd, I),
+            "sdh": sc(), "dHq": e(M, I2), "dX": t(M, Hd), "dHc": e(I2, Mp), "Xc": e(Hd, Mp), "dW1": t(G, I2, Hd),
+            "ws": e(ws), "err": torch.zeros(1, dtype=torch.int32, device=dev),
+        }
+        return b
+
+
+def fp8_layer_step(b: Fp8LayerBuffers, between=None):
+    """One FP8 tensor-wise expert-layer fwd + bwd: 4 tensor scales, 8 quantizations and 6 grouped
+    GEMMs (FC1 and FC2-dgrad with the SwiGLU and its backward in the epilogue)."""
+    u, gl = b.bufs, b.group_lens
+    err, Mp, ws = u["err"], b.M_pad, u["ws"]
+    M, Hd = b.X.shape
+    I = u["A"].shape[1]
+    G = gl.numel()
+    g = B.fp8_grouped_gemm
+    calls = (
+        lambda: B.fp8_tensor_scale(b.X, u["sx"]),
+        lambda: B.fp8_quantize_rowwise(b.X, u["sx"], u["Xq"]),
+        lambda: g(B.MODE_FWD, u["Xq"], u["sx"], b.W1q, b.s_w1, gl, M, 2 * I, Hd, out=u["A"], out2=u["H"],
+                  epilogue=B.EPI_SWIGLU, ws=ws, err=err),
+        lambda: B.fp8_tensor_scale(u["A"], u["sa"]),
+        lambda: B.fp8_quantize_rowwise(u["A"], u["sa"], u["Aq"]),
+        lambda: g(B.MODE_FWD, u["Aq"], u["sa"], b.W2q, b.s_w2, gl, M, Hd, I, out=u["Y"], ws=ws, err=err),
+        lambda: B.fp8_tensor_scale(b.dY, u["sdy"]),
+        lambda: B.fp8_quantize_rowwise(b.dY, u["sdy"], u["dYq"]),
+        lambda: g(B.MODE_DGRAD, u["dYq"], u["sdy"], b.W2t, b.s_w2, gl, M, Hd, I, out=u["dH"], H=u["H"],
+                  epilogue=B.EPI_SWIGLU, ws=ws, err=err),
+        lambda: B.fp8_quantize_colwise(b.dY, gl, u["sdy"], Mp, u["dYc"], err=err),
+        lambda: B.fp8_quantize_colwise(u["A"], gl, u["sa"], Mp, u["Ac"], err=err),
+        lambda: g(B.MODE_WGRAD, u["dYc"], u["sdy"], u["Ac"], u["sa"], gl, M, Hd, I, out=u["dW2"], M_pad=Mp, ws=ws,
+                  err=err),
+        lambda: B.fp8_tensor_scale(u["dH"], u["sdh"]),
+        lambda: B.fp8_quantize_rowwise(u["dH"], u["sdh"], u["dHq"]),
+        lambda: g(B.MODE_DGRAD, u["dHq"], u["sdh"], b.W1t, b.s_w1, gl, M, 2 * I, Hd, out=u["dX"], ws=ws, err=err),
+        lambda: B.fp8_quantize_colwise(u["dH"], gl, u["sdh"], Mp, u["dHc"], err=err),
+        lambda: B.fp8_quantize_colwise(b.X, gl, u["sx"], Mp, u["Xc"], err=err),
+        lambda: g(B.MODE_WGRAD, u["dHc"], u["sdh"], u["Xc"], u["sx"], gl, M, 2 * I, Hd, out=u["dW1"], M_pad=Mp,
+                  ws=ws, err=err),
+    )
+    assert len(calls) == len(FP8_STEP_NAMES) and G > 0
+    for i, c in enumerate(calls):
+        if between:
+            between(i)
+        c()
+    if between:
+        between(len(calls))
+
+
+def fp8_layer_work(M: int, G: int, Hd: int, I: int, M_pad: int) -> dict:
+    """Algorithmic flops and bytes of each FP8-layer call: codes at 1 B per element, bf16
+    activations and outputs at 2; a tensor scale reads its tensor once."""
+    f1, f2 = 2.0 * M * 2 * I * Hd, 2.0 * M * Hd * I
+    W1, W2 = G * 2 * I * Hd, G * Hd * I       # elements
+    lens = 4 * G
+    return {
+        "s_x": (0.0, M * Hd * 2),
+        "q_x_row": (0.0, M * Hd * 3),
+        "fc1_fwd_swiglu": (f1, M * Hd + W1 + M * I * 2 + M * 2 * I * 2 + lens),
+        "s_a": (0.0, M * I * 2),
+        "q_a_row": (0.0, M * I * 3),
+        "fc2_fwd": (f2, M * I + W2 + M * Hd * 2 + lens),
+        "s_dy": (0.0, M * Hd * 2),
+        "q_dy_row": (0.0, M * Hd * 3),
+        "fc2_dgrad_swiglu_bwd": (f2, M * Hd + W2 + M * 2 * I * 2 + M * 2 * I * 2 + lens),
+        "q_dy_col": (0.0, M * Hd * 2 + Hd * M_pad + lens),
+        "q_a_col": (0.0, M * I * 2 + I * M_pad + lens),
+        "fc2_wgrad": (f2, (Hd + I) * M_pad + W2 * 2 + lens),
+        "s_dh": (0.0, M * 2 * I * 2),
+        "q_dh_row": (0.0, M * 2 * I * 3),
+        "fc1_dgrad": (f1, M * 2 * I + W1 + M * Hd * 2 + lens),
+        "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M_pad + lens),
+        "q_x_col": (0.0, M * Hd * 2 + Hd * M_pad + lens),
+        "fc1_wgrad": (f1, (2 * I + Hd) * M_pad + W1 * 2 + lens),
+    }

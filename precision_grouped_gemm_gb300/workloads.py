@@ -149,13 +149,13 @@ def lens_tiny(seed: int, G: int = 4, M: int = 512) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
-# the five workloads
+# the workloads
 # ----------------------------------------------------------------------------
 
 @dataclasses.dataclass(frozen=True)
 class Workload:
     name: str
-    fmt: str            # "bf16", "e4m3" or "e2m1"
+    fmt: str            # "bf16", "e4m3", "e2m1" (MX block scales) or "fp8" (e4m3, one scale per tensor)
     hidden: int         # K of FC1, N of FC2
     inter: int          # I (FC1 produces 2I = gate | up)
     experts: int
@@ -203,8 +203,11 @@ GPTOSS_BF16 = Workload("gptoss20b_moe_bf16_h2880_e32_top4_t8192_i2880", "bf16", 
                        32, 8192, 4, seed=3, routing="softmax", blocked=_gptoss_blocked(3))
 ZIPF_MXFP4 = Workload("zipf_moe_mxfp4_h4096_e256_top8_t16384_i2048", "e2m1", 4096, 2048,
                       256, 16384, 8, seed=4, routing="zipf", zipf_s=1.2)
+# the DeepSeek-shaped layer in FP8 with one current-scaling scale per tensor
+DSV4_FP8 = Workload("dsv4flash_moe_fp8_h4096_e256_top6_t4096_i2048", "fp8", 4096, 2048,
+                    256, 4096, 6, seed=1, routing="softmax")
 
-WORKLOADS = {w.name: w for w in (TINY, DSV4_BF16, DSV4_MXFP8, GPTOSS_BF16, ZIPF_MXFP4)}
+WORKLOADS = {w.name: w for w in (TINY, DSV4_BF16, DSV4_MXFP8, GPTOSS_BF16, ZIPF_MXFP4, DSV4_FP8)}
 
 
 def layer_flops(lens: np.ndarray, hidden: int, inter: int) -> dict:

@@ -162,13 +162,23 @@ def test_fp8_entry_points_host_validation_without_gpu(lib):
     assert c(g, 64, 16, g + 2, 2, g, g, 128, None, None) == 3  # misaligned group_lens
     assert c(g, 64, 16, None, 3, g, g, 128, None, None) == 1  # G > 1 without group_lens
     f = lib.pgg_fp8_grouped_gemm
-    f.argtypes = [I32, P, P, P, P, P, P, I64, I64, I64, I32, I64, P, ctypes.c_size_t, P, P]
-    assert f(0, g, None, g, g, g, g, 64, 128, 256, 2, 0, g, 1 << 20, None, None) == 1   # no scale_a
-    assert f(0, g, g, g, g, g, g, 64, 128, 256, 2, 0, g + 8, 1 << 20, None, None) == 3  # misaligned ws
-    assert f(1, g, g, g, g, g, g, 64, 128, 256, 2, 0, g, 512, None, None) == 1        # ws < 4 G N
-    assert f(0, g, g, g, g, g, g, 64, 128, 200, 2, 0, g, 1 << 20, None, None) == 3    # fwd K % 128
-    assert f(0, g, g, g, g, g, g, 0, 128, 256, 2, 0, g, 1 << 20, None, None) == 0     # M == 0 is a no-op
-    assert f(3, g, g, g, g, g, g, 64, 128, 256, 2, 0, g, 1 << 20, None, None) == 1    # bad mode
+    f.argtypes = [I32, I32, P, P, P, P, P, P, P, P, I64, I64, I64, I32, I64, ctypes.c_float, P, ctypes.c_size_t,
+                  P, P]
+    ok = dict(mode=0, epi=0, sa=g, ws=g, wsb=1 << 20, K=256, M=64, lim=0.0)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["mode"], a["epi"], g, a["sa"], g, g, None, g, g, None, a["M"], 128, a["K"], 2, 0, a["lim"],
+                 a["ws"], a["wsb"], None, None)
+    assert call(sa=None) == 1                    # no scale_a
+    assert call(ws=g + 8) == 3                   # misaligned ws
+    assert call(mode=1, wsb=512) == 1            # ws < 4 G N
+    assert call(K=200) == 3                      # fwd K % 128
+    assert call(M=0) == 0                        # M == 0 is a no-op
+    assert call(mode=3) == 1                     # bad mode
+    assert call(lim=1.0) == 1                    # a clamp limit needs the SwiGLU epilogue
+    assert call(epi=1, lim=-1.0) == 1            # negative limit
+    assert call(mode=2, epi=1) == 1              # no SwiGLU wgrad
 
 
 def test_scalar_operand_alignment_is_checked(lib):

@@ -14,7 +14,7 @@ if ROOT not in sys.path:
 
 import bench  # noqa: E402
 from precision_grouped_gemm_gb300 import workloads as wl  # noqa: E402
-from precision_grouped_gemm_gb300.layer import layer_work, mx_layer_work  # noqa: E402
+from precision_grouped_gemm_gb300.layer import FP8_STEP_NAMES, fp8_layer_work, layer_work, mx_layer_work  # noqa: E402
 
 
 def test_bf16_layer_work_deepseek_shape():
@@ -46,6 +46,22 @@ def test_mx_layer_work_matches_bf16_flops_and_scales_bytes(fmt, c):
         (M * Hd + W1) * (q - 2) + M * I * q)
     # the column-wise quantizers read bf16 and write the padded transposed codes
     assert mx["q_x_col"][1] == M * Hd * 2 + Hd * M_pad * q + 4 * G
+
+
+def test_fp8_layer_work_matches_mxfp8_without_scales():
+    # the FP8 tensor-wise layer does the same GEMMs as MXFP8 with no per-block scale bytes, plus
+    # one read of each current-scaled tensor for its amax
+    M, G, Hd, I = 24576, 256, 4096, 2048
+    M_pad = G * 128
+    f8, mx = fp8_layer_work(M, G, Hd, I, M_pad), mx_layer_work("e4m3", M, G, Hd, I, M_pad)
+    assert tuple(f8) == FP8_STEP_NAMES
+    assert sum(v[0] for v in f8.values()) == pytest.approx(sum(v[0] for v in mx.values()))
+    W1 = G * 2 * I * Hd
+    assert f8["fc1_fwd_swiglu"][1] == M * Hd + W1 + M * I * 2 + M * 2 * I * 2 + 4 * G
+    assert mx["fc1_dgrad"][1] - f8["fc1_dgrad"][1] == pytest.approx((M * 2 * I + W1) / 32)
+    assert f8["q_x_col"][1] == M * Hd * 2 + Hd * M_pad + 4 * G
+    assert sum(f8[n][1] for n in ("s_x", "s_a", "s_dy", "s_dh")) == 2 * M * (Hd + I + Hd + 2 * I)
+    assert bench.PEAK_RATIO["fp8"] == bench.PEAK_RATIO["e4m3"] and bench.ARITH["fp8"] == "e4m3"
 
 
 def test_kernel_traffic_only_for_matching_sources(tmp_path, monkeypatch):

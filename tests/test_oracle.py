@@ -655,3 +655,34 @@ def test_fp8_colwise_is_the_group_padded_transpose():
             for c in range(C):
                 assert ct[c, poff[g] + i] == codes[off[g] + i, c]
     assert not ct[:, ~used].any()
+
+
+def test_fp8_swiglu_gemms_lossless_operands():
+    # lossless FP8 operands (e4m3 grid values times 2^-6, amax 7: s = 64) make the FP8 SwiGLU
+    # GEMMs equal the fp64 BF16-path oracle on the original values, clamp included
+    rng = np.random.default_rng(34)
+    grid = omx.decode_e4m3(np.arange(0x7F))
+
+    def on_grid(shape):
+        v = grid[rng.integers(0, len(grid), size=shape)] * np.where(rng.random(shape) < 0.5, -1, 1) / 64.0
+        v.flat[0] = 448.0 / 64.0
+        return v
+
+    G, I, K = 2, 3, 5
+    lens = np.array([3, 4], dtype=np.int32)
+    M = int(lens.sum())
+    X, W1 = on_grid((M, K)), on_grid((G * 2 * I, K))
+    (cx, sx), (cw, sw) = of8.fp8_quantize_tensorwise(X), of8.fp8_quantize_tensorwise(W1)
+    assert sx == sw == np.float32(64.0)
+    for limit in (None, 7.0):
+        A, H = of8.fp8_grouped_fc1_swiglu(cx, sx, cw, sw, lens, G, limit)
+        rA, rH = og.grouped_fc1_swiglu(X, W1.reshape(G, 2 * I, K), lens, limit)
+        np.testing.assert_allclose(H, rH, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(A, rA, rtol=1e-13, atol=1e-13)
+    dY, W2 = on_grid((M, 4)), on_grid((G * 4, I))
+    (cd, sd), (cw2, sw2) = of8.fp8_quantize_tensorwise(dY), of8.fp8_quantize_tensorwise(W2)
+    Hs = rng.standard_normal((M, 2 * I))
+    dH = of8.fp8_grouped_fc2_dgrad_swiglu_bwd(cd, sd, cw2, sw2, Hs, lens, G, 0.5)
+    ref = og.grouped_fc2_dgrad_swiglu_bwd(dY, W2.reshape(G, 4, I), Hs, lens, 0.5)
+    np.testing.assert_allclose(dH, ref, rtol=1e-13, atol=1e-13)
+    assert (dH == 0).any()                  # the clamp at 0.5 zeroes some gradients

@@ -156,3 +156,38 @@ def test_fp8_wgrad(lens, N, K):
     util.assert_close(dW, ref, "fp8 wgrad")
     for g in np.nonzero(lens == 0)[0]:
         assert not dW[int(g)].any(), f"empty group {g} must give dW = 0"
+
+
+@pytest.mark.parametrize("I,limit", [(192, 0.0), (256, 0.75)])
+def test_fp8_swiglu_fwd_bwd(I, limit):
+    # the fused GroupedMLP epilogues on FP8 operands; I = 192 takes the weights' scale atoms row
+    # by row (gate / up halves off the 128-row atoms), limit > 0 the clamped SwiGLU
+    lens = np.array([70, 0, 190], dtype=np.int32)
+    G, M, K, Hd = 3, 260, 256, 256
+    gl = torch.from_numpy(lens).to(DEV)
+    X, W1 = util.gen(wl.KEY_X, M, K, 1.0, 44), util.gen(wl.KEY_W1, G * 2 * I, K, 0.1, 44)
+    A, sa = _q_row(X.to(DEV))
+    B, sb = _q_row(W1.to(DEV))
+    H = torch.empty((M, 2 * I), dtype=torch.bfloat16, device=DEV)
+    err = _err()
+    Aout = pgg.fp8_grouped_gemm(pgg.MODE_FWD, A, sa, B, sb, gl, M, 2 * I, K, out2=H, epilogue=pgg.EPI_SWIGLU,
+                                err=err, swiglu_limit=limit)
+    assert pgg.read_error(err) == 0
+    cx, sx = of8.fp8_quantize_tensorwise(util.f64(X))
+    cw, sw = of8.fp8_quantize_tensorwise(util.f64(W1))
+    rA, rH = of8.fp8_grouped_fc1_swiglu(cx, sx, cw, sw, lens, G, limit or None)
+    util.assert_close(H, rH, "fp8 fc1 H")
+    util.assert_close(Aout, rA, "fp8 fc1 swiglu")
+    dY, W2 = util.gen(wl.KEY_DY, M, Hd, 1.0, 45), util.gen(wl.KEY_W2, G * Hd, I, 0.1, 45)
+    Hs = util.gen(wl.KEY_H, M, 2 * I, 1.0, 45)
+    Ad, sad = _q_row(dY.to(DEV))
+    W2d = W2.to(DEV)
+    sw2 = pgg.fp8_tensor_scale(W2d)
+    Bt = pgg.fp8_quantize_colwise(W2d, torch.full((G,), Hd, dtype=torch.int32, device=DEV), sw2, G * Hd)
+    dH = pgg.fp8_grouped_gemm(pgg.MODE_DGRAD, Ad, sad, Bt, sw2, gl, M, Hd, I, H=Hs.to(DEV),
+                              epilogue=pgg.EPI_SWIGLU, err=err, swiglu_limit=limit)
+    assert pgg.read_error(err) == 0
+    cd, sd = of8.fp8_quantize_tensorwise(util.f64(dY))
+    cw2, s2 = of8.fp8_quantize_tensorwise(util.f64(W2))
+    ref = of8.fp8_grouped_fc2_dgrad_swiglu_bwd(cd, sd, cw2, s2, util.f64(Hs), lens, G, limit or None)
+    util.assert_close(dH, ref, "fp8 fc2 dgrad swiglu bwd")

@@ -244,9 +244,10 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
 // is clamped to the largest finite fp32), codes = e4m3 RNE of the fp32 product x s,
 // saturating.  amax_scale is a device float[2] = {s, amax}; while the amax kernel runs,
 // word 1 holds the largest finite bf16 magnitude as bits (their integer order is the
-// values' order), one atomicMax per warp.
+// values' order), one atomicMax per block after a shared-memory reduction.
 __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ in, int64_t n_chunks,
                                                        uint32_t* __restrict__ amax_bits) {
+  __shared__ uint32_t s_max[256 / 32];
   uint32_t am = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
@@ -260,7 +261,13 @@ __global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__
     }
   }
   am = __reduce_max_sync(0xffffffffu, am);
-  if ((threadIdx.x & 31) == 0 && am != 0u) atomicMax(amax_bits, am);
+  if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = am;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    am = threadIdx.x < (blockDim.x >> 5) ? s_max[threadIdx.x] : 0u;
+    am = __reduce_max_sync(0xffffffffu, am);
+    if (threadIdx.x == 0 && am != 0u) atomicMax(amax_bits, am);
+  }
 }
 
 __global__ void fp8_scale_kernel(float* amax_scale) {

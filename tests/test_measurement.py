@@ -112,3 +112,18 @@ def test_clock_samples_parse_reasons_and_median():
     bad = bench.parse_clock_samples("0, 1400, 2070, 900, 0x8, Active, Not Active, Not Active, Not Active")
     assert bad["reasons"] == ["hw_slowdown"]
     assert bench.parse_clock_samples("")["sm_mhz"] is None
+
+
+def test_generator_values_are_bounded_below_the_fp8_plants():
+    # gen_f32 maps a sum of four 16-bit fields (0 .. 262140) to (s - 131070) * std / 37837.23,
+    # so |v| <= 3.4641 std; the FP8 full-size test plants one element above that bound in each
+    # current-scaled tensor, which makes the plant the tensor's amax
+    import torch
+    bound = 131070 / wl._IH4_SD
+    assert bound == pytest.approx(3.4641, abs=1e-4)
+    v = wl.gen_f32(wl.KEY_X, torch.arange(2048), 1024, 1.0, 7).abs()
+    assert float(v.max()) <= bound and float(v.max()) > 0.6 * bound
+    vb = wl.gen_bf16(wl.KEY_W1, torch.arange(2048), 1024, 0.02, 7).float().abs()
+    assert float(vb.max()) <= bound * 0.02 * (1 + 2.0 ** -8)    # bf16 rounding at most half an ulp up
+    for std, plant in ((1.0, 8.0), (0.02, 0.25), (0.5, 4.0), (0.25, 2.0)):
+        assert bound * std * (1 + 2.0 ** -8) < plant

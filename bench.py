@@ -282,6 +282,9 @@ def kernel_traffic(workload, name):
 
 PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0, "fp8": 2.0}  # dense tensor peak vs bf16 (nominal ratios)
 ARITH = {"fp8": "e4m3"}  # the operand type a layer format computes in, where the names differ
+# library kernels per call where a call launches more than one (an FP8 tensor scale: the amax
+# and the scale kernels; the memsets around kernels are not counted)
+KERNELS_PER_CALL = {"s_x": 2, "s_a": 2, "s_dy": 2, "s_dh": 2}
 
 
 def setup_workload(w, device, cap=0):
@@ -381,7 +384,7 @@ def measure(w, steps, warmup, device, peaks, cap=0, e2e_steps=0, world=1, sample
                      "frac": achieved / peak, "traffic": kernel_traffic(w.name, dom),
                      "peak_source": f"{load_peaks()[1]} ({src})", "algo_bytes_per_launch": b,
                      "flops_per_launch": f},
-        "kernels": per, "gpu_launches": len(names) * K, "clocks": clocks,
+        "kernels": per, "gpu_launches": sum(KERNELS_PER_CALL.get(n, 1) for n in names) * K, "clocks": clocks,
         "weights_gb": sum(t.numel() * t.element_size() for t in ins[1:3]) / 1e9 if w.fmt == "bf16" else None,
     }
     if e2e_steps:

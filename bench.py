@@ -12,8 +12,8 @@ Prints one JSON line.  `value` counts 2*M*N*K flops per GEMM (padding rows the
 MMA wastes are not counted) over all ranks divided by the slowest rank's time.
 `extra` adds the same measurement for the MXFP8 DeepSeek-shaped, GPT-OSS-shaped
 BF16 and Zipf-routed MXFP4 layers (--workload makes any of them the main line),
-the fp32 main_grad accumulation and the single-GPU MoE permute / combine.  The
-DeepSeek-shaped FP8 tensor-wise layer runs only when --workload names it.
+the DeepSeek-shaped FP8 tensor-wise (current scaling) layer, the fp32 main_grad
+accumulation and the single-GPU MoE permute / combine.
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload instead (the only other code path this file runs).
 """
@@ -416,7 +416,7 @@ def barrier(world):
         dist.barrier()
 
 
-EXTRA = [wl.DSV4_MXFP8, wl.GPTOSS_BF16, wl.ZIPF_MXFP4]
+EXTRA = [wl.DSV4_MXFP8, wl.GPTOSS_BF16, wl.ZIPF_MXFP4, wl.DSV4_FP8]
 
 
 def measure_wgrad_accumulate(device, peaks, steps):

@@ -376,12 +376,13 @@ def test_colwise_equals_rowwise_of_group_slices():
         assert np.all(ct[:, poff:] == 0) and np.all(st[:, poff // 32:] == 0)
 
 
-def _grid_operand(rng, fmt, rows, cols):
-    """bf16 bits of values that MX-quantize losslessly (block amax on the grid top)."""
+def _grid_operand(rng, fmt, rows, cols, shift=0):
+    """bf16 bits of values that MX-quantize losslessly (block amax on the grid top); block
+    exponents are drawn from [shift - 4, shift + 4)."""
     grid = omx._grid(fmt)
     codes = rng.integers(0, len(grid), size=(rows, cols))
     codes[:, ::32] = len(grid) - 1
-    E = rng.integers(-4, 4, size=(rows, cols // 32)).repeat(32, axis=1)
+    E = rng.integers(shift - 4, shift + 4, size=(rows, cols // 32)).repeat(32, axis=1)
     vals = grid[codes] * np.ldexp(1.0, E) * np.where(rng.random((rows, cols)) < 0.5, -1, 1)
     return _bf16_bits(vals), vals
 
@@ -415,6 +416,90 @@ def test_mx_grouped_gemm_lossless_equals_fp64(fmt):
     Bt2, SBt2 = omx.mx_quantize_colwise(xc_b, lens, fmt, M_pad, P)
     dW = omx.mx_grouped_gemm_wgrad(fmt, At, SAt, Bt2, SBt2, lens, P)
     np.testing.assert_array_equal(dW, og.grouped_gemm_wgrad(Xc, dYc, lens))
+
+
+def _brute_swiglu_rows(Hrows, I, limit):
+    """A = silu(gate) * up row by row with plain loops and math.exp; the clamp written out."""
+    out = []
+    for h in Hrows:
+        row = []
+        for j in range(I):
+            g, u = float(h[j]), float(h[I + j])
+            if limit:
+                g, u = min(g, limit), max(-limit, min(u, limit))
+            row.append(g / (1.0 + math.exp(-g)) * u)
+        out.append(row)
+    return np.array(out).reshape(len(Hrows), I)
+
+
+def _brute_swiglu_bwd_rows(dArows, Hrows, I, limit):
+    """dH row by row: d/dgate and d/dup of silu(gate) * up, zero where a clamp is active."""
+    out = []
+    for da_r, h in zip(dArows, Hrows):
+        dg_row, du_row = [], []
+        for j in range(I):
+            g, u, da = float(h[j]), float(h[I + j]), float(da_r[j])
+            pg = pu = True
+            if limit:
+                pg, pu = g <= limit, abs(u) <= limit
+                g, u = min(g, limit), max(-limit, min(u, limit))
+            s = 1.0 / (1.0 + math.exp(-g))
+            dg_row.append(da * u * (s + g * s * (1.0 - s)) if pg else 0.0)
+            du_row.append(da * g * s if pu else 0.0)
+        out.append(dg_row + du_row)
+    return np.array(out).reshape(len(Hrows), 2 * I)
+
+
+@pytest.mark.parametrize("fmt", omx.FORMATS)
+def test_mx_swiglu_gemms_lossless_operands(fmt):
+    # operands on the MX grid quantize exactly, so the MX FC1+SwiGLU and FC2-dgrad+SwiGLU'
+    # compositions must equal (1) brute-force loops over the original values and (2) the
+    # BF16-path oracle on those values; with and without a clamp that is active somewhere,
+    # so a limit that is not passed on, a swapped H, or a mis-shaped weight stack all fail
+    rng = np.random.default_rng(35)
+    G, I, K, Hd = 3, 3, 64, 32
+    lens = np.array([5, 0, 7], dtype=np.int32)
+    M = int(lens.sum())
+    owner = [0] * 5 + [2] * 7
+    # grid values times a power of two stay on the grid (only the block exponent moves);
+    # the shift keeps |H| in the range where the SwiGLU is not saturated
+    shift = -12 if fmt == "e4m3" else -6
+    xb, X = _grid_operand(rng, fmt, M, K, shift)
+    wb, W1 = _grid_operand(rng, fmt, G * 2 * I, K, shift)
+    A, SA = omx.mx_quantize_rowwise(xb, fmt)
+    B, SB = omx.mx_quantize_rowwise(wb, fmt)
+    W1g = W1.reshape(G, 2 * I, K)
+    Hb = np.array([[sum(X[r, k] * W1g[owner[r], n, k] for k in range(K)) for n in range(2 * I)]
+                   for r in range(M)])
+    gate_max = float(np.max(Hb[:, :I]))
+    results = {}
+    for limit in (None, 0.5 * gate_max):
+        Am, Hm = omx.mx_grouped_fc1_swiglu(fmt, A, SA, B, SB, lens, G, limit)
+        np.testing.assert_allclose(Hm, Hb, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(Am, _brute_swiglu_rows(Hb, I, limit), rtol=1e-12, atol=1e-12)
+        rA, rH = og.grouped_fc1_swiglu(X, W1g, lens, limit)
+        np.testing.assert_allclose(Am, rA, rtol=1e-13, atol=1e-13)
+        results[limit] = Am
+    assert not np.allclose(results[None], results[0.5 * gate_max])  # the clamp is active somewhere
+    # FC2 dgrad + SwiGLU': dY [M, Hd] row-wise along Hd; W2 quantized along Hd, stored [I, G*Hd]
+    dyb, dY = _grid_operand(rng, fmt, M, Hd, shift)
+    wtb, Wt = _grid_operand(rng, fmt, I, G * Hd, shift)
+    Ad, SAd = omx.mx_quantize_rowwise(dyb, fmt)
+    Bt, SBt = omx.mx_quantize_rowwise(wtb, fmt)
+    W2g = Wt.T.reshape(G, Hd, I)
+    Hs = rng.standard_normal((M, 2 * I)) * 1.5
+    dA = np.array([[sum(dY[r, n] * W2g[owner[r], n, j] for n in range(Hd)) for j in range(I)] for r in range(M)])
+    grads = {}
+    for limit in (None, 0.75):
+        dH = omx.mx_grouped_fc2_dgrad_swiglu_bwd(fmt, Ad, SAd, Bt, SBt, Hs, lens, G, limit)
+        np.testing.assert_allclose(dH, _brute_swiglu_bwd_rows(dA, Hs, I, limit), rtol=1e-12, atol=1e-12)
+        ref = og.grouped_fc2_dgrad_swiglu_bwd(dY, W2g, Hs, lens, limit)
+        np.testing.assert_allclose(dH, ref, rtol=1e-13, atol=1e-13)
+        grads[limit] = dH
+    assert (grads[0.75] == 0).any() and not np.allclose(grads[None], grads[0.75])
+    # a different H changes the result: the composition consumes the H it is given
+    dH_other = omx.mx_grouped_fc2_dgrad_swiglu_bwd(fmt, Ad, SAd, Bt, SBt, Hs[:, ::-1].copy(), lens, G)
+    assert not np.allclose(dH_other, grads[None])
 
 
 def _colwise_grid(rng, fmt, lens, C):

@@ -549,11 +549,32 @@ def run_pgg(args, w):
         "roofline": main["roofline"], "kernels": main["kernels"], "gpu_launches": main["gpu_launches"],
         "clocks": main["clocks"], "e2e": main.get("e2e"), "cpu_baseline": cpu, "extra": extra,
     }
+    # last key: one short line per extra workload, so that every number survives a reader that
+    # keeps only the end of the output
+    line["extra_summary"] = extra_summary(extra)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def extra_summary(extra: dict) -> str:
+    """The extra measurements as one compact string (workload: value, ms/step, % of dense peak,
+    % of the attainable roofline, dominant call and its roofline fraction)."""
+    parts = []
+    for name, r in extra.items():
+        if "value" in r:
+            rf = r["roofline"]
+            parts.append(f"{name}: {r['value']:.1f} TFLOP/s {r['ms_per_step']:.3f} ms "
+                         f"{100 * r['pct_of_dense_peak']:.1f}% dense {100 * r['pct_of_attainable_roofline']:.1f}% "
+                         f"attainable, {rf['kernel']} {rf['bound']} {100 * rf['frac']:.1f}%")
+        elif name == "wgrad_accumulate_fp32":
+            parts.append(f"{name}: {r['ms']:.3f} ms {100 * r['roofline']['frac']:.1f}% hbm")
+        elif name == "moe_glue":
+            parts.append(name + ": " + ", ".join(f"{k} {1e3 * r[k]['ms']:.1f} us {100 * r[k]['frac_of_measured_hbm']:.1f}% hbm"
+                                                 for k in ("permute", "combine", "combine_bwd")))
+    return "; ".join(parts)
 
 
 def run_e2e(step_fn, bufs, io, flops, n):

@@ -369,7 +369,9 @@ int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, co
  *   PGG_ERR_TOO_LARGE and launches nothing.
  *   The first call on each device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
- *   stream capture.
+ *   stream capture.  The cache is keyed on the context: after a device reset
+ *   (cudaDeviceReset) the next call looks the address up again, in the new
+ *   context, so that call too should come before any stream capture.
  *   All calls on one device share the one array: calls that may overlap on
  *   the GPU (different streams without ordering between them) race and give
  *   wrong results.  Calls ordered on one stream are safe. */
@@ -385,6 +387,21 @@ int pgg_mx_grouped_gemm_clamped(int mode, int fmt, const uint8_t* A, const uint8
                                 const uint8_t* SB, const void* H, const int32_t* group_lens, void* out,
                                 void* out2, uint8_t* out_codes, uint8_t* out_scales, int64_t M, int64_t N,
                                 int64_t K, int G, float swiglu_limit, int32_t* err, void* stream);
+
+/* Test hook; the pages have no counterpart.  Runs the forward grouped GEMM --
+ * BF16 when fmt == 0 (A = X, B = W, SA and SB unused), else the block-scaled
+ * forward in `fmt` (arguments as pgg_mx_grouped_gemm with PGG_MODE_FWD and
+ * PGG_EPI_NONE) -- with every pipeline wait limited to `wait_ns` and the load
+ * producer of each CTA told to stop before its `stall_at`-th k-block.  The MMA
+ * and epilogue waits behind that k-block then run out, and the kernel must take
+ * its failure path: raise the CTA's abort flag, drain what it issued, free its
+ * tensor memory, exit, and write PGG_ERR_TIMEOUT to *err, leaving the device
+ * usable for the next call.  It exists so that tests can run that path without
+ * faulting or hanging the GPU.  stall_at >= 0; 100 us <= wait_ns <= 1 s.  The
+ * output is incomplete. */
+int pgg_test_stalled_fwd(int fmt, const void* A, const uint8_t* SA, const void* B, const uint8_t* SB,
+                         const int32_t* group_lens, void* out, int64_t M, int64_t N, int64_t K, int G,
+                         int64_t stall_at, uint64_t wait_ns, int32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -46,6 +46,7 @@ SIGNATURES = {
     "pgg_fp8_grouped_gemm": [_I32, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, _F32, _P,
                              ctypes.c_size_t, _P, _P],
     "pgg_moe_combine_bwd": [_P, _P, _P, _P, _P, _P, _I64, _I32, _I64, _P],
+    "pgg_test_stalled_fwd": [_I32, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I32, _I64, ctypes.c_uint64, _P, _P],
 }
 
 

@@ -9,8 +9,8 @@
 
 namespace pgg {
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
-  bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl) {
+  bool ok = mbar_wait(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
 }
 

@@ -69,6 +69,8 @@ int launch_bf16(const Bf16Call& c) {
   a.err = c.err;
   a.I = (int)c.I;
   a.swiglu_limit = c.limit;
+  a.wait_ns = c.wait_ns;
+  a.stall_at = c.stall_at;
   int tiles_ub = 0;
   int wbk = 64;
 

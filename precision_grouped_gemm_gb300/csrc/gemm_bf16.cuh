@@ -54,6 +54,8 @@ struct GemmArgs {
   int c4d;          // wgrad: tmC is the 4-D atom view (cols % 64 == 0)
   int a_multi;      // wgrad: tmA is the atom view {64, M, N/64} (one load per k-block)
   int b_multi;      // wgrad / dgrad: tmB is the atom view of X {64, M, K/64} / W {64, N, K/64, G}
+  unsigned long long wait_ns;  // pipeline wait limit (0: kWaitTimeoutNs)
+  long long stall_at;          // test hook: the producer stops before this k-block (-1: never)
 };
 
 // Shared memory: STAGES x (A tile | B tile), the epilogue staging buffers
@@ -136,6 +138,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   constexpr bool kAmn = (MODE == kWgrad);
   constexpr bool kBmn = (MODE != kFwd);
   constexpr uint32_t kIdesc = idesc_bf16(kBM, BN, kAmn, kBmn);
+  // barriers, the wait control (16 B), the TMEM address and the bad-lens flag
+  static_assert((2 * STAGES + 2 * 2 + 1) * 8 + 24 <= L::kBarBytes, "barrier area");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,9 +149,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = bars + 2 * STAGES;   // [2]
   uint64_t* tempty = tfull + 2;          // [2]
   uint64_t* drain = tempty + 2;          // [1]
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  volatile WaitCtl* s_ctl = reinterpret_cast<volatile WaitCtl*>(drain + 1);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(const_cast<WaitCtl*>(s_ctl) + 1);
+  int* s_bad = reinterpret_cast<int*>(s_tmem + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
   int32_t* s_tile = s_off + (args.G + 1);
 
@@ -164,7 +168,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(smem_u32(&tempty[a]), 128);
     }
     mbar_init(smem_u32(drain), 1);
-    *s_abort = 0;
+    s_ctl->abort = 0;
+    s_ctl->limit_ns = args.wait_ns ? args.wait_ns : kWaitTimeoutNs;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -208,10 +213,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
-    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+    bool stalled = false;
+    for (int t = blockIdx.x; t < total_tiles && !aborted && !stalled; t += gridDim.x) {
       const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
-        if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
+        // test hook: stop producing, so that the consumers' waits run out (every load
+        // issued so far is consumed, and so complete, before they do)
+        if (issued == args.stall_at) { stalled = true; break; }
+        if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_ctl)) { aborted = true; break; }
         if (lane == 0) {
           const uint32_t fb = smem_u32(&full[stage]);
           const uint32_t sa = smem_a0 + stage * L::kABytes;
@@ -262,7 +271,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t p = phase;
       for (long long i = 0; i < n; ++i) {
         if (--s < 0) { s = STAGES - 1; p ^= 1u; }
-        mbar_wait(smem_u32(&full[s]), p, nullptr, kDrainTimeoutNs);
+        mbar_wait_drain(smem_u32(&full[s]), p);
       }
     }
   } else if (warp == 1) {
@@ -275,11 +284,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
       if (T.nkb == 0) continue;  // empty wgrad group: the epilogue writes zeros
-      if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
+      if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_ctl)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < T.nkb; ++kb) {
-        if (!warp_wait(smem_u32(&full[stage]), phase, s_abort)) { aborted = true; break; }
+        if (!warp_wait(smem_u32(&full[stage]), phase, s_ctl)) { aborted = true; break; }
         tc_fence_after();
         const uint32_t sa = smem_a0 + stage * L::kABytes;
         const uint32_t sb = smem_b0 + stage * L::kBBytes;
@@ -330,7 +339,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (aborted && lane == 0) {
       mma_commit(smem_u32(drain));
-      mbar_wait(smem_u32(drain), 0, nullptr, kDrainTimeoutNs);
+      mbar_wait_drain(smem_u32(drain), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;  // empty group: dW_g = 0, no accumulator
         if (!zero) {
-          if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+          if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_ctl)) { aborted = true; break; }
           tc_fence_after();
         }
         const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
@@ -375,7 +384,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (EPI == kEpiSwiGLUBwd)  // the saved H of this tile streams into L2 while the MMAs run
         epi_swiglu_bwd_prefetch<BN>(reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
                                     args.I);
-      if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+      if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_ctl)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {

@@ -83,6 +83,8 @@ struct MxArgs {
   const float* ts_b;
   FastDiv nct;  // wgrad: column tiles per row tile
   int c4d;      // wgrad: tmC is the 4-D atom view
+  unsigned long long wait_ns;  // pipeline wait limit (0: kWaitTimeoutNs)
+  long long stall_at;          // test hook: the producer stops before this k-block (-1: never)
 };
 
 template <int FMT>
@@ -158,7 +160,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kSfCol0 = NACC * BN;                 // scale-factor columns after the accumulators
   constexpr uint32_t kSfPer = 4 + 4 * (BN / 128);         // per stage: SFA 4 + SFB 4 per 128 rows
   static_assert(kSfCol0 + STAGES * kSfPer <= kTmemCols, "TMEM columns");
-  static_assert((2 * STAGES + 2 * NACC + 1) * 8 + 12 <= L::kGroupOff - L::kBarOff, "barrier area");
+  // barriers, the wait control (16 B), the TMEM address and the bad-lens code
+  static_assert((2 * STAGES + 2 * NACC + 1) * 8 + 24 <= L::kGroupOff - L::kBarOff, "barrier area");
   // Scale factors of an operand are either row-major [rows, K/32] (activations, whose
   // tiles start at ragged group offsets), gathered 4 bytes per row by cp.async into
   // the atom, or in the blocked atom layout (column-wise operands: wgrad A and B,
@@ -177,9 +180,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + NACC;
   uint64_t* drain = tempty + NACC;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(drain + 1);
-  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
-  int* s_bad = reinterpret_cast<int*>(s_tmem + 2);
+  volatile WaitCtl* s_ctl = reinterpret_cast<volatile WaitCtl*>(drain + 1);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(const_cast<WaitCtl*>(s_ctl) + 1);
+  int* s_bad = reinterpret_cast<int*>(s_tmem + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
   int32_t* s_tile = s_off + (args.G + 1);
   int32_t* s_poff = s_tile + (args.G + 1);
@@ -195,7 +198,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       mbar_init(smem_u32(&tempty[a]), 128);
     }
     mbar_init(smem_u32(drain), 1);
-    *s_abort = 0;
+    s_ctl->abort = 0;
+    s_ctl->limit_ns = args.wait_ns ? args.wait_ns : kWaitTimeoutNs;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -240,10 +244,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     long long issued = 0;
-    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+    bool stalled = false;
+    for (int t = blockIdx.x; t < total_tiles && !aborted && !stalled; t += gridDim.x) {
       const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
-        if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_abort)) { aborted = true; break; }
+        // test hook: stop producing, so that the consumers' waits run out (every load
+        // issued so far is consumed, and so complete, before they do)
+        if (issued == args.stall_at) { stalled = true; break; }
+        if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_ctl)) { aborted = true; break; }
         const uint32_t sa = smem0 + stage * L::kStage;
         const uint32_t sb = sa + L::kA;
         const uint32_t ssf = sb + L::kB;
@@ -340,7 +348,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       uint32_t p = phase;
       for (long long i = 0; i < n; ++i) {
         if (--s < 0) { s = STAGES - 1; p ^= 1u; }
-        mbar_wait(smem_u32(&full[s]), p, nullptr, kDrainTimeoutNs);
+        mbar_wait_drain(smem_u32(&full[s]), p);
       }
     }
   } else if (warp == 1) {
@@ -353,11 +361,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       if (T.nkb == 0) continue;
-      if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_abort)) { aborted = true; break; }
+      if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_ctl)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < T.nkb; ++kb) {
-        if (!warp_wait(smem_u32(&full[stage]), phase, s_abort)) { aborted = true; break; }
+        if (!warp_wait(smem_u32(&full[stage]), phase, s_ctl)) { aborted = true; break; }
         tc_fence_after();
         if (lane == 0) {
           const uint32_t sa = smem0 + stage * L::kStage;
@@ -399,7 +407,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
     if (aborted && lane == 0) {
       mma_commit(smem_u32(drain));
-      mbar_wait(smem_u32(drain), 0, nullptr, kDrainTimeoutNs);
+      mbar_wait_drain(smem_u32(drain), 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -412,14 +420,16 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (32 * BN * 2);
     int nstore = 0;
     float alpha = 1.0f;  // TS: 1 / (s_A s_B), written by the quantizers earlier on the stream
-    if constexpr (TS) alpha = 1.0f / (__ldg(args.ts_a) * __ldg(args.ts_b));
+    // The product of two fp32 scales is exact in fp64 and cannot overflow there (each scale is at
+    // most FLT_MAX, for a tensor whose amax is tiny); its reciprocal may be an fp32 subnormal.
+    if constexpr (TS) alpha = (float)(1.0 / ((double)__ldg(args.ts_a) * (double)__ldg(args.ts_b)));
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;
         if (!zero) {
-          if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+          if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_ctl)) { aborted = true; break; }
           tc_fence_after();
         }
         const uint32_t tbw = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
@@ -440,7 +450,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       if (EPI == kEpiSwiGLUBwd)  // the saved H of this tile streams into L2 while the MMAs run
         epi_swiglu_bwd_prefetch<BN>(reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
                                     args.I);
-      if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_abort)) { aborted = true; break; }
+      if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_ctl)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
@@ -545,6 +555,8 @@ int launch_mx_gemm(const MxCall& c) {
   a.swiglu_limit = c.limit;
   a.ts_a = c.ts_a;
   a.ts_b = c.ts_b;
+  a.wait_ns = c.wait_ns;
+  a.stall_at = c.stall_at;
   const bool ts = c.ts_a != nullptr;
   if (ts && (!e4 || !c.ts_b || c.q_codes)) return PGG_ERR_INVALID_ARG;
   const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width

@@ -52,6 +52,8 @@ struct Bf16Call {
   int32_t* err;
   cudaStream_t stream;
   float limit = 0.0f;  // SwiGLU clamp limit (0: none)
+  unsigned long long wait_ns = 0;  // pipeline wait limit (0: the kernels' default)
+  long long stall_at = -1;         // test hook: producer stops before this k-block (-1: never)
 };
 int launch_bf16(const Bf16Call& c);
 
@@ -83,6 +85,8 @@ struct MxCall {
   // a buffer of mx_unit_scale_bytes() bytes of 127 (unit block scales)
   const float* ts_a = nullptr;
   const float* ts_b = nullptr;
+  unsigned long long wait_ns = 0;  // pipeline wait limit (0: the kernels' default)
+  long long stall_at = -1;         // test hook: producer stops before this k-block (-1: never)
 };
 int launch_mx_gemm(const MxCall& c);
 

@@ -350,21 +350,61 @@ constexpr int64_t kNoAllocScratchInts = PGG_MOE_NOALLOC_MAX_WS_INTS;
 __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 constexpr int kScratchDevices = 64;
-int32_t* g_scratch_ptr[kScratchDevices] = {};
+
+// The cached address of g_permute_scratch per device, with the unique ID of the
+// context it was looked up in: a device reset (cudaDeviceReset) destroys that
+// context and reloads the module in a new one, whose array may sit elsewhere, so
+// an address is reused only while the current context is the one it came from.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;
+  int32_t* ptr = nullptr;
+};
+ScratchSlot g_scratch[kScratchDevices];
 std::mutex g_scratch_mu;
 
-// Device address of g_permute_scratch on `device` (the current device),
-// looked up on the first call per device and cached.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// ID of the current context, or 0 when no context is current yet (called with g_scratch_mu held).
+int current_ctx_id(unsigned long long* id) {
+  if (!g_ctx_get_current || !g_ctx_get_id) {
+    void* f1 = nullptr;
+    void* f2 = nullptr;
+    cudaDriverEntryPointQueryResult q1, q2;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return PGG_ERR_CUDA;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  }
+  CUcontext c = nullptr;
+  *id = 0;
+  if (g_ctx_get_current(&c) != CUDA_SUCCESS) return PGG_ERR_CUDA;
+  if (c && g_ctx_get_id(c, id) != CUDA_SUCCESS) return PGG_ERR_CUDA;
+  return PGG_OK;
+}
+
+// Device address of g_permute_scratch on `device` (the current device): looked up
+// with cudaGetSymbolAddress on the first call in each context and cached.
 int scratch_for(int device, int32_t** out) {
   if (device < 0 || device >= kScratchDevices) return PGG_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[device]) {
+  ScratchSlot& slot = g_scratch[device];
+  unsigned long long id = 0;
+  int st = current_ctx_id(&id);
+  if (st != PGG_OK) return st;
+  if (!slot.ptr || id == 0 || id != slot.ctx_id) {
     void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_permute_scratch);  // makes the context current
     if (e != cudaSuccess || p == nullptr) return PGG_ERR_CUDA;
-    g_scratch_ptr[device] = static_cast<int32_t*>(p);
+    if ((st = current_ctx_id(&id)) != PGG_OK) return st;
+    slot.ptr = static_cast<int32_t*>(p);
+    slot.ctx_id = id;
   }
-  *out = g_scratch_ptr[device];
+  *out = slot.ptr;
   return PGG_OK;
 }
 

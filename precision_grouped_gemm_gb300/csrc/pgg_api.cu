@@ -144,7 +144,7 @@ static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const
                         const int32_t* group_lens, void* out, void* out2, uint8_t* out_codes,
                         uint8_t* out_scales, int64_t M, int64_t N, int64_t K, int G, int64_t M_pad,
                         float limit, int32_t* err, void* stream, const float* ts_a = nullptr,
-                        const float* ts_b = nullptr) {
+                        const float* ts_b = nullptr, unsigned long long wait_ns = 0, long long stall_at = -1) {
   int st;
   if (mode < 0 || mode > 2) return PGG_ERR_INVALID_ARG;
   if (fmt != PGG_FMT_E4M3 && fmt != PGG_FMT_E2M1) return PGG_ERR_INVALID_ARG;
@@ -180,6 +180,8 @@ static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const
   c.limit = limit;
   c.ts_a = ts_a;
   c.ts_b = ts_b;
+  c.wait_ns = wait_ns;
+  c.stall_at = stall_at;
   return launch_mx_gemm(c);
 }
 
@@ -479,6 +481,27 @@ int pgg_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, co
   if (!aligned16(dOut) || !aligned16(Ys) || !aligned16(dYs) || !aligned4(pos) || !aligned4(w) || !aligned4(dw))
     return PGG_ERR_ALIGNMENT;
   return launch_moe_combine_bwd(dOut, Ys, pos, w, T, k, H, dYs, dw, as_stream(stream));
+}
+
+int pgg_test_stalled_fwd(int fmt, const void* A, const uint8_t* SA, const void* B, const uint8_t* SB,
+                         const int32_t* group_lens, void* out, int64_t M, int64_t N, int64_t K, int G,
+                         int64_t stall_at, uint64_t wait_ns, int32_t* err, void* stream) {
+  if (stall_at < 0 || wait_ns < 100000ull || wait_ns > 1000000000ull) return PGG_ERR_INVALID_ARG;
+  if (fmt != 0)
+    return mx_gemm_impl(PGG_MODE_FWD, fmt, PGG_EPI_NONE, static_cast<const uint8_t*>(A), SA,
+                        static_cast<const uint8_t*>(B), SB, nullptr, group_lens, out, nullptr, nullptr, nullptr, M, N,
+                        K, G, 0, 0.0f, err, stream, nullptr, nullptr, wait_ns, stall_at);
+  int st;
+  if ((st = check_common(M, G, group_lens))) return st;
+  if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
+  if (M == 0) return PGG_OK;
+  if (!A || !B || !out) return PGG_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(out)) return PGG_ERR_ALIGNMENT;
+  if (err && !aligned4(err)) return PGG_ERR_ALIGNMENT;
+  Bf16Call c{0, 0, A, B, group_lens, out, nullptr, nullptr, M, N, K, 0, G, err, as_stream(stream)};
+  c.wait_ns = wait_ns;
+  c.stall_at = stall_at;
+  return launch_bf16(c);
 }
 
 }  // extern "C"

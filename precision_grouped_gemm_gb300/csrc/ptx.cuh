@@ -2,10 +2,11 @@
 // tensor loads, tcgen05 (TMEM allocation, MMA, commit, loads) and the shared
 // memory / instruction descriptors the tensor cores read.
 //
-// Every wait in this library is bounded: a wait that does not complete within
-// kWaitTimeoutNs (measured on %globaltimer) or that sees the CTA's abort flag
-// returns false, and the caller unwinds to the kernel's teardown, which drains
-// in-flight copies and MMAs and frees TMEM before the CTA exits.
+// Every wait in this library is bounded: a wait that does not complete within the
+// launch's limit (kWaitTimeoutNs unless the launch sets a shorter one; measured on
+// %globaltimer) or that sees the CTA's abort flag returns false, and the caller
+// unwinds to the kernel's teardown, which drains in-flight copies and MMAs and
+// frees TMEM before the CTA exits.
 #pragma once
 #include <cstdint>
 #include <cuda.h>
@@ -60,21 +61,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete. Returns false on timeout (and
-// raises *abort) or when *abort was raised by another role of this CTA.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint64_t timeout_ns = kWaitTimeoutNs) {
+// A CTA's shared wait control: the abort flag its roles raise and watch, and the
+// wait limit of this launch (kWaitTimeoutNs unless the launch asked for another).
+// Both are read only on a wait's slow path, so they cost the pipelines nothing.
+struct WaitCtl {
+  int abort;
+  int pad;
+  unsigned long long limit_ns;
+};
+
+// Wait for the phase of `parity` to complete. Returns false when the wait outlives
+// ctl->limit_ns (and raises ctl->abort) or when another role of this CTA raised it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile WaitCtl* ctl) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > timeout_ns) {
-        *abort = 1;
+      if (ctl->abort) return false;
+      if (globaltimer() - t0 > ctl->limit_ns) {
+        ctl->abort = 1;
         return false;
       }
     }
+  }
+}
+
+// Teardown wait with its own fixed limit and no abort flag (drains of in-flight copies
+// and MMAs after an abort). Returns false if the limit passes.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 63u && globaltimer() - t0 > kDrainTimeoutNs) return false;
   }
 }
 

@@ -246,7 +246,10 @@ def mx_layer_step(b: MxLayerBuffers, between=None):
 
 def mx_layer_work(fmt: str, M: int, G: int, Hd: int, I: int, M_pad: int) -> dict:
     """Algorithmic flops and bytes of each MX-layer call (codes at 1 or 0.5 B/element,
-    scales at 1/32 B/element, bf16 activations and outputs at 2 B/element)."""
+    scales at 1/32 B/element, bf16 activations and outputs at 2 B/element).  The column-wise
+    operands count their M real rows, not the M_pad columns of their padded layout: padding
+    the kernels read or write is not algorithmic work (M_pad is kept in the signature for
+    callers that size buffers with it)."""
     c = 1.0 if fmt == "e4m3" else 0.5
     q = c + 1.0 / 32                          # bytes per quantized element (codes + scale)
     f1, f2 = 2.0 * M * 2 * I * Hd, 2.0 * M * Hd * I
@@ -258,13 +261,13 @@ def mx_layer_work(fmt: str, M: int, G: int, Hd: int, I: int, M_pad: int) -> dict
         "fc2_fwd": (f2, M * I * q + W2 * q + M * Hd * 2 + lens),
         "q_dy_row": (0.0, M * Hd * (2 + q)),
         "fc2_dgrad_swiglu_bwd": (f2, M * Hd * q + W2 * q + M * 2 * I * 2 + M * 2 * I * (2 + q) + lens),
-        "q_dy_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),
-        "q_a_col": (0.0, M * I * 2 + I * M_pad * q + lens),
-        "fc2_wgrad": (f2, (Hd + I) * M_pad * q + W2 * 2 + lens),
+        "q_dy_col": (0.0, M * Hd * 2 + Hd * M * q + lens),
+        "q_a_col": (0.0, M * I * 2 + I * M * q + lens),
+        "fc2_wgrad": (f2, (Hd + I) * M * q + W2 * 2 + lens),
         "fc1_dgrad": (f1, M * 2 * I * q + W1 * q + M * Hd * 2 + lens),
-        "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M_pad * q + lens),
-        "q_x_col": (0.0, M * Hd * 2 + Hd * M_pad * q + lens),
-        "fc1_wgrad": (f1, (2 * I + Hd) * M_pad * q + W1 * 2 + lens),
+        "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M * q + lens),
+        "q_x_col": (0.0, M * Hd * 2 + Hd * M * q + lens),
+        "fc1_wgrad": (f1, (2 * I + Hd) * M * q + W1 * 2 + lens),
     }
 
 
@@ -386,7 +389,8 @@ def fp8_layer_step(b: Fp8LayerBuffers, between=None):
 
 def fp8_layer_work(M: int, G: int, Hd: int, I: int, M_pad: int) -> dict:
     """Algorithmic flops and bytes of each FP8-layer call: codes at 1 B per element, bf16
-    activations and outputs at 2; a tensor scale reads its tensor once."""
+    activations and outputs at 2; a tensor scale reads its tensor once.  Column-wise operands
+    count their M real rows (padding is not algorithmic work)."""
     f1, f2 = 2.0 * M * 2 * I * Hd, 2.0 * M * Hd * I
     W1, W2 = G * 2 * I * Hd, G * Hd * I       # elements
     lens = 4 * G
@@ -400,13 +404,13 @@ def fp8_layer_work(M: int, G: int, Hd: int, I: int, M_pad: int) -> dict:
         "s_dy": (0.0, M * Hd * 2),
         "q_dy_row": (0.0, M * Hd * 3),
         "fc2_dgrad_swiglu_bwd": (f2, M * Hd + W2 + M * 2 * I * 2 + M * 2 * I * 2 + lens),
-        "q_dy_col": (0.0, M * Hd * 2 + Hd * M_pad + lens),
-        "q_a_col": (0.0, M * I * 2 + I * M_pad + lens),
-        "fc2_wgrad": (f2, (Hd + I) * M_pad + W2 * 2 + lens),
+        "q_dy_col": (0.0, M * Hd * 2 + Hd * M + lens),
+        "q_a_col": (0.0, M * I * 2 + I * M + lens),
+        "fc2_wgrad": (f2, (Hd + I) * M + W2 * 2 + lens),
         "s_dh": (0.0, M * 2 * I * 2),
         "q_dh_row": (0.0, M * 2 * I * 3),
         "fc1_dgrad": (f1, M * 2 * I + W1 + M * Hd * 2 + lens),
-        "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M_pad + lens),
-        "q_x_col": (0.0, M * Hd * 2 + Hd * M_pad + lens),
-        "fc1_wgrad": (f1, (2 * I + Hd) * M_pad + W1 * 2 + lens),
+        "q_dh_col": (0.0, M * 2 * I * 2 + 2 * I * M + lens),
+        "q_x_col": (0.0, M * Hd * 2 + Hd * M + lens),
+        "fc1_wgrad": (f1, (2 * I + Hd) * M + W1 * 2 + lens),
     }

@@ -200,3 +200,15 @@ def test_scalar_operand_alignment_is_checked(lib):
     b = lib.pgg_moe_combine_bwd
     b.argtypes = [P, P, P, P, P, P, I64, I32, I64, P]
     assert b(g, g, g, g, g, g + 2, 8, 4, 64, None) == 3               # dw
+
+
+def test_stall_hook_validation_without_gpu(lib):
+    # the test hook rejects a negative stall point and a wait limit outside [100 us, 1 s]
+    # before any CUDA call
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    f = lib.pgg_test_stalled_fwd
+    f.argtypes = [ctypes.c_int, P, P, P, P, P, P, I64, I64, I64, ctypes.c_int, I64, ctypes.c_uint64, P, P]
+    g = P(1 << 20)
+    assert f(0, g, None, g, None, g, g, 256, 256, 256, 1, -1, 2_000_000, None, None) == 1
+    assert f(0, g, None, g, None, g, g, 256, 256, 256, 1, 0, 50_000, None, None) == 1
+    assert f(0, g, None, g, None, g, g, 256, 256, 256, 1, 0, 2_000_000_000, None, None) == 1

@@ -81,3 +81,163 @@ def test_mx_layer_full_size_isolated(w):
         util.assert_close(dX[r0:r1], omx.mx_grouped_gemm_dgrad(f, *dhq, *w1t, one(n), 1), f"expert {e} fc1 dgrad")
         dhc, xc = omx.mx_quantize_colwise(B(dh), [n], f, mp), omx.mx_quantize_colwise(B(X), [n], f, mp)
         util.assert_close(dW1[e], omx.mx_grouped_gemm_wgrad(f, *dhc, *xc, one(n))[0], f"expert {e} fc1 wgrad")
+
+
+# ---------------------------------------------------------------------------------------------
+# chained: the exact launch sequence bench.py times (layer.mx_layer_step), fused MX outputs
+# of the FC1 and FC2-dgrad epilogues included
+# ---------------------------------------------------------------------------------------------
+
+EMAX = {"e4m3": 8, "e2m1": 2}
+HALF_STEP_MAX = {"e4m3": 16.0, "e2m1": 1.0}  # half the widest element spacing (416..448; 4..6)
+
+
+def _bf16_bits_of(v):
+    """fp64 values that are exact bf16 numbers -> their uint16 bit patterns."""
+    return (np.asarray(v, dtype=np.float64).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def _elems(fmt, codes):
+    return omx.unpack_e2m1(codes) if fmt == "e2m1" else np.asarray(codes)
+
+
+def _check_quantized(fmt, g_codes, g_scales, o_codes, o_scales, g_bits, o_bits, what):
+    """The GPU's MX quantization of ITS bf16 tensor (g_bits) against the oracle's quantization of the
+    oracle's bf16 rounding (o_bits), both [R, C] with blocks of 32 along C.
+
+    Blocks whose 32 bf16 inputs agree bit for bit must give identical codes and scale.  The others
+    (an element whose fp32 and fp64 sums straddle a bf16 rounding midpoint) must still be a valid
+    quantization of the GPU's own values: the scale is 2^(floor(log2 amax) - emax) and every element
+    lies within half the widest element spacing.  Returns the dequantized difference GPU - oracle,
+    which is zero outside those blocks."""
+    R, C = g_bits.shape
+    nb = C // 32
+    same = np.all(g_bits.reshape(R, nb, 32) == o_bits.reshape(R, nb, 32), axis=2)
+    gc, oc = _elems(fmt, g_codes).reshape(R, nb, 32), _elems(fmt, o_codes).reshape(R, nb, 32)
+    gs, os_ = np.asarray(g_scales).reshape(R, nb), np.asarray(o_scales).reshape(R, nb)
+    assert np.array_equal(gc[same], oc[same]) and np.array_equal(gs[same], os_[same]), \
+        f"{what}: codes or scales differ in blocks whose bf16 inputs agree"
+    assert same.mean() > 0.5, f"{what}: only {same.mean():.2%} of blocks comparable"
+    diff = ~same
+    if diff.any():
+        v = og.bf16_to_f64(g_bits).reshape(R, nb, 32)[diff]
+        amax = np.abs(v).max(axis=1)
+        _, ex = np.frexp(amax)
+        E = np.clip(np.where(amax > 0, ex - 1, -1000) - EMAX[fmt], -127, 127)
+        assert np.array_equal(gs[diff].astype(np.int64) - 127, E), f"{what}: scale selection"
+        deq = omx.decode(fmt, gc[diff]) * np.ldexp(1.0, E)[:, None]
+        assert np.all(np.abs(deq - v) <= HALF_STEP_MAX[fmt] * np.ldexp(1.0, E)[:, None]), f"{what}: codes"
+    g_deq = omx.mx_dequantize(g_codes, g_scales, fmt)
+    o_deq = omx.mx_dequantize(o_codes, o_scales, fmt)
+    return g_deq - o_deq
+
+
+def _colwise_bits(bits, n, mp):
+    """[n, C] bf16 bits -> the column-wise arrangement [C, mp] (tail positions zero)."""
+    out = np.zeros((bits.shape[1], mp), dtype=np.uint16)
+    out[:, :n] = bits.T
+    return out
+
+
+def _experts_chained(w, lens):
+    nz = np.nonzero(lens)[0]
+    order = nz[np.argsort(lens[nz], kind="stable")]
+    picks = [int(order[0]), int(order[len(order) // 2])]
+    if w is wl.DSV4_MXFP8:
+        picks.append(int(order[-1]))
+    return picks
+
+
+@pytest.mark.parametrize("w", [wl.DSV4_MXFP8, wl.ZIPF_MXFP4], ids=lambda w: w.name)
+def test_mx_layer_full_size_chained(w):
+    """The twelve launches of one MX layer step on the complete workload, each call consuming the
+    previous one's output: A and dH leave the FC1 / FC2-dgrad epilogues in bf16 AND already MX-quantized
+    (the fused outputs the next GEMM reads), the column-wise operands are quantized from the GPU's bf16
+    A and dH.  The oracle runs the same chain from the generator inputs, rounding its own A, H and dH to
+    bf16 and quantizing them itself.  Where a bf16 intermediate lands one ulp away from the oracle's
+    rounding, its MX block may quantize differently; those blocks are validated on their own and their
+    dequantized difference is propagated exactly into the downstream outputs' bound
+    (|delta| . |other operand|).  H carries the BF16 chained allowance into the SwiGLU backward."""
+    from precision_grouped_gemm_gb300.layer import mx_layer_step
+    f = w.fmt
+    lens, row_token, b = build_layer_inputs(w, torch.device(DEV), allocate=False)
+    M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
+    mb = MxLayerBuffers.build(f, b.X, b.W1, b.W2, b.dY, b.group_lens, host_lens=lens)
+    del b
+    torch.cuda.empty_cache()
+    mx_layer_step(mb)
+    torch.cuda.synchronize()
+    u, Mp = mb.bufs, mb.M_pad
+    assert pgg.read_error(u["err"]) == 0
+    poff = np.concatenate([[0], np.cumsum(-(-lens // 128) * 128)])
+    one = lambda n: np.array([n], dtype=np.int32)
+    B = util.bits
+    cb = (lambda c: c) if f == "e4m3" else (lambda c: c // 2)
+    ulp = 2.0 ** -7
+    ab = np.abs
+    for e in _experts_chained(w, lens):
+        X, W1, W2, dY, (r0, r1) = expert_inputs_cpu(w, lens, row_token, e)
+        n, p0, mp = r1 - r0, int(poff[e]), int(poff[e + 1] - poff[e])
+        rows = slice(r0, r1)
+        cols = slice(cb(p0), cb(p0 + mp))
+        scols = slice(p0 // 32, (p0 + mp) // 32)
+        tag = f"{w.name} expert {e} ({n} rows)"
+        # ---- forward: FC1 + SwiGLU, then FC2
+        xq, w1q = omx.mx_quantize_rowwise(B(X), f), omx.mx_quantize_rowwise(B(W1), f)
+        A_ref, H_ref = omx.mx_grouped_fc1_swiglu(f, *xq, *w1q, one(n), 1)
+        util.assert_close(u["H"][rows], H_ref, f"{tag} H")
+        util.assert_close(u["A"][rows], A_ref, f"{tag} A")
+        A16, H16 = og.round_bf16(A_ref), og.round_bf16(H_ref)
+        gA, oA = B(u["A"][rows]), _bf16_bits_of(A16)
+        aq_o = omx.mx_quantize_rowwise(oA, f)
+        dAq = _check_quantized(f, u["Aq"][0][rows].cpu().numpy(), u["Aq"][1][rows].cpu().numpy(), *aq_o, gA, oA,
+                               f"{tag} fused Aq")
+        w2q = omx.mx_quantize_rowwise(B(W2), f)
+        W2d = omx.mx_dequantize(*w2q, f)                                   # [Hd, I]
+        Y_ref = omx.mx_grouped_gemm_fwd(f, *aq_o, *w2q, one(n), 1)
+        util.assert_close(u["Y"][rows], Y_ref, f"{tag} Y (chained)", extra=ab(dAq) @ ab(W2d).T)
+        # ---- FC2 dgrad + SwiGLU backward on the bf16 H
+        dyq = omx.mx_quantize_rowwise(B(dY), f)
+        w2t = omx.mx_quantize_colwise(B(W2), [Hd], f, Hd)
+        dH_ref = omx.mx_grouped_fc2_dgrad_swiglu_bwd(f, *dyq, *w2t, H16, one(n), 1)
+        dA = omx.mx_grouped_gemm_dgrad(f, *dyq, *w2t, one(n), 1)
+        g_, u_ = H16[:, :I], H16[:, I:]
+        sg = og.sigmoid(g_)
+        phi = sg * (1 + g_ * (1 - sg))
+        dphi = sg * (1 - sg) * (2 + g_ * (1 - 2 * sg))
+        ex_dH = ulp * np.concatenate([ab(dA * phi) * ab(u_) + ab(dA * u_ * dphi) * ab(g_), ab(dA * phi) * ab(g_)], 1)
+        util.assert_close(u["dH"][rows], dH_ref, f"{tag} dH (chained)", extra=ex_dH)
+        dH16 = og.round_bf16(dH_ref)
+        gdH, odH = B(u["dH"][rows]), _bf16_bits_of(dH16)
+        dhq_o = omx.mx_quantize_rowwise(odH, f)
+        ddHq = _check_quantized(f, u["dHq"][0][rows].cpu().numpy(), u["dHq"][1][rows].cpu().numpy(), *dhq_o, gdH,
+                                odH, f"{tag} fused dHq")
+        # ---- FC2 wgrad on the column-wise dY and A
+        dyc = omx.mx_quantize_colwise(B(dY), [n], f, mp)
+        ac_o = omx.mx_quantize_colwise(oA, [n], f, mp)
+        g_ac = (u["Ac"][0][:, cols].cpu().numpy(), util.unblock_scales(u["Ac"][1], I, Mp)[:, scols])
+        g_dyc = (u["dYc"][0][:, cols].cpu().numpy(), util.unblock_scales(u["dYc"][1], Hd, Mp)[:, scols])
+        assert np.array_equal(g_dyc[0], dyc[0]) and np.array_equal(g_dyc[1], dyc[1]), f"{tag} dY column-wise"
+        dAc = _check_quantized(f, *g_ac, *ac_o, _colwise_bits(gA, n, mp), _colwise_bits(oA, n, mp),
+                               f"{tag} A column-wise")
+        dW2_ref = omx.mx_grouped_gemm_wgrad(f, *dyc, *ac_o, one(n))[0]
+        dYc_d = omx.mx_dequantize(*dyc, f)                                 # [Hd, mp]
+        util.assert_close(u["dW2"][e], dW2_ref, f"{tag} dW2 (chained)", extra=ab(dYc_d) @ ab(dAc).T)
+        # ---- FC1 dgrad on the fused dHq
+        w1t = omx.mx_quantize_colwise(B(W1), [2 * I], f, 2 * I)
+        W1d = omx.mx_dequantize(*w1t, f).T                                  # [2I, Hd]
+        dX_ref = omx.mx_grouped_gemm_dgrad(f, *dhq_o, *w1t, one(n), 1)
+        util.assert_close(u["dX"][rows], dX_ref, f"{tag} dX (chained)", extra=ab(ddHq) @ ab(W1d))
+        # ---- FC1 wgrad on the column-wise dH and X
+        xc = omx.mx_quantize_colwise(B(X), [n], f, mp)
+        g_xc = (u["Xc"][0][:, cols].cpu().numpy(), util.unblock_scales(u["Xc"][1], Hd, Mp)[:, scols])
+        assert np.array_equal(g_xc[0], xc[0]) and np.array_equal(g_xc[1], xc[1]), f"{tag} X column-wise"
+        dhc_o = omx.mx_quantize_colwise(odH, [n], f, mp)
+        g_dhc = (u["dHc"][0][:, cols].cpu().numpy(), util.unblock_scales(u["dHc"][1], 2 * I, Mp)[:, scols])
+        ddHc = _check_quantized(f, *g_dhc, *dhc_o, _colwise_bits(gdH, n, mp), _colwise_bits(odH, n, mp),
+                                f"{tag} dH column-wise")
+        dW1_ref = omx.mx_grouped_gemm_wgrad(f, *dhc_o, *xc, one(n))[0]
+        Xc_d = omx.mx_dequantize(*xc, f)                                   # [Hd, mp]
+        util.assert_close(u["dW1"][e], dW1_ref, f"{tag} dW1 (chained)", extra=ab(ddHc) @ ab(Xc_d).T)
+    for e in np.nonzero(lens == 0)[0]:
+        assert torch.count_nonzero(u["dW1"][e]).item() == 0 and torch.count_nonzero(u["dW2"][e]).item() == 0

@@ -44,8 +44,10 @@ def test_mx_layer_work_matches_bf16_flops_and_scales_bytes(fmt, c):
     W1 = G * 2 * I * Hd
     assert mx["fc1_fwd_swiglu"][1] - bf["fc1_fwd_swiglu"][1] == pytest.approx(
         (M * Hd + W1) * (q - 2) + M * I * q)
-    # the column-wise quantizers read bf16 and write the padded transposed codes
-    assert mx["q_x_col"][1] == M * Hd * 2 + Hd * M_pad * q + 4 * G
+    # the column-wise quantizers read bf16 and write transposed codes; padding is not counted
+    assert mx["q_x_col"][1] == M * Hd * 2 + Hd * M * q + 4 * G
+    assert mx["fc1_wgrad"][1] == (2 * I + Hd) * M * q + W1 * 2 + 4 * G
+    assert mx_layer_work(fmt, M, G, Hd, I, 2 * M_pad) == mx              # independent of the padding
 
 
 def test_fp8_layer_work_matches_mxfp8_without_scales():
@@ -59,7 +61,8 @@ def test_fp8_layer_work_matches_mxfp8_without_scales():
     W1 = G * 2 * I * Hd
     assert f8["fc1_fwd_swiglu"][1] == M * Hd + W1 + M * I * 2 + M * 2 * I * 2 + 4 * G
     assert mx["fc1_dgrad"][1] - f8["fc1_dgrad"][1] == pytest.approx((M * 2 * I + W1) / 32)
-    assert f8["q_x_col"][1] == M * Hd * 2 + Hd * M_pad + 4 * G
+    assert f8["q_x_col"][1] == M * Hd * 2 + Hd * M + 4 * G
+    assert fp8_layer_work(M, G, Hd, I, 2 * M_pad) == f8
     assert sum(f8[n][1] for n in ("s_x", "s_a", "s_dy", "s_dh")) == 2 * M * (Hd + I + Hd + 2 * I)
     assert bench.PEAK_RATIO["fp8"] == bench.PEAK_RATIO["e4m3"] and bench.ARITH["fp8"] == "e4m3"
     # library kernels per FP8 step: two per tensor scale, one per quantization and GEMM

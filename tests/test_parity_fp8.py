@@ -117,6 +117,25 @@ def test_fp8_fwd(lens, N, K):
     util.assert_close(Y, of8.fp8_grouped_gemm_fwd(cx, sx, cw, sw, lens, G), "fp8 fwd")
 
 
+def test_fp8_fwd_tiny_scales_do_not_overflow():
+    # amax 3.5e-30 and 3.5e-7 give s_A ~ 1.3e32 and s_B ~ 1.3e9: their fp32 product overflows, while
+    # 1 / (s_A s_B) ~ 6e-42 (an fp32 subnormal) and the outputs (~1e-35) are ordinary bf16 numbers
+    lens = np.asarray([40, 0, 157], dtype=np.int32)
+    G, M, N, K = 3, 197, 256, 256
+    X, W = util.gen(wl.KEY_X, M, K, 1e-30, 44), util.gen(wl.KEY_W1, G * N, K, 1e-7, 44)
+    A, sa = _q_row(X.to(DEV))
+    B, sb = _q_row(W.to(DEV))
+    assert float(sa[0].item()) * float(sb[0].item()) > 3.4e38
+    err = _err()
+    Y = pgg.fp8_grouped_gemm(pgg.MODE_FWD, A, sa, B, sb, torch.from_numpy(lens).to(DEV), M, N, K, err=err)
+    assert pgg.read_error(err) == 0
+    cx, sx = of8.fp8_quantize_tensorwise(util.f64(X))
+    cw, sw = of8.fp8_quantize_tensorwise(util.f64(W))
+    ref = of8.fp8_grouped_gemm_fwd(cx, sx, cw, sw, lens, G)
+    assert np.abs(ref).max() > 1e-37
+    util.assert_close(Y, ref, "fp8 fwd with tiny operand scales")
+
+
 @pytest.mark.parametrize("lens,N,K", [([40, 0, 157], 256, 256), ([129, 1, 300, 0, 77], 384, 320),
                                       ([300, 0, 129, 1, 517, 64, 1000, 3], 512, 200)])
 def test_fp8_dgrad(lens, N, K):

@@ -1,5 +1,7 @@
 """pgg_moe_permute_noalloc (fixed module scratch, no caller workspace) against
-pgg_moe_permute (caller workspace), both called through the C ABI.
+pgg_moe_permute (caller workspace), both called through the C ABI, and against
+the oracle's stable expert sort (positions, group_lens and the gathered rows,
+bit for bit).
 
 The file name sorts last so that it runs after every other test: it must pass
 both alone and after the rest of the suite."""
@@ -9,6 +11,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import moe_glue as omg
 from precision_grouped_gemm_gb300 import _binding
 from precision_grouped_gemm_gb300 import workloads as wl
 import util
@@ -62,10 +65,15 @@ def _permute_both(ids_np, E, H, seed):
     torch.cuda.synchronize()
     assert err.cpu().tolist() == [0, 0]
     M = int(lens_ref.sum())
+    o_pos, o_lens, o_row_token = omg.permute(ids_np, E)
+    Xb = util.bits(X)
     for Xs, lens, pos in outs:
         assert torch.equal(lens, lens_ref)
         assert torch.equal(pos, pos_ref)
         assert torch.equal(Xs[:M], Xs_ref[:M])
+        np.testing.assert_array_equal(lens.cpu().numpy(), o_lens)
+        np.testing.assert_array_equal(pos.cpu().numpy(), o_pos)
+        np.testing.assert_array_equal(util.bits(Xs[:M]), Xb[o_row_token])
 
 
 @pytest.mark.gpu

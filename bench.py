@@ -282,9 +282,9 @@ def kernel_traffic(workload, name):
 
 PEAK_RATIO = {"bf16": 1.0, "e4m3": 2.0, "e2m1": 6.0, "fp8": 2.0}  # dense tensor peak vs bf16 (nominal ratios)
 ARITH = {"fp8": "e4m3"}  # the operand type a layer format computes in, where the names differ
-# library kernels per call where a call launches more than one (an FP8 tensor scale: the amax
-# and the scale kernels; the memsets around kernels are not counted)
-KERNELS_PER_CALL = {"s_x": 2, "s_a": 2, "s_dy": 2, "s_dh": 2}
+# library kernels per call where a call launches more than one (none at present: an FP8 tensor
+# scale is one kernel after a memset; the memsets around kernels are not counted)
+KERNELS_PER_CALL = {}
 
 
 def setup_workload(w, device, cap=0):

@@ -245,42 +245,66 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
 // saturating.  amax_scale is a device float[2] = {s, amax}; while the amax kernel runs,
 // word 1 holds the largest finite bf16 magnitude as bits (their integer order is the
 // values' order), one atomicMax per block after a shared-memory reduction.
-__global__ void __launch_bounds__(256) fp8_amax_kernel(const uint4* __restrict__ in, int64_t n_chunks,
-                                                       uint32_t* __restrict__ amax_bits) {
+// {s, amax} of a bf16 tensor in one pass.  amax_scale = {0, 0} on entry (the launcher's
+// memset): word 1 collects the integer max of the finite bf16 magnitude bits (one atomicMax
+// per block) and word 0 counts finished blocks; the last block to finish turns the max into
+// the fp32 pair {s = 448 / amax, amax}.  Each thread keeps kAmaxUnroll 16-byte loads in
+// flight per iteration.
+constexpr int kAmaxUnroll = 4;
+
+__device__ __forceinline__ uint32_t amax_bits8(uint4 v, uint32_t am) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
+    if (lo < 0x7F80u) am = max(am, lo);  // Inf / NaN excluded
+    if (hi < 0x7F80u) am = max(am, hi);
+  }
+  return am;
+}
+
+__global__ void __launch_bounds__(256) fp8_amax_scale_kernel(const uint4* __restrict__ in, int64_t n_chunks,
+                                                             float* __restrict__ amax_scale) {
   __shared__ uint32_t s_max[256 / 32];
+  __shared__ bool s_last;
+  uint32_t* words = reinterpret_cast<uint32_t*>(amax_scale);
   uint32_t am = 0;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_chunks; i += stride) {
-    const uint4 v = __ldg(in + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; i + (kAmaxUnroll - 1) * stride < n_chunks; i += kAmaxUnroll * stride) {
+    uint4 v[kAmaxUnroll];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t lo = w[j] & 0x7FFFu, hi = (w[j] >> 16) & 0x7FFFu;
-      if (lo < 0x7F80u) am = max(am, lo);  // Inf / NaN excluded
-      if (hi < 0x7F80u) am = max(am, hi);
-    }
+    for (int u = 0; u < kAmaxUnroll; ++u) v[u] = __ldg(in + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < kAmaxUnroll; ++u) am = amax_bits8(v[u], am);
   }
+  for (; i < n_chunks; i += stride) am = amax_bits8(__ldg(in + i), am);
   am = __reduce_max_sync(0xffffffffu, am);
   if ((threadIdx.x & 31) == 0) s_max[threadIdx.x >> 5] = am;
   __syncthreads();
   if (threadIdx.x < 32) {
     am = threadIdx.x < (blockDim.x >> 5) ? s_max[threadIdx.x] : 0u;
     am = __reduce_max_sync(0xffffffffu, am);
-    if (threadIdx.x == 0 && am != 0u) atomicMax(amax_bits, am);
+    if (threadIdx.x == 0) {
+      if (am != 0u) atomicMax(words + 1, am);
+      __threadfence();  // this block's max is visible before its arrival is counted
+      s_last = atomicAdd(words, 1u) == gridDim.x - 1;
+    }
   }
-}
-
-__global__ void fp8_scale_kernel(float* amax_scale) {
-  const uint32_t bits = reinterpret_cast<const uint32_t*>(amax_scale)[1];
-  const float amax = __uint_as_float(bits << 16);
-  float s = 1.0f;
-  if (bits != 0u) {
-    const float fmax = __uint_as_float(0x7F7FFFFFu);
-    s = __fdiv_rn(448.0f, amax);
-    if (!(s <= fmax)) s = fmax;
+  __syncthreads();
+  if (s_last && threadIdx.x == 0) {
+    __threadfence();
+    const uint32_t bits = atomicMax(words + 1, 0u);  // the final max (an atomic read)
+    const float amax = __uint_as_float(bits << 16);
+    float sc = 1.0f;
+    if (bits != 0u) {
+      const float fmax = __uint_as_float(0x7F7FFFFFu);
+      sc = __fdiv_rn(448.0f, amax);
+      if (!(sc <= fmax)) sc = fmax;
+    }
+    amax_scale[0] = sc;
+    amax_scale[1] = amax;
   }
-  amax_scale[0] = s;
-  amax_scale[1] = amax;
 }
 
 // codes[i] = e4m3(x[i] s), eight elements (one 16-byte load, one 8-byte store) per chunk
@@ -376,16 +400,12 @@ int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32
 }
 
 int launch_fp8_tensor_scale(const void* in, int64_t n, float* amax_scale, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(amax_scale + 1, 0, sizeof(float), s);
+  cudaError_t e = cudaMemsetAsync(amax_scale, 0, 2 * sizeof(float), s);
   if (e != cudaSuccess) return cuda_status(e);
-  if (n > 0) {
-    const int grid = stream_grid(n / 8);
-    if (grid == 0) return PGG_ERR_CUDA;
-    fp8_amax_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(in), n / 8,
-                                         reinterpret_cast<uint32_t*>(amax_scale) + 1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_status(e);
-  }
-  fp8_scale_kernel<<<1, 1, 0, s>>>(amax_scale);
+  // n == 0 runs one block over nothing: amax 0, s = 1
+  const int grid = n > 0 ? stream_grid(n / 8) : 1;
+  if (grid == 0) return PGG_ERR_CUDA;
+  fp8_amax_scale_kernel<<<grid, 256, 0, s>>>(static_cast<const uint4*>(in), n / 8, amax_scale);
   return cuda_status(cudaGetLastError());
 }
 

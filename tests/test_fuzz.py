@@ -112,13 +112,18 @@ def test_fuzz_mx(fmt, seed):
 def test_fuzz_fp8(seed):
     rng, lens = _case(300 + seed)
     G, M = len(lens), int(lens.sum())
-    N, K = _mult(rng, 32, 512, 32), _mult(rng, 32, 512, 32)
+    # the FP8 GEMM takes the MX operand layouts: K-major K (fwd) and N (dgrad) in whole
+    # 128-element k-blocks; the wgrad output [G, Nw, Kw] is free in multiples of 32
+    N, K = _mult(rng, 128, 512, 128), _mult(rng, 128, 512, 128)
+    Nw, Kw = _mult(rng, 32, 480, 32), _mult(rng, 32, 480, 32)
     gl = torch.from_numpy(lens).to(DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     X = util.gen(wl.KEY_X, max(M, 1), K, 1.0, seed)[:M].contiguous()
     W = util.gen(wl.KEY_W1, G * N, K, 0.5, seed)
     dY = util.gen(wl.KEY_DY, max(M, 1), N, 1.0, seed)[:M].contiguous()
-    Xd, Wd, dYd = X.to(DEV), W.to(DEV), dY.to(DEV)
+    Xw = util.gen(wl.KEY_X, max(M, 1), Kw, 1.0, seed + 50)[:M].contiguous()
+    dYw = util.gen(wl.KEY_DY, max(M, 1), Nw, 1.0, seed + 50)[:M].contiguous()
+    Xd, Wd, dYd, Xwd, dYwd = X.to(DEV), W.to(DEV), dY.to(DEV), Xw.to(DEV), dYw.to(DEV)
     Mp = pgg.mx_pad_rows(M, G)
     sx, sw, sd = (pgg.fp8_tensor_scale(t) if t.numel() else None for t in (Xd, Wd, dYd))
     what = f"fp8 seed {seed} G={G} M={M} N={N} K={K}"
@@ -136,8 +141,13 @@ def test_fuzz_fp8(seed):
         wt = pgg.fp8_quantize_colwise(Wd, torch.full((G,), N, dtype=torch.int32, device=DEV), sw, G * N)
         dX = g(pgg.MODE_DGRAD, pgg.fp8_quantize_rowwise(dYd, sd), sd, wt, sw, gl, M, N, K, err=err)
         util.assert_close(dX, of8.fp8_grouped_gemm_dgrad(dq, s_d, wq, s_w, lens, G), f"{what} dgrad")
-        dW = g(pgg.MODE_WGRAD, pgg.fp8_quantize_colwise(dYd, gl, sd, Mp, err=err), sd,
-               pgg.fp8_quantize_colwise(Xd, gl, sx, Mp, err=err), sx, gl, M, N, K, M_pad=Mp, err=err)
+        sxw, sdw = pgg.fp8_tensor_scale(Xwd), pgg.fp8_tensor_scale(dYwd)
+        dW = g(pgg.MODE_WGRAD, pgg.fp8_quantize_colwise(dYwd, gl, sdw, Mp, err=err), sdw,
+               pgg.fp8_quantize_colwise(Xwd, gl, sxw, Mp, err=err), sxw, gl, M, Nw, Kw, M_pad=Mp, err=err)
         assert pgg.read_error(err) == 0
-        util.assert_close(dW, of8.fp8_grouped_gemm_wgrad(xq, s_x, dq, s_d, lens), f"{what} wgrad")
+        xw, dyw = util.f64(Xw), util.f64(dYw)
+        s_xw, s_dw = of8.fp8_tensor_scale(xw), of8.fp8_tensor_scale(dyw)
+        xwq, _ = of8.fp8_quantize_tensorwise(xw, scale=s_xw)
+        dwq, _ = of8.fp8_quantize_tensorwise(dyw, scale=s_dw)
+        util.assert_close(dW, of8.fp8_grouped_gemm_wgrad(xwq, s_xw, dwq, s_dw, lens), f"{what} wgrad Nw={Nw} Kw={Kw}")
         _empty_groups_zero(dW, lens)

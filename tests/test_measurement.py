@@ -65,8 +65,8 @@ def test_fp8_layer_work_matches_mxfp8_without_scales():
     assert fp8_layer_work(M, G, Hd, I, 2 * M_pad) == f8
     assert sum(f8[n][1] for n in ("s_x", "s_a", "s_dy", "s_dh")) == 2 * M * (Hd + I + Hd + 2 * I)
     assert bench.PEAK_RATIO["fp8"] == bench.PEAK_RATIO["e4m3"] and bench.ARITH["fp8"] == "e4m3"
-    # library kernels per FP8 step: two per tensor scale, one per quantization and GEMM
-    assert sum(bench.KERNELS_PER_CALL.get(n, 1) for n in FP8_STEP_NAMES) == 22
+    # library kernels per FP8 step: one per tensor scale, quantization and GEMM
+    assert sum(bench.KERNELS_PER_CALL.get(n, 1) for n in FP8_STEP_NAMES) == 18
 
 
 def test_kernel_traffic_only_for_matching_sources(tmp_path, monkeypatch):

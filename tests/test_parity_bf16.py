@@ -39,6 +39,11 @@ CASES = [
     ("ragged_tails", [0, 1, 129, 300, 37], 320, 200),
     ("single_group", [257], 264, 72),
     ("many_small", [3, 0, 0, 17, 128, 1, 0, 64, 65, 127], 128, 128),
+    # long groups whose ends fall just past a 128-row tile (129, 257, 383 = 2 x 128 + 127,
+    # 600); N = 320 leaves a 64-wide last tile, K = 200 a ragged reduction and 3-D (not 4-D)
+    # wgrad stores
+    ("long_ragged", [600, 0, 129, 257, 383], 320, 200),
+    ("long_single_group", [700], 512, 256),
 ]
 
 
@@ -62,7 +67,8 @@ def test_fwd_dgrad_wgrad(name, lens, N, K):
         assert torch.count_nonzero(dW[g]).item() == 0, "empty group must give dW = 0 exactly"
 
 
-@pytest.mark.parametrize("lens,I,K", [([5, 0, 200, 131], 200, 192), (list(wl.lens_tiny(1)), 256, 256)])
+@pytest.mark.parametrize("lens,I,K", [([5, 0, 200, 131], 200, 192), (list(wl.lens_tiny(1)), 256, 256),
+                                      ([600, 0, 431], 384, 256)])
 def test_fc1_swiglu_and_fc2_bwd(lens, I, K):
     lens = np.asarray(lens, dtype=np.int32)
     M, G = int(lens.sum()), len(lens)

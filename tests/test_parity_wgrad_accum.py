@@ -17,6 +17,7 @@ def _f32(t):
 
 
 @pytest.mark.parametrize("lens,N,K", [([0, 1, 129, 300, 37], 320, 200), ([100, 0, 57], 256, 256),
+                                      ([600, 0, 431], 320, 256),
                                       ([257], 264, 72), ([64, 65, 0, 3], 128, 96)])
 def test_wgrad_accumulate(lens, N, K):
     lens = np.asarray(lens, dtype=np.int32)

@@ -5,9 +5,8 @@
 // Pull Request #891, "Changes": MXFP4 grouped GEMM on float4_e2m1fn_x2 buffers).
 //
 // Both operands are K-major along the reduction axis (the quantizers write them
-// that way), tiles are 128 x 128 with a 128-element k-block: 128 bytes per row
-// with the 128-byte swizzle for e4m3, 64 bytes with the 64-byte swizzle for
-// packed e2m1.  The producer warp loads codes with TMA and gathers the k-block's
+// that way), and a k-block is 128 bytes of every row with the 128-byte swizzle:
+// 128 e4m3 elements, or 256 packed e2m1 elements.  The producer warp loads codes with TMA and gathers the k-block's
 // scale factors with 4-byte cp.async straight into the 512-byte atom the MMA
 // wants (row m's 4 scales at byte 16 (m % 32) + 4 (m / 32)); the MMA warp copies
 // each atom into TMEM with tcgen05.cp (32x128b, replicated to the four lane
@@ -34,7 +33,10 @@
 namespace pgg {
 namespace {
 
-constexpr int kMxBM = 128, kMxBN = 128, kMxBK = 128;  // k-block in elements
+constexpr int kMxBM = 128, kMxBN = 128;
+// Reduction elements per 512-byte scale atom (four 32-element blocks per row); also the
+// padding granule of the column-wise layout.
+constexpr int kMxAtomK = 128;
 // wgrad tiles: 128 x 128 with a double-buffered accumulator.  (128 x 256 with one
 // accumulator -- TMEM cannot hold two next to the scale factors -- measured 12%
 // slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
@@ -87,12 +89,22 @@ struct MxArgs {
   long long stall_at;          // test hook: the producer stops before this k-block (-1: never)
 };
 
+// A k-block is 128 bytes of each row in both formats: 128 e4m3 elements (four K=32 MMAs,
+// one scale atom per 128-row block) or 256 packed e2m1 elements (four K=64 MMAs, two scale
+// atoms).  The e2m1 k-block was 128 elements (64-byte rows) before: per k-block the load
+// producer issues the same handful of TMA / bulk copies and the MMA warp the same commit
+// and loop work whatever the k-block's size, and at 128 elements those fixed costs --
+// ~470 ns of producer time and ~290 ns of MMA-warp time per k-block, measured with clock64
+// on the Zipf-routed MXFP4 layer -- dwarfed the ~94 ns of tensor work.
 template <int FMT>
 struct MxCfg {
-  static constexpr int kRowBytes = FMT == kE4M3 ? 128 : 64;       // bytes per row per k-block
-  static constexpr uint32_t kSwizzle = FMT == kE4M3 ? kSwizzle128B : kSwizzle64B;
+  static constexpr int kBK = FMT == kE4M3 ? 128 : 256;            // k-block in elements
+  static constexpr int kRowBytes = 128;                           // bytes per row per k-block
+  static constexpr uint32_t kSwizzle = kSwizzle128B;
   static constexpr uint32_t kSbo = 8 * kRowBytes;                 // 8-row swizzle atom
-  static constexpr int kMmas = FMT == kE4M3 ? 4 : 2;              // MMAs per k-block
+  static constexpr int kMmas = 4;                                 // MMAs per k-block (32 bytes of K each)
+  static constexpr int kSub = kBK / kMxAtomK;                     // scale atoms per 128 rows per k-block
+  static constexpr int kPerMma = kBK / kMmas;                     // reduction elements per MMA
   static constexpr uint32_t kElem = FMT == kE4M3 ? 0 : 1;         // idesc element type code
   static constexpr int kTileBytes = 128 * kRowBytes;
 };
@@ -103,7 +115,10 @@ template <int FMT, int BN, int STAGES, int EPI_BYTES>
 struct MxSmem {
   static constexpr int kA = MxCfg<FMT>::kTileBytes;
   static constexpr int kB = MxCfg<FMT>::kRowBytes * BN;
-  static constexpr int kSF = BN == 256 ? 2048 : 1024;  // SFA atom + BN/128 SFB atoms (512 B each), padded
+  // kSub SFA atoms, then kSub SFB atoms for each 128 rows of B (512 B each), padded to keep
+  // every stage's tiles 1024-byte aligned
+  static constexpr int kSFA = MxCfg<FMT>::kSub * 512;
+  static constexpr int kSF = (kSFA * (1 + BN / 128) + 1023) / 1024 * 1024;
   static constexpr int kStage = kA + kB + kSF;
   static constexpr int kEpiOff = STAGES * kStage;
   static constexpr int kBarOff = kEpiOff + EPI_BYTES;
@@ -118,7 +133,7 @@ struct MxTile {
 template <int EPI, int BN>
 __device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? BN / 2 : BN; }
 
-template <int MODE, int EPI, int BN>
+template <int MODE, int EPI, int BN, int BK>
 __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_t* s_off,
                                             const int32_t* s_tile, const int32_t* s_poff, GroupCursor& cur) {
   MxTile T;
@@ -134,14 +149,14 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
     T.row0 = rt * kMxBM;
     T.rows = min(kMxBM, a.wg_rows - T.row0);
     T.col0 = (local - rt * (int)a.nct.d) * BN;
-    T.nkb = (len + kMxBK - 1) / kMxBK;
+    T.nkb = (len + BK - 1) / BK;
   } else {
     const int nmt = (len + kMxBM - 1) / kMxBM;
     const int mt = local % nmt;
     T.row0 = cur.off + mt * kMxBM;
     T.rows = min(kMxBM, len - mt * kMxBM);
     T.col0 = (local / nmt) * mx_tile_cols<EPI, BN>();
-    T.nkb = (a.red + kMxBK - 1) / kMxBK;
+    T.nkb = (a.red + BK - 1) / BK;
   }
   return T;
 }
@@ -158,7 +173,9 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kSfCol0 = NACC * BN;                 // scale-factor columns after the accumulators
-  constexpr uint32_t kSfPer = 4 + 4 * (BN / 128);         // per stage: SFA 4 + SFB 4 per 128 rows
+  // per stage: for each of the kSub scale sub-blocks, SFA 4 columns and SFB 4 per 128 rows
+  constexpr uint32_t kSfbPer = 4 * (BN / 128);            // SFB columns of one sub-block
+  constexpr uint32_t kSfPer = C::kSub * (4 + kSfbPer);
   static_assert(kSfCol0 + STAGES * kSfPer <= kTmemCols, "TMEM columns");
   // barriers, the wait control (16 B), the TMEM address and the bad-lens code
   static_assert((2 * STAGES + 2 * NACC + 1) * 8 + 24 <= L::kGroupOff - L::kBarOff, "barrier area");
@@ -170,7 +187,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   // a multiple of 128) is gathered row by row from the blocked layout instead.
   constexpr bool kGatherA = MODE != kWgrad;
   const bool gather_b = MODE == kFwd && (!args.b_bulk || (EPI == kEpiSwiGLU && BN < 256));
-  const uint32_t sf_bulk = (kGatherA ? 0u : 512u) + (gather_b ? 0u : 512u * (BN / 128));
+  // reduction elements of the operands (wgrad: the group's own length, per tile)
+  const int red_all = MODE == kWgrad ? 0 : args.red;
+  // bytes of one row of the reduction axis of a group's slice of the dgrad B operand
+  const int gbytes = FMT == kE4M3 ? args.red : args.red / 2;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,7 +241,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc.bm = kMxBM;
       tc.per_row_tile = (args.out_cols + tcw - 1) / tcw;
     }
-    bool bad = scan_groups(args.group_lens, args.G, args.M, tc, s_off, s_tile, s_poff, kMxBK, lane);
+    bool bad = scan_groups(args.group_lens, args.G, args.M, tc, s_off, s_tile, s_poff, kMxAtomK, lane);
     int code = bad ? kErrBadGroupLens : 0;
     if (!bad && MODE == kWgrad && (int64_t)s_poff[args.G] > args.M_pad) code = kErrPadOverflow;
     if (lane == 0) {
@@ -246,7 +266,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     long long issued = 0;
     bool stalled = false;
     for (int t = blockIdx.x; t < total_tiles && !aborted && !stalled; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
+      const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
       for (int kb = 0; kb < T.nkb; ++kb) {
         // test hook: stop producing, so that the consumers' waits run out (every load
         // issued so far is consumed, and so complete, before they do)
@@ -257,8 +277,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const uint32_t ssf = sb + L::kB;
         const uint32_t fb = smem_u32(&full[stage]);
         const int kbyte = kb * C::kRowBytes;  // byte offset of this k-block along a row
+        // scale sub-blocks (128 reduction elements each) of this k-block that hold data: a
+        // k-block past the end of K / N, or past a wgrad group's last row, copies none of them
+        const int valid = (MODE == kWgrad ? T.len : red_all) - kb * C::kBK;
+        const int nsub = min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK);
+        const int p0 = kb * C::kSub;  // first scale atom of this k-block along the reduction axis
         if (lane == 0) {
-          mbar_arrive_expect_tx(fb, L::kA + L::kB + sf_bulk);
+          const uint32_t sf_bytes = 512u * (uint32_t)nsub * ((kGatherA ? 0u : 1u) + (gather_b ? 0u : BN / 128u));
+          mbar_arrive_expect_tx(fb, L::kA + L::kB + sf_bytes);
           if (MODE == kFwd) {
             tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
             if (EPI == kEpiSwiGLU) {
@@ -269,18 +295,19 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
           } else if (MODE == kDgrad) {
             tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
-            tma_load_2d(sb, &tmB, fb, T.g * (args.red / kMxBK) * C::kRowBytes + kbyte, T.col0);
+            tma_load_2d(sb, &tmB, fb, T.g * gbytes + kbyte, T.col0);
           } else {
-            const int pb = (T.poff / kMxBK) * C::kRowBytes + kbyte;
+            const int pb = (FMT == kE4M3 ? T.poff : T.poff / 2) + kbyte;
             tma_load_2d(sa, &tmA, fb, pb, T.row0);
             tma_load_2d(sb, &tmB, fb, pb, T.col0);
           }
-          // blocked scale atoms: ((row block) * atoms-per-row-block + k-block) * 512
+          // blocked scale atoms: ((row block) * atoms-per-row-block + atom along K) * 512; the
+          // nsub atoms of a k-block are adjacent, so one bulk copy takes them all
           if (!kGatherA)
-            bulk_load(ssf, args.SA + ((int64_t)(T.row0 >> 7) * (args.sa_ld >> 2) + (T.poff >> 7) + kb) * 512, 512,
-                      fb);
+            bulk_load(ssf, args.SA + ((int64_t)(T.row0 >> 7) * (args.sa_ld >> 2) + (T.poff >> 7) + p0) * 512,
+                      512u * nsub, fb);
           if (!gather_b) {
-            const int p = MODE == kWgrad ? (T.poff >> 7) + kb : MODE == kDgrad ? T.g * (args.red >> 7) + kb : kb;
+            const int p = MODE == kWgrad ? (T.poff >> 7) + p0 : MODE == kDgrad ? T.g * (args.red >> 7) + p0 : p0;
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h) {
               // first B row of this 128-row group: wgrad / dgrad col0 + 128 h; fwd the weight
@@ -295,46 +322,50 @@ __global__ void __launch_bounds__(kMxThreads, 1)
               // of 256): its scales only feed outputs that are not stored, so the copy reads the
               // last existing atom row instead of running past the buffer
               const int64_t rb = min(r0 >> 7, args.sb_blocks - 1);
-              bulk_load(ssf + 512 + 512 * h, args.SB + (rb * (args.sb_ld >> 2) + p) * 512, 512, fb);
+              bulk_load(ssf + L::kSFA * (1 + h), args.SB + (rb * (args.sb_ld >> 2) + p) * 512, 512u * nsub, fb);
             }
           }
         }
-        // gathered scale factors (row-major operands): lane l fetches rows l, l+32, l+64,
-        // l+96 of the operand tile (4 bytes = the k-block's 4 block scales) into word
-        // 4 l + i of the atom
-        const int sfa_col = kb * 4;  // byte column of this k-block in the row-major A scales
+        // gathered scale factors (row-major operands): for scale sub-block s, lane l fetches
+        // rows l, l+32, l+64, l+96 of the operand tile (4 bytes = the sub-block's 4 block
+        // scales) into word 4 l + i of atom s
 #pragma unroll
-        for (int i = 0; i < BN / 32; ++i) {
-          const int m = lane + 32 * i;
-          // A rows: fwd/dgrad token rows
-          if (kGatherA && i < 4) {
-            const int ar = T.row0 + m;
-            const bool aok = ar < args.a_rows;
-            cp_async_4(ssf + (lane * 4 + i) * 4, args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0),
-                       aok ? 4u : 0u);
+        for (int sub = 0; sub < C::kSub; ++sub) {
+          if (sub >= nsub) break;
+          const int sfa_col = (p0 + sub) * 4;  // byte column of this sub-block in the row-major A scales
+#pragma unroll
+          for (int i = 0; i < BN / 32; ++i) {
+            const int m = lane + 32 * i;
+            // A rows: fwd/dgrad token rows
+            if (kGatherA && i < 4) {
+              const int ar = T.row0 + m;
+              const bool aok = ar < args.a_rows;
+              cp_async_4(ssf + sub * 512 + (lane * 4 + i) * 4,
+                         args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0), aok ? 4u : 0u);
+            }
+            // B rows
+            int br;
+            bool bok;
+            if (MODE == kFwd) {
+              constexpr int kHalf = BN / 2;  // SwiGLU: gate rows, then the matching up rows
+              const int n = (EPI == kEpiSwiGLU) ? (m < kHalf ? T.col0 + m : args.I + T.col0 + (m - kHalf))
+                                                : T.col0 + m;
+              const int lim = (EPI == kEpiSwiGLU) ? (m < kHalf ? args.I : 2 * args.I) : args.nw;
+              bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m % kHalf) < args.I);
+              br = T.g * args.nw + n;
+            } else {
+              br = T.col0 + m;
+              bok = br < args.b_rows;
+            }
+            // B row m goes to atom (m / 128, sub), word 4 (m % 32) + (m % 128) / 32; the source
+            // is row br's 4 bytes of this sub-block in the blocked layout
+            if (gather_b)
+              cp_async_4(ssf + L::kSFA * (1 + i / 4) + sub * 512 + (lane * 4 + (i % 4)) * 4,
+                         args.SB + (bok ? ((((int64_t)br >> 7) * (args.sb_ld >> 2) + p0 + sub) << 9) +
+                                              16 * (br & 31) + 4 * ((br >> 5) & 3)
+                                        : 0),
+                         bok ? 4u : 0u);
           }
-          // B rows
-          int br;
-          bool bok;
-          if (MODE == kFwd) {
-            constexpr int kHalf = BN / 2;  // SwiGLU: gate rows, then the matching up rows
-            const int n = (EPI == kEpiSwiGLU) ? (m < kHalf ? T.col0 + m : args.I + T.col0 + (m - kHalf))
-                                              : T.col0 + m;
-            const int lim = (EPI == kEpiSwiGLU) ? (m < kHalf ? args.I : 2 * args.I) : args.nw;
-            bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m % kHalf) < args.I);
-            br = T.g * args.nw + n;
-          } else {
-            br = T.col0 + m;
-            bok = br < args.b_rows;
-          }
-          // B row m goes to atom m / 128, word 4 (m % 32) + (m % 128) / 32; the source is
-          // row br's 4 bytes of k-block kb in the blocked layout
-          if (gather_b)
-            cp_async_4(ssf + 512 + (i / 4) * 512 + (lane * 4 + (i % 4)) * 4,
-                       args.SB + (bok ? ((((int64_t)br >> 7) * (args.sb_ld >> 2) + kb) << 9) + 16 * (br & 31) +
-                                            4 * ((br >> 5) & 3)
-                                      : 0),
-                       bok ? 4u : 0u);
         }
         if (kGatherA || gather_b) cp_async_arrive_noinc(fb);
         __syncwarp();
@@ -359,7 +390,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
+      const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
       if (T.nkb == 0) continue;
       if (!warp_wait(smem_u32(&tempty[acc]), acc_phase ^ 1u, s_ctl)) { aborted = true; break; }
       tc_fence_after();
@@ -371,29 +402,37 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const uint32_t sa = smem0 + stage * L::kStage;
           const uint32_t sb = sa + L::kA;
           const uint32_t ssf = sb + L::kB;
-          const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;
-          const uint32_t sfb_t = sfa_t + 4;
+          const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;  // kSub x 4 SFA columns
+          const uint32_t sfb_t = sfa_t + 4 * C::kSub;                    // kSub x kSfbPer SFB columns
+          // scale sub-blocks and MMAs of this k-block that hold data: past the end of K / N (an
+          // e2m1 K that is an odd multiple of 128) or past a wgrad group's rows, the k-steps cover
+          // only zeros and are skipped (exact); so are their scale copies
+          const int valid = (MODE == kWgrad ? T.len : red_all) - kb * C::kBK;
+          const int nsub = min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK);
+          const int nmma = min(C::kMmas, (valid + C::kPerMma - 1) / C::kPerMma);
           if (kGatherA) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
-          tmem_cp_32x128b_x4(sfa_t, smem_desc(ssf, 0, 128, kSwizzleNone));
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32: 4 columns per 128 rows
-            tmem_cp_32x128b_x4(sfb_t + 4 * h, smem_desc(ssf + 512 + 512 * h, 0, 128, kSwizzleNone));
-          // wgrad: k-steps that cover only a group's zero padding are skipped (exact)
-          int nmma = C::kMmas;
-          if (MODE == kWgrad) {
-            const int valid = T.len - kb * kMxBK;
-            const int per = kMxBK / C::kMmas;  // elements per MMA
-            if (valid < kMxBK) nmma = (valid + per - 1) / per;
+          for (int sub = 0; sub < C::kSub; ++sub) {
+            if (sub >= nsub) break;
+            tmem_cp_32x128b_x4(sfa_t + 4 * sub, smem_desc(ssf + sub * 512, 0, 128, kSwizzleNone));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32 of the sub-block: 4 columns per 128 rows
+              tmem_cp_32x128b_x4(sfb_t + sub * kSfbPer + 4 * h,
+                                 smem_desc(ssf + L::kSFA * (1 + h) + sub * 512, 0, 128, kSwizzleNone));
           }
 #pragma unroll
           for (int j = 0; j < C::kMmas; ++j) {
             if (j >= nmma) break;
+            const int sub = j / (C::kMmas / C::kSub);  // the scale sub-block this MMA's K-range lies in
             const uint64_t ad = smem_desc(sa + j * 32, 16, C::kSbo, C::kSwizzle);
             const uint64_t bd = smem_desc(sb + j * 32, 16, C::kSbo, C::kSwizzle);
-            const uint32_t sfid = FMT == kE4M3 ? (uint32_t)j : (uint32_t)(2 * j);
+            // scale bytes of the MMA's K-range within its atom: e4m3 one 32-block (j), e2m1 the
+            // pair of 32-blocks (2 (j % 2), 2 (j % 2) + 1)
+            const uint32_t sfid = FMT == kE4M3 ? (uint32_t)j : (uint32_t)(2 * (j % 2));
             const uint32_t id = kIdesc | idesc_sf_ids(sfid, sfid);
-            if (FMT == kE4M3) mma_mxf8(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || j > 0) ? 1u : 0u);
-            else mma_mxf4(d_tmem, ad, bd, id, sfa_t, sfb_t, (kb > 0 || j > 0) ? 1u : 0u);
+            const uint32_t sfa = sfa_t + 4 * sub, sfb = sfb_t + sub * kSfbPer;
+            if (FMT == kE4M3) mma_mxf8(d_tmem, ad, bd, id, sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
+            else mma_mxf4(d_tmem, ad, bd, id, sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&empty[stage]));
         }
@@ -424,7 +463,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     // most FLT_MAX, for a tensor whose amax is tiny); its reciprocal may be an fp32 subnormal.
     if constexpr (TS) alpha = (float)(1.0 / ((double)__ldg(args.ts_a) * (double)__ldg(args.ts_b)));
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
-      const MxTile T = mx_decode<MODE, EPI, BN>(t, args, s_off, s_tile, s_poff, cur);
+      const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
       const bool row_ok = r < T.rows;
       if (MODE == kWgrad) {
         const bool zero = T.nkb == 0;
@@ -498,16 +537,24 @@ template <int FMT>
 int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kBN = FMT == kE4M3 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;
-  // stages for fwd / dgrad: as many as fit next to the group tables (e4m3 128-wide: 6, e2m1 256-wide: 8)
-  constexpr int kS = FMT == kE4M3 ? (kBN == 128 ? 6 : 4) : (kBN == 128 ? 8 : 8);
+  // stages for fwd / dgrad: 4 x (16 KB A + 32 KB B + 2 / 3 KB of scale atoms) next to the group tables
+  constexpr int kS = 4;
   constexpr int kWBN = FMT == kE4M3 ? kMxWgradBNE4M3 : kMxWgradBNE2M1;
-  // wgrad keeps 4 x 32 rows x kWBN bf16 of TMA-store staging next to the stages
-  constexpr int kSw = FMT == kE4M3 ? (kWBN == 128 ? 5 : 2) : (kWBN == 128 ? 8 : 5);
+  // wgrad keeps 4 x 32 rows x kWBN bf16 of TMA-store staging next to the stages: e4m3 5 x 33 KB
+  // + 32 KB, e2m1 3 x 51 KB + 64 KB (2 stages when the group tables of a large G leave no room)
+  constexpr int kSw = FMT == kE4M3 ? 5 : 3;
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS, kBN>(ta, tb, tc, a, grid, s);
-  if (mode == 2 && epi == 0) return run_mx<FMT, kWgrad, kEpiStore, kSw, kWBN>(ta, tb, tc, a, grid, s);
+  if (mode == 2 && epi == 0) {
+    using L = MxSmem<FMT, kWBN, kSw, 4 * 32 * kWBN * 2>;
+    DeviceInfo dev;
+    int st = current_device(&dev);
+    if (st != PGG_OK) return st;
+    if (L::bytes(a.G) > dev.smem_optin) return run_mx<FMT, kWgrad, kEpiStore, kSw - 1, kWBN>(ta, tb, tc, a, grid, s);
+    return run_mx<FMT, kWgrad, kEpiStore, kSw, kWBN>(ta, tb, tc, a, grid, s);
+  }
   return PGG_ERR_INVALID_ARG;
 }
 
@@ -534,9 +581,9 @@ int launch_mx_gemm(const MxCall& c) {
   int st = current_device(&dev);
   if (st != PGG_OK) return st;
   const bool e4 = c.fmt == PGG_FMT_E4M3;
-  const uint32_t rb = e4 ? 128 : 64;  // bytes per row per 128-element k-block
+  const uint32_t rb = 128;  // bytes per row per k-block (128 e4m3 or 256 packed e2m1 elements)
   auto bytes = [&](int64_t elems) { return (uint64_t)(e4 ? elems : elems / 2); };
-  const auto sw = e4 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   const auto u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUtensorMap ta, tb, tc;
   MxArgs a{};

@@ -40,7 +40,9 @@ def _stream():
 def test_stalled_pipeline_times_out_and_the_next_call_passes(fmt, stall_at):
     L = _binding.lib()
     lens = np.asarray([100, 0, 157, 300], dtype=np.int32)
-    G, M, N, K = len(lens), int(lens.sum()), 256, 512   # 8 (BF16) / 4 (MX) k-blocks per tile
+    # K = 1024: 16 (BF16), 8 (e4m3) and 4 (e2m1) k-blocks per tile, so every CTA's producer
+    # reaches k-block 3 (each CTA gets at least one tile)
+    G, M, N, K = len(lens), int(lens.sum()), 256, 1024
     gl = torch.from_numpy(lens).to(DEV)
     X, W = util.gen(wl.KEY_X, M, K, 1.0, 61), util.gen(wl.KEY_W1, G * N, K, 0.5, 61)
     Xd, Wd = X.to(DEV), W.to(DEV)

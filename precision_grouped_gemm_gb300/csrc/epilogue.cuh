@@ -19,85 +19,111 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // up the producer and MMA warps that share issue slots with the epilogue warps.
 __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
-// Store 32 consecutive fp32 values of one row as bf16 at dst[0..31], columns
-// limited to ncols (<= 32).  16-byte vector stores when the chunk is whole.
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float* v, int ncols) {
-  if (ncols >= 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
+// ---------------------------------------------------------------- warp-transposed row I/O
+// In the fwd / dgrad epilogues each lane owns one accumulator row, so a plain 16-byte-per-
+// lane access touches 32 rows at once: 32 L1 wavefronts per instruction.  Staged through
+// the warp's 2 KB buffer, each global access instead covers 8 rows x 64 contiguous bytes.
+// (Per-role clock64 timing of the MXFP4 FC2 dgrad + SwiGLU backward: leaving out its dH
+// stores halved the kernel, leaving out its H loads cut it by a fifth.)
+// The buffer holds 32 rows x 64 bytes; 16-byte chunk j of row r sits at
+// r * 64 + 16 (j ^ ((r >> 1) & 3)), so that both the row-wise accesses (lane = row) and
+// the transposed ones (8 rows x 4 chunks per instruction) spread over all banks.
+__device__ __forceinline__ uint32_t stg_off(int r, int j) { return r * 64 + ((j ^ ((r >> 1) & 3)) << 4); }
+
+// Lane `lane` holds row `lane`'s 32 bf16 values packed in w[16]; rows [0, nrows) of the
+// warp's 32 and columns [0, ncols) (a multiple of 8) are stored at dst (row 0, column 0;
+// row stride ld elements).  Warp-collective: every lane calls it with the same arguments
+// except w.
+__device__ __forceinline__ void store_rows32_t(uint8_t* stg, const uint32_t (&w)[16], __nv_bfloat16* dst,
+                                               size_t ld, int nrows, int ncols, int lane) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-      w.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-      w.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-      w.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-      d4[q] = w;
-    }
-  } else {
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(stg + stg_off(lane, j)) = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+  __syncwarp();
+  const int J = lane & 3;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (j < ncols) dst[j] = __float2bfloat16_rn(v[j]);
+  for (int i = 0; i < 4; ++i) {
+    const int R = 8 * i + (lane >> 2);
+    const uint4 v = *reinterpret_cast<const uint4*>(stg + stg_off(R, J));
+    if (R < nrows && 8 * J < ncols) *reinterpret_cast<uint4*>(dst + (size_t)R * ld + 8 * J) = v;
   }
+  __syncwarp();
 }
 
-__device__ __forceinline__ void load_row32(const __nv_bfloat16* src, float* v, int ncols) {
-  if (ncols >= 32) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+// Global half of the transposed load: lane `lane` fetches 16 bytes (columns 8 J .. 8 J + 7,
+// J = lane % 4) of rows 8 i + lane / 4, i = 0..3, of a 32-row x 32-column bf16 chunk at src;
+// rows past nrows and columns past ncols read as 0.
+__device__ __forceinline__ void load_rows32_issue(const __nv_bfloat16* src, size_t ld, int nrows, int ncols,
+                                                  uint4 (&v)[4], int lane) {
+  const int J = lane & 3;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w = __ldg(s4 + q);
-      v[q * 8 + 0] = bf16_lo(w.x); v[q * 8 + 1] = bf16_hi(w.x);
-      v[q * 8 + 2] = bf16_lo(w.y); v[q * 8 + 3] = bf16_hi(w.y);
-      v[q * 8 + 4] = bf16_lo(w.z); v[q * 8 + 5] = bf16_hi(w.z);
-      v[q * 8 + 6] = bf16_lo(w.w); v[q * 8 + 7] = bf16_hi(w.w);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = j < ncols ? __bfloat162float(src[j]) : 0.0f;
+  for (int i = 0; i < 4; ++i) {
+    const int R = 8 * i + (lane >> 2);
+    v[i] = (R < nrows && 8 * J < ncols) ? __ldg(reinterpret_cast<const uint4*>(src + (size_t)R * ld + 8 * J))
+                                        : make_uint4(0, 0, 0, 0);
   }
 }
+// Shared half: the fetched chunk, transposed through stg, lands in w[16] as row `lane`.
+__device__ __forceinline__ void load_rows32_finish(uint8_t* stg, const uint4 (&v)[4], uint32_t (&w)[16], int lane) {
+  const int J = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(stg + stg_off(8 * i + (lane >> 2), J)) = v[i];
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 x = *reinterpret_cast<const uint4*>(stg + stg_off(lane, j));
+    w[4 * j] = x.x; w[4 * j + 1] = x.y; w[4 * j + 2] = x.z; w[4 * j + 3] = x.w;
+  }
+  __syncwarp();
+}
 
-// Plain store: row `dst_row` (already offset to this thread's output row),
-// accumulator columns 0..BN-1 -> output columns col0.., bounded by ncols.
-// SCALED: every accumulator is multiplied by alpha first (per-tensor operand scales).
+// 32 fp32 values -> 16 words of bf16 pairs (round to nearest even).
+__device__ __forceinline__ void pack32(const float* v, uint32_t (&w)[16]) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+}
+
+// Staging bytes per epilogue warp of the fwd / dgrad epilogues: one 2 KB chunk buffer, which
+// every transposed load and store reuses in turn (each completes behind a warp barrier).
+constexpr int kEpiRowStageBytes = 2048;
+
+// Plain store: the warp's 32 accumulator rows are output rows row0w .. row0w + 31, of which
+// the first nrows exist; accumulator columns 0..BN-1 -> output columns col0.., bounded by
+// ncols; output row stride ld.  SCALED: every accumulator is multiplied by alpha first
+// (per-tensor operand scales).
 template <int BN, bool SCALED = false>
-__device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* dst_row, bool row_ok, int col0,
-                                          int ncols, float alpha = 1.0f) {
+__device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* out, size_t ld, size_t row0w, int nrows,
+                                          int col0, int ncols, uint8_t* stg, int lane, float alpha = 1.0f) {
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t rv[32];
     tmem_ld32(tb + c * 32, rv);
     tmem_ld_wait();
     const int c0 = col0 + c * 32;
-    if (row_ok && c0 < ncols) {
+    if (c0 < ncols) {
       float v[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         v[j] = __uint_as_float(rv[j]);
         if constexpr (SCALED) v[j] *= alpha;
       }
-      store_row32(dst_row + c0, v, min(32, ncols - c0));
+      uint32_t w[16];
+      pack32(v, w);
+      store_rows32_t(stg, w, out + row0w * ld + c0, ld, nrows, min(32, ncols - c0), lane);
     }
   }
 }
 
-// bf16 bit patterns of 32 fp32 values (round to nearest even, as store_row32).
-__device__ __forceinline__ void bf16_bits32(const float* v, uint32_t (&b)[32]) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) b[j] = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
-}
-
 // Optional fused MX output (QF = kE4M3 / kE2M1): the 32 bf16 values just stored at
-// columns c0..c0+31 of row `grow` of a [rows, ld] tensor form one row-wise MX block;
-// its codes and scale go to codes[grow, c0 ..] / scales[grow, c0 / 32] exactly as
-// the row-wise quantize kernel would write them for the stored tensor.
+// columns c0..c0+31 of row `grow` of a [rows, ld] tensor -- w[16], packed in pairs exactly
+// as stored -- form one row-wise MX block; its codes and scale go to codes[grow, c0 ..] /
+// scales[grow, c0 / 32] exactly as the row-wise quantize kernel would write them for the
+// stored tensor.
 template <int QF>
-__device__ __forceinline__ void mx_emit(const float* v, uint8_t* codes, uint8_t* scales, size_t grow, int ld,
-                                        int c0) {
-  uint32_t b[32];
-  bf16_bits32(v, b);
+__device__ __forceinline__ void mx_emit(const uint32_t (&w)[16], uint8_t* codes, uint8_t* scales, size_t grow,
+                                        int ld, int c0) {
   const size_t cb = QF == kE4M3 ? (size_t)ld : (size_t)ld / 2;  // code bytes per row
-  const uint32_t sc = quantize_block32<QF>(b, codes + grow * cb + (QF == kE4M3 ? c0 : c0 / 2));
+  const uint32_t sc = quantize_block32_packed<QF>(w, codes + grow * cb + (QF == kE4M3 ? c0 : c0 / 2));
   scales[grow * (size_t)(ld / 32) + c0 / 32] = (uint8_t)sc;
 }
 
@@ -107,10 +133,12 @@ __device__ __forceinline__ void mx_emit(const float* v, uint8_t* codes, uint8_t*
 // QF != 0 and qcodes != null: A is also emitted MX-quantized (row-wise, I % 32 == 0).
 // limit > 0 clamps first: gate <- min(gate, limit), up <- clamp(up, -limit, limit); H
 // keeps the values before the clamp.  SCALED: gate and up are the accumulators times alpha.
+// Rows as epi_store; this thread's own row is grow (row_ok: it exists).
 template <int BN, int QF = 0, bool SCALED = false>
-__device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t grow,
-                                           bool row_ok, int col0, int I, uint8_t* qcodes = nullptr,
-                                           uint8_t* qscales = nullptr, float limit = 0.0f, float alpha = 1.0f) {
+__device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t row0w,
+                                           int nrows, bool row_ok, size_t grow, int col0, int I, uint8_t* stg,
+                                           int lane, uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr,
+                                           float limit = 0.0f, float alpha = 1.0f) {
 #pragma unroll 1
   for (int c = 0; c < BN / 64; ++c) {
     uint32_t rg[32], ru[32];
@@ -118,7 +146,7 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
     tmem_ld32(tb + BN / 2 + c * 32, ru);
     tmem_ld_wait();
     const int c0 = col0 + c * 32;
-    if (row_ok && c0 < I) {
+    if (c0 < I) {
       float g[32], u[32], a[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -133,11 +161,16 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
         a[j] = silu_f(gc) * uc;
       }
       const int nc = min(32, I - c0);
-      store_row32(A + grow * I + c0, a, nc);
-      if (QF != 0 && qcodes) mx_emit<QF == 0 ? 1 : QF>(a, qcodes, qscales, grow, I, c0);
+      uint32_t w[16];
+      pack32(a, w);
+      store_rows32_t(stg, w, A + row0w * I + c0, I, nrows, nc, lane);
+      if (QF != 0 && qcodes && row_ok) mx_emit<QF == 0 ? 1 : QF>(w, qcodes, qscales, grow, I, c0);
       if (H) {
-        store_row32(H + grow * (2 * (size_t)I) + c0, g, nc);
-        store_row32(H + grow * (2 * (size_t)I) + I + c0, u, nc);
+        const size_t ldh = 2 * (size_t)I;
+        pack32(g, w);
+        store_rows32_t(stg, w, H + row0w * ldh + c0, ldh, nrows, nc, lane);
+        pack32(u, w);
+        store_rows32_t(stg, w, H + row0w * ldh + I + c0, ldh, nrows, nc, lane);
       }
     }
   }
@@ -146,9 +179,9 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
 // FC2 dgrad + SwiGLU backward: accumulator = dA[row, col0 ..]; with g, u from
 // the saved H: dH[:, c] = dA u s (1 + g (1 - s)), dH[:, I + c] = dA g s, s = sigmoid(g).
 // QF != 0 and qcodes != null: dH [rows, 2I] is also emitted MX-quantized (row-wise).
-// The saved H is read a chunk ahead of its use (raw bf16 words in registers), so the
-// load latency overlaps the previous chunk's arithmetic; epi_swiglu_bwd_prefetch,
-// called before the accumulator wait, has already pulled the tile's H into L2.
+// Each lane reads its own row of H a chunk ahead of its use (the loads of chunk c + 1 are
+// in flight during chunk c's arithmetic and stores); epi_swiglu_bwd_prefetch, called
+// before the accumulator wait, has already pulled the tile's H into L2.
 template <int BN>
 __device__ __forceinline__ void epi_swiglu_bwd_prefetch(const __nv_bfloat16* H, size_t grow, bool row_ok,
                                                         int col0, int I) {
@@ -163,62 +196,58 @@ __device__ __forceinline__ void epi_swiglu_bwd_prefetch(const __nv_bfloat16* H, 
   }
 }
 
-// 32 bf16 of a row (ncols < 32: the tail, zero-filled) as raw words.
-__device__ __forceinline__ void load_raw32(const __nv_bfloat16* src, uint4 (&w)[4], int ncols) {
-  if (ncols >= 32) {
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = __ldg(s4 + q);
-  } else {
-    const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
-    uint32_t* ww = reinterpret_cast<uint32_t*>(w);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t lo = 2 * j < ncols ? s16[2 * j] : 0u, hi = 2 * j + 1 < ncols ? s16[2 * j + 1] : 0u;
-      ww[j] = lo | (hi << 16);
-    }
-  }
-}
-
 // limit > 0: the forward's clamp is applied to the saved g, u again, and the gradient
 // is zero where a clamp was active (g > limit, |u| > limit).  SCALED: dA is the
-// accumulator times alpha.
-template <int BN, int QF = 0, bool SCALED = false>
+// accumulator times alpha.  TSTORE: dH goes out warp-transposed through stg; otherwise each
+// lane stores its own row.  (Timed on the full layer steps: transposed stores are faster in
+// the BF16 kernel, per-lane stores in the block-scaled one; transposed H loads lost in both.)
+// Warp-collective (stg, TSTORE): every lane calls it with the same tile arguments.
+__device__ __forceinline__ void ld_row32(const __nv_bfloat16* src, uint4 (&w)[4], int ncols) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    w[q] = 8 * q < ncols ? __ldg(reinterpret_cast<const uint4*>(src) + q) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ void st_row32(__nv_bfloat16* dst, const uint32_t (&w)[16], int ncols) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (8 * q < ncols)
+      reinterpret_cast<uint4*>(dst)[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+}
+template <int BN, int QF = 0, bool SCALED = false, bool TSTORE = true>
 __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
-                                               size_t grow, bool row_ok, int col0, int I,
-                                               uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr,
-                                               float limit = 0.0f, float alpha = 1.0f) {
-  const __nv_bfloat16* hrow = H + grow * (2 * (size_t)I);
-  uint4 ng[4], nu[4];  // the next chunk's gate / up words
+                                               size_t row0w, int nrows, bool row_ok, size_t grow, int col0, int I,
+                                               uint8_t* stg, int lane, uint8_t* qcodes = nullptr,
+                                               uint8_t* qscales = nullptr, float limit = 0.0f, float alpha = 1.0f) {
+  const size_t ldh = 2 * (size_t)I;
+  const __nv_bfloat16* hrow = H + grow * ldh;
+  uint4 ng[4], nu[4];  // the next chunk's gate / up words of this lane's row
   if (row_ok && col0 < I) {
-    load_raw32(hrow + col0, ng, I - col0);
-    load_raw32(hrow + I + col0, nu, I - col0);
+    ld_row32(hrow + col0, ng, I - col0);
+    ld_row32(hrow + I + col0, nu, I - col0);
   }
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int c0 = col0 + c * 32;
-    uint4 wg[4], wu[4];
+    uint32_t hgw[16], huw[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      wg[q] = ng[q];
-      wu[q] = nu[q];
+      hgw[4 * q] = ng[q].x; hgw[4 * q + 1] = ng[q].y; hgw[4 * q + 2] = ng[q].z; hgw[4 * q + 3] = ng[q].w;
+      huw[4 * q] = nu[q].x; huw[4 * q + 1] = nu[q].y; huw[4 * q + 2] = nu[q].z; huw[4 * q + 3] = nu[q].w;
     }
     if (row_ok && c0 + 32 < I && c + 1 < BN / 32) {
-      load_raw32(hrow + c0 + 32, ng, I - c0 - 32);
-      load_raw32(hrow + I + c0 + 32, nu, I - c0 - 32);
+      ld_row32(hrow + c0 + 32, ng, I - c0 - 32);
+      ld_row32(hrow + I + c0 + 32, nu, I - c0 - 32);
     }
     uint32_t rd[32];
     tmem_ld32(tb + c * 32, rd);
     tmem_ld_wait();
-    if (row_ok && c0 < I) {
+    if (c0 < I) {
       const int nc = min(32, I - c0);
-      const uint32_t* pg = reinterpret_cast<const uint32_t*>(wg);
-      const uint32_t* pu = reinterpret_cast<const uint32_t*>(wu);
       float dg[32], du[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        float hg = (j & 1) ? bf16_hi(pg[j >> 1]) : bf16_lo(pg[j >> 1]);
-        float hu = (j & 1) ? bf16_hi(pu[j >> 1]) : bf16_lo(pu[j >> 1]);
+        float hg = (j & 1) ? bf16_hi(hgw[j >> 1]) : bf16_lo(hgw[j >> 1]);
+        float hu = (j & 1) ? bf16_hi(huw[j >> 1]) : bf16_lo(huw[j >> 1]);
         const float da = SCALED ? __uint_as_float(rd[j]) * alpha : __uint_as_float(rd[j]);
         bool pass_g = true, pass_u = true;
         if (limit > 0.0f) {
@@ -231,12 +260,15 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
         dg[j] = pass_g ? da * hu * s * (1.0f + hg * (1.0f - s)) : 0.0f;
         du[j] = pass_u ? da * hg * s : 0.0f;
       }
-      store_row32(dH + grow * (2 * (size_t)I) + c0, dg, nc);
-      store_row32(dH + grow * (2 * (size_t)I) + I + c0, du, nc);
-      if (QF != 0 && qcodes) {
-        mx_emit<QF == 0 ? 1 : QF>(dg, qcodes, qscales, grow, 2 * I, c0);
-        mx_emit<QF == 0 ? 1 : QF>(du, qcodes, qscales, grow, 2 * I, I + c0);
-      }
+      uint32_t w[16];
+      pack32(dg, w);
+      if constexpr (TSTORE) store_rows32_t(stg, w, dH + row0w * ldh + c0, ldh, nrows, nc, lane);
+      else if (row_ok) st_row32(dH + grow * ldh + c0, w, nc);
+      if (QF != 0 && qcodes && row_ok) mx_emit<QF == 0 ? 1 : QF>(w, qcodes, qscales, grow, 2 * I, c0);
+      pack32(du, w);
+      if constexpr (TSTORE) store_rows32_t(stg, w, dH + row0w * ldh + I + c0, ldh, nrows, nc, lane);
+      else if (row_ok) st_row32(dH + grow * ldh + I + c0, w, nc);
+      if (QF != 0 && qcodes && row_ok) mx_emit<QF == 0 ? 1 : QF>(w, qcodes, qscales, grow, 2 * I, I + c0);
     }
   }
 }

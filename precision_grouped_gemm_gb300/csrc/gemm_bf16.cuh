@@ -76,11 +76,13 @@ struct GemmSmem {
 };
 
 // Epilogue staging bytes: the wgrad store keeps a ring of kWgradRing 4 KB atoms per
-// epilogue warp; the fp32 accumulate two 8 KB halves per warp.
+// epilogue warp; the fp32 accumulate two 8 KB halves per warp; the fwd / dgrad epilogues
+// a 2 KB chunk buffer per warp.
 constexpr int kWgradRing = 2;
 template <int MODE, int EPI>
 __host__ __device__ constexpr int epi_bytes() {
-  return MODE != kWgrad ? 0 : (EPI == kEpiAccumF32 ? 4 * 16384 : 4 * kWgradRing * 4096);
+  return MODE != kWgrad ? 4 * kEpiRowStageBytes
+                        : (EPI == kEpiAccumF32 ? 4 * 16384 : 4 * kWgradRing * 4096);
 }
 
 struct Tile {
@@ -349,7 +351,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
     GroupCursor cur;
-    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (epi_bytes<MODE, EPI>() / 4);  // wgrad: this warp's staging
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (epi_bytes<MODE, EPI>() / 4);  // this warp's staging
     int nstore = 0;
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
@@ -381,6 +383,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         continue;
       }
       const size_t grow = (size_t)T.row0 + r;
+      const size_t row0w = (size_t)T.row0 + q * 32;         // the warp's first output row
+      const int nrows = max(0, min(32, T.rows - q * 32));    // of which this many exist
       if (EPI == kEpiSwiGLUBwd)  // the saved H of this tile streams into L2 while the MMAs run
         epi_swiglu_bwd_prefetch<BN>(reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
                                     args.I);
@@ -388,13 +392,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
-        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0, args.I, nullptr,
-                       nullptr, args.swiglu_limit);
+        epi_swiglu<BN>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), row0w, nrows, row_ok, grow, T.col0,
+                       args.I, stg, lane, nullptr, nullptr, args.swiglu_limit);
       } else if (EPI == kEpiSwiGLUBwd) {
-        epi_swiglu_bwd<BN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
-                           args.I, nullptr, nullptr, args.swiglu_limit);
+        epi_swiglu_bwd<BN>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), row0w, nrows, row_ok, grow,
+                           T.col0, args.I, stg, lane, nullptr, nullptr, args.swiglu_limit);
       } else {
-        epi_store<BN>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols);
+        epi_store<BN>(tb, out, args.out_cols, row0w, nrows, T.col0, args.out_cols, stg, lane);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));

@@ -109,6 +109,13 @@ struct MxCfg {
   static constexpr int kTileBytes = 128 * kRowBytes;
 };
 
+// Epilogue staging: the wgrad store stages each epilogue warp's 32 rows x BN bf16; the fwd /
+// dgrad epilogues a 2 KB chunk buffer per warp.
+template <int MODE, int EPI, int BN>
+constexpr int mx_epi_bytes() {
+  return MODE == kWgrad ? 4 * 32 * BN * 2 : 4 * kEpiRowStageBytes;
+}
+
 // BN = 128 (kMxAccBufs accumulators) or 256 (one accumulator: TMEM cannot hold
 // two 256-column accumulators next to the scale factors).
 template <int FMT, int BN, int STAGES, int EPI_BYTES>
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   using C = MxCfg<FMT>;
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(!TS || FMT == kE4M3, "per-tensor scales are e4m3");
-  using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
+  using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<MODE, EPI, BN>()>;
   constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
   constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
   constexpr uint32_t kTmemCols = 512;
@@ -456,7 +463,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
     GroupCursor cur;
-    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (32 * BN * 2);
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (mx_epi_bytes<MODE, EPI, BN>() / 4);  // this warp's staging
     int nstore = 0;
     float alpha = 1.0f;  // TS: 1 / (s_A s_B), written by the quantizers earlier on the stream
     // The product of two fp32 scales is exact in fp64 and cannot overflow there (each scale is at
@@ -486,6 +493,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         continue;
       }
       const size_t grow = (size_t)T.row0 + r;
+      const size_t row0w = (size_t)T.row0 + q * 32;         // the warp's first output row
+      const int nrows = max(0, min(32, T.rows - q * 32));    // of which this many exist
       if (EPI == kEpiSwiGLUBwd)  // the saved H of this tile streams into L2 while the MMAs run
         epi_swiglu_bwd_prefetch<BN>(reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
                                     args.I);
@@ -493,13 +502,14 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
-        epi_swiglu<BN, FMT, TS>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), grow, row_ok, T.col0,
-                                args.I, args.q_codes, args.q_scales, args.swiglu_limit, alpha);
+        epi_swiglu<BN, FMT, TS>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), row0w, nrows, row_ok, grow,
+                                T.col0, args.I, stg, lane, args.q_codes, args.q_scales, args.swiglu_limit, alpha);
       } else if (EPI == kEpiSwiGLUBwd) {
-        epi_swiglu_bwd<BN, FMT, TS>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok,
-                                    T.col0, args.I, args.q_codes, args.q_scales, args.swiglu_limit, alpha);
+        epi_swiglu_bwd<BN, FMT, TS, false>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), row0w, nrows, row_ok,
+                                    grow, T.col0, args.I, stg, lane, args.q_codes, args.q_scales, args.swiglu_limit,
+                                    alpha);
       } else {
-        epi_store<BN, TS>(tb, out + grow * args.out_cols, row_ok, T.col0, args.out_cols, alpha);
+        epi_store<BN, TS>(tb, out, args.out_cols, row0w, nrows, T.col0, args.out_cols, stg, lane, alpha);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&tempty[acc]));
@@ -520,7 +530,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 template <int FMT, int MODE, int EPI, int STAGES, int BN = kMxBN, bool TS = false>
 int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a, int grid,
            cudaStream_t s) {
-  using L = MxSmem<FMT, BN, STAGES, MODE == kWgrad ? 4 * 32 * BN * 2 : 0>;
+  using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<MODE, EPI, BN>()>;
   auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES, BN, TS>;
   const size_t smem = L::bytes(a.G);
   static size_t attr_bytes = 0;  // per instantiation: raised to the largest G seen
@@ -538,7 +548,8 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
                 const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kBN = FMT == kE4M3 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;
   // stages for fwd / dgrad: 4 x (16 KB A + 32 KB B + 2 / 3 KB of scale atoms) next to the group tables
-  constexpr int kS = 4;
+  // and the epilogue staging
+  constexpr int kS = 4, kSb = 4;
   constexpr int kWBN = FMT == kE4M3 ? kMxWgradBNE4M3 : kMxWgradBNE2M1;
   // wgrad keeps 4 x 32 rows x kWBN bf16 of TMA-store staging next to the stages: e4m3 5 x 33 KB
   // + 32 KB, e2m1 3 x 51 KB + 64 KB (2 stages when the group tables of a large G leave no room)
@@ -546,7 +557,7 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kS, kBN>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kSb, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) {
     using L = MxSmem<FMT, kWBN, kSw, 4 * 32 * kWBN * 2>;
     DeviceInfo dev;
@@ -562,12 +573,12 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
 int dispatch_ts(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kBN = kMxFwdBNE4M3, kWBN = kMxWgradBNE4M3;
-  constexpr int kS = kBN == 128 ? 6 : 4;
-  constexpr int kSw = kWBN == 128 ? 5 : 2;
+  constexpr int kS = 4, kSb = 4;
+  constexpr int kSw = 5;
   if (mode == 0 && epi == 0) return run_mx<kE4M3, kFwd, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<kE4M3, kFwd, kEpiSwiGLU, kS, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<kE4M3, kDgrad, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 1) return run_mx<kE4M3, kDgrad, kEpiSwiGLUBwd, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<kE4M3, kDgrad, kEpiSwiGLUBwd, kSb, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<kE4M3, kWgrad, kEpiStore, kSw, kWBN, true>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }

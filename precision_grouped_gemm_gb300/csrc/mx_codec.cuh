@@ -88,4 +88,45 @@ __device__ __forceinline__ uint32_t quantize_block32(const uint32_t (&v16)[32], 
   return sc;
 }
 
+// The same block held as 16 words of bf16 pairs (element 2k in the low half of w[k]), as
+// the GEMM epilogues store it; the amax is a tree over the pairs (the max is associative,
+// so the result is the same as a running max, with a 5-deep dependency chain instead of 32).
+template <int FMT>
+__device__ __forceinline__ uint32_t quantize_block32_packed(const uint32_t (&w)[16], uint8_t* codes) {
+  uint32_t m[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) m[k] = max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu);
+#pragma unroll
+  for (int d = 8; d >= 1; d >>= 1)
+#pragma unroll
+    for (int k = 0; k < d; ++k) m[k] = max(m[k], m[k + d]);
+  uint32_t sc;
+  float mult;
+  const bool fin = block_scale<FMT>(m[0], sc, mult);
+  float f[32];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    f[2 * k] = fin ? __uint_as_float(w[k] << 16) * mult : 0.0f;
+    f[2 * k + 1] = fin ? __uint_as_float(w[k] & 0xFFFF0000u) * mult : 0.0f;
+  }
+  if (FMT == kE4M3) {
+    uint4 o[2];
+    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      ow[k] = cvt_e4m3x2(f[4 * k], f[4 * k + 1]) | (cvt_e4m3x2(f[4 * k + 2], f[4 * k + 3]) << 16);
+    reinterpret_cast<uint4*>(codes)[0] = o[0];
+    reinterpret_cast<uint4*>(codes)[1] = o[1];
+  } else {
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      ow[k] = cvt_e2m1x2(f[8 * k], f[8 * k + 1]) | (cvt_e2m1x2(f[8 * k + 2], f[8 * k + 3]) << 8) |
+              (cvt_e2m1x2(f[8 * k + 4], f[8 * k + 5]) << 16) | (cvt_e2m1x2(f[8 * k + 6], f[8 * k + 7]) << 24);
+    *reinterpret_cast<uint4*>(codes) = o;
+  }
+  return sc;
+}
+
 }  // namespace pgg

@@ -56,6 +56,9 @@ def parse_args():
     p.add_argument("--extra-steps", type=int, default=30)
     p.add_argument("--experts-cap", type=int, default=0,
                    help="keep only the first N experts (same per-expert shapes; small profiling case)")
+    p.add_argument("--only-extra", default=None, choices=["wgrad_accumulate_fp32", "moe_glue"],
+                   help="run only this one of the extra measurements (--extra-steps calls; with "
+                        "--experts-cap for the accumulate) and print its JSON: a profiling case")
     return p.parse_args()
 
 
@@ -419,13 +422,14 @@ def barrier(world):
 EXTRA = [wl.DSV4_MXFP8, wl.GPTOSS_BF16, wl.ZIPF_MXFP4, wl.DSV4_FP8]
 
 
-def measure_wgrad_accumulate(device, peaks, steps):
+def measure_wgrad_accumulate(device, peaks, steps, cap=0):
     """FC1 wgrad of the DeepSeek-shaped layer accumulated into an fp32 main_grad
-    [256, 4096, 4096]: algorithmic bytes = X + dH + fp32 read + write of main_grad."""
+    [256, 4096, 4096] (the first `cap` experts when cap > 0): algorithmic bytes = X + dH +
+    fp32 read + write of main_grad."""
     import precision_grouped_gemm_gb300 as pgg
     from precision_grouped_gemm_gb300.layer import build_layer_inputs
     w = wl.DSV4_BF16
-    lens, _, b = build_layer_inputs(w, device, allocate=False)
+    lens, _, b = build_layer_inputs(w, device, cap, allocate=False)
     M, G, Hd, I = int(lens.sum()), len(lens), w.hidden, w.inter
     del b.W1, b.W2
     dH = wl.gen_matrix(wl.KEY_DH, M, 2 * I, 0.25, w.seed, device=device)
@@ -447,10 +451,11 @@ def measure_wgrad_accumulate(device, peaks, steps):
     flops = 2.0 * M * 2 * I * Hd
     nbytes = 2.0 * M * Hd + 2.0 * M * 2 * I + 8.0 * G * 2 * I * Hd
     hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
-    res = {"call": "pgg_grouped_gemm_wgrad_accumulate (fc1 shape: dW_f32[256, 4096, 4096] += dH_g^T X_g)",
+    res = {"call": f"pgg_grouped_gemm_wgrad_accumulate (fc1 shape: dW_f32[{G}, 4096, 4096] += dH_g^T X_g)",
            "ms": ms, "tflops": flops / ms / 1e9, "gbs": nbytes / ms / 1e6,
            "roofline": {"bound": "hbm", "achieved": nbytes / ms / 1e6, "peak": hbm, "unit": "GB/s",
-                        "frac": nbytes / ms / 1e6 / hbm, "algo_bytes_per_launch": nbytes}}
+                        "frac": nbytes / ms / 1e6 / hbm, "algo_bytes_per_launch": nbytes,
+                        "traffic": None if cap else kernel_traffic("wgrad_accumulate_fp32", "fc1_wgrad_accumulate")}}
     del acc, dH, b
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
@@ -516,6 +521,14 @@ def run_pgg(args, w):
     device = torch.device("cuda", local)
     pgg.init(local)
     peaks, _ = load_peaks()
+    if args.only_extra:
+        if args.only_extra == "wgrad_accumulate_fp32":
+            r = measure_wgrad_accumulate(device, peaks, args.extra_steps, args.experts_cap)
+        else:
+            r = measure_moe_glue(device, peaks, args.extra_steps)
+        if rank == 0:
+            print(json.dumps({"only_extra": args.only_extra, **r}), flush=True)
+        return
     main = measure(w, args.steps, args.warmup, device, peaks, args.experts_cap,
                    0 if args.no_e2e else args.e2e_steps, world)
     extra = {}

@@ -89,11 +89,14 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
 // once.  One warp handles one 128-wide k-block p (blocks j = 4 p .. 4 p + 3, one
 // scale atom; it never straddles groups, whose spans are padded to 128) x 64 input
 // columns: for each block, lane l reads columns c0 + 2l, c0 + 2l + 1 of the
-// block's rows (32 coalesced 128-byte row loads in flight, no shared memory, no
-// block barrier), takes each column's amax and writes the column's 32 codes
-// (32 bytes e4m3 / 16 bytes e2m1).  The column's four scales of the k-block leave
-// together as one 32-bit store: one-byte scale stores were two thirds of the
-// kernel's store sectors.  Work items run with p fastest.
+// block's rows (32 coalesced 128-byte row loads), takes each column's amax and
+// converts the column's 32 codes.  The loads of block q + 1 are issued before block
+// q is converted, so 64 row loads per warp are in flight.  The codes collect in
+// the warp's shared-memory stage (64 columns x 128 codes) and leave as whole
+// output-row segments -- 128 bytes e4m3 / 64 bytes e2m1 per column, written by 8 /
+// 4 lanes at once -- instead of 16- or 32-byte pieces per lane (partial sectors).
+// The column's four scales of the k-block leave together as one 32-bit store.
+// Work items run with p fastest.
 //
 // Scales go to the blocked layout the block-scaled MMA reads: for every 128-row
 // block rb of the C rows and every 128-column k-block p of [0, M_pad), one 512-byte
@@ -103,19 +106,38 @@ __global__ void __launch_bounds__(256) mx_quant_rowwise_kernel(const uint4* __re
 constexpr int kColSlab = 64;
 constexpr int kColThreads = 256;
 
+// Shared-memory bytes of one warp's code stage, and of the kernel for G groups (the two
+// [G + 1] scan tables, rounded up to 16 bytes, then eight stages).
+template <int FMT>
+__host__ __device__ constexpr int col_stage_bytes() { return kColSlab * (FMT == kE4M3 ? 128 : 64); }
+template <int FMT>
+__host__ __device__ constexpr size_t col_smem_bytes(int G) {
+  return ((8 * (size_t)(G + 1) + 15) & ~(size_t)15) + (kColThreads / 32) * (size_t)col_stage_bytes<FMT>();
+}
+
+// Byte offset in a warp's stage of 16-byte chunk ch of stage column k (its codes
+// 16 ch .. 16 ch + 15, e4m3 bytes or e2m1 pairs): the stage is a run of 128-byte rows
+// whose chunks are permuted by ((k / 2) % 8), so that both the lane-per-column writes
+// and the row-segment reads spread over all banks.
+template <int FMT>
+__device__ __forceinline__ uint32_t col_stage_off(int k, int ch) {
+  const uint32_t lin = (uint32_t)k * (FMT == kE4M3 ? 128u : 64u) + 16u * ch;
+  return (lin & ~127u) | ((((lin >> 4) & 7u) ^ ((k >> 1) & 7u)) << 4);
+}
+
 // Byte offset of row r's four scales of k-block p in the blocked layout.
 __device__ __forceinline__ int64_t blocked_atom_word(int r, int p, int64_t M_pad) {
   const int m = r & 127;
   return (((int64_t)(r >> 7) * (M_pad >> 7) + p) << 9) + 16 * (m & 31) + 4 * (m >> 5);
 }
 
-// Quantize column `half` of the packed bf16 pairs v (zero past `valid`) and store its
-// 32 codes at position j; returns the scale byte (0 when the block holds no rows).
-// TENSOR (FP8 tensor-wise, e4m3): the multiplier is the tensor scale ts for every
-// block and no scale byte exists (a non-finite element converts on its own).
+// Quantize column `half` of the packed bf16 pairs v (zero past `valid`): its 32 codes
+// land in o (32 bytes e4m3 / 16 bytes e2m1, o[1] unused for e2m1); returns the scale
+// byte (0 when the block holds no rows).  TENSOR (FP8 tensor-wise, e4m3): the
+// multiplier is the tensor scale ts for every block and no scale byte exists (a
+// non-finite element converts on its own).
 template <int FMT, bool TENSOR = false>
-__device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int half, int valid, int c,
-                                                  int64_t M_pad, int j, uint8_t* __restrict__ codes_t,
+__device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int half, int valid, uint4 (&o)[2],
                                                   float ts = 0.0f) {
   uint32_t sc = 0;
   float mult = 0.0f;
@@ -124,15 +146,18 @@ __device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int h
     mult = ts;
     keep = valid > 0;
   } else {
-    uint32_t am = 0;
+    uint32_t m[16];
 #pragma unroll
-    for (int r = 0; r < 32; ++r) am = max(am, ((v[r] >> (16 * half)) & 0x7FFFu));
-    const bool fin = valid > 0 ? block_scale<FMT>(am, sc, mult) : true;
+    for (int r = 0; r < 16; ++r) m[r] = max((v[2 * r] >> (16 * half)) & 0x7FFFu, (v[2 * r + 1] >> (16 * half)) & 0x7FFFu);
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1)
+#pragma unroll
+      for (int r = 0; r < d; ++r) m[r] = max(m[r], m[r + d]);
+    const bool fin = valid > 0 ? block_scale<FMT>(m[0], sc, mult) : true;
     keep = valid > 0 && fin;
   }
+  uint32_t* ow = reinterpret_cast<uint32_t*>(o);
   if (FMT == kE4M3) {
-    uint4 o[2];
-    uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       float f[4];
@@ -140,12 +165,7 @@ __device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int h
       for (int e = 0; e < 4; ++e) f[e] = keep ? __uint_as_float((v[4 * k + e] >> (16 * half)) << 16) * mult : 0.0f;
       ow[k] = cvt_e4m3x2(f[0], f[1]) | (cvt_e4m3x2(f[2], f[3]) << 16);
     }
-    uint4* dst = reinterpret_cast<uint4*>(codes_t + (int64_t)c * M_pad + (int64_t)j * 32);
-    dst[0] = o[0];
-    dst[1] = o[1];
   } else {
-    uint4 o;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       float f[8];
@@ -154,9 +174,17 @@ __device__ __forceinline__ uint32_t colwise_codes(const uint32_t (&v)[32], int h
       ow[k] = cvt_e2m1x2(f[0], f[1]) | (cvt_e2m1x2(f[2], f[3]) << 8) | (cvt_e2m1x2(f[4], f[5]) << 16) |
               (cvt_e2m1x2(f[6], f[7]) << 24);
     }
-    *reinterpret_cast<uint4*>(codes_t + (int64_t)c * (M_pad / 2) + (int64_t)j * 16) = o;
   }
   return valid > 0 ? sc : 0u;
+}
+
+// Rows 32 q .. 32 q + 31 of the k-block's group rows (zero past `valid`), columns c, c + 1
+// as packed bf16 pairs.
+__device__ __forceinline__ void col_load32(const __nv_bfloat16* __restrict__ in, int64_t row0, int C, int c,
+                                           int valid, uint32_t (&v)[32]) {
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(in + row0 * C + c);
+#pragma unroll
+  for (int r = 0; r < 32; ++r) v[r] = r < valid ? __ldg(src + (int64_t)r * (C / 2)) : 0u;
 }
 
 // TENSOR: FP8 tensor-wise codes (multiplier amax_scale[0] for every element), no scales.
@@ -166,11 +194,14 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
     int G, uint8_t* __restrict__ codes_t, uint8_t* __restrict__ scales_t, int64_t M_pad,
     int32_t* err, const float* __restrict__ amax_scale = nullptr) {
   static_assert(!TENSOR || FMT == kE4M3, "tensor-wise scaling is e4m3");
-  extern __shared__ int32_t s_dyn[];
+  constexpr int kCB = FMT == kE4M3 ? 128 : 64;  // code bytes of one column in one k-block
+  extern __shared__ __align__(16) int32_t s_dyn[];
   int32_t* s_off = s_dyn;             // [G+1] row offsets
   int32_t* s_blk = s_dyn + (G + 1);   // [G+1] prefix of 32-blocks in the padded layout
   __shared__ int s_bad;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* stg = reinterpret_cast<uint8_t*>(s_dyn) + ((8 * (size_t)(G + 1) + 15) & ~(size_t)15) +
+                 (size_t)warp * col_stage_bytes<FMT>();
   if (warp == 0) {
     bool bad;
     if (lens) {
@@ -203,14 +234,16 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
   const int64_t nwarps = (int64_t)gridDim.x * (kColThreads / 32);
   for (int64_t t = (int64_t)blockIdx.x * (kColThreads / 32) + warp; t < total; t += nwarps) {
     const int p = (int)(t % nkb);
-    const int c = (int)(t / nkb) * kColSlab + 2 * lane;
-    if (c >= C) {  // pad rows of the last atom: scale 0, no codes
+    const int c0 = (int)(t / nkb) * kColSlab;  // the warp's first column
+    const int c = c0 + 2 * lane;               // this lane's two columns
+    if (c0 >= C) {  // a slab of pad rows of the last atom: scale 0, no codes
       if (!TENSOR && c < C128) {
         *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = 0u;
         *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = 0u;
       }
       continue;
     }
+    const bool live = c < C;  // columns past C (warp-divergent only in the last slab): zero codes, scale 0
     int len = 0, b0 = 0;
     int64_t grow0 = 0;
     if (4 * p < used) {
@@ -219,18 +252,45 @@ __global__ void __launch_bounds__(kColThreads) mx_quant_colwise_kernel(
       len = s_off[g + 1] - s_off[g];
       grow0 = s_off[g];
     }
+    if (!live) len = 0;
     uint32_t sc0 = 0, sc1 = 0;
+    uint32_t v[32], nv[32];
+    col_load32(in, grow0 + 32 * b0, C, c, min(32, max(0, len - 32 * b0)), nv);
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {
       const int valid = min(32, max(0, len - 32 * (b0 + q)));
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(in + (grow0 + 32 * (b0 + q)) * C + c);
-      uint32_t v[32];
 #pragma unroll
-      for (int r = 0; r < 32; ++r) v[r] = r < valid ? __ldg(src + (int64_t)r * (C / 2)) : 0u;
-      sc0 |= colwise_codes<FMT, TENSOR>(v, 0, valid, c, M_pad, 4 * p + q, codes_t, ts) << (8 * q);
-      sc1 |= colwise_codes<FMT, TENSOR>(v, 1, valid, c + 1, M_pad, 4 * p + q, codes_t, ts) << (8 * q);
+      for (int r = 0; r < 32; ++r) v[r] = nv[r];
+      if (q < 3) col_load32(in, grow0 + 32 * (b0 + q + 1), C, c, min(32, max(0, len - 32 * (b0 + q + 1))), nv);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint4 o[2];
+        const uint32_t sc = colwise_codes<FMT, TENSOR>(v, h, valid, o, ts);
+        if (h == 0) sc0 |= sc << (8 * q); else sc1 |= sc << (8 * q);
+        const int k = 2 * lane + h;
+        if (FMT == kE4M3) {
+          *reinterpret_cast<uint4*>(stg + col_stage_off<FMT>(k, 2 * q)) = o[0];
+          *reinterpret_cast<uint4*>(stg + col_stage_off<FMT>(k, 2 * q + 1)) = o[1];
+        } else {
+          *reinterpret_cast<uint4*>(stg + col_stage_off<FMT>(k, q)) = o[0];
+        }
+      }
     }
-    if (!TENSOR) {
+    __syncwarp();
+    // write-out: column k's kCB code bytes of this k-block are one contiguous stretch of
+    // output row c0 + k; kCB / 16 lanes per column, 32 * 16 / kCB columns per instruction
+    constexpr int kLpc = kCB / 16;
+    const int ch = lane % kLpc;
+#pragma unroll
+    for (int i = 0; i < kColSlab * kLpc / 32; ++i) {
+      const int k = i * (32 / kLpc) + lane / kLpc;
+      const uint4 x = *reinterpret_cast<const uint4*>(stg + col_stage_off<FMT>(k, ch));
+      if (c0 + k < C)
+        *reinterpret_cast<uint4*>(codes_t + (int64_t)(c0 + k) * (FMT == kE4M3 ? M_pad : M_pad / 2) +
+                                  (int64_t)p * kCB + 16 * ch) = x;
+    }
+    __syncwarp();
+    if (!TENSOR && c < C128) {
       *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c, p, M_pad)) = sc0;
       *reinterpret_cast<uint32_t*>(scales_t + blocked_atom_word(c + 1, p, M_pad)) = sc1;
     }
@@ -381,21 +441,18 @@ int launch_mx_quantize_colwise(const void* in, int64_t M, int64_t C, const int32
   int st = current_device(&dev);
   if (st != PGG_OK) return st;
   const int64_t total = (M_pad / 128) * (((C + 127) / 128 * 128) / kColSlab);  // warp work items
-  const size_t smem = 8 * (size_t)(G + 1);
+  const bool e4 = fmt == PGG_FMT_E4M3;
+  const size_t smem = e4 ? col_smem_bytes<kE4M3>(G) : col_smem_bytes<kE2M1>(G);
+  auto kern = e4 ? mx_quant_colwise_kernel<kE4M3> : mx_quant_colwise_kernel<kE2M1>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
   int per_sm = 0;  // resident CTAs per SM: the grid-stride loop runs one wave of them
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      &per_sm, fmt == PGG_FMT_E4M3 ? mx_quant_colwise_kernel<kE4M3> : mx_quant_colwise_kernel<kE2M1>, kColThreads,
-      smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kColThreads, smem);
   if (e != cudaSuccess) return cuda_status(e);
   const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * std::max(per_sm, 1)));
-  auto* x = static_cast<const __nv_bfloat16*>(in);
-  if (fmt == PGG_FMT_E4M3)
-    mx_quant_colwise_kernel<kE4M3><<<grid, kColThreads, smem, s>>>(x, M, (int)C, group_lens, G,
-                                                                   codes_t, scales_t, M_pad, err);
-  else
-    mx_quant_colwise_kernel<kE2M1><<<grid, kColThreads, smem, s>>>(x, M, (int)C, group_lens, G,
-                                                                   codes_t, scales_t, M_pad, err);
+  kern<<<grid, kColThreads, smem, s>>>(static_cast<const __nv_bfloat16*>(in), M, (int)C, group_lens, G, codes_t,
+                                       scales_t, M_pad, err, nullptr);
   return cuda_status(cudaGetLastError());
 }
 
@@ -425,10 +482,12 @@ int launch_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int3
   int st = current_device(&dev);
   if (st != PGG_OK) return st;
   const int64_t total = (M_pad / 128) * (((C + 127) / 128 * 128) / kColSlab);  // warp work items
-  const size_t smem = 8 * (size_t)(G + 1);
+  const size_t smem = col_smem_bytes<kE4M3>(G);
   auto kern = mx_quant_colwise_kernel<kE4M3, true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return cuda_status(e);
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kColThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kColThreads, smem);
   if (e != cudaSuccess) return cuda_status(e);
   const int64_t want = (total + kColThreads / 32 - 1) / (kColThreads / 32);
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(want, (int64_t)dev.sms * std::max(per_sm, 1)));

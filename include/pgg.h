@@ -279,8 +279,8 @@ int pgg_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t
                              const float* amax_scale, uint8_t* codes_t, int64_t M_pad, int32_t* err,
                              void* stream);
 
-/* Bytes of the workspace pgg_fp8_grouped_gemm needs: 4 * max(K, G*N, M_pad)
- * rounded up to 512 (pass M_pad = 0 outside wgrad). */
+/* Bytes of the workspace pgg_fp8_grouped_gemm needs: 0 (the FP8 MMAs read no
+ * scale factors).  Kept so that callers sizing a workspace keep working. */
 size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad);
 
 /* FP8 tensor-wise grouped GEMM (grouped_gemm_fp8): the operands, shapes and
@@ -299,11 +299,11 @@ size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad);
  * pgg_grouped_fc1_swiglu_clamped (0: none; SwiGLU epilogue only).  There is no
  * fused quantized output: a current-scaled operand needs the amax of the whole
  * tensor before any of its codes.
- * scale_a / scale_b point at each operand's s (its amax_scale).  ws: device
- * scratch of pgg_fp8_workspace_size bytes, 16-byte aligned, owned by the
- * caller and overwritten on the stream by each call (it holds the unit block
- * scales the tensor cores read).  The size rules, errors and group semantics
- * are pgg_mx_grouped_gemm's (fwd K and dgrad N multiples of 128). */
+ * scale_a / scale_b point at each operand's s (its amax_scale).  The tensor
+ * cores run the plain FP8 MMA (tcgen05 kind::f8f6f4, e4m3 x e4m3, fp32
+ * accumulation); 1 / (s_A s_B) is applied in the epilogue.  ws / ws_bytes:
+ * reserved, ignored (may be NULL / 0).  The size rules, errors and group
+ * semantics are pgg_mx_grouped_gemm's (fwd K and dgrad N multiples of 128). */
 int pgg_fp8_grouped_gemm(int mode, int epilogue, const uint8_t* A, const float* scale_a, const uint8_t* B,
                          const float* scale_b, const void* H, const int32_t* group_lens, void* out, void* out2,
                          int64_t M, int64_t N, int64_t K, int G, int64_t M_pad, float swiglu_limit, void* ws,

@@ -362,14 +362,12 @@ def fp8_grouped_gemm(mode, A, scale_a, B, scale_b, group_lens, M, N, K, out=None
         else:
             shape = (G, N, K)
         out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
-    need = fp8_workspace_size(N, K, G, M_pad if mode == MODE_WGRAD else 0)
-    if ws is None:
-        ws = torch.empty(need, dtype=torch.uint8, device=dev)
     _dev(A, scale_a, B, scale_b, group_lens, out, out2, H, ws, err)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().pgg_fp8_grouped_gemm(mode, epilogue, _ptr(A), _ptr(scale_a), _ptr(B), _ptr(scale_b), _ptr(H),
                                       _ptr(_lens(group_lens)), _ptr(out), _ptr(out2), M, N, K, G, M_pad,
-                                      swiglu_limit, _ptr(ws), ws.numel() * ws.element_size(), _ptr(err),
-                                      _stream(stream)), "pgg_fp8_grouped_gemm")
+                                      swiglu_limit, _ptr(ws), ws_bytes, _ptr(err), _stream(stream)),
+           "pgg_fp8_grouped_gemm")
     return out
 
 

@@ -18,10 +18,10 @@
 //                         the column-wise operands At = dY^T [N, M_pad], Bt = X^T [K, M_pad]
 //
 // FP8 tensor-wise operands (one fp32 scale s per tensor, codes = e4m3(x s)) run the
-// e4m3 instantiations with TS = true: every block scale is 1 (E8M0 127), read from a
-// small constant buffer through zero row strides (each tile reads the same atoms), and
-// the epilogue multiplies the accumulator by 1 / (s_A s_B) before the store or the
-// SwiGLU (forward) / SwiGLU backward (dgrad).
+// e4m3 instantiations with TS = true: the plain FP8 MMA (kind::f8f6f4, no block scales:
+// no scale loads, no scale copies to tensor memory), and the epilogue multiplies the
+// accumulator by 1 / (s_A s_B) before the store or the SwiGLU (forward) / SwiGLU
+// backward (dgrad).
 #include <algorithm>
 
 #include "epilogue.cuh"
@@ -117,15 +117,16 @@ constexpr int mx_epi_bytes() {
 }
 
 // BN = 128 (kMxAccBufs accumulators) or 256 (one accumulator: TMEM cannot hold
-// two 256-column accumulators next to the scale factors).
-template <int FMT, int BN, int STAGES, int EPI_BYTES>
+// two 256-column accumulators next to the scale factors).  SF: the stages hold scale
+// atoms (block-scaled operands; not the FP8 tensor-wise ones).
+template <int FMT, int BN, int STAGES, int EPI_BYTES, bool SF = true>
 struct MxSmem {
   static constexpr int kA = MxCfg<FMT>::kTileBytes;
   static constexpr int kB = MxCfg<FMT>::kRowBytes * BN;
   // kSub SFA atoms, then kSub SFB atoms for each 128 rows of B (512 B each), padded to keep
   // every stage's tiles 1024-byte aligned
   static constexpr int kSFA = MxCfg<FMT>::kSub * 512;
-  static constexpr int kSF = (kSFA * (1 + BN / 128) + 1023) / 1024 * 1024;
+  static constexpr int kSF = SF ? (kSFA * (1 + BN / 128) + 1023) / 1024 * 1024 : 0;
   static constexpr int kStage = kA + kB + kSF;
   static constexpr int kEpiOff = STAGES * kStage;
   static constexpr int kBarOff = kEpiOff + EPI_BYTES;
@@ -175,9 +176,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   using C = MxCfg<FMT>;
   static_assert(BN == 128 || BN == 256, "BN");
   static_assert(!TS || FMT == kE4M3, "per-tensor scales are e4m3");
-  using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<MODE, EPI, BN>()>;
+  using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<MODE, EPI, BN>(), !TS>;
+  constexpr bool kSF = !TS;                              // block scale factors (else plain FP8 MMAs)
   constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
-  constexpr uint32_t kIdesc = idesc_mx(C::kElem, kMxBM, BN);
+  constexpr uint32_t kIdesc = TS ? idesc_f8f6f4(0, kMxBM, BN) : idesc_mx(C::kElem, kMxBM, BN);
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kSfCol0 = NACC * BN;                 // scale-factor columns after the accumulators
   // per stage: for each of the kSub scale sub-blocks, SFA 4 columns and SFB 4 per 128 rows
@@ -192,8 +194,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   // dgrad B; forward weights B), fetched as whole 512-byte atoms by bulk copy.  A
   // forward weight tile whose rows do not start on an atom (N, or I for SwiGLU, not
   // a multiple of 128) is gathered row by row from the blocked layout instead.
-  constexpr bool kGatherA = MODE != kWgrad;
-  const bool gather_b = MODE == kFwd && (!args.b_bulk || (EPI == kEpiSwiGLU && BN < 256));
+  constexpr bool kGatherA = kSF && MODE != kWgrad;
+  const bool gather_b = kSF && MODE == kFwd && (!args.b_bulk || (EPI == kEpiSwiGLU && BN < 256));
   // reduction elements of the operands (wgrad: the group's own length, per tile)
   const int red_all = MODE == kWgrad ? 0 : args.red;
   // bytes of one row of the reduction axis of a group's slice of the dgrad B operand
@@ -290,7 +292,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         const int nsub = min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK);
         const int p0 = kb * C::kSub;  // first scale atom of this k-block along the reduction axis
         if (lane == 0) {
-          const uint32_t sf_bytes = 512u * (uint32_t)nsub * ((kGatherA ? 0u : 1u) + (gather_b ? 0u : BN / 128u));
+          const uint32_t sf_bytes =
+              kSF ? 512u * (uint32_t)nsub * ((kGatherA ? 0u : 1u) + (gather_b ? 0u : BN / 128u)) : 0u;
           mbar_arrive_expect_tx(fb, L::kA + L::kB + sf_bytes);
           if (MODE == kFwd) {
             tma_load_2d(sa, &tmA, fb, kbyte, T.row0);
@@ -310,10 +313,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           }
           // blocked scale atoms: ((row block) * atoms-per-row-block + atom along K) * 512; the
           // nsub atoms of a k-block are adjacent, so one bulk copy takes them all
-          if (!kGatherA)
+          if (kSF && !kGatherA)
             bulk_load(ssf, args.SA + ((int64_t)(T.row0 >> 7) * (args.sa_ld >> 2) + (T.poff >> 7) + p0) * 512,
                       512u * nsub, fb);
-          if (!gather_b) {
+          if (kSF && !gather_b) {
             const int p = MODE == kWgrad ? (T.poff >> 7) + p0 : MODE == kDgrad ? T.g * (args.red >> 7) + p0 : p0;
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h) {
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           if (kGatherA) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
 #pragma unroll
           for (int sub = 0; sub < C::kSub; ++sub) {
-            if (sub >= nsub) break;
+            if (!kSF || sub >= nsub) break;
             tmem_cp_32x128b_x4(sfa_t + 4 * sub, smem_desc(ssf + sub * 512, 0, 128, kSwizzleNone));
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32 of the sub-block: 4 columns per 128 rows
@@ -438,7 +441,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             const uint32_t sfid = FMT == kE4M3 ? (uint32_t)j : (uint32_t)(2 * (j % 2));
             const uint32_t id = kIdesc | idesc_sf_ids(sfid, sfid);
             const uint32_t sfa = sfa_t + 4 * sub, sfb = sfb_t + sub * kSfbPer;
-            if (FMT == kE4M3) mma_mxf8(d_tmem, ad, bd, id, sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
+            if (TS) mma_f8f6f4(d_tmem, ad, bd, kIdesc, (kb > 0 || j > 0) ? 1u : 0u);
+            else if (FMT == kE4M3) mma_mxf8(d_tmem, ad, bd, id, sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
             else mma_mxf4(d_tmem, ad, bd, id, sfa, sfb, (kb > 0 || j > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&empty[stage]));
@@ -530,7 +534,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
 template <int FMT, int MODE, int EPI, int STAGES, int BN = kMxBN, bool TS = false>
 int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const MxArgs& a, int grid,
            cudaStream_t s) {
-  using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<MODE, EPI, BN>()>;
+  using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<MODE, EPI, BN>(), !TS>;
   auto kern = grouped_gemm_mx_kernel<FMT, MODE, EPI, STAGES, BN, TS>;
   const size_t smem = L::bytes(a.G);
   static size_t attr_bytes = 0;  // per instantiation: raised to the largest G seen
@@ -675,15 +679,7 @@ int launch_mx_gemm(const MxCall& c) {
   if (c.mode != 2) tc = ta;  // unused outside wgrad
   const int grid = std::max(1, std::min(dev.sms, tiles_ub));
   if (ts) {
-    // unit block scales: zero row strides make every row (block) of SA and SB read the
-    // first row block's atoms, so SA = SB = one buffer of mx_unit_scale_bytes() bytes of 127
-    // (largest offset read: fwd K / 128, dgrad G N / 128, wgrad M_pad / 128 atoms of 512 B),
-    // written here on the stream ahead of the kernel
-    const size_t ub = mx_unit_scale_bytes(c.N, c.K, c.G, c.mode == 2 ? c.M_pad : 0);
-    cudaError_t e = cudaMemsetAsync(const_cast<uint8_t*>(c.SA), 127, ub, c.stream);
-    if (e != cudaSuccess) return cuda_status(e);
-    a.SA = a.SB = c.SA;
-    a.sa_ld = a.sb_ld = 0;
+    a.SA = a.SB = nullptr;  // no block scales
     return dispatch_ts(c.mode, c.epi, ta, tb, tc, a, grid, c.stream);
   }
   return e4 ? dispatch_mx<kE4M3>(c.mode, c.epi, ta, tb, tc, a, grid, c.stream)

@@ -81,8 +81,7 @@ struct MxCall {
   int32_t* err;
   cudaStream_t stream;
   float limit = 0.0f;  // SwiGLU clamp limit (0: none)
-  // FP8 tensor-wise operands (e4m3, plain store): device fp32 scales s_A, s_B; SA = SB =
-  // a buffer of mx_unit_scale_bytes() bytes of 127 (unit block scales)
+  // FP8 tensor-wise operands (e4m3, plain FP8 MMAs): device fp32 scales s_A, s_B; SA, SB unused
   const float* ts_a = nullptr;
   const float* ts_b = nullptr;
   unsigned long long wait_ns = 0;  // pipeline wait limit (0: the kernels' default)
@@ -90,14 +89,6 @@ struct MxCall {
 };
 int launch_mx_gemm(const MxCall& c);
 
-// Bytes of unit block scales a tensor-scaled MX GEMM reads (any mode): 512-byte atoms for
-// the longest scale row, 4 max(K, G N, M_pad) rounded up to 512.
-inline size_t mx_unit_scale_bytes(int64_t N, int64_t K, int G, int64_t M_pad) {
-  int64_t m = K;
-  if ((int64_t)G * N > m) m = (int64_t)G * N;
-  if (M_pad > m) m = M_pad;
-  return (size_t)((4 * m + 511) / 512 * 512);
-}
 
 // FP8 tensor-wise current scaling (mx_quant.cu): amax_scale = device float[2] {s, amax}
 int launch_fp8_tensor_scale(const void* in, int64_t n, float* amax_scale, cudaStream_t s);

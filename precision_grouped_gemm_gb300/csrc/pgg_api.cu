@@ -151,14 +151,16 @@ static int mx_gemm_impl(int mode, int fmt, int epilogue, const uint8_t* A, const
   if (epilogue != PGG_EPI_NONE && epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
   if (epilogue == PGG_EPI_SWIGLU && mode == PGG_MODE_WGRAD) return PGG_ERR_INVALID_ARG;
   if ((st = check_common(M, G, group_lens))) return st;
-  if (!A || !SA || !B || !SB || !out) return PGG_ERR_INVALID_ARG;
+  const bool block_scaled = ts_a == nullptr;  // else FP8 tensor-wise: no scale factors
+  if (!A || !B || !out || (block_scaled && (!SA || !SB))) return PGG_ERR_INVALID_ARG;
   if (mode == PGG_MODE_DGRAD && epilogue == PGG_EPI_SWIGLU && !H) return PGG_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(B) || !aligned16(out) || (out2 && !aligned16(out2)) ||
       (H && !aligned16(H)))
     return PGG_ERR_ALIGNMENT;
   // blocked scale atoms (SB always, wgrad SA) are fetched by 16-byte-aligned bulk copies,
   // row-major scales (fwd / dgrad SA) by 4-byte copies
-  if ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned4(SA) || !aligned16(SB)) return PGG_ERR_ALIGNMENT;
+  if (block_scaled && ((mode == PGG_MODE_WGRAD && !aligned16(SA)) || !aligned4(SA) || !aligned16(SB)))
+    return PGG_ERR_ALIGNMENT;
   if (err && !aligned4(err)) return PGG_ERR_ALIGNMENT;
   if ((st = check_dim(N, 8)) || (st = check_dim(K, 8))) return st;
   if (mode == PGG_MODE_FWD && (K % 128 || (epilogue == PGG_EPI_SWIGLU && N % 16)))
@@ -408,26 +410,22 @@ int pgg_fp8_quantize_colwise(const void* in, int64_t M, int64_t C, const int32_t
 }
 
 size_t pgg_fp8_workspace_size(int64_t N, int64_t K, int G, int64_t M_pad) {
-  if (N < 0 || K < 0 || G < 1 || M_pad < 0) return 0;
-  return mx_unit_scale_bytes(N, K, G, M_pad);
+  (void)N; (void)K; (void)G; (void)M_pad;
+  return 0;  // the plain FP8 MMAs read no scale factors: no scratch
 }
 
 int pgg_fp8_grouped_gemm(int mode, int epilogue, const uint8_t* A, const float* scale_a, const uint8_t* B,
                          const float* scale_b, const void* H, const int32_t* group_lens, void* out, void* out2,
                          int64_t M, int64_t N, int64_t K, int G, int64_t M_pad, float swiglu_limit, void* ws,
                          size_t ws_bytes, int32_t* err, void* stream) {
-  if (!scale_a || !scale_b || !ws) return PGG_ERR_INVALID_ARG;
-  if (!aligned4(scale_a) || !aligned4(scale_b) || !aligned16(ws)) return PGG_ERR_ALIGNMENT;
+  (void)ws; (void)ws_bytes;  // reserved: no scratch is needed
+  if (!scale_a || !scale_b) return PGG_ERR_INVALID_ARG;
+  if (!aligned4(scale_a) || !aligned4(scale_b)) return PGG_ERR_ALIGNMENT;
   if (!(swiglu_limit >= 0.0f) || swiglu_limit > 3.0e38f) return PGG_ERR_INVALID_ARG;
   if (swiglu_limit > 0.0f && epilogue != PGG_EPI_SWIGLU) return PGG_ERR_INVALID_ARG;
   if (N < 0 || K < 0 || M_pad < 0 || G < 1 || G > kMaxGroups) return PGG_ERR_INVALID_ARG;
-  const size_t need = mx_unit_scale_bytes(N, K, G, mode == PGG_MODE_WGRAD ? M_pad : 0);
-  if (ws_bytes < need) return PGG_ERR_INVALID_ARG;
-  // ws receives the unit block scales (E8M0 127 = 2^0) on the stream before each launch:
-  // the caller owns it and may have reused it since the last call
-  return mx_gemm_impl(mode, PGG_FMT_E4M3, epilogue, A, static_cast<const uint8_t*>(ws), B,
-                      static_cast<const uint8_t*>(ws), H, group_lens, out, out2, nullptr, nullptr, M, N, K, G,
-                      M_pad, swiglu_limit, err, stream, scale_a, scale_b);
+  return mx_gemm_impl(mode, PGG_FMT_E4M3, epilogue, A, nullptr, B, nullptr, H, group_lens, out, out2, nullptr,
+                      nullptr, M, N, K, G, M_pad, swiglu_limit, err, stream, scale_a, scale_b);
 }
 
 size_t pgg_moe_permute_workspace_size(int64_t T, int E) {

@@ -297,6 +297,18 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// Plain FP8 / FP6 / FP4 MMA (kind::f8f6f4, no block scales): D[tmem] (+)= A[smem] B[smem]^T,
+// K = 32 elements of an 8-bit type per instruction.
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Shared -> tensor memory copy of a 32-row x 128-bit matrix, replicated into all
 // four 32-lane quarters (the layout block-scaled MMAs read scale factors from).
 __device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
@@ -340,6 +352,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
          | (1u << 10)                   // B format: bf16
          | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f8f6f4: fp32 D, A and B of element type `elem` (e4m3 = 0),
+// both K-major, M x N (the kind::f16 layout with the 8-bit type codes).
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t elem, uint32_t M, uint32_t N) {
+  return (1u << 4)             // D format: f32
+         | (elem << 7)         // A format
+         | (elem << 10)        // B format
+         | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // Instruction descriptor for the block-scaled kinds (fp32 D implied): A/B element

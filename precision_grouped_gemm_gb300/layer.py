@@ -330,8 +330,6 @@ class Fp8LayerBuffers:
         else:
             b.M_pad = B.mx_pad_rows(M, G)
         Mp = b.M_pad
-        ws = max(B.fp8_workspace_size(I2, Hd, G), B.fp8_workspace_size(Hd, I, G),
-                 B.fp8_workspace_size(Hd, I, G, Mp), B.fp8_workspace_size(I2, Hd, G, Mp))
         u8, bf, f32 = torch.uint8, torch.bfloat16, torch.float32
         e = lambda *s: torch.empty(s, dtype=u8, device=dev)
         t = lambda *s: torch.empty(s, dtype=bf, device=dev)
@@ -340,7 +338,7 @@ class Fp8LayerBuffers:
             "sx": sc(), "Xq": e(M, Hd), "A": t(M, I), "H": t(M, I2), "sa": sc(), "Aq": e(M, I), "Y": t(M, Hd),
             "sdy": sc(), "dYq": e(M, Hd), "dH": t(M, I2), "dYc": e(Hd, Mp), "Ac": e(I, Mp), "dW2": t(G, Hd, I),
             "sdh": sc(), "dHq": e(M, I2), "dX": t(M, Hd), "dHc": e(I2, Mp), "Xc": e(Hd, Mp), "dW1": t(G, I2, Hd),
-            "ws": e(ws), "err": torch.zeros(1, dtype=torch.int32, device=dev),
+            "err": torch.zeros(1, dtype=torch.int32, device=dev),
         }
         return b
 
@@ -349,7 +347,7 @@ def fp8_layer_step(b: Fp8LayerBuffers, between=None):
     """One FP8 tensor-wise expert-layer fwd + bwd: 4 tensor scales, 8 quantizations and 6 grouped
     GEMMs (FC1 and FC2-dgrad with the SwiGLU and its backward in the epilogue)."""
     u, gl = b.bufs, b.group_lens
-    err, Mp, ws = u["err"], b.M_pad, u["ws"]
+    err, Mp = u["err"], b.M_pad
     M, Hd = b.X.shape
     I = u["A"].shape[1]
     G = gl.numel()
@@ -358,25 +356,25 @@ def fp8_layer_step(b: Fp8LayerBuffers, between=None):
         lambda: B.fp8_tensor_scale(b.X, u["sx"]),
         lambda: B.fp8_quantize_rowwise(b.X, u["sx"], u["Xq"]),
         lambda: g(B.MODE_FWD, u["Xq"], u["sx"], b.W1q, b.s_w1, gl, M, 2 * I, Hd, out=u["A"], out2=u["H"],
-                  epilogue=B.EPI_SWIGLU, ws=ws, err=err),
+                  epilogue=B.EPI_SWIGLU, err=err),
         lambda: B.fp8_tensor_scale(u["A"], u["sa"]),
         lambda: B.fp8_quantize_rowwise(u["A"], u["sa"], u["Aq"]),
-        lambda: g(B.MODE_FWD, u["Aq"], u["sa"], b.W2q, b.s_w2, gl, M, Hd, I, out=u["Y"], ws=ws, err=err),
+        lambda: g(B.MODE_FWD, u["Aq"], u["sa"], b.W2q, b.s_w2, gl, M, Hd, I, out=u["Y"], err=err),
         lambda: B.fp8_tensor_scale(b.dY, u["sdy"]),
         lambda: B.fp8_quantize_rowwise(b.dY, u["sdy"], u["dYq"]),
         lambda: g(B.MODE_DGRAD, u["dYq"], u["sdy"], b.W2t, b.s_w2, gl, M, Hd, I, out=u["dH"], H=u["H"],
-                  epilogue=B.EPI_SWIGLU, ws=ws, err=err),
+                  epilogue=B.EPI_SWIGLU, err=err),
         lambda: B.fp8_quantize_colwise(b.dY, gl, u["sdy"], Mp, u["dYc"], err=err),
         lambda: B.fp8_quantize_colwise(u["A"], gl, u["sa"], Mp, u["Ac"], err=err),
-        lambda: g(B.MODE_WGRAD, u["dYc"], u["sdy"], u["Ac"], u["sa"], gl, M, Hd, I, out=u["dW2"], M_pad=Mp, ws=ws,
+        lambda: g(B.MODE_WGRAD, u["dYc"], u["sdy"], u["Ac"], u["sa"], gl, M, Hd, I, out=u["dW2"], M_pad=Mp,
                   err=err),
         lambda: B.fp8_tensor_scale(u["dH"], u["sdh"]),
         lambda: B.fp8_quantize_rowwise(u["dH"], u["sdh"], u["dHq"]),
-        lambda: g(B.MODE_DGRAD, u["dHq"], u["sdh"], b.W1t, b.s_w1, gl, M, 2 * I, Hd, out=u["dX"], ws=ws, err=err),
+        lambda: g(B.MODE_DGRAD, u["dHq"], u["sdh"], b.W1t, b.s_w1, gl, M, 2 * I, Hd, out=u["dX"], err=err),
         lambda: B.fp8_quantize_colwise(u["dH"], gl, u["sdh"], Mp, u["dHc"], err=err),
         lambda: B.fp8_quantize_colwise(b.X, gl, u["sx"], Mp, u["Xc"], err=err),
         lambda: g(B.MODE_WGRAD, u["dHc"], u["sdh"], u["Xc"], u["sx"], gl, M, 2 * I, Hd, out=u["dW1"], M_pad=Mp,
-                  ws=ws, err=err),
+                  err=err),
     )
     assert len(calls) == len(FP8_STEP_NAMES) and G > 0
     for i, c in enumerate(calls):

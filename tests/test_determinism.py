@@ -111,8 +111,6 @@ def test_fp8_gemms_bitwise():
     W = util.gen(wl.KEY_W1, G * N, K, 0.5, 45, device=DEV)
     Mp = pgg.mx_pad_rows(M, G)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    ws = torch.empty(max(pgg.fp8_workspace_size(N, K, G), pgg.fp8_workspace_size(N, K, G, Mp)),
-                     dtype=torch.uint8, device=DEV)
 
     def run():
         sx, sd, sw = pgg.fp8_tensor_scale(X), pgg.fp8_tensor_scale(dY), pgg.fp8_tensor_scale(W)
@@ -120,9 +118,9 @@ def test_fp8_gemms_bitwise():
         wt = pgg.fp8_quantize_colwise(W, torch.full((G,), N, dtype=torch.int32, device=DEV), sw, G * N)
         xc, dc = pgg.fp8_quantize_colwise(X, gl, sx, Mp, err=err), pgg.fp8_quantize_colwise(dY, gl, sd, Mp, err=err)
         g = pgg.fp8_grouped_gemm
-        y = g(pgg.MODE_FWD, xq, sx, wq, sw, gl, M, N, K, ws=ws, err=err)
-        dx = g(pgg.MODE_DGRAD, dq, sd, wt, sw, gl, M, N, K, ws=ws, err=err)
-        dw = g(pgg.MODE_WGRAD, dc, sd, xc, sx, gl, M, N, K, M_pad=Mp, ws=ws, err=err)
+        y = g(pgg.MODE_FWD, xq, sx, wq, sw, gl, M, N, K, err=err)
+        dx = g(pgg.MODE_DGRAD, dq, sd, wt, sw, gl, M, N, K, err=err)
+        dw = g(pgg.MODE_WGRAD, dc, sd, xc, sx, gl, M, N, K, M_pad=Mp, err=err)
         return (sx, sd, sw, xq, dq, wq, wt, xc, dc, y, dx, dw)
 
     a, b = _twice(run)

@@ -237,27 +237,27 @@ def test_fp8_layer_full_size_isolated():
     Hs = syn(wl.KEY_H, M, 2 * I, SYN_STD["H"], device=DEV)
     dHs = syn(wl.KEY_DH, M, 2 * I, SYN_STD["dH"], device=DEV)
     As[0, 0], dHs[0, 0] = PLANT["A"], PLANT["dH"]
-    u, gl, err, Mp, ws = fb.bufs, fb.group_lens, fb.bufs["err"], fb.M_pad, fb.bufs["ws"]
+    u, gl, err, Mp = fb.bufs, fb.group_lens, fb.bufs["err"], fb.M_pad
     g = pgg.fp8_grouped_gemm
     # the six GEMMs of the layer step, each on generator inputs scaled and quantized by the GPU
     sx = pgg.fp8_tensor_scale(fb.X)
     Xq = pgg.fp8_quantize_rowwise(fb.X, sx)
     g(pgg.MODE_FWD, Xq, sx, fb.W1q, fb.s_w1, gl, M, 2 * I, Hd, out=u["A"], out2=u["H"], epilogue=pgg.EPI_SWIGLU,
-      ws=ws, err=err)
+      err=err)
     sa = pgg.fp8_tensor_scale(As)
-    Y = g(pgg.MODE_FWD, pgg.fp8_quantize_rowwise(As, sa), sa, fb.W2q, fb.s_w2, gl, M, Hd, I, ws=ws, err=err)
+    Y = g(pgg.MODE_FWD, pgg.fp8_quantize_rowwise(As, sa), sa, fb.W2q, fb.s_w2, gl, M, Hd, I, err=err)
     sdy = pgg.fp8_tensor_scale(fb.dY)
     dH = g(pgg.MODE_DGRAD, pgg.fp8_quantize_rowwise(fb.dY, sdy), sdy, fb.W2t, fb.s_w2, gl, M, Hd, I, H=Hs,
-           epilogue=pgg.EPI_SWIGLU, ws=ws, err=err)
+           epilogue=pgg.EPI_SWIGLU, err=err)
     dYc = pgg.fp8_quantize_colwise(fb.dY, gl, sdy, Mp, err=err)
     Ac = pgg.fp8_quantize_colwise(As, gl, sa, Mp, err=err)
-    dW2 = g(pgg.MODE_WGRAD, dYc, sdy, Ac, sa, gl, M, Hd, I, M_pad=Mp, ws=ws, err=err)
+    dW2 = g(pgg.MODE_WGRAD, dYc, sdy, Ac, sa, gl, M, Hd, I, M_pad=Mp, err=err)
     sdh = pgg.fp8_tensor_scale(dHs)
-    dX = g(pgg.MODE_DGRAD, pgg.fp8_quantize_rowwise(dHs, sdh), sdh, fb.W1t, fb.s_w1, gl, M, 2 * I, Hd, ws=ws,
+    dX = g(pgg.MODE_DGRAD, pgg.fp8_quantize_rowwise(dHs, sdh), sdh, fb.W1t, fb.s_w1, gl, M, 2 * I, Hd,
            err=err)
     dHc = pgg.fp8_quantize_colwise(dHs, gl, sdh, Mp, err=err)
     Xc = pgg.fp8_quantize_colwise(fb.X, gl, sx, Mp, err=err)
-    dW1 = g(pgg.MODE_WGRAD, dHc, sdh, Xc, sx, gl, M, 2 * I, Hd, M_pad=Mp, ws=ws, err=err)
+    dW1 = g(pgg.MODE_WGRAD, dHc, sdh, Xc, sx, gl, M, 2 * I, Hd, M_pad=Mp, err=err)
     assert pgg.read_error(err) == 0
     # each tensor's {s, amax}: the planted element and 448 / it, bit for bit
     ref_s = {k: of8.fp8_tensor_scale(np.array([v])) for k, v in PLANT.items()}

@@ -56,7 +56,13 @@ constexpr int kMxWgradStoreAtoms = 2;  // 64-column atoms per bulk store of a wg
 // start before the epilogue has drained tile t: a wgrad tile has a single k-block,
 // so the accumulator hand-off round trip is as long as the epilogue itself.
 constexpr int kMxAccBufs = 3;
-constexpr int kMxThreads = 192;
+// Warps: 0 load producer (TMA tiles, bulk scale atoms), 1 MMA issuer, 2-5 epilogue, and for the
+// fwd / dgrad of block-scaled operands 6, the scale gatherer: the row-major scales of the A
+// operand (and of a forward weight tile not on whole atoms) are gathered into the atom layout
+// by 4-byte cp.async copies, which took the producer about as long as its TMA issue (clock64
+// on the Zipf-routed MXFP4 layer: 273 of 629 ns per k-block), so they run beside it.
+template <int MODE, bool TS>
+__host__ __device__ constexpr int mx_threads() { return MODE != kWgrad && !TS ? 224 : 192; }
 
 struct MxArgs {
   const int32_t* group_lens;
@@ -170,7 +176,7 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
 }
 
 template <int FMT, int MODE, int EPI, int STAGES, int BN, bool TS = false>
-__global__ void __launch_bounds__(kMxThreads, 1)
+__global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
   using C = MxCfg<FMT>;
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   bool aborted = false;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer: TMA codes + cp.async scales
+    // ------------------------------------------------------------ producer: TMA codes + bulk scale atoms
     GroupCursor cur;
     int stage = 0;
     uint32_t phase = 0;
@@ -336,48 +342,6 @@ __global__ void __launch_bounds__(kMxThreads, 1)
             }
           }
         }
-        // gathered scale factors (row-major operands): for scale sub-block s, lane l fetches
-        // rows l, l+32, l+64, l+96 of the operand tile (4 bytes = the sub-block's 4 block
-        // scales) into word 4 l + i of atom s
-#pragma unroll
-        for (int sub = 0; sub < C::kSub; ++sub) {
-          if (sub >= nsub) break;
-          const int sfa_col = (p0 + sub) * 4;  // byte column of this sub-block in the row-major A scales
-#pragma unroll
-          for (int i = 0; i < BN / 32; ++i) {
-            const int m = lane + 32 * i;
-            // A rows: fwd/dgrad token rows
-            if (kGatherA && i < 4) {
-              const int ar = T.row0 + m;
-              const bool aok = ar < args.a_rows;
-              cp_async_4(ssf + sub * 512 + (lane * 4 + i) * 4,
-                         args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0), aok ? 4u : 0u);
-            }
-            // B rows
-            int br;
-            bool bok;
-            if (MODE == kFwd) {
-              constexpr int kHalf = BN / 2;  // SwiGLU: gate rows, then the matching up rows
-              const int n = (EPI == kEpiSwiGLU) ? (m < kHalf ? T.col0 + m : args.I + T.col0 + (m - kHalf))
-                                                : T.col0 + m;
-              const int lim = (EPI == kEpiSwiGLU) ? (m < kHalf ? args.I : 2 * args.I) : args.nw;
-              bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m % kHalf) < args.I);
-              br = T.g * args.nw + n;
-            } else {
-              br = T.col0 + m;
-              bok = br < args.b_rows;
-            }
-            // B row m goes to atom (m / 128, sub), word 4 (m % 32) + (m % 128) / 32; the source
-            // is row br's 4 bytes of this sub-block in the blocked layout
-            if (gather_b)
-              cp_async_4(ssf + L::kSFA * (1 + i / 4) + sub * 512 + (lane * 4 + (i % 4)) * 4,
-                         args.SB + (bok ? ((((int64_t)br >> 7) * (args.sb_ld >> 2) + p0 + sub) << 9) +
-                                              16 * (br & 31) + 4 * ((br >> 5) & 3)
-                                        : 0),
-                         bok ? 4u : 0u);
-          }
-        }
-        if (kGatherA || gather_b) cp_async_arrive_noinc(fb);
         __syncwarp();
         ++issued;
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -458,6 +422,75 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     if (aborted && lane == 0) {
       mma_commit(smem_u32(drain));
       mbar_wait_drain(smem_u32(drain), 0);
+    }
+  } else if (warp == 6) {
+    // ------------------------------------------------------------ scale gatherer (fwd / dgrad, block-scaled)
+    // the producer's tile and k-block sequence; its 32 cp.async arrivals complete each stage's
+    // full barrier together with the producer's expect_tx arrival and copies
+    if (kGatherA || gather_b) {
+      GroupCursor cur;
+      int stage = 0;
+      uint32_t phase = 0;
+      long long issued = 0;
+      bool stalled = false;
+      for (int t = blockIdx.x; t < total_tiles && !aborted && !stalled; t += gridDim.x) {
+        const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
+        for (int kb = 0; kb < T.nkb; ++kb) {
+          if (issued == args.stall_at) { stalled = true; break; }
+          if (!warp_wait(smem_u32(&empty[stage]), phase ^ 1u, s_ctl)) { aborted = true; break; }
+          const uint32_t ssf = smem0 + stage * L::kStage + L::kA + L::kB;
+          const uint32_t fb = smem_u32(&full[stage]);
+          const int valid = red_all - kb * C::kBK;
+          const int nsub = min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK);
+          const int p0 = kb * C::kSub;
+          // gathered scale factors (row-major operands): for scale sub-block s, lane l fetches
+          // rows l, l+32, l+64, l+96 of the operand tile (4 bytes = the sub-block's 4 block
+          // scales) into word 4 l + i of atom s
+#pragma unroll
+          for (int sub = 0; sub < C::kSub; ++sub) {
+            if (sub >= nsub) break;
+            const int sfa_col = (p0 + sub) * 4;  // byte column of this sub-block in the row-major A scales
+#pragma unroll
+            for (int i = 0; i < BN / 32; ++i) {
+              const int m = lane + 32 * i;
+              // A rows: fwd/dgrad token rows
+              if (kGatherA && i < 4) {
+                const int ar = T.row0 + m;
+                const bool aok = ar < args.a_rows;
+                cp_async_4(ssf + sub * 512 + (lane * 4 + i) * 4,
+                           args.SA + (aok ? (int64_t)ar * args.sa_ld + sfa_col : 0), aok ? 4u : 0u);
+              }
+              // B rows
+              int br;
+              bool bok;
+              if (MODE == kFwd) {
+                constexpr int kHalf = BN / 2;  // SwiGLU: gate rows, then the matching up rows
+                const int n = (EPI == kEpiSwiGLU) ? (m < kHalf ? T.col0 + m : args.I + T.col0 + (m - kHalf))
+                                                  : T.col0 + m;
+                const int lim = (EPI == kEpiSwiGLU) ? (m < kHalf ? args.I : 2 * args.I) : args.nw;
+                bok = n < lim && (EPI != kEpiSwiGLU || T.col0 + (m % kHalf) < args.I);
+                br = T.g * args.nw + n;
+              } else {
+                br = T.col0 + m;
+                bok = br < args.b_rows;
+              }
+              // B row m goes to atom (m / 128, sub), word 4 (m % 32) + (m % 128) / 32; the source
+              // is row br's 4 bytes of this sub-block in the blocked layout
+              if (gather_b)
+                cp_async_4(ssf + L::kSFA * (1 + i / 4) + sub * 512 + (lane * 4 + (i % 4)) * 4,
+                           args.SB + (bok ? ((((int64_t)br >> 7) * (args.sb_ld >> 2) + p0 + sub) << 9) +
+                                                16 * (br & 31) + 4 * ((br >> 5) & 3)
+                                          : 0),
+                           bok ? 4u : 0u);
+            }
+          }
+          cp_async_arrive_noinc(fb);
+          __syncwarp();
+          ++issued;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      cp_async_wait_all();  // nothing of this warp's lands after the block exits
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -543,7 +576,7 @@ int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, 
     if (e != cudaSuccess) return e == cudaErrorInvalidValue ? PGG_ERR_UNSUPPORTED : cuda_status(e);
     attr_bytes = smem;
   }
-  kern<<<grid, kMxThreads, smem, s>>>(ta, tb, tc, a);
+  kern<<<grid, mx_threads<MODE, TS>(), smem, s>>>(ta, tb, tc, a);
   return cuda_status(cudaGetLastError());
 }
 

@@ -51,6 +51,17 @@ constexpr int kMxWgradBNE2M1 = 256;
 // 2.62 -> 1.71 ms; MXFP8 fc2 fwd 0.403 -> 0.368 ms, fc1 dgrad 0.762 -> 0.724 ms.
 constexpr int kMxFwdBNE4M3 = 256;
 constexpr int kMxFwdBNE2M1 = 256;
+// The e4m3 FC2 dgrad + SwiGLU backward is the exception: its epilogue (read H, write dH and
+// its MX codes) takes about as long as its MMAs, and the single accumulator of a 256-wide tile
+// serialises the two; 128-wide tiles with three accumulators overlap them (timed on the
+// DeepSeek-shaped layers: MXFP8 0.61 -> 0.55 ms, FP8 tensor-wise 0.54 -> 0.47 ms; the e2m1
+// one is slower at 128, 1.61 -> 1.80 ms, and every other fwd / dgrad call at either format).
+constexpr int kMxSwiGLUBwdBNE4M3 = 128;
+// Tile width of a fwd / dgrad call; swiglu: the call's SwiGLU epilogue flag (a dgrad with it is
+// the SwiGLU backward).
+__host__ __device__ constexpr int mx_fwd_bn(bool e4m3, int mode, int swiglu) {
+  return e4m3 ? (mode == kDgrad && swiglu ? kMxSwiGLUBwdBNE4M3 : kMxFwdBNE4M3) : kMxFwdBNE2M1;
+}
 constexpr int kMxWgradStoreAtoms = 2;  // 64-column atoms per bulk store of a wgrad tile
 // TMEM accumulator buffers of a 128-column tile.  Three let the MMA for tile t+2
 // start before the epilogue has drained tile t: a wgrad tile has a single k-block,
@@ -584,9 +595,10 @@ template <int FMT>
 int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kBN = FMT == kE4M3 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;
+  constexpr int kBNb = mx_fwd_bn(FMT == kE4M3, kDgrad, 1);  // the SwiGLU backward's tile width
   // stages for fwd / dgrad: 4 x (16 KB A + 32 KB B + 2 / 3 KB of scale atoms) next to the group tables
-  // and the epilogue staging
-  constexpr int kS = 4, kSb = 4;
+  // and the epilogue staging; 6 x (16 KB + 16 KB + 1 KB) for a 128-wide tile
+  constexpr int kS = 4, kSb = kBNb == 128 ? 6 : 4;
   constexpr int kWBN = FMT == kE4M3 ? kMxWgradBNE4M3 : kMxWgradBNE2M1;
   // wgrad keeps 4 x 32 rows x kWBN bf16 of TMA-store staging next to the stages: e4m3 5 x 33 KB
   // + 32 KB, e2m1 3 x 51 KB + 64 KB (2 stages when the group tables of a large G leave no room)
@@ -594,7 +606,7 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   if (mode == 0 && epi == 0) return run_mx<FMT, kFwd, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<FMT, kDgrad, kEpiStore, kS, kBN>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kSb, kBN>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kSb, kBNb>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) {
     using L = MxSmem<FMT, kWBN, kSw, 4 * 32 * kWBN * 2>;
     DeviceInfo dev;
@@ -610,12 +622,13 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
 int dispatch_ts(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                 const MxArgs& a, int grid, cudaStream_t s) {
   constexpr int kBN = kMxFwdBNE4M3, kWBN = kMxWgradBNE4M3;
-  constexpr int kS = 4, kSb = 4;
+  constexpr int kBNb = mx_fwd_bn(true, kDgrad, 1);
+  constexpr int kS = 4, kSb = kBNb == 128 ? 6 : 4;
   constexpr int kSw = 5;
   if (mode == 0 && epi == 0) return run_mx<kE4M3, kFwd, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 0 && epi == 1) return run_mx<kE4M3, kFwd, kEpiSwiGLU, kS, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx<kE4M3, kDgrad, kEpiStore, kS, kBN, true>(ta, tb, tc, a, grid, s);
-  if (mode == 1 && epi == 1) return run_mx<kE4M3, kDgrad, kEpiSwiGLUBwd, kSb, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 1 && epi == 1) return run_mx<kE4M3, kDgrad, kEpiSwiGLUBwd, kSb, kBNb, true>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<kE4M3, kWgrad, kEpiStore, kSw, kWBN, true>(ta, tb, tc, a, grid, s);
   return PGG_ERR_INVALID_ARG;
 }
@@ -654,7 +667,7 @@ int launch_mx_gemm(const MxCall& c) {
   a.stall_at = c.stall_at;
   const bool ts = c.ts_a != nullptr;
   if (ts && (!e4 || !c.ts_b || c.q_codes)) return PGG_ERR_INVALID_ARG;
-  const int fbn = e4 ? kMxFwdBNE4M3 : kMxFwdBNE2M1;  // fwd / dgrad tile width
+  const int fbn = mx_fwd_bn(e4, c.mode, c.epi);  // fwd / dgrad tile width
   int tiles_ub;
   if (c.mode == 0) {
     const int64_t N = c.N, K = c.K;

@@ -283,6 +283,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // Descriptors of stage 0's A and B tiles.  The start-address field holds address / 16 in 14
+    // bits, which every address of this block fits, so the descriptor of address + d (d a
+    // multiple of 16) is the base descriptor + d / 16.
+    const uint64_t kDescA = kAmn ? smem_desc(smem_a0, BK * 128, 1024, kSwizzle128B)
+                                 : smem_desc(smem_a0, 16, 1024, kSwizzle128B);
+    const uint64_t kDescB = kBmn ? smem_desc(smem_b0, BK * 128, 1024, kSwizzle128B)
+                                 : smem_desc(smem_b0, 16, 1024, kSwizzle128B);
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const Tile T = decode_tile<MODE, EPI, BN, BK>(t, args, s_off, s_tile, cur);
       if (T.nkb == 0) continue;  // empty wgrad group: the epilogue writes zeros
@@ -320,13 +327,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
         if (lane == 0) {
+          const uint64_t ao = (uint64_t)(sa - smem_a0) >> 4, bo = (uint64_t)(sb - smem_b0) >> 4;
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
-            uint64_t ad, bd;
-            if (kAmn) ad = smem_desc(sa + ks * 2048, BK * 128, 1024, kSwizzle128B);
-            else ad = smem_desc(sa + ks * 32, 16, 1024, kSwizzle128B);
-            if (kBmn) bd = smem_desc(sb + ks * 2048, BK * 128, 1024, kSwizzle128B);
-            else bd = smem_desc(sb + ks * 32, 16, 1024, kSwizzle128B);
+            // K step ks: 16 rows (2048 bytes) further along an MN-major tile, 32 bytes along a K-major one
+            const uint64_t ad = kDescA + ao + (kAmn ? 128 * ks : 2 * ks);
+            const uint64_t bd = kDescB + bo + (kBmn ? 128 * ks : 2 * ks);
             mma_f16(d_tmem, ad, bd, kIdesc, (kb > 0 || ks > 0) ? 1u : 0u);
           }
           mma_commit(smem_u32(&empty[stage]));

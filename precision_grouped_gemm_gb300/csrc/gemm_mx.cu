@@ -374,6 +374,12 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // Shared-memory descriptors of stage 0's A tile, B tile and first scale atom.  A descriptor's
+    // start-address field holds address / 16 in 14 bits, which every address of this block fits,
+    // so the descriptor of address + d (d a multiple of 16) is the base descriptor + d / 16.
+    const uint64_t kDescA = smem_desc(smem0, 16, C::kSbo, C::kSwizzle);
+    const uint64_t kDescB = smem_desc(smem0 + L::kA, 16, C::kSbo, C::kSwizzle);
+    const uint64_t kDescSf = smem_desc(smem0 + L::kA + L::kB, 0, 128, kSwizzleNone);
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
       if (T.nkb == 0) continue;
@@ -384,9 +390,7 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
         if (!warp_wait(smem_u32(&full[stage]), phase, s_ctl)) { aborted = true; break; }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sa = smem0 + stage * L::kStage;
-          const uint32_t sb = sa + L::kA;
-          const uint32_t ssf = sb + L::kB;
+          const uint64_t so = (uint64_t)(stage * L::kStage) >> 4;  // this stage's descriptor offset
           const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;  // kSub x 4 SFA columns
           const uint32_t sfb_t = sfa_t + 4 * C::kSub;                    // kSub x kSfbPer SFB columns
           // scale sub-blocks and MMAs of this k-block that hold data: past the end of K / N (an
@@ -399,18 +403,17 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
 #pragma unroll
           for (int sub = 0; sub < C::kSub; ++sub) {
             if (!kSF || sub >= nsub) break;
-            tmem_cp_32x128b_x4(sfa_t + 4 * sub, smem_desc(ssf + sub * 512, 0, 128, kSwizzleNone));
+            tmem_cp_32x128b_x4(sfa_t + 4 * sub, kDescSf + so + (sub * 512 >> 4));
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32 of the sub-block: 4 columns per 128 rows
-              tmem_cp_32x128b_x4(sfb_t + sub * kSfbPer + 4 * h,
-                                 smem_desc(ssf + L::kSFA * (1 + h) + sub * 512, 0, 128, kSwizzleNone));
+              tmem_cp_32x128b_x4(sfb_t + sub * kSfbPer + 4 * h, kDescSf + so + ((L::kSFA * (1 + h) + sub * 512) >> 4));
           }
 #pragma unroll
           for (int j = 0; j < C::kMmas; ++j) {
             if (j >= nmma) break;
             const int sub = j / (C::kMmas / C::kSub);  // the scale sub-block this MMA's K-range lies in
-            const uint64_t ad = smem_desc(sa + j * 32, 16, C::kSbo, C::kSwizzle);
-            const uint64_t bd = smem_desc(sb + j * 32, 16, C::kSbo, C::kSwizzle);
+            const uint64_t ad = kDescA + so + 2 * j;  // + 32 bytes of K per MMA
+            const uint64_t bd = kDescB + so + 2 * j;
             // scale bytes of the MMA's K-range within its atom: e4m3 one 32-block (j), e2m1 the
             // pair of 32-blocks (2 (j % 2), 2 (j % 2) + 1)
             const uint32_t sfid = FMT == kE4M3 ? (uint32_t)j : (uint32_t)(2 * (j % 2));

@@ -114,6 +114,56 @@ __device__ __forceinline__ void epi_store(uint32_t tb, __nv_bfloat16* out, size_
   }
 }
 
+// Plain store through a whole-tile stage, so that tensor memory is free before the global
+// stores: pass 1 (epi_stage_tile) converts the warp's 32 rows x BN accumulators to bf16 into
+// stg (32 rows x 2 BN bytes, 16-byte chunk j of row r at position j ^ (r % 8) of its row);
+// the caller then releases the accumulator; pass 2 (epi_store_staged) writes the rows out,
+// 8 rows x 64 contiguous bytes per instruction.  SCALED as epi_store.
+template <int BN, bool SCALED = false>
+__device__ __forceinline__ void epi_stage_tile(uint32_t tb, uint8_t* stg, int lane, float alpha = 1.0f) {
+  uint8_t* row = stg + lane * (2 * BN);
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t rv[32];
+    tmem_ld32(tb + c * 32, rv);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = __uint_as_float(rv[j]);
+      if constexpr (SCALED) v[j] *= alpha;
+    }
+    uint32_t w[16];
+    pack32(v, w);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(row + (((4 * c + k) ^ (lane & 7)) << 4)) =
+          make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+  }
+}
+// Pass 2: NC staged columns starting at stage column s0 (a multiple of 32; the stage's rows hold
+// PITCH columns) go to output columns col0 .. of rows row0w ..; columns from ncols on are dropped.
+template <int NC, int PITCH = NC>
+__device__ __forceinline__ void epi_store_staged(const uint8_t* stg, __nv_bfloat16* out, size_t ld, size_t row0w,
+                                                 int nrows, int col0, int ncols, int lane, int s0 = 0) {
+  __syncwarp();
+  const int J = lane & 3;
+#pragma unroll 1
+  for (int c = 0; c < NC / 32; ++c) {
+    const int c0 = col0 + c * 32;
+    if (c0 >= ncols) break;
+    const int nc = min(32, ncols - c0);
+    const int ch = s0 / 8 + 4 * c + J;  // 16-byte chunk of the staged row
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int R = 8 * i + (lane >> 2);
+      const uint4 x = *reinterpret_cast<const uint4*>(stg + R * (2 * PITCH) + ((ch ^ (R & 7)) << 4));
+      if (R < nrows && 8 * J < nc) *reinterpret_cast<uint4*>(out + (row0w + R) * ld + c0 + 8 * J) = x;
+    }
+  }
+  __syncwarp();
+}
+
 // Optional fused MX output (QF = kE4M3 / kE2M1): the 32 bf16 values just stored at
 // columns c0..c0+31 of row `grow` of a [rows, ld] tensor -- w[16], packed in pairs exactly
 // as stored -- form one row-wise MX block; its codes and scale go to codes[grow, c0 ..] /

@@ -224,3 +224,30 @@ def test_mx_fused_quantized_outputs(fmt):
     # fused outputs exist only for the SwiGLU epilogues
     with pytest.raises(pgg.PggError):
         pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, gl, M, 2 * I, K, out_q=(qc, qs))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_mx_fwd_dgrad_max_groups(fmt):
+    # 1024 groups (the most the kernels scan): their shared-memory group tables leave the
+    # plain-store kernels one pipeline stage fewer than at a few hundred groups
+    rng = np.random.default_rng(71)
+    G, N, K = 1024, 128, 128
+    lens = np.where(rng.random(G) < 0.1, rng.integers(1, 40, G), 0).astype(np.int32)
+    M = int(lens.sum())
+    gl = torch.from_numpy(lens).to(DEV)
+    X, W = _bf16(wl.KEY_X, M, K, 1.0, 71), _bf16(wl.KEY_W1, G * N, K, 0.5, 71)
+    dY = _bf16(wl.KEY_DY, M, N, 1.0, 71)
+    A, SA = pgg.mx_quantize_rowwise(X.to(DEV), fmt)
+    B, SB = pgg.mx_quantize_rowwise_blocked(W.to(DEV), fmt)
+    err = _err()
+    Y = pgg.mx_grouped_gemm(pgg.MODE_FWD, fmt, A, SA, B, SB, gl, M, N, K, err=err)
+    dA, dSA = pgg.mx_quantize_rowwise(dY.to(DEV), fmt)
+    Bt, SBt = pgg.mx_quantize_colwise(W.to(DEV), torch.full((G,), N, dtype=torch.int32, device=DEV), fmt, G * N)
+    dX = pgg.mx_grouped_gemm(pgg.MODE_DGRAD, fmt, dA, dSA, Bt, SBt, gl, M, N, K, err=err)
+    assert pgg.read_error(err) == 0
+    oA, oSA = omx.mx_quantize_rowwise(util.bits(X), fmt)
+    oB, oSB = omx.mx_quantize_rowwise(util.bits(W), fmt)
+    util.assert_close(Y, omx.mx_grouped_gemm_fwd(fmt, oA, oSA, oB, oSB, lens, G), f"mx fwd {fmt}, G = 1024")
+    odA, odSA = omx.mx_quantize_rowwise(util.bits(dY), fmt)
+    oBt, oSBt = omx.mx_quantize_colwise(util.bits(W), [N] * G, fmt, G * N)
+    util.assert_close(dX, omx.mx_grouped_gemm_dgrad(fmt, odA, odSA, oBt, oSBt, lens, G), f"mx dgrad {fmt}, G = 1024")

@@ -179,26 +179,13 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& y) {
   acc[6] += w * bf16_lo(y.w); acc[7] += w * bf16_hi(y.w);
 }
 
-// Choice j of the token whose positions / weights lanes hold in (my_p, my_w): its weight
-// and the 16-byte piece v of its row (not loaded when j >= k, the entry is dropped, or v is
-// past the row).  Every lane takes part in the shuffles.
-struct Choice {
-  uint4 y;
-  float w;
-  bool use;
-};
-__device__ __forceinline__ Choice load_choice(const __nv_bfloat16* __restrict__ Ys, int32_t my_p, float my_w, int j,
-                                              int k, int64_t H, int64_t v, int64_t nvec) {
-  Choice c;
-  const int32_t p = __shfl_sync(0xffffffffu, my_p, j & 31);
-  c.w = __shfl_sync(0xffffffffu, my_w, j & 31);
-  c.use = j < k && p >= 0 && v < nvec;
-  c.y = c.use ? __ldg(reinterpret_cast<const uint4*>(Ys + (int64_t)p * H) + v) : make_uint4(0, 0, 0, 0);
-  return c;
-}
-
 // out[t] = sum_j w[t, j] * Ys[pos[t, j]] (w = 1 when w == nullptr), fp32 accumulation in
-// choice order, bf16 output.  One warp per token; lane j < k holds pos / w of choice j.
+// choice order, bf16 output.  One warp per token; lane j < k holds pos / w of choice j.  A lane
+// owns kCombineU 16-byte column pieces at once, and the next choice's pieces are loaded while
+// the current one is accumulated: up to 2 kCombineU loads in flight per lane.  (With one warp
+// per token the DeepSeek-shaped routing gives ~27 warps per SM; two loads in flight per lane
+// left the kernel latency-bound at about half the DRAM bandwidth.)
+constexpr int kCombineU = 4;
 __global__ void __launch_bounds__(kCopyThreads) moe_combine_kernel(const __nv_bfloat16* __restrict__ Ys,
                                                                    const int32_t* __restrict__ pos,
                                                                    const float* __restrict__ w, int64_t T, int k,
@@ -209,24 +196,55 @@ __global__ void __launch_bounds__(kCopyThreads) moe_combine_kernel(const __nv_bf
   for (int64_t t = (int64_t)blockIdx.x * (kCopyThreads / 32) + (threadIdx.x >> 5); t < T; t += nwarp) {
     const int32_t my_p = lane < k ? __ldg(pos + t * k + lane) : -1;
     const float my_w = (lane < k && w) ? __ldg(w + t * k + lane) : 1.0f;
-    // warp-uniform trip count: every lane takes part in the shuffles, only the loads are guarded
-    for (int64_t v0 = 0; v0 < nvec; v0 += 32) {
-      const int64_t v = v0 + lane;
-      float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      // two choices' rows in flight at a time, summed in choice order (four spilled)
-      for (int j0 = 0; j0 < k; j0 += 2) {
-        const Choice c0 = load_choice(Ys, my_p, my_w, j0, k, H, v, nvec);
-        const Choice c1 = load_choice(Ys, my_p, my_w, j0 + 1, k, H, v, nvec);
-        if (c0.use) fma8(acc, c0.w, c0.y);
-        if (c1.use) fma8(acc, c1.w, c1.y);
+    // warp-uniform trip counts: every lane takes part in the shuffles, only the loads are guarded
+    for (int64_t v0 = 0; v0 < nvec; v0 += 32 * kCombineU) {
+      float acc[kCombineU][8];
+#pragma unroll
+      for (int u = 0; u < kCombineU; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[u][e] = 0.0f;
+      // nxt: choice j's pieces v0 + lane + 32 u, u < kCombineU (zero when the choice is dropped)
+      uint4 nxt[kCombineU];
+      int32_t pn = __shfl_sync(0xffffffffu, my_p, 0);
+      float wn = __shfl_sync(0xffffffffu, my_w, 0);
+#pragma unroll
+      for (int u = 0; u < kCombineU; ++u) {
+        const int64_t v = v0 + lane + 32 * u;
+        nxt[u] = (pn >= 0 && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(Ys + (int64_t)pn * H) + v)
+                                       : make_uint4(0, 0, 0, 0);
       }
-      if (v >= nvec) continue;
-      uint4 o;
-      o.x = pack_bf16x2(acc[0], acc[1]);
-      o.y = pack_bf16x2(acc[2], acc[3]);
-      o.z = pack_bf16x2(acc[4], acc[5]);
-      o.w = pack_bf16x2(acc[6], acc[7]);
-      reinterpret_cast<uint4*>(out + t * H)[v] = o;
+      for (int j = 0; j < k; ++j) {
+        uint4 cur[kCombineU];
+#pragma unroll
+        for (int u = 0; u < kCombineU; ++u) cur[u] = nxt[u];
+        const int32_t pc = pn;
+        const float wc = wn;
+        if (j + 1 < k) {
+          pn = __shfl_sync(0xffffffffu, my_p, (j + 1) & 31);
+          wn = __shfl_sync(0xffffffffu, my_w, (j + 1) & 31);
+#pragma unroll
+          for (int u = 0; u < kCombineU; ++u) {
+            const int64_t v = v0 + lane + 32 * u;
+            nxt[u] = (pn >= 0 && v < nvec) ? __ldg(reinterpret_cast<const uint4*>(Ys + (int64_t)pn * H) + v)
+                                           : make_uint4(0, 0, 0, 0);
+          }
+        }
+        if (pc >= 0) {
+#pragma unroll
+          for (int u = 0; u < kCombineU; ++u) fma8(acc[u], wc, cur[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kCombineU; ++u) {
+        const int64_t v = v0 + lane + 32 * u;
+        if (v >= nvec) continue;
+        uint4 o;
+        o.x = pack_bf16x2(acc[u][0], acc[u][1]);
+        o.y = pack_bf16x2(acc[u][2], acc[u][3]);
+        o.z = pack_bf16x2(acc[u][4], acc[u][5]);
+        o.w = pack_bf16x2(acc[u][6], acc[u][7]);
+        reinterpret_cast<uint4*>(out + t * H)[v] = o;
+      }
     }
   }
 }
@@ -252,20 +270,32 @@ __global__ void __launch_bounds__(kCopyThreads) moe_combine_bwd_kernel(
       const uint4* y = reinterpret_cast<const uint4*>(Ys + (int64_t)p * H);
       uint4* d = reinterpret_cast<uint4*>(dYs + (int64_t)p * H);
       float dot = 0.0f;
-      for (int64_t v = lane; v < nvec; v += 32) {
-        const uint4 gv = __ldg(g + v);
-        const uint4 yv = __ldg(y + v);
-        const uint32_t ga[4] = {gv.x, gv.y, gv.z, gv.w};
-        const uint32_t ya[4] = {yv.x, yv.y, yv.z, yv.w};
-        uint32_t o[4];
+      // kCombineU pieces per lane at a time (2 kCombineU loads in flight); the lane's partial
+      // sum still runs over v = lane, lane + 32, ... in order
+      for (int64_t v0 = 0; v0 < nvec; v0 += 32 * kCombineU) {
+        uint4 gv[kCombineU], yv[kCombineU];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float g0 = bf16_lo(ga[q]), g1 = bf16_hi(ga[q]);
-          dot += g0 * bf16_lo(ya[q]);
-          dot += g1 * bf16_hi(ya[q]);
-          o[q] = pack_bf16x2(wj * g0, wj * g1);
+        for (int u = 0; u < kCombineU; ++u) {
+          const int64_t v = v0 + lane + 32 * u;
+          gv[u] = v < nvec ? __ldg(g + v) : make_uint4(0, 0, 0, 0);
+          yv[u] = v < nvec ? __ldg(y + v) : make_uint4(0, 0, 0, 0);
         }
-        d[v] = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int u = 0; u < kCombineU; ++u) {
+          const int64_t v = v0 + lane + 32 * u;
+          if (v >= nvec) continue;
+          const uint32_t ga[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+          const uint32_t ya[4] = {yv[u].x, yv[u].y, yv[u].z, yv[u].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float g0 = bf16_lo(ga[q]), g1 = bf16_hi(ga[q]);
+            dot += g0 * bf16_lo(ya[q]);
+            dot += g1 * bf16_hi(ya[q]);
+            o[q] = pack_bf16x2(wj * g0, wj * g1);
+          }
+          d[v] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
@@ -315,8 +345,16 @@ int launch_moe_permute(const int32_t* ids, const void* X, int64_t T, int k, int6
 int launch_moe_combine(const void* Ys, const int32_t* pos, const float* w, int64_t T, int k, int64_t H,
                        void* out, cudaStream_t s) {
   if (T == 0) return PGG_OK;
-  const int blocks = copy_grid(T);
-  if (blocks == 0) return PGG_ERR_CUDA;
+  // one wave of resident blocks (the kernel walks tokens with a grid stride): its registers
+  // allow fewer blocks per SM than copy_grid assumes
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_combine_kernel, kCopyThreads, 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int64_t need = (T + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)dev.sms * std::max(per_sm, 1)));
   moe_combine_kernel<<<blocks, kCopyThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(Ys), pos, w, T, k, H,
                                                      static_cast<__nv_bfloat16*>(out));
   return cuda_status(cudaGetLastError());
@@ -325,8 +363,14 @@ int launch_moe_combine(const void* Ys, const int32_t* pos, const float* w, int64
 int launch_moe_combine_bwd(const void* dOut, const void* Ys, const int32_t* pos, const float* w, int64_t T, int k,
                            int64_t H, void* dYs, float* dw, cudaStream_t s) {
   if (T == 0) return PGG_OK;
-  const int blocks = copy_grid(T);
-  if (blocks == 0) return PGG_ERR_CUDA;
+  DeviceInfo dev;
+  int st = current_device(&dev);
+  if (st != PGG_OK) return st;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, moe_combine_bwd_kernel, kCopyThreads, 0);
+  if (e != cudaSuccess) return cuda_status(e);
+  const int64_t need = (T + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(need, (int64_t)dev.sms * std::max(per_sm, 1)));
   moe_combine_bwd_kernel<<<blocks, kCopyThreads, 0, s>>>(
       static_cast<const __nv_bfloat16*>(dOut), static_cast<const __nv_bfloat16*>(Ys), pos, w, T, k, H,
       static_cast<__nv_bfloat16*>(dYs), dw);

@@ -4,6 +4,8 @@ inputs (synthetic A, H, dH in place of the previous call's output).  The GPU qua
 with its own kernels; the oracle quantizes the same bf16 values of whole sampled experts
 itself and compares each call's output against the fp64 GEMM of its dequantized
 operands at |gpu - ref| <= 1e-2 |ref| + 1e-2 rms(ref)."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -24,7 +26,14 @@ def _syn(w, key, rows, cols, std, row0=0, device="cpu"):
     return wl.gen_matrix(key, rows, cols, std, w.seed, device=device, row0=row0)
 
 
-@pytest.mark.parametrize("w", [wl.DSV4_MXFP8, wl.ZIPF_MXFP4], ids=lambda w: w.name)
+# The Zipf-routed workload as drawn (exponent 1.2) leaves no expert empty; with exponent 2.5 the
+# same draw leaves 12 of the 256 experts without tokens (and gives expert 0 every token), so the
+# MXFP4 path also runs empty groups at full size.
+ZIPF_MXFP4_SKEWED = dataclasses.replace(wl.ZIPF_MXFP4, name="zipf_moe_mxfp4_h4096_e256_top8_t16384_i2048_s2.5",
+                                        zipf_s=2.5)
+
+
+@pytest.mark.parametrize("w", [wl.DSV4_MXFP8, wl.ZIPF_MXFP4, ZIPF_MXFP4_SKEWED], ids=lambda w: w.name)
 def test_mx_layer_full_size_isolated(w):
     f = w.fmt
     lens, row_token, b = build_layer_inputs(w, torch.device(DEV), allocate=False)
@@ -82,6 +91,9 @@ def test_mx_layer_full_size_isolated(w):
         util.assert_close(dX[r0:r1], omx.mx_grouped_gemm_dgrad(f, *dhq, *w1t, one(n), 1), f"expert {e} fc1 dgrad")
         dhc, xc = omx.mx_quantize_colwise(B(dh), [n], f, mp), omx.mx_quantize_colwise(B(X), [n], f, mp)
         util.assert_close(dW1[e], omx.mx_grouped_gemm_wgrad(f, *dhc, *xc, one(n))[0], f"expert {e} fc1 wgrad")
+    # experts without tokens: their weight gradients are exactly zero
+    for e in np.nonzero(lens == 0)[0]:
+        assert not bool(dW1[int(e)].any()) and not bool(dW2[int(e)].any()), f"empty expert {e}: dW not zero"
 
 
 # ---------------------------------------------------------------------------------------------

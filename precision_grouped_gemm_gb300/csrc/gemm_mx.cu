@@ -6,9 +6,10 @@
 //
 // Both operands are K-major along the reduction axis (the quantizers write them
 // that way), and a k-block is 128 bytes of every row with the 128-byte swizzle:
-// 128 e4m3 elements, or 256 packed e2m1 elements.  The producer warp loads codes with TMA and gathers the k-block's
-// scale factors with 4-byte cp.async straight into the 512-byte atom the MMA
-// wants (row m's 4 scales at byte 16 (m % 32) + 4 (m / 32)); the MMA warp copies
+// 128 e4m3 elements, or 256 packed e2m1 elements.  The producer warp loads codes with
+// TMA and blocked scale atoms with bulk copies; row-major scales (activations) are
+// gathered by a separate warp with 4-byte cp.async straight into the 512-byte atom the
+// MMA wants (row m's 4 scales at byte 16 (m % 32) + 4 (m / 32)); the MMA warp copies
 // each atom into TMEM with tcgen05.cp (32x128b, replicated to the four lane
 // quarters) and issues the block-scaled MMAs selecting scale bytes by ID.
 //
@@ -37,10 +38,10 @@ constexpr int kMxBM = 128, kMxBN = 128;
 // Reduction elements per 512-byte scale atom (four 32-element blocks per row); also the
 // padding granule of the column-wise layout.
 constexpr int kMxAtomK = 128;
-// wgrad tiles: 128 x 128 with a double-buffered accumulator.  (128 x 256 with one
-// accumulator -- TMEM cannot hold two next to the scale factors -- measured 12%
-// slower on the DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA.)
-// wgrad tile width per format (e2m1 reduces long group k-loops with little work per MMA)
+// wgrad tiles: e4m3 128 x 128 with three accumulators (128 x 256 with one accumulator --
+// TMEM cannot hold two next to the scale factors -- measured 12% slower on the
+// DeepSeek-shaped MXFP8 wgrads: the epilogue no longer overlaps the MMA); e2m1 128 x 256
+// with one, which halves the scale copies per flop of the long Zipf-routed group k-loops.
 constexpr int kMxWgradBNE4M3 = 128;
 constexpr int kMxWgradBNE2M1 = 256;
 // Forward / dgrad tile width per format.  A block-scaled MMA carries little work
@@ -54,7 +55,7 @@ constexpr int kMxFwdBNE2M1 = 256;
 // The e4m3 FC2 dgrad + SwiGLU backward is the exception: its epilogue (read H, write dH and
 // its MX codes) takes about as long as its MMAs, and the single accumulator of a 256-wide tile
 // serialises the two; 128-wide tiles with three accumulators overlap them (timed on the
-// DeepSeek-shaped layers: MXFP8 0.61 -> 0.55 ms, FP8 tensor-wise 0.54 -> 0.47 ms; the e2m1
+// DeepSeek-shaped layers: MXFP8 0.61 -> 0.55 ms, FP8 tensor-wise 0.54 -> 0.44 ms; the e2m1
 // one is slower at 128, 1.61 -> 1.80 ms, and every other fwd / dgrad call at either format).
 constexpr int kMxSwiGLUBwdBNE4M3 = 128;
 // Tile width of a fwd / dgrad call; swiglu: the call's SwiGLU epilogue flag (a dgrad with it is

@@ -183,14 +183,15 @@ __device__ __forceinline__ void mx_emit(const uint32_t (&w)[16], uint8_t* codes,
 // QF != 0 and qcodes != null: A is also emitted MX-quantized (row-wise, I % 32 == 0).
 // limit > 0 clamps first: gate <- min(gate, limit), up <- clamp(up, -limit, limit); H
 // keeps the values before the clamp.  SCALED: gate and up are the accumulators times alpha.
-// Rows as epi_store; this thread's own row is grow (row_ok: it exists).
+// Rows as epi_store; this thread's own row is grow (row_ok: it exists).  The warp handles the
+// 32-column chunks [cb, ce) of each half (all of them by default).
 template <int BN, int QF = 0, bool SCALED = false>
 __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_bfloat16* H, size_t row0w,
                                            int nrows, bool row_ok, size_t grow, int col0, int I, uint8_t* stg,
                                            int lane, uint8_t* qcodes = nullptr, uint8_t* qscales = nullptr,
-                                           float limit = 0.0f, float alpha = 1.0f) {
+                                           float limit = 0.0f, float alpha = 1.0f, int cb = 0, int ce = BN / 64) {
 #pragma unroll 1
-  for (int c = 0; c < BN / 64; ++c) {
+  for (int c = cb; c < ce; ++c) {
     uint32_t rg[32], ru[32];
     tmem_ld32(tb + c * 32, rg);
     tmem_ld32(tb + BN / 2 + c * 32, ru);
@@ -234,10 +235,10 @@ __device__ __forceinline__ void epi_swiglu(uint32_t tb, __nv_bfloat16* A, __nv_b
 // before the accumulator wait, has already pulled the tile's H into L2.
 template <int BN>
 __device__ __forceinline__ void epi_swiglu_bwd_prefetch(const __nv_bfloat16* H, size_t grow, bool row_ok,
-                                                        int col0, int I) {
+                                                        int col0, int I, int cb = 0, int ce = BN / 32) {
   if (!row_ok) return;
-  const __nv_bfloat16* g = H + grow * (2 * (size_t)I) + col0;
-  const int n = min(BN, I - col0);  // columns of this tile in each half
+  const __nv_bfloat16* g = H + grow * (2 * (size_t)I) + col0 + cb * 32;
+  const int n = min(32 * (ce - cb), I - col0 - cb * 32);  // columns of the chunks [cb, ce) in each half
   if (n <= 0) return;
 #pragma unroll 1
   for (int b = 0; b < n * 2; b += 128) {  // 128-byte lines of the gate and up segments
@@ -251,6 +252,7 @@ __device__ __forceinline__ void epi_swiglu_bwd_prefetch(const __nv_bfloat16* H, 
 // accumulator times alpha.  TSTORE: dH goes out warp-transposed through stg; otherwise each
 // lane stores its own row.  (Timed on the full layer steps: transposed stores are faster in
 // the BF16 kernel, per-lane stores in the block-scaled one; transposed H loads lost in both.)
+// The warp handles the 32-column chunks [cb, ce) of the tile (all of them by default).
 // Warp-collective (stg, TSTORE): every lane calls it with the same tile arguments.
 __device__ __forceinline__ void ld_row32(const __nv_bfloat16* src, uint4 (&w)[4], int ncols) {
 #pragma unroll
@@ -267,16 +269,17 @@ template <int BN, int QF = 0, bool SCALED = false, bool TSTORE = true>
 __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, const __nv_bfloat16* H,
                                                size_t row0w, int nrows, bool row_ok, size_t grow, int col0, int I,
                                                uint8_t* stg, int lane, uint8_t* qcodes = nullptr,
-                                               uint8_t* qscales = nullptr, float limit = 0.0f, float alpha = 1.0f) {
+                                               uint8_t* qscales = nullptr, float limit = 0.0f, float alpha = 1.0f,
+                                               int cb = 0, int ce = BN / 32) {
   const size_t ldh = 2 * (size_t)I;
   const __nv_bfloat16* hrow = H + grow * ldh;
   uint4 ng[4], nu[4];  // the next chunk's gate / up words of this lane's row
-  if (row_ok && col0 < I) {
-    ld_row32(hrow + col0, ng, I - col0);
-    ld_row32(hrow + I + col0, nu, I - col0);
+  if (row_ok && col0 + cb * 32 < I) {
+    ld_row32(hrow + col0 + cb * 32, ng, I - col0 - cb * 32);
+    ld_row32(hrow + I + col0 + cb * 32, nu, I - col0 - cb * 32);
   }
 #pragma unroll 1
-  for (int c = 0; c < BN / 32; ++c) {
+  for (int c = cb; c < ce; ++c) {
     const int c0 = col0 + c * 32;
     uint32_t hgw[16], huw[16];
 #pragma unroll
@@ -284,7 +287,7 @@ __device__ __forceinline__ void epi_swiglu_bwd(uint32_t tb, __nv_bfloat16* dH, c
       hgw[4 * q] = ng[q].x; hgw[4 * q + 1] = ng[q].y; hgw[4 * q + 2] = ng[q].z; hgw[4 * q + 3] = ng[q].w;
       huw[4 * q] = nu[q].x; huw[4 * q + 1] = nu[q].y; huw[4 * q + 2] = nu[q].z; huw[4 * q + 3] = nu[q].w;
     }
-    if (row_ok && c0 + 32 < I && c + 1 < BN / 32) {
+    if (row_ok && c0 + 32 < I && c + 1 < ce) {
       ld_row32(hrow + c0 + 32, ng, I - c0 - 32);
       ld_row32(hrow + I + c0 + 32, nu, I - c0 - 32);
     }

@@ -68,13 +68,34 @@ constexpr int kMxWgradStoreAtoms = 2;  // 64-column atoms per bulk store of a wg
 // start before the epilogue has drained tile t: a wgrad tile has a single k-block,
 // so the accumulator hand-off round trip is as long as the epilogue itself.
 constexpr int kMxAccBufs = 3;
-// Warps: 0 load producer (TMA tiles, bulk scale atoms), 1 MMA issuer, 2-5 epilogue, and for the
-// fwd / dgrad of block-scaled operands 6, the scale gatherer: the row-major scales of the A
-// operand (and of a forward weight tile not on whole atoms) are gathered into the atom layout
-// by 4-byte cp.async copies, which took the producer about as long as its TMA issue (clock64
-// on the Zipf-routed MXFP4 layer: 273 of 629 ns per k-block), so they run beside it.
-template <int MODE, bool TS>
-__host__ __device__ constexpr int mx_threads() { return MODE != kWgrad && !TS ? 224 : 192; }
+// Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the SwiGLU forward, where two warps
+// share a lane quarter and split the tile's columns: that epilogue holds the tile's single
+// accumulator while it computes and stores three outputs per value, and the next tile's MMAs
+// wait for its release.
+template <int EPI>
+__host__ __device__ constexpr int mx_epi_warps() { return EPI == kEpiSwiGLU ? 8 : 4; }
+// Warps: 0 load producer (TMA tiles, bulk scale atoms), 1 MMA issuer, 2 .. 1 + mx_epi_warps
+// epilogue; then for the fwd / dgrad of block-scaled operands the scale gatherer, and for every
+// block-scaled kernel the scale copier.
+// - Gatherer: the row-major scales of the A operand (and of a forward weight tile not on whole
+//   atoms) are gathered into the atom layout by 4-byte cp.async copies, which took the producer
+//   about as long as its TMA issue (clock64 on the Zipf-routed MXFP4 layer: 273 of 629 ns per
+//   k-block), so they run beside it.
+// - Copier: moves each stage's scale atoms into that stage's TMEM slot (tcgen05.cp) and commits
+//   them to the stage's scale barrier, on which the MMA issuer waits.  A tcgen05.cp costs its
+//   issuing thread ~48 ns; issued by the MMA thread, the six of an e2m1 k-block overlapped its
+//   four MMAs only partly (413 ns per k-block against 267 ns for the MMAs alone, timed on a
+//   GB300 with all SMs busy), and from a second warp they run beside them (290 ns).  On the
+//   Zipf-routed MXFP4 layer: fc1 fwd 1.744 -> 1.624 ms, fc1 wgrad 2.207 -> 2.083 ms; MXFP8 SwiGLU
+//   backward 0.543 -> 0.503 ms.  The e2m1 SwiGLU backward keeps the copies in the MMA thread
+//   (1.606 -> 1.660 ms with the copier): its single accumulator is drained by an epilogue that
+//   takes longer than the MMAs, and early copies for the next tile only compete with it.
+template <int FMT, int EPI, bool TS>
+__host__ __device__ constexpr bool mx_sf_copier() { return !TS && !(FMT == kE2M1 && EPI == kEpiSwiGLUBwd); }
+template <int FMT, int MODE, int EPI, bool TS>
+__host__ __device__ constexpr int mx_threads() {
+  return 32 * (2 + mx_epi_warps<EPI>() + (MODE != kWgrad && !TS ? 1 : 0) + (mx_sf_copier<FMT, EPI, TS>() ? 1 : 0));
+}
 
 struct MxArgs {
   const int32_t* group_lens;
@@ -133,12 +154,17 @@ struct MxCfg {
 // 3 pipeline stages, not 4); the HBM-bound e4m3 calls measured 2% slower that way and keep 4 stages.
 template <int FMT, int MODE, int EPI>
 __host__ __device__ constexpr bool mx_staged_store() { return FMT == kE2M1 && MODE != kWgrad && EPI == kEpiStore; }
-// Epilogue staging: the wgrad store and the staged plain store hold each epilogue warp's 32 rows x
-// BN bf16; the other fwd / dgrad epilogues a 2 KB chunk buffer per warp.
+// Epilogue staging per epilogue warp: the wgrad store and the staged plain store hold the warp's
+// 32 rows x BN bf16; the plain and SwiGLU forward stores a 2 KB chunk buffer; the SwiGLU backward
+// (per-lane stores) none.
 template <int FMT, int MODE, int EPI, int BN>
-constexpr int mx_epi_bytes() {
-  return MODE == kWgrad || mx_staged_store<FMT, MODE, EPI>() ? 4 * 32 * BN * 2 : 4 * kEpiRowStageBytes;
+constexpr int mx_epi_warp_bytes() {
+  return MODE == kWgrad || mx_staged_store<FMT, MODE, EPI>() ? 32 * BN * 2
+         : EPI == kEpiSwiGLUBwd                               ? 0
+                                                              : kEpiRowStageBytes;
 }
+template <int FMT, int MODE, int EPI, int BN>
+constexpr int mx_epi_bytes() { return mx_epi_warps<EPI>() * mx_epi_warp_bytes<FMT, MODE, EPI, BN>(); }
 
 // BN = 128 (kMxAccBufs accumulators) or 256 (one accumulator: TMEM cannot hold
 // two 256-column accumulators next to the scale factors).  SF: the stages hold scale
@@ -161,6 +187,25 @@ struct MxSmem {
 struct MxTile {
   int g, row0, rows, col0, nkb, poff, len;
 };
+
+// The scale atoms of one stage (descriptor desc_sf: its first atom) into its TMEM slot at sfa_t:
+// for each of the nsub sub-blocks that hold data, SFA 4 columns, then SFB 4 columns per 128 rows
+// of B (column n / 32 of the sub-block), after the kSub x 4 SFA columns.  SFA_BYTES: the stage's
+// SFA atoms, after which each 128-row block of B has its own.
+template <int FMT, int BN, int SFA_BYTES>
+__device__ __forceinline__ void mx_copy_scales(uint32_t sfa_t, uint64_t desc_sf, int nsub) {
+  constexpr int kSub = MxCfg<FMT>::kSub;
+  constexpr uint32_t kSfbPer = 4 * (BN / 128);
+  const uint32_t sfb_t = sfa_t + 4 * kSub;
+#pragma unroll
+  for (int sub = 0; sub < kSub; ++sub) {
+    if (sub >= nsub) break;
+    tmem_cp_32x128b_x4(sfa_t + 4 * sub, desc_sf + (sub * 512 >> 4));
+#pragma unroll
+    for (int h = 0; h < BN / 128; ++h)
+      tmem_cp_32x128b_x4(sfb_t + sub * kSfbPer + 4 * h, desc_sf + ((SFA_BYTES * (1 + h) + sub * 512) >> 4));
+  }
+}
 
 template <int EPI, int BN>
 __device__ __forceinline__ int mx_tile_cols() { return EPI == kEpiSwiGLU ? BN / 2 : BN; }
@@ -194,7 +239,7 @@ __device__ __forceinline__ MxTile mx_decode(int t, const MxArgs& a, const int32_
 }
 
 template <int FMT, int MODE, int EPI, int STAGES, int BN, bool TS = false>
-__global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
+__global__ void __launch_bounds__(mx_threads<FMT, MODE, EPI, TS>(), 1)
     grouped_gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const __grid_constant__ CUtensorMap tmC, const MxArgs args) {
   using C = MxCfg<FMT>;
@@ -203,6 +248,11 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
   using L = MxSmem<FMT, BN, STAGES, mx_epi_bytes<FMT, MODE, EPI, BN>(), !TS>;
   constexpr bool kSF = !TS;                              // block scale factors (else plain FP8 MMAs)
   constexpr int NACC = BN == 256 ? 1 : kMxAccBufs;       // accumulator buffers
+  constexpr int kEpiW = mx_epi_warps<EPI>();              // epilogue warps 2 .. 1 + kEpiW
+  constexpr bool kHasGather = MODE != kWgrad && !TS;
+  constexpr int kGatherWarp = 2 + kEpiW;                  // the scale gatherer, where there is one
+  constexpr bool kCopier = mx_sf_copier<FMT, EPI, TS>();  // scale copies by a warp of their own
+  constexpr int kCopyWarp = kGatherWarp + (kHasGather ? 1 : 0);  // the scale copier, where there is one
   constexpr uint32_t kIdesc = TS ? idesc_f8f6f4(0, kMxBM, BN) : idesc_mx(C::kElem, kMxBM, BN);
   constexpr uint32_t kTmemCols = 512;
   constexpr uint32_t kSfCol0 = NACC * BN;                 // scale-factor columns after the accumulators
@@ -211,7 +261,7 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
   constexpr uint32_t kSfPer = C::kSub * (4 + kSfbPer);
   static_assert(kSfCol0 + STAGES * kSfPer <= kTmemCols, "TMEM columns");
   // barriers, the wait control (16 B), the TMEM address and the bad-lens code
-  static_assert((2 * STAGES + 2 * NACC + 1) * 8 + 24 <= L::kGroupOff - L::kBarOff, "barrier area");
+  static_assert((3 * STAGES + 2 * NACC + 2) * 8 + 24 <= L::kGroupOff - L::kBarOff, "barrier area");
   // Scale factors of an operand are either row-major [rows, K/32] (activations, whose
   // tiles start at ragged group offsets), gathered 4 bytes per row by cp.async into
   // the atom, or in the blocked atom layout (column-wise operands: wgrad A and B,
@@ -233,7 +283,9 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + NACC;
   uint64_t* drain = tempty + NACC;
-  volatile WaitCtl* s_ctl = reinterpret_cast<volatile WaitCtl*>(drain + 1);
+  uint64_t* sfull = drain + 1;      // a stage's scale atoms are in its TMEM slot
+  uint64_t* cdrain = sfull + STAGES;
+  volatile WaitCtl* s_ctl = reinterpret_cast<volatile WaitCtl*>(cdrain + 1);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(const_cast<WaitCtl*>(s_ctl) + 1);
   int* s_bad = reinterpret_cast<int*>(s_tmem + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + L::kGroupOff);
@@ -248,9 +300,11 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
     }
     for (int a = 0; a < NACC; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 128);
+      mbar_init(smem_u32(&tempty[a]), 32 * kEpiW);
     }
     mbar_init(smem_u32(drain), 1);
+    for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&sfull[s]), 1);
+    mbar_init(smem_u32(cdrain), 1);
     s_ctl->abort = 0;
     s_ctl->limit_ns = args.wait_ns ? args.wait_ns : kWaitTimeoutNs;
     fence_mbar_init();
@@ -381,12 +435,12 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    // Shared-memory descriptors of stage 0's A tile, B tile and first scale atom.  A descriptor's
-    // start-address field holds address / 16 in 14 bits, which every address of this block fits,
-    // so the descriptor of address + d (d a multiple of 16) is the base descriptor + d / 16.
+    // Shared-memory descriptors of stage 0's A and B tiles.  A descriptor's start-address field
+    // holds address / 16 in 14 bits, which every address of this block fits, so the descriptor of
+    // address + d (d a multiple of 16) is the base descriptor + d / 16 (here and in the copier).
     const uint64_t kDescA = smem_desc(smem0, 16, C::kSbo, C::kSwizzle);
     const uint64_t kDescB = smem_desc(smem0 + L::kA, 16, C::kSbo, C::kSwizzle);
-    const uint64_t kDescSf = smem_desc(smem0 + L::kA + L::kB, 0, 128, kSwizzleNone);
+    const uint64_t kDescSf = smem_desc(smem0 + L::kA + L::kB, 0, 128, kSwizzleNone);  // first scale atom
     for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
       const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
       if (T.nkb == 0) continue;
@@ -395,25 +449,20 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
       const uint32_t d_tmem = tmem_base + acc * BN;
       for (int kb = 0; kb < T.nkb; ++kb) {
         if (!warp_wait(smem_u32(&full[stage]), phase, s_ctl)) { aborted = true; break; }
+        if (kCopier && !warp_wait(smem_u32(&sfull[stage]), phase, s_ctl)) { aborted = true; break; }
         tc_fence_after();
         if (lane == 0) {
           const uint64_t so = (uint64_t)(stage * L::kStage) >> 4;  // this stage's descriptor offset
           const uint32_t sfa_t = tmem_base + kSfCol0 + stage * kSfPer;  // kSub x 4 SFA columns
           const uint32_t sfb_t = sfa_t + 4 * C::kSub;                    // kSub x kSfbPer SFB columns
-          // scale sub-blocks and MMAs of this k-block that hold data: past the end of K / N (an
-          // e2m1 K that is an odd multiple of 128) or past a wgrad group's rows, the k-steps cover
-          // only zeros and are skipped (exact); so are their scale copies
+          // MMAs of this k-block that hold data: past the end of K / N (an e2m1 K that is an odd
+          // multiple of 128) or past a wgrad group's rows, the k-steps cover only zeros and are
+          // skipped (exact); so are their scale copies
           const int valid = (MODE == kWgrad ? T.len : red_all) - kb * C::kBK;
-          const int nsub = min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK);
           const int nmma = min(C::kMmas, (valid + C::kPerMma - 1) / C::kPerMma);
-          if (kGatherA) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
-#pragma unroll
-          for (int sub = 0; sub < C::kSub; ++sub) {
-            if (!kSF || sub >= nsub) break;
-            tmem_cp_32x128b_x4(sfa_t + 4 * sub, kDescSf + so + (sub * 512 >> 4));
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)  // SFB column n / 32 of the sub-block: 4 columns per 128 rows
-              tmem_cp_32x128b_x4(sfb_t + sub * kSfbPer + 4 * h, kDescSf + so + ((L::kSFA * (1 + h) + sub * 512) >> 4));
+          if (kSF && !kCopier) {
+            if (kGatherA) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
+            mx_copy_scales<FMT, BN, L::kSFA>(sfa_t, kDescSf + so, min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK));
           }
 #pragma unroll
           for (int j = 0; j < C::kMmas; ++j) {
@@ -444,7 +493,39 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
       mma_commit(smem_u32(drain));
       mbar_wait_drain(smem_u32(drain), 0);
     }
-  } else if (warp == 6) {
+  } else if (kCopier && warp == kCopyWarp) {
+    // ------------------------------------------------------------ scale copier (block-scaled)
+    // the MMA issuer's stage sequence: once a stage has landed, its scale atoms go to the stage's
+    // TMEM slot (SFA: 4 columns per sub-block; SFB: 4 per sub-block and 128 rows of B) and a
+    // commit arrives on the stage's scale barrier when they are there.  A slot is rewritten only
+    // after the stage was refilled, i.e. after the MMAs that read the slot last completed.
+    GroupCursor cur;
+    int stage = 0;
+    uint32_t phase = 0;
+    const uint64_t kDescSf = smem_desc(smem0 + L::kA + L::kB, 0, 128, kSwizzleNone);
+    for (int t = blockIdx.x; t < total_tiles && !aborted; t += gridDim.x) {
+      const MxTile T = mx_decode<MODE, EPI, BN, C::kBK>(t, args, s_off, s_tile, s_poff, cur);
+      for (int kb = 0; kb < T.nkb; ++kb) {
+        if (!warp_wait(smem_u32(&full[stage]), phase, s_ctl)) { aborted = true; break; }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t so = (uint64_t)(stage * L::kStage) >> 4;
+          // scale sub-blocks of this k-block that hold data (the MMAs past them are skipped)
+          const int valid = (MODE == kWgrad ? T.len : red_all) - kb * C::kBK;
+          if (kGatherA) fence_proxy_async_smem();  // cp.async-written scales -> async proxy
+          mx_copy_scales<FMT, BN, L::kSFA>(tmem_base + kSfCol0 + stage * kSfPer, kDescSf + so,
+                                           min(C::kSub, (valid + kMxAtomK - 1) / kMxAtomK));
+          mma_commit(smem_u32(&sfull[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (aborted && lane == 0) {  // copies nobody waited for complete before TMEM is freed
+      mma_commit(smem_u32(cdrain));
+      mbar_wait_drain(smem_u32(cdrain), 0);
+    }
+  } else if (warp == kGatherWarp) {
     // ------------------------------------------------------------ scale gatherer (fwd / dgrad, block-scaled)
     // the producer's tile and k-block sequence; its 32 cp.async arrivals complete each stage's
     // full barrier together with the producer's expect_tx arrival and copies
@@ -514,14 +595,15 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
       cp_async_wait_all();  // nothing of this warp's lands after the block exits
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 2..5)
-    const int q = warp & 3;
+    // ------------------------------------------------------------ epilogue (warps 2 .. 1 + kEpiW)
+    const int q = warp & 3;                 // TMEM lane quarter
+    const int half = (warp - 2) >> 2;       // with 8 epilogue warps: which half of the tile's columns
     const int r = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out);
     GroupCursor cur;
-    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * (mx_epi_bytes<FMT, MODE, EPI, BN>() / 4);  // this warp's staging
+    uint8_t* stg = smem + L::kEpiOff + (warp - 2) * mx_epi_warp_bytes<FMT, MODE, EPI, BN>();  // this warp's staging
     int nstore = 0;
     float alpha = 1.0f;  // TS: 1 / (s_A s_B), written by the quantizers earlier on the stream
     // The product of two fp32 scales is exact in fp64 and cannot overflow there (each scale is at
@@ -553,19 +635,24 @@ __global__ void __launch_bounds__(mx_threads<MODE, TS>(), 1)
       const size_t grow = (size_t)T.row0 + r;
       const size_t row0w = (size_t)T.row0 + q * 32;         // the warp's first output row
       const int nrows = max(0, min(32, T.rows - q * 32));    // of which this many exist
+      // 32-column chunks of this warp: of each SwiGLU half (BN / 64 per half), or of the tile
+      constexpr int kChunks = EPI == kEpiSwiGLU ? BN / 64 : BN / 32;
+      constexpr int kMine = kChunks * 4 / kEpiW;
+      const int cb = half * kMine, ce = cb + kMine;
       if (EPI == kEpiSwiGLUBwd)  // the saved H of this tile streams into L2 while the MMAs run
         epi_swiglu_bwd_prefetch<BN>(reinterpret_cast<const __nv_bfloat16*>(args.aux), grow, row_ok, T.col0,
-                                    args.I);
+                                    args.I, cb, ce);
       if (!warp_wait(smem_u32(&tfull[acc]), acc_phase, s_ctl)) { aborted = true; break; }
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == kEpiSwiGLU) {
         epi_swiglu<BN, FMT, TS>(tb, out, reinterpret_cast<__nv_bfloat16*>(args.out2), row0w, nrows, row_ok, grow,
-                                T.col0, args.I, stg, lane, args.q_codes, args.q_scales, args.swiglu_limit, alpha);
+                                T.col0, args.I, stg, lane, args.q_codes, args.q_scales, args.swiglu_limit, alpha, cb,
+                                ce);
       } else if (EPI == kEpiSwiGLUBwd) {
         epi_swiglu_bwd<BN, FMT, TS, false>(tb, out, reinterpret_cast<const __nv_bfloat16*>(args.aux), row0w, nrows, row_ok,
                                     grow, T.col0, args.I, stg, lane, args.q_codes, args.q_scales, args.swiglu_limit,
-                                    alpha);
+                                    alpha, cb, ce);
       } else if constexpr (mx_staged_store<FMT, MODE, EPI>()) {
         epi_stage_tile<BN, TS>(tb, stg, lane, alpha);
         tc_fence_before();
@@ -604,7 +691,7 @@ int run_mx(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, 
     if (e != cudaSuccess) return e == cudaErrorInvalidValue ? PGG_ERR_UNSUPPORTED : cuda_status(e);
     attr_bytes = smem;
   }
-  kern<<<grid, mx_threads<MODE, TS>(), smem, s>>>(ta, tb, tc, a);
+  kern<<<grid, mx_threads<FMT, MODE, EPI, TS>(), smem, s>>>(ta, tb, tc, a);
   return cuda_status(cudaGetLastError());
 }
 
@@ -635,7 +722,7 @@ int dispatch_mx(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   // + 32 KB, e2m1 3 x 51 KB + 64 KB (2 stages when the group tables of a large G leave no room)
   constexpr int kSw = FMT == kE4M3 ? 5 : 3;
   if (mode == 0 && epi == 0) return run_mx_fit<FMT, kFwd, kEpiStore, kSp, kBN>(ta, tb, tc, a, grid, s);
-  if (mode == 0 && epi == 1) return run_mx<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 1) return run_mx_fit<FMT, kFwd, kEpiSwiGLU, kS, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx_fit<FMT, kDgrad, kEpiStore, kSp, kBN>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 1) return run_mx<FMT, kDgrad, kEpiSwiGLUBwd, kSb, kBNb>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) {
@@ -658,7 +745,7 @@ int dispatch_ts(int mode, int epi, const CUtensorMap& ta, const CUtensorMap& tb,
   constexpr int kSp = 4;
   constexpr int kSw = 5;
   if (mode == 0 && epi == 0) return run_mx_fit<kE4M3, kFwd, kEpiStore, kSp, kBN, true>(ta, tb, tc, a, grid, s);
-  if (mode == 0 && epi == 1) return run_mx<kE4M3, kFwd, kEpiSwiGLU, kS, kBN, true>(ta, tb, tc, a, grid, s);
+  if (mode == 0 && epi == 1) return run_mx_fit<kE4M3, kFwd, kEpiSwiGLU, kS, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 0) return run_mx_fit<kE4M3, kDgrad, kEpiStore, kSp, kBN, true>(ta, tb, tc, a, grid, s);
   if (mode == 1 && epi == 1) return run_mx<kE4M3, kDgrad, kEpiSwiGLUBwd, kSb, kBNb, true>(ta, tb, tc, a, grid, s);
   if (mode == 2 && epi == 0) return run_mx<kE4M3, kWgrad, kEpiStore, kSw, kWBN, true>(ta, tb, tc, a, grid, s);

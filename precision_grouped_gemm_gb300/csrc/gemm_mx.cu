@@ -9,9 +9,10 @@
 // 128 e4m3 elements, or 256 packed e2m1 elements.  The producer warp loads codes with
 // TMA and blocked scale atoms with bulk copies; row-major scales (activations) are
 // gathered by a separate warp with 4-byte cp.async straight into the 512-byte atom the
-// MMA wants (row m's 4 scales at byte 16 (m % 32) + 4 (m / 32)); the MMA warp copies
-// each atom into TMEM with tcgen05.cp (32x128b, replicated to the four lane
-// quarters) and issues the block-scaled MMAs selecting scale bytes by ID.
+// MMA wants (row m's 4 scales at byte 16 (m % 32) + 4 (m / 32)); a copier warp (or, in
+// the e2m1 SwiGLU backward, the MMA warp itself) copies each atom into TMEM with
+// tcgen05.cp (32x128b, replicated to the four lane quarters), and the MMA warp issues
+// the block-scaled MMAs selecting scale bytes by ID.
 //
 //   fwd    out[M, N]    = A[M, K] . B_g[N, K]^T     A = X rows, B = W [G, N, K]
 //   dgrad  out[M, K]    = A[M, N] . Bt_g[K, N]^T    Bt = W^T [K, G*N] (blocks along N)
@@ -87,9 +88,9 @@ __host__ __device__ constexpr int mx_epi_warps() { return EPI == kEpiSwiGLU ? 8 
 //   four MMAs only partly (413 ns per k-block against 267 ns for the MMAs alone, timed on a
 //   GB300 with all SMs busy), and from a second warp they run beside them (290 ns).  On the
 //   Zipf-routed MXFP4 layer: fc1 fwd 1.744 -> 1.624 ms, fc1 wgrad 2.207 -> 2.083 ms; MXFP8 SwiGLU
-//   backward 0.543 -> 0.503 ms.  The e2m1 SwiGLU backward keeps the copies in the MMA thread
-//   (1.606 -> 1.660 ms with the copier): its single accumulator is drained by an epilogue that
-//   takes longer than the MMAs, and early copies for the next tile only compete with it.
+//   backward 0.543 -> 0.503 ms.  The e2m1 SwiGLU backward keeps the copies in the MMA thread:
+//   with the copier it measured 1.606 -> 1.660 ms, and 1.615 -> 1.684 ms with the copies of a tile
+//   held back until the previous tile's epilogue had released the accumulator.
 template <int FMT, int EPI, bool TS>
 __host__ __device__ constexpr bool mx_sf_copier() { return !TS && !(FMT == kE2M1 && EPI == kEpiSwiGLUBwd); }
 template <int FMT, int MODE, int EPI, bool TS>
